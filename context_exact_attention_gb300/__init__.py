@@ -1,0 +1,234 @@
+"""Exact context-parallel attention on one GB300: thin Python binding of libringattn.so.
+
+Every function here only checks tensor properties, allocates outputs with
+torch when the caller passes none, and forwards raw device pointers to the C
+ABI declared in ``include/ring_attn.h``.  All arithmetic runs in the library's
+CUDA kernels; there is no fallback of any kind, and calling into a missing or
+unbuilt library raises.
+
+Layout: q, k, v, out are contiguous [B, L, H, D]; lse is fp32 [B, L, H].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import workloads  # noqa: F401  (seeded inputs; no attention arithmetic)
+
+__all__ = [
+    "RingAttnError", "library_path", "load_library", "ring_attn_fwd", "ring_attn_fwd_f32",
+    "ring_attn_fwd_trace", "attn_merge_partials", "ulysses_seq2head", "ulysses_head2seq",
+    "ulysses_attention", "check_status", "probe_wait_timeout", "EXPORTED_SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libringattn.so")
+_lock = threading.Lock()
+_lib = None
+
+RA_BF16, RA_F32 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned",
+           4: "not divisible", 5: "CUDA error", 6: "device-side wait timed out"}
+
+EXPORTED_SYMBOLS = (
+    "ring_attn_fwd", "ring_attn_fwd_f32", "ring_attn_fwd_trace", "attn_merge_partials",
+    "ulysses_seq2head", "ulysses_head2seq", "ra_check_status", "ra_status_string",
+    "ra_probe_wait_timeout",
+)
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {_STATUS.get(code, 'unknown')} (status {code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(build_if_missing: bool = False):
+    """Load libringattn.so (ctypes).  Raises if it is absent and not built here."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            from . import _build
+            _build.build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i, ll, f_p = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p
+        sigs = {
+            "ring_attn_fwd": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp],
+            "ring_attn_fwd_f32": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp],
+            "ring_attn_fwd_trace": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, vp, vp],
+            "attn_merge_partials": [vp, vp, vp, vp, vp, vp, ll, i, i, vp],
+            "ulysses_seq2head": [vp, vp, i, i, i, i, i, i, vp],
+            "ulysses_head2seq": [vp, vp, i, i, i, i, i, i, vp],
+            "ra_check_status": [vp],
+            "ra_probe_wait_timeout": [ctypes.c_ulonglong, vp],
+        }
+        for name, args in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.ra_status_string.argtypes = [ctypes.c_int]
+        lib.ra_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _call(name, *args):
+    rc = getattr(load_library(), name)(*args)
+    if rc != 0:
+        raise RingAttnError(name, rc)
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check_qkv(q, k, v, dtype):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, L, H, D] tensor")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k, v must have the same shape")
+
+
+def _attn(name, q, k, v, P, causal, out, lse, want_lse, dtype, stream, trace=None):
+    _check_qkv(q, k, v, dtype)
+    B, L, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, L, H), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, L, H)
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [B, L, H] tensor")
+    if trace is None:
+        _call(name, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, H, D, P,
+              int(bool(causal)), _stream(stream))
+    else:
+        _call(name, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, H, D, P,
+              int(bool(causal)), RA_BF16 if dtype == torch.bfloat16 else RA_F32, _ptr(trace),
+              _stream(stream))
+    return out, lse
+
+
+def ring_attn_fwd(q, k, v, P: int = 1, causal: bool = False, out=None, lse=None,
+                  want_lse: bool = True, stream=None):
+    """bf16 ring attention forward over P virtual shards.  Returns (out, lse)."""
+    return _attn("ring_attn_fwd", q, k, v, P, causal, out, lse, want_lse, torch.bfloat16, stream)
+
+
+def ring_attn_fwd_f32(q, k, v, P: int = 1, causal: bool = False, out=None, lse=None,
+                      want_lse: bool = True, stream=None):
+    """fp32 ring attention forward (SIMT path).  Returns (out, lse)."""
+    return _attn("ring_attn_fwd_f32", q, k, v, P, causal, out, lse, want_lse, torch.float32,
+                 stream)
+
+
+def ring_attn_fwd_trace(q, k, v, P: int = 1, causal: bool = False, stream=None):
+    """Attention forward that also returns the [P, P] schedule trace (source shard per
+    (shard, step), -1 where skipped).  Returns (out, lse, trace)."""
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q must be bf16 or fp32")
+    trace = torch.full((P, P), -7, dtype=torch.int32, device=q.device)
+    out, lse = _attn("ring_attn_fwd_trace", q, k, v, P, causal, None, None, True, dtype, stream,
+                     trace=trace)
+    return out, lse, trace
+
+
+def attn_merge_partials(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):
+    """LSE merge of two partials: o_*: [..., D] (bf16 or fp32), lse_*: [...] fp32."""
+    for t in (o_a, o_b, lse_a, lse_b):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("merge inputs must be contiguous CUDA tensors")
+    if o_a.dtype not in (torch.bfloat16, torch.float32) or o_b.dtype != o_a.dtype:
+        raise ValueError("o_a, o_b must both be bf16 or both fp32")
+    if lse_a.dtype != torch.float32 or lse_b.dtype != torch.float32:
+        raise ValueError("lse tensors must be fp32")
+    if o_a.shape != o_b.shape or lse_a.shape != o_a.shape[:-1] or lse_b.shape != lse_a.shape:
+        raise ValueError("shape mismatch")
+    D = o_a.shape[-1]
+    rows = o_a.numel() // D
+    if o_out is None:
+        o_out = torch.empty_like(o_a)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    _call("attn_merge_partials", _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o_out),
+          _ptr(lse_out), rows, D, RA_BF16 if o_a.dtype == torch.bfloat16 else RA_F32,
+          _stream(stream))
+    return o_out, lse_out
+
+
+def _permute(name, x, P, out_shape, B, L, H, D, out, stream):
+    if not x.is_cuda or not x.is_contiguous() or x.element_size() not in (2, 4):
+        raise ValueError("x must be a contiguous CUDA tensor of 2- or 4-byte elements")
+    if out is None:
+        out = torch.empty(out_shape, dtype=x.dtype, device=x.device)
+    _call(name, _ptr(x), _ptr(out), B, L, H, D, P, x.element_size(), _stream(stream))
+    return out
+
+
+def ulysses_seq2head(x, P: int, out=None, stream=None):
+    """[P, B, L/P, H, D] sequence-sharded -> [P, B, L, H/P, D] head-sharded (bit copy)."""
+    Pp, B, Ls, H, D = x.shape
+    if Pp != P or H % P:
+        raise ValueError("x must be [P, B, L/P, H, D] with H divisible by P")
+    return _permute("ulysses_seq2head", x, P, (P, B, Ls * P, H // P, D), B, Ls * P, H, D, out,
+                    stream)
+
+
+def ulysses_head2seq(x, P: int, out=None, stream=None):
+    """[P, B, L, H/P, D] head-sharded -> [P, B, L/P, H, D] sequence-sharded (bit copy)."""
+    Pp, B, L, Hg, D = x.shape
+    if Pp != P or L % P:
+        raise ValueError("x must be [P, B, L, H/P, D] with L divisible by P")
+    return _permute("ulysses_head2seq", x, P, (P, B, L // P, Hg * P, D), B, L, Hg * P, D, out,
+                    stream)
+
+
+def ulysses_attention(q_seq, k_seq, v_seq, P: int, stream=None, buffers=None):
+    """Ulysses path: seq->head transpose of q, k, v; full non-causal attention per head
+    group (the head-sharded buffer is a [P*B, L, H/P, D] batch); head->seq transpose of
+    the output.  Inputs [P, B, L/P, H, D] bf16.  Returns the output in the same layout."""
+    Pp, B, Ls, H, D = q_seq.shape
+    L, Hg = Ls * P, H // P
+    if buffers is None:
+        buffers = {n: torch.empty((P, B, L, Hg, D), dtype=q_seq.dtype, device=q_seq.device)
+                   for n in ("q", "k", "v", "o")}
+    qh = ulysses_seq2head(q_seq, P, out=buffers["q"], stream=stream)
+    kh = ulysses_seq2head(k_seq, P, out=buffers["k"], stream=stream)
+    vh = ulysses_seq2head(v_seq, P, out=buffers["v"], stream=stream)
+    shape = (P * B, L, Hg, D)
+    ring_attn_fwd(qh.view(shape), kh.view(shape), vh.view(shape), P=1, causal=False,
+                  out=buffers["o"].view(shape), want_lse=False, stream=stream)
+    return ulysses_head2seq(buffers["o"], P, stream=stream)
+
+
+def check_status(stream=None) -> int:
+    """Synchronise the stream and read/clear the device status word; returns the status code."""
+    return getattr(load_library(), "ra_check_status")(_stream(stream))
+
+
+def probe_wait_timeout(timeout_ns: int = 1_000_000, stream=None):
+    _call("ra_probe_wait_timeout", ctypes.c_ulonglong(timeout_ns), _stream(stream))

@@ -1,0 +1,310 @@
+// api.cu -- the extern "C" entry points of libringattn.so: host-side argument
+// checks (nothing is launched on a bad argument), TMA tensor-map encoding
+// through the driver entry point, dispatch to the kernels, and the per-device
+// status word that bounded device-side waits report into.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+
+namespace {
+
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s for any single wait
+constexpr int kMaxDevices = 64;
+
+// Status word of each device: bit RA_STATUS_TIMEOUT is set by a kernel whose
+// bounded wait ran out.  Read and cleared by ra_check_status().
+__device__ unsigned int g_status_word;
+
+unsigned int* g_status_ptr[kMaxDevices] = {nullptr};
+std::mutex g_mutex;
+
+ra_status status_word(unsigned int** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_status_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return RA_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return RA_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// q/k/v as a 4-D bf16 tensor {D, H, L, B} (innermost first); boxes of 64 head-dim
+// elements (128 bytes, the swizzle span) by 128 sequence rows, 128-byte swizzle.
+bool encode_qkv_map(CUtensorMap* map, const void* base, int B, int L, int H, int D)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(H) * D * 2,
+                                   static_cast<cuuint64_t>(L) * H * D * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void* a, unsigned long long na, const void* b, unsigned long long nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+ra_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
+
+// Shared checks of the attention entry points.  elem: element bytes.
+ra_status check_attn(const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, int B, int L, int H, int D, int P, int elem,
+                     unsigned long long* elems)
+{
+    if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
+    if (B < 1 || L < 1 || H < 1 || D < 1 || P < 1) return RA_ERR_INVALID_ARG;
+    const unsigned long long n = static_cast<unsigned long long>(B) * L * H * D;
+    if (n >= (1ull << 40)) return RA_ERR_INVALID_ARG;
+    if (L % P != 0) return RA_ERR_NOT_DIVISIBLE;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+        return RA_ERR_MISALIGNED;
+    if (lse && !aligned(lse, 4)) return RA_ERR_MISALIGNED;
+    const unsigned long long bytes = n * elem;
+    if (overlap(out, bytes, q, bytes) || overlap(out, bytes, k, bytes) || overlap(out, bytes, v, bytes))
+        return RA_ERR_INVALID_ARG;
+    if (lse) {
+        const unsigned long long lb = static_cast<unsigned long long>(B) * L * H * 4;
+        if (overlap(lse, lb, q, bytes) || overlap(lse, lb, k, bytes) || overlap(lse, lb, v, bytes) ||
+            overlap(lse, lb, out, bytes))
+            return RA_ERR_INVALID_ARG;
+    }
+    *elems = n;
+    return RA_OK;
+}
+
+ra_status attn_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                    int L, int H, int D, int P, int causal, ra_dtype dtype, int* trace,
+                    cudaStream_t stream)
+{
+    if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_UNSUPPORTED;
+    const int elem = dtype == RA_BF16 ? 2 : 4;
+    unsigned long long n = 0;
+    ra_status st = check_attn(q, k, v, out, lse, B, L, H, D, P, elem, &n);
+    if (st != RA_OK) return st;
+    if (dtype == RA_BF16 && D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
+    if (dtype == RA_F32 && (D % 4 != 0 || D > 256)) return RA_ERR_UNSUPPORTED;
+    if (trace) {
+        if (!aligned(trace, 4)) return RA_ERR_MISALIGNED;
+        const unsigned long long tb = static_cast<unsigned long long>(P) * P * 4;
+        if (overlap(trace, tb, out, n * elem)) return RA_ERR_INVALID_ARG;
+    }
+    ra::AttnArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.lse = lse;
+    a.trace = trace;
+    a.B = B;
+    a.L = L;
+    a.H = H;
+    a.D = D;
+    a.P = P;
+    a.causal = causal ? 1 : 0;
+    a.timeout_ns = kWaitLimitNs;
+    a.stream = stream;
+    st = status_word(&a.status);
+    if (st != RA_OK) return st;
+    if (dtype == RA_F32) return from_cuda(ra::launch_attn_f32(a));
+    CUtensorMap tq, tk, tv;
+    if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, H, D) ||
+        !encode_qkv_map(&tv, v, B, L, H, D))
+        return RA_ERR_CUDA;
+    return from_cuda(ra::launch_attn_bf16(a, tq, tk, tv));
+}
+
+ra_status permute_impl(const void* in, void* out, int B, int L, int H, int D, int P,
+                       int elem_bytes, int dir, cudaStream_t stream)
+{
+    if (!in || !out) return RA_ERR_INVALID_ARG;
+    if (B < 1 || L < 1 || H < 1 || D < 1 || P < 1) return RA_ERR_INVALID_ARG;
+    if (elem_bytes != 2 && elem_bytes != 4) return RA_ERR_UNSUPPORTED;
+    const unsigned long long n = static_cast<unsigned long long>(B) * L * H * D;
+    if (n >= (1ull << 40)) return RA_ERR_INVALID_ARG;
+    if (L % P != 0 || H % P != 0) return RA_ERR_NOT_DIVISIBLE;
+    if ((D * elem_bytes) % 16 != 0) return RA_ERR_UNSUPPORTED;
+    if (!aligned(in, 16) || !aligned(out, 16)) return RA_ERR_MISALIGNED;
+    const unsigned long long bytes = n * elem_bytes;
+    if (overlap(in, bytes, out, bytes)) return RA_ERR_INVALID_ARG;
+    return from_cuda(ra::launch_ulysses_permute(in, out, B, L, H, D, P, elem_bytes, dir, stream));
+}
+
+}  // namespace
+
+namespace ra {
+namespace {
+
+__global__ void wait_probe_kernel(unsigned int* status, unsigned long long timeout_ns)
+{
+    __shared__ __align__(8) uint64_t bar_storage;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        const uint32_t bar = smem_addr(&bar_storage);
+        abort_flag = 0;
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        const WaitCtx w{&abort_flag, status, timeout_ns};
+        // nobody arrives: the wait can only end by running out of time
+        mbar_wait(bar, 0, w);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_probe(unsigned int* status, unsigned long long timeout_ns,
+                              cudaStream_t stream)
+{
+    wait_probe_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace ra
+
+extern "C" {
+
+ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int L, int H, int D, int P, int causal, ra_stream_t stream)
+{
+    return attn_impl(q, k, v, out, lse, B, L, H, D, P, causal, RA_BF16, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_fwd_f32(const float* q, const float* k, const float* v, float* out,
+                            float* lse, int B, int L, int H, int D, int P, int causal,
+                            ra_stream_t stream)
+{
+    return attn_impl(q, k, v, out, lse, B, L, H, D, P, causal, RA_F32, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_fwd_trace(const void* q, const void* k, const void* v, void* out, float* lse,
+                              int B, int L, int H, int D, int P, int causal, ra_dtype dtype,
+                              int* trace, ra_stream_t stream)
+{
+    if (!trace) return RA_ERR_INVALID_ARG;
+    return attn_impl(q, k, v, out, lse, B, L, H, D, P, causal, dtype, trace,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+ra_status attn_merge_partials(const void* o_a, const float* lse_a, const void* o_b,
+                              const float* lse_b, void* o_out, float* lse_out, long long rows,
+                              int D, ra_dtype dtype, ra_stream_t stream)
+{
+    if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_UNSUPPORTED;
+    if (rows < 0 || D < 1) return RA_ERR_INVALID_ARG;
+    if (rows == 0) return RA_OK;
+    if (!o_a || !lse_a || !o_b || !lse_b || !o_out || !lse_out) return RA_ERR_INVALID_ARG;
+    const int elem = dtype == RA_BF16 ? 2 : 4;
+    if ((D * elem) % 16 != 0) return RA_ERR_UNSUPPORTED;
+    if (static_cast<unsigned long long>(rows) * D >= (1ull << 40)) return RA_ERR_INVALID_ARG;
+    if (!aligned(o_a, 16) || !aligned(o_b, 16) || !aligned(o_out, 16) || !aligned(lse_a, 4) ||
+        !aligned(lse_b, 4) || !aligned(lse_out, 4))
+        return RA_ERR_MISALIGNED;
+    const unsigned long long ob = static_cast<unsigned long long>(rows) * D * elem;
+    const unsigned long long lb = static_cast<unsigned long long>(rows) * 4;
+    // in place is allowed (same base pointer); any partial overlap is not
+    if ((o_out != o_a && overlap(o_out, ob, o_a, ob)) || (o_out != o_b && overlap(o_out, ob, o_b, ob)))
+        return RA_ERR_INVALID_ARG;
+    if ((lse_out != lse_a && overlap(lse_out, lb, lse_a, lb)) ||
+        (lse_out != lse_b && overlap(lse_out, lb, lse_b, lb)))
+        return RA_ERR_INVALID_ARG;
+    if (overlap(o_out, ob, lse_out, lb) || overlap(o_out, ob, lse_a, lb) ||
+        overlap(o_out, ob, lse_b, lb))
+        return RA_ERR_INVALID_ARG;
+    return from_cuda(ra::launch_merge(o_a, lse_a, o_b, lse_b, o_out, lse_out, rows, D, elem,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ra_status ulysses_seq2head(const void* in, void* out, int B, int L, int H, int D, int P,
+                           int elem_bytes, ra_stream_t stream)
+{
+    return permute_impl(in, out, B, L, H, D, P, elem_bytes, 0,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+ra_status ulysses_head2seq(const void* in, void* out, int B, int L, int H, int D, int P,
+                           int elem_bytes, ra_stream_t stream)
+{
+    return permute_impl(in, out, B, L, H, D, P, elem_bytes, 1,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+ra_status ra_check_status(ra_stream_t stream)
+{
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RA_ERR_CUDA;
+    unsigned int* word = nullptr;
+    ra_status st = status_word(&word);
+    if (st != RA_OK) return st;
+    unsigned int value = 0;
+    if (cudaMemcpy(&value, word, sizeof(value), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RA_ERR_CUDA;
+    if (value == 0) return RA_OK;
+    if (cudaMemset(word, 0, sizeof(value)) != cudaSuccess) return RA_ERR_CUDA;
+    return (value & RA_STATUS_TIMEOUT) ? RA_ERR_TIMEOUT : RA_ERR_CUDA;
+}
+
+const char* ra_status_string(ra_status status)
+{
+    switch (status) {
+    case RA_OK: return "ok";
+    case RA_ERR_INVALID_ARG: return "invalid argument";
+    case RA_ERR_UNSUPPORTED: return "unsupported head dim, element size or dtype";
+    case RA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case RA_ERR_NOT_DIVISIBLE: return "sequence (or head) count not divisible by P";
+    case RA_ERR_CUDA: return "CUDA error";
+    case RA_ERR_TIMEOUT: return "a device-side wait ran out of time";
+    }
+    return "unknown status";
+}
+
+ra_status ra_probe_wait_timeout(unsigned long long timeout_ns, ra_stream_t stream)
+{
+    if (timeout_ns < 1 || timeout_ns > 1000000000ull) return RA_ERR_INVALID_ARG;
+    unsigned int* word = nullptr;
+    ra_status st = status_word(&word);
+    if (st != RA_OK) return st;
+    return from_cuda(ra::launch_wait_probe(word, timeout_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

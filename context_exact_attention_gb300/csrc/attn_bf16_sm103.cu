@@ -1,0 +1,473 @@
+// attn_bf16_sm103.cu -- exact attention forward over P virtual ring shards,
+// bf16 in / fp32 accumulate, on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes ("序列并行与 Ring Attention"): O = softmax(Q K^T / sqrt(D)) V
+// (section 3.1) by the online-softmax recurrence of section 3.2 (running max m,
+// denominator l, unnormalised sum u, rescale alpha = exp(m_t - m_{t+1}),
+// o = u / l), visiting K/V in the ring order of section 3.3 (the queries of
+// shard r meet shard (r - t) mod P at step t) and, under causal masking,
+// skipping shards wholly in the future and masking the diagonal shard by
+// global position (section 3.4).
+//
+// One CTA owns two 128-row query tiles of one shard of one (batch, head) and
+// walks that shard's K/V blocks (128 keys each) in ring order.  Warp roles:
+//   warp 0      TMA producer: Q tiles once, then K and V blocks through two
+//               2-deep shared-memory rings (the next block loads while the
+//               current one is used: the ring's double buffer, section 6.3).
+//   warp 1      MMA issuer (one thread): S_t = Q_t K^T into TMEM, then
+//               O_t += P_t V with P_t read from TMEM.
+//   warps 4-7   softmax of query tile 0; warps 8-11 softmax of query tile 1.
+//               One thread per query row (TMEM lane): row max, exp2, row sum,
+//               P packed to bf16 back into TMEM over S, O rescale when needed.
+// The two tiles ping-pong: while one tile's softmax runs, the tensor core
+// computes the other tile's P V and next S.
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+//
+// The reference max used in the exponentials is raised only when a row's max
+// grows by more than 2^8 (in base-2 units); otherwise the old one is kept.
+// Any common reference leaves u / l unchanged (section 3.2: old numerator and
+// denominator are scaled together), so the result stays exact; it only bounds
+// p by 256, well inside fp32 and bf16 range.
+#include <cuda_bf16.h>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+constexpr int kRows = 128;    // query rows per tile = TMEM lanes
+constexpr int kKeys = 128;    // keys per K/V block
+constexpr int kTiles = 2;     // query tiles per CTA
+constexpr int kThreads = 384;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct Layout {
+    static constexpr int kBoxes = D / 64;              // 64-element (128-byte) swizzle boxes
+    static constexpr int kTileBytes = kRows * D * 2;   // one Q, K or V tile
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kTiles * kTileBytes;
+    static constexpr int kV = kK + 2 * kTileBytes;
+    static constexpr int kBar = kV + 2 * kTileBytes;
+    static constexpr int kSmem = kBar + 256 + 1024;    // barriers + alignment slack
+    static constexpr uint32_t kTmemCols = 512;
+    __device__ static constexpr uint32_t col_s(int tq) { return 128u * tq; }
+    __device__ static constexpr uint32_t col_o(int tq)
+    {
+        return 256u + static_cast<uint32_t>(D) * tq;
+    }
+};
+
+// Barrier slots (8 bytes each) after the tiles.
+enum : int {
+    kBarQ = 0,
+    kBarKFull = 1,   // +stage
+    kBarKEmpty = 3,  // +stage
+    kBarVFull = 5,   // +stage
+    kBarVEmpty = 7,  // +stage
+    kBarSFull = 9,   // +tile
+    kBarPFull = 11,  // +tile
+    kBarOFull = 13,  // +tile
+    kBarDone = 15,
+    kBarCount = 16
+};
+
+struct Params {
+    __nv_bfloat16* out;
+    float* lse;
+    int* trace;
+    unsigned int* status;
+    unsigned long long timeout_ns;
+    int B, L, H, P, Ls, causal;
+    int n_kt;        // K/V blocks per shard
+    int n_pair;      // query-tile pairs per shard
+    float scale_log2;
+};
+
+// Ring schedule of one CTA: the n-th K/V block it visits is block kt of shard
+// s, met at ring step t.  Step 0 is the CTA's own shard r; under causal
+// masking only blocks up to the diagonal are listed there, and steps whose
+// source lies in the future (s > r, i.e. t > r) are absent.
+struct Sched {
+    int r, P, n_kt, n_first, n_blocks;
+    __device__ __forceinline__ void block(int n, int& s, int& kt, int& t) const
+    {
+        if (n < n_first) {
+            t = 0;
+            s = r;
+            kt = n;
+            return;
+        }
+        const int m = n - n_first;
+        t = 1 + m / n_kt;
+        kt = m - (t - 1) * n_kt;
+        s = r - t;
+        if (s < 0) s += P;
+    }
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                          const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const Params p)
+{
+    using Lay = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kBar + kBarCount * 8);
+    int* abort_flag = reinterpret_cast<int*>(smem + Lay::kBar + kBarCount * 8 + 4);
+    auto bar = [&](int i) -> uint32_t { return sbase + Lay::kBar + 8u * i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work unit: (batch, head) outer; inside, heaviest (shard, pair) first
+    const int units_per_bh = p.P * p.n_pair;
+    const int bh = blockIdx.x / units_per_bh;
+    const int u = blockIdx.x - bh * units_per_bh;
+    const int r = p.P - 1 - u / p.n_pair;
+    const int pair = p.n_pair - 1 - (u - (u / p.n_pair) * p.n_pair);
+    const int b = bh / p.H;
+    const int h = bh - b * p.H;
+    const int q0_local = pair * (kTiles * kRows);     // first query row of the pair, within shard
+    const int q0 = r * p.Ls + q0_local;               // global
+
+    Sched sc;
+    sc.r = r;
+    sc.P = p.P;
+    sc.n_kt = p.n_kt;
+    if (p.causal) {
+        const int q_last = min(p.Ls - 1, q0_local + kTiles * kRows - 1);
+        sc.n_first = min(p.n_kt, q_last / kKeys + 1);
+        sc.n_blocks = sc.n_first + r * p.n_kt;
+    } else {
+        sc.n_first = p.n_kt;
+        sc.n_blocks = p.P * p.n_kt;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(kBarQ), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kBarKFull + i), 1);
+            mbar_init(bar(kBarKEmpty + i), 1);
+            mbar_init(bar(kBarVFull + i), 1);
+            mbar_init(bar(kBarVEmpty + i), 1);
+            mbar_init(bar(kBarSFull + i), 1);
+            mbar_init(bar(kBarPFull + i), kRows);
+            mbar_init(bar(kBarOFull + i), 1);
+        }
+        mbar_init(bar(kBarDone), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+            const bool tracing = p.trace != nullptr && bh == 0 && pair == 0;
+            if (tracing)
+                for (int t = 0; t < p.P; ++t) p.trace[r * p.P + t] = -1;
+            const uint64_t keep = l2_policy_evict_last();    // K/V: read by every tile pair of the head
+            const uint64_t once = l2_policy_evict_first();   // Q: read once
+            mbar_arrive_expect_tx(bar(kBarQ), kTiles * Lay::kTileBytes);
+            for (int tq = 0; tq < kTiles; ++tq)
+                for (int bx = 0; bx < Lay::kBoxes; ++bx)
+                    tma_load_4d(sbase + Lay::kQ + tq * Lay::kTileBytes + bx * 16384, &tmap_q,
+                                bar(kBarQ), bx * 64, h, q0 + tq * kRows, b, once);
+            int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+            for (int n = 0; n < sc.n_blocks; ++n) {
+                int s, kt, t;
+                sc.block(n, s, kt, t);
+                if (tracing && kt == 0) p.trace[r * p.P + t] = s;
+                const int st = n & 1;
+                const uint32_t ph = (n >> 1) & 1;
+                const int row = s * p.Ls + kt * kKeys;
+                if (!mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc)) break;
+                mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kTileBytes);
+                for (int bx = 0; bx < Lay::kBoxes; ++bx)
+                    tma_load_4d(sbase + Lay::kK + st * Lay::kTileBytes + bx * 16384, &tmap_k,
+                                bar(kBarKFull + st), bx * 64, h, row, b, keep);
+                last_k[st] = n;
+                if (!mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc)) break;
+                mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kTileBytes);
+                for (int bx = 0; bx < Lay::kBoxes; ++bx)
+                    tma_load_4d(sbase + Lay::kV + st * Lay::kTileBytes + bx * 16384, &tmap_v,
+                                bar(kBarVFull + st), bx * 64, h, row, b, keep);
+                last_v[st] = n;
+            }
+            // let this CTA's own copies land before anyone leaves
+            mbar_wait_drain(bar(kBarQ), 0, wc);
+            for (int st = 0; st < 2; ++st) {
+                if (last_k[st] >= 0) mbar_wait_drain(bar(kBarKFull + st), (last_k[st] >> 1) & 1, wc);
+                if (last_v[st] >= 0) mbar_wait_drain(bar(kBarVFull + st), (last_v[st] >> 1) & 1, wc);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescQK = idesc_bf16_f32(kRows, kKeys, false);
+            constexpr uint32_t kIdescPV = idesc_bf16_f32(kRows, D, true);
+            // S_tq = Q_tq K^T: both operands K-major (head dim contiguous), 128-byte
+            // swizzled rows of 64 elements; 16-element K steps advance 32 bytes
+            // inside a swizzle row, then jump to the next 64-wide box.
+            auto issue_qk = [&](int tq, int st) {
+                const uint32_t d_t = tmem + Lay::col_s(tq);
+                const uint32_t qa = sbase + Lay::kQ + tq * Lay::kTileBytes;
+                const uint32_t ka = sbase + Lay::kK + st * Lay::kTileBytes;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_ss(d_t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                           kIdescQK, k > 0 ? 1u : 0u);
+                }
+            };
+            // O_tq += P_tq V: P (128 x 128 keys, bf16 pairs) sits in TMEM over S_tq; V is
+            // the MN-major B operand (head dim contiguous): 8 key rows of 128 bytes per
+            // swizzle atom (stride 1024), the second 64-wide box 16 KiB further.
+            auto issue_pv = [&](int tq, int st, bool acc) {
+                const uint32_t d_t = tmem + Lay::col_o(tq);
+                const uint32_t pa = tmem + Lay::col_s(tq);
+                const uint32_t va = sbase + Lay::kV + st * Lay::kTileBytes;
+#pragma unroll
+                for (int k = 0; k < kKeys / 16; ++k)
+                    mma_ts(d_t, pa + k * 8, sdesc_sw128(va + k * 2048, 16384, 1024), kIdescPV,
+                           (acc || k > 0) ? 1u : 0u);
+            };
+
+            bool ok = mbar_wait(bar(kBarQ), 0, wc);
+            if (ok) ok = mbar_wait(bar(kBarKFull + 0), 0, wc);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(0, 0);
+                tc_commit(bar(kBarSFull + 0));
+                issue_qk(1, 0);
+                tc_commit(bar(kBarSFull + 1));
+                tc_commit(bar(kBarKEmpty + 0));
+            }
+            for (int n = 0; ok && n < sc.n_blocks; ++n) {
+                const int st = n & 1;
+                const uint32_t ph = (n >> 1) & 1;
+                const bool more = n + 1 < sc.n_blocks;
+                const int st1 = (n + 1) & 1;
+                const uint32_t ph1 = ((n + 1) >> 1) & 1;
+                if (!(ok = mbar_wait(bar(kBarVFull + st), ph, wc))) break;
+                if (!(ok = mbar_wait(bar(kBarPFull + 0), n & 1, wc))) break;
+                tc_fence_after();
+                issue_pv(0, st, n > 0);
+                if (!more) tc_commit(bar(kBarOFull + 0));
+                if (more) {
+                    if (!(ok = mbar_wait(bar(kBarKFull + st1), ph1, wc))) break;
+                    tc_fence_after();
+                    issue_qk(0, st1);
+                    tc_commit(bar(kBarSFull + 0));
+                }
+                if (!(ok = mbar_wait(bar(kBarPFull + 1), n & 1, wc))) break;
+                tc_fence_after();
+                issue_pv(1, st, n > 0);
+                tc_commit(bar(kBarVEmpty + st));
+                if (!more) tc_commit(bar(kBarOFull + 1));
+                if (more) {
+                    issue_qk(1, st1);
+                    tc_commit(bar(kBarSFull + 1));
+                    tc_commit(bar(kBarKEmpty + st1));
+                }
+            }
+            // every MMA this CTA issued has finished before TMEM is released
+            tc_commit(bar(kBarDone));
+            mbar_wait_drain(bar(kBarDone), 0, wc);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ----------------------------------------------------------- softmax
+        const int tq = (warp - 4) >> 2;
+        const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+        const int row = quarter * 32 + lane;          // row within the tile
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + Lay::col_s(tq);
+        const uint32_t tO = tmem + lane_off + Lay::col_o(tq);
+        const int row_local = q0_local + tq * kRows + row;   // within shard r
+        const int row_glob = r * p.Ls + row_local;
+        const float sl2 = p.scale_log2;
+
+        float m = -INFINITY;   // running max of scaled scores, base-2 units
+        float l = 0.f;         // running denominator, relative to m
+        bool ok = true;
+        for (int n = 0; n < sc.n_blocks; ++n) {
+            int s, kt, t;
+            sc.block(n, s, kt, t);
+            ok = mbar_wait(bar(kBarSFull + tq), n & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+
+            uint32_t sraw[128];
+            tmem_ld128(tS, sraw);
+            float sv[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) sv[c] = u2f(sraw[c]);
+
+            // visible columns: inside the shard, and under causal masking on the
+            // diagonal shard, key position <= query position (global positions)
+            int lim = min(kKeys - 1, p.Ls - kt * kKeys - 1);
+            if (p.causal && s == r) lim = min(lim, row_local - kt * kKeys);
+            if (lim < kKeys - 1) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) sv[c] = (c > lim) ? -INFINITY : sv[c];
+            }
+
+            float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+            for (int c = 4; c < 128; c += 4) {
+                mx0 = fmaxf(mx0, sv[c]);
+                mx1 = fmaxf(mx1, sv[c + 1]);
+                mx2 = fmaxf(mx2, sv[c + 2]);
+                mx3 = fmaxf(mx3, sv[c + 3]);
+            }
+            const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            const float m_new = fmaxf(m, m_blk);
+            const bool raise = m_new > m + kRescaleThreshold;   // always on the first finite block
+            const float m_ref = raise ? m_new : m;
+            const float alpha = raise ? ex2(m - m_ref) : 1.f;    // ex2(-inf) = 0
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2(fmaf(sv[64 * half + 2 * i], sl2, neg_m));
+                    const float p1 = ex2(fmaf(sv[64 * half + 2 * i + 1], sl2, neg_m));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + 32 * half, pk);
+            }
+            l = l * alpha + (sum0 + sum1);
+            m = m_ref;
+
+            // O was last written by P V of the previous block, which finished
+            // before this block's S (same issuing thread, in order).
+            if (n > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32 * c, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                    tmem_st32(tO + 32 * c, o);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(kBarPFull + tq));
+        }
+
+        if (ok) {
+            ok = mbar_wait(bar(kBarOFull + tq), 0, wc);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            const bool valid = row_local < p.Ls;
+            const float inv_l = 1.f / l;
+            __nv_bfloat16* dst =
+                p.out + ((static_cast<size_t>(b) * p.L + row_glob) * p.H + h) * static_cast<size_t>(D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32 * c, o);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+                if (valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                }
+            }
+            if (valid && p.lse != nullptr)
+                p.lse[(static_cast<size_t>(b) * p.L + row_glob) * p.H + h] = (m + log2f(l)) * kLn2;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Lay::kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv)
+{
+    using Lay = Layout<D>;
+    static int configured[64] = {0};  // dynamic shared memory attribute, once per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(ring_attn_bf16_kernel<D>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    Params p;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.lse = a.lse;
+    p.trace = a.trace;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.B = a.B;
+    p.L = a.L;
+    p.H = a.H;
+    p.P = a.P;
+    p.Ls = a.L / a.P;
+    p.causal = a.causal;
+    p.n_kt = (p.Ls + kKeys - 1) / kKeys;
+    p.n_pair = (p.n_kt + kTiles - 1) / kTiles;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    const long long grid = static_cast<long long>(a.B) * a.H * a.P * p.n_pair;
+    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    ring_attn_bf16_kernel<D><<<static_cast<unsigned>(grid), kThreads, Lay::kSmem, a.stream>>>(
+        tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                             const CUtensorMap& tv)
+{
+    if (a.D == 64) return launch_d<64>(a, tq, tk, tv);
+    if (a.D == 128) return launch_d<128>(a, tq, tk, tv);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ra

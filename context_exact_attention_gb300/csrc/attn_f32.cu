@@ -1,0 +1,137 @@
+// attn_f32.cu -- fp32 exact attention over P virtual ring shards on the SIMT
+// cores, for results at fp32 tolerance (tensor-core tf32 would not meet it).
+//
+// Same operation and schedule as the bf16 kernel ("序列并行与 Ring Attention",
+// sections 3.1-3.4): the queries of shard r meet shard (r - t) mod P at step t,
+// wholly-future shards are skipped under causal masking, and the online-softmax
+// recurrence of section 3.2 runs over blocks of 32 keys with natural-base
+// exponentials (expf, full precision).
+//
+// One warp owns one query row.  Lane j scores key j of the current 32-key
+// block (query row broadcast from shared memory), the block max and sum are
+// warp reductions, and lane d accumulates output columns d, d+32, ...
+#include <cmath>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kMaxD = 256;
+
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    ring_attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                         const float* __restrict__ v, float* __restrict__ out,
+                         float* __restrict__ lse, int* __restrict__ trace, int B, int L, int H,
+                         int D, int P, int causal, float scale)
+{
+    __shared__ float qs[kWarps][kMaxD];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long row_id = static_cast<long long>(blockIdx.x) * kWarps + warp;  // (b, h, i)
+    const long long n_rows = static_cast<long long>(B) * H * L;
+    if (row_id >= n_rows) return;                     // whole warp leaves together
+    const int i = static_cast<int>(row_id % L);       // query position
+    const long long bh = row_id / L;
+    const int h = static_cast<int>(bh % H);
+    const int b = static_cast<int>(bh / H);
+    const int Ls = L / P;
+    const int r = i / Ls;
+    const size_t row_stride = static_cast<size_t>(H) * D;   // between consecutive positions
+    const float* qrow = q + (static_cast<size_t>(b) * L + i) * row_stride + static_cast<size_t>(h) * D;
+    for (int d = lane; d < D; d += 32) qs[warp][d] = qrow[d];
+    __syncwarp();
+
+    const bool tracing = trace != nullptr && b == 0 && h == 0 && i == r * Ls;
+    float m = -INFINITY, l = 0.f;
+    float acc[kMaxD / 32];
+#pragma unroll
+    for (int c = 0; c < kMaxD / 32; ++c) acc[c] = 0.f;
+
+    const float* kb = k + static_cast<size_t>(b) * L * row_stride + static_cast<size_t>(h) * D;
+    const float* vb = v + static_cast<size_t>(b) * L * row_stride + static_cast<size_t>(h) * D;
+
+    for (int t = 0; t < P; ++t) {
+        int s = r - t;
+        if (s < 0) s += P;
+        const bool skip = causal && s > r;
+        if (tracing && lane == 0) trace[r * P + t] = skip ? -1 : s;
+        if (skip) continue;
+        const int j_begin = s * Ls;
+        const int j_end = (causal && s == r) ? i + 1 : j_begin + Ls;   // keys j <= i on the diagonal
+        for (int j0 = j_begin; j0 < j_end; j0 += 32) {
+            const int j = j0 + lane;
+            float sc = -INFINITY;
+            if (j < j_end) {
+                const float* krow = kb + static_cast<size_t>(j) * row_stride;
+                float dot = 0.f;
+                for (int d = 0; d < D; d += 4) {
+                    const float4 kk = *reinterpret_cast<const float4*>(krow + d);
+                    dot = fmaf(qs[warp][d], kk.x, dot);
+                    dot = fmaf(qs[warp][d + 1], kk.y, dot);
+                    dot = fmaf(qs[warp][d + 2], kk.z, dot);
+                    dot = fmaf(qs[warp][d + 3], kk.w, dot);
+                }
+                sc = dot * scale;
+            }
+            const float m_new = fmaxf(m, warp_max(sc));
+            const float alpha = (m == -INFINITY) ? 0.f : expf(m - m_new);
+            const float pj = (sc == -INFINITY) ? 0.f : expf(sc - m_new);
+            l = l * alpha + warp_sum(pj);
+            const int n_here = min(32, j_end - j0);
+#pragma unroll
+            for (int c = 0; c < kMaxD / 32; ++c) acc[c] *= alpha;
+            for (int jj = 0; jj < n_here; ++jj) {
+                const float pw = __shfl_sync(0xffffffffu, pj, jj);
+                const float* vrow = vb + static_cast<size_t>(j0 + jj) * row_stride;
+#pragma unroll
+                for (int c = 0; c < kMaxD / 32; ++c) {
+                    const int d = lane + 32 * c;
+                    if (d < D) acc[c] = fmaf(pw, vrow[d], acc[c]);
+                }
+            }
+            m = m_new;
+        }
+    }
+    float* orow = out + (static_cast<size_t>(b) * L + i) * row_stride + static_cast<size_t>(h) * D;
+    const float inv_l = 1.f / l;
+#pragma unroll
+    for (int c = 0; c < kMaxD / 32; ++c) {
+        const int d = lane + 32 * c;
+        if (d < D) orow[d] = acc[c] * inv_l;
+    }
+    if (lse != nullptr && lane == 0)
+        lse[(static_cast<size_t>(b) * L + i) * H + h] = m + logf(l);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_f32(const AttnArgs& a)
+{
+    const long long rows = static_cast<long long>(a.B) * a.H * a.L;
+    const long long blocks = (rows + kWarps - 1) / kWarps;
+    if (blocks <= 0 || blocks > 0x7fffffffLL || a.D > kMaxD) return cudaErrorInvalidConfiguration;
+    ring_attn_f32_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, a.stream>>>(
+        static_cast<const float*>(a.q), static_cast<const float*>(a.k),
+        static_cast<const float*>(a.v), static_cast<float*>(a.out), a.lse, a.trace, a.B, a.L,
+        a.H, a.D, a.P, a.causal, 1.0f / sqrtf(static_cast<float>(a.D)));
+    return cudaGetLastError();
+}
+
+}  // namespace ra

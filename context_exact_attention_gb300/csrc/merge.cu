@@ -1,0 +1,129 @@
+// merge.cu -- log-sum-exp merge of two partial attention results, as a
+// coalesced 16-byte-vector HBM stream (the juejin ring-attention page, section
+// 四, `combine`: lse = logaddexp(lse_a, lse_b), o = o_a e^(lse_a - lse) +
+// o_b e^(lse_b - lse)).
+//
+// A group of G lanes (G = 16-byte vectors per row rounded up to a power of two,
+// at most 32) owns one row at a time: every lane of the group reads the two lse
+// values, the lanes stream the row's vectors, and after a __syncwarp() the
+// group's first lane writes the merged lse.  Reading before the warp barrier
+// and writing after it keeps in-place merges (lse_out == lse_a) race-free;
+// each output vector is written by the thread that read it, so o_out == o_a
+// is race-free as well.
+#include <cuda_bf16.h>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+constexpr int kBlock = 256;
+
+struct Weights {
+    float wa, wb, lse;
+};
+
+// Partial with lse = -inf covers no key: weight 0.  Both empty: o = 0, lse = -inf.
+__device__ __forceinline__ Weights merge_weights(float a, float b)
+{
+    Weights w;
+    if (a == -INFINITY && b == -INFINITY) {
+        w.wa = 0.f;
+        w.wb = 0.f;
+        w.lse = -INFINITY;
+        return w;
+    }
+    const float hi = fmaxf(a, b), lo = fminf(a, b);
+    w.lse = hi + log1pf(expf(lo - hi));
+    w.wa = expf(a - w.lse);
+    w.wb = expf(b - w.lse);
+    return w;
+}
+
+__device__ __forceinline__ uint4 combine_vec_bf16(uint4 x, uint4 y, float wa, float wb)
+{
+    const __nv_bfloat162* xa = reinterpret_cast<const __nv_bfloat162*>(&x);
+    const __nv_bfloat162* ya = reinterpret_cast<const __nv_bfloat162*>(&y);
+    uint4 res;
+    __nv_bfloat162* ro = reinterpret_cast<__nv_bfloat162*>(&res);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 fx = __bfloat1622float2(xa[i]);
+        const float2 fy = __bfloat1622float2(ya[i]);
+        ro[i] = __floats2bfloat162_rn(fmaf(fx.x, wa, fy.x * wb), fmaf(fx.y, wa, fy.y * wb));
+    }
+    return res;
+}
+
+__device__ __forceinline__ uint4 combine_vec_f32(uint4 x, uint4 y, float wa, float wb)
+{
+    uint4 res;
+    res.x = __float_as_uint(fmaf(__uint_as_float(x.x), wa, __uint_as_float(y.x) * wb));
+    res.y = __float_as_uint(fmaf(__uint_as_float(x.y), wa, __uint_as_float(y.y) * wb));
+    res.z = __float_as_uint(fmaf(__uint_as_float(x.z), wa, __uint_as_float(y.z) * wb));
+    res.w = __float_as_uint(fmaf(__uint_as_float(x.w), wa, __uint_as_float(y.w) * wb));
+    return res;
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kBlock)
+    merge_kernel(const uint4* o_a, const float* lse_a, const uint4* o_b, const float* lse_b,
+                 uint4* o_out, float* lse_out, long long rows, int vpr, int group_log2)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = 1 << group_log2;
+    const int rows_per_warp = 32 >> group_log2;
+    const int sub = lane & (G - 1);
+    const long long warp_global = (static_cast<long long>(blockIdx.x) * kBlock + threadIdx.x) >> 5;
+    const long long n_warps = (static_cast<long long>(gridDim.x) * kBlock) >> 5;
+    for (long long base = warp_global * rows_per_warp; base < rows; base += n_warps * rows_per_warp) {
+        const long long row = base + (lane >> group_log2);
+        const bool valid = row < rows;
+        Weights w{0.f, 0.f, -INFINITY};
+        if (valid) {
+            w = merge_weights(lse_a[row], lse_b[row]);
+            const long long off = row * vpr;
+            for (int c = sub; c < vpr; c += G) {
+                const uint4 x = o_a[off + c];
+                const uint4 y = o_b[off + c];
+                o_out[off + c] = kBf16 ? combine_vec_bf16(x, y, w.wa, w.wb)
+                                       : combine_vec_f32(x, y, w.wa, w.wb);
+            }
+        }
+        __syncwarp();
+        if (valid && sub == 0) lse_out[row] = w.lse;
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
+                         void* o_out, float* lse_out, long long rows, int D, int elem_bytes,
+                         cudaStream_t stream)
+{
+    const int vpr = D * elem_bytes / 16;
+    int group_log2 = 0;
+    while ((1 << group_log2) < vpr && group_log2 < 5) ++group_log2;
+    const long long rows_per_warp = 32 >> group_log2;
+    const long long warps_needed = (rows + rows_per_warp - 1) / rows_per_warp;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long blocks = (warps_needed * 32 + kBlock - 1) / kBlock;
+    const long long cap = static_cast<long long>(sms) * 8;   // 8 resident blocks of 256 per SM
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (elem_bytes == 2)
+        merge_kernel<true><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
+            static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b), lse_b,
+            static_cast<uint4*>(o_out), lse_out, rows, vpr, group_log2);
+    else
+        merge_kernel<false><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
+            static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b), lse_b,
+            static_cast<uint4*>(o_out), lse_out, rows, vpr, group_log2);
+    return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -1,0 +1,45 @@
+// ra_internal.h -- host-side interface between the C ABI layer (api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ring_attn.h"
+
+namespace ra {
+
+// Everything one attention launch needs; validated by the ABI layer.
+struct AttnArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    float* lse;      // may be null
+    int* trace;      // may be null
+    int B, L, H, D, P, causal;
+    unsigned int* status;          // device status word
+    unsigned long long timeout_ns; // limit of one bounded wait
+    cudaStream_t stream;
+};
+
+// bf16 tcgen05 kernel; tensor maps describe q, k, v as 4-D [B][L][H][D] with
+// 64-element, 128-byte-swizzled boxes of 128 rows.
+cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tmap_q,
+                             const CUtensorMap& tmap_k, const CUtensorMap& tmap_v);
+
+// fp32 SIMT kernel.
+cudaError_t launch_attn_f32(const AttnArgs& a);
+
+cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
+                         void* o_out, float* lse_out, long long rows, int D, int elem_bytes,
+                         cudaStream_t stream);
+
+// dir = 0: seq2head, dir = 1: head2seq.
+cudaError_t launch_ulysses_permute(const void* in, void* out, int B, int L, int H, int D, int P,
+                                   int elem_bytes, int dir, cudaStream_t stream);
+
+cudaError_t launch_wait_probe(unsigned int* status, unsigned long long timeout_ns,
+                              cudaStream_t stream);
+
+}  // namespace ra

@@ -1,0 +1,155 @@
+/*
+ * ring_attn.h -- C ABI of libringattn.so: exact context-parallel attention on
+ * one GB300 (sm_103a), with P virtual sequence shards living in one HBM.
+ *
+ * Common conventions
+ * ------------------
+ * - Every pointer argument named q, k, v, out, lse, o_*, in, trace is a DEVICE
+ *   pointer owned by the caller; the library never allocates, frees or keeps
+ *   them.  All calls are asynchronous on `stream` (NULL = the legacy default
+ *   stream) and never synchronise the host, except ra_check_status().
+ * - Sequence tensors are contiguous row-major [B, L, H, D] (batch, sequence,
+ *   head, head dim), the layout of the verify script on the juejin page
+ *   "ring attention 没做通信" (section 三: "q/k/v: (B, S, H, D)").  lse tensors
+ *   are fp32 [B, L, H], natural logarithm (same page, section 五).
+ * - Virtual shard r (0 <= r < P) is the token range [r*L/P, (r+1)*L/P); L must be
+ *   divisible by P ("序列并行与 Ring Attention", section 6.4; the Ulysses
+ *   guideline page on aitangshan.cn, section 四, on divisibility by cp_size).
+ * - Argument errors are detected on the host before anything is launched and
+ *   reported through the return value; nothing is written in that case.
+ *   Launch failures return RA_ERR_CUDA.  Kernels that give up waiting (a
+ *   bounded wait ran out) record RA_ERR_TIMEOUT in a per-device status word
+ *   that ra_check_status() reads and clears; they never trap.
+ */
+#ifndef RING_ATTN_H
+#define RING_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* ra_stream_t;
+
+typedef enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, overlapping in/out, overflow */
+    RA_ERR_UNSUPPORTED = 2,   /* head dim or dtype the kernels do not implement */
+    RA_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    RA_ERR_NOT_DIVISIBLE = 4, /* L % P != 0, or H % P != 0 for the Ulysses transposes */
+    RA_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+    RA_ERR_TIMEOUT = 6        /* a kernel's bounded wait ran out (reported by ra_check_status) */
+} ra_status;
+
+typedef enum { RA_BF16 = 0, RA_F32 = 1 } ra_dtype;
+
+/*
+ * ring_attn_fwd -- bf16 exact attention forward over P virtual ring shards.
+ *
+ * Computes, for every batch b, head h and query row i,
+ *   out[b,i,h,:] = sum_j softmax_j( q[b,i,h,:] . k[b,j,h,:] / sqrt(D) ) v[b,j,h,:]
+ *   lse[b,i,h]   = ln sum_j exp( q[b,i,h,:] . k[b,j,h,:] / sqrt(D) )
+ * ("序列并行与 Ring Attention", section 3.1), using the blockwise online-softmax
+ * recurrence of section 3.2 with the ring schedule of section 3.3: the queries
+ * of shard r meet the K/V of shard (r - t) mod P at step t = 0..P-1.  With
+ * causal != 0 key j is visible to query i iff j <= i in GLOBAL positions, and
+ * shards wholly in the future of shard r are skipped (section 3.4).
+ *
+ * q, k, v, out: device bf16 [B, L, H, D], 16-byte aligned; out must not overlap
+ *               q, k or v.  D must be 64 or 128.
+ * lse:          device fp32 [B, L, H] or NULL (not written).
+ * Scores and the softmax run in fp32 on tensor-core accumulators; out is
+ * rounded to bf16 (round to nearest even).  Repeated calls on the same inputs
+ * give bit-identical results (no atomics in the reduction).
+ * Limits: B, L, H, P >= 1; L % P == 0; B*L*H*D < 2^40; L < 2^31.
+ */
+ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int L, int H, int D, int P, int causal, ra_stream_t stream);
+
+/*
+ * ring_attn_fwd_f32 -- the same operation on fp32 tensors, computed in fp32
+ * (SIMT, no tensor cores), for checks at fp32 tolerance.  Any D with
+ * 4 <= D <= 256 and D % 4 == 0.  Same layout, limits and errors as above.
+ */
+ra_status ring_attn_fwd_f32(const float* q, const float* k, const float* v, float* out,
+                            float* lse, int B, int L, int H, int D, int P, int causal,
+                            ra_stream_t stream);
+
+/*
+ * ring_attn_fwd_trace -- ring_attn_fwd (dtype RA_BF16) or ring_attn_fwd_f32
+ * (RA_F32) that also records the schedule it ran: trace is a device int32
+ * [P, P] array; trace[r*P + t] receives the source shard whose K/V the queries
+ * of shard r met at ring step t, or -1 if that step was skipped as wholly
+ * future ("序列并行与 Ring Attention", section 6.6: dump the K/V source of every
+ * round).  Identical numerics to the untraced call.
+ */
+ra_status ring_attn_fwd_trace(const void* q, const void* k, const void* v, void* out, float* lse,
+                              int B, int L, int H, int D, int P, int causal, ra_dtype dtype,
+                              int* trace, ra_stream_t stream);
+
+/*
+ * attn_merge_partials -- log-sum-exp merge of two partial attention results
+ * over disjoint key sets (the `combine` of the juejin page, section 四):
+ *   lse_out = ln(e^lse_a + e^lse_b)
+ *   o_out   = o_a * e^(lse_a - lse_out) + o_b * e^(lse_b - lse_out)
+ * A partial with lse = -inf (it saw no key) gets weight 0; if both are -inf,
+ * o_out = 0 and lse_out = -inf.
+ *
+ * o_a, o_b, o_out: device [rows, D] of dtype (RA_BF16 or RA_F32), 16-byte
+ *                  aligned; D*sizeof(dtype) must be a multiple of 16.
+ * lse_a, lse_b, lse_out: device fp32 [rows].
+ * o_out may be the same pointer as o_a or o_b and lse_out the same as lse_a or
+ * lse_b (in-place merge); any other overlap is rejected.  Math in fp32; bf16
+ * results are rounded to nearest even.
+ */
+ra_status attn_merge_partials(const void* o_a, const float* lse_a, const void* o_b,
+                              const float* lse_b, void* o_out, float* lse_out, long long rows,
+                              int D, ra_dtype dtype, ra_stream_t stream);
+
+/*
+ * ulysses_seq2head -- the Ulysses all-to-all as a layout transpose on one
+ * device ("序列并行与 Ring Attention", section 3.5: [B, L/P, H, D] per rank ->
+ * [B, L, H/P, D] per rank).
+ *
+ * in:  sequence-sharded buffer [P][B][L/P][H][D]: slice r is what rank r holds.
+ * out: head-sharded buffer [P][B][L][H/P][D]: slice g is what rank g holds,
+ *   out[g][b][r*L/P + l][hh][d] = in[r][b][l][g*H/P + hh][d].
+ * elem_bytes: 2 or 4 (bit copy; values are never interpreted).  Requires
+ * L % P == 0, H % P == 0, (D*elem_bytes) % 16 == 0, 16-byte aligned pointers,
+ * and non-overlapping in/out.  The whole of `out` is a [P*B, L, H/P, D]
+ * batch that ring_attn_fwd accepts directly (with P = 1).
+ */
+ra_status ulysses_seq2head(const void* in, void* out, int B, int L, int H, int D, int P,
+                           int elem_bytes, ra_stream_t stream);
+
+/* ulysses_head2seq -- the inverse transpose (head-sharded -> sequence-sharded):
+ *   out[r][b][l][g*H/P + hh][d] = in[g][b][r*L/P + l][hh][d].
+ * Same requirements as ulysses_seq2head. */
+ra_status ulysses_head2seq(const void* in, void* out, int B, int L, int H, int D, int P,
+                           int elem_bytes, ra_stream_t stream);
+
+/*
+ * ra_check_status -- synchronise `stream`, then read and clear the status word
+ * of the current device.  Returns RA_ERR_TIMEOUT if a kernel gave up on a
+ * bounded wait since the last check, RA_ERR_CUDA if the stream reports an
+ * error, RA_OK otherwise.
+ */
+ra_status ra_check_status(ra_stream_t stream);
+
+/* Static English text for a status code (never NULL). */
+const char* ra_status_string(ra_status status);
+
+/*
+ * ra_probe_wait_timeout -- launch one CTA that waits on a shared-memory
+ * barrier nothing will ever complete, with a limit of timeout_ns nanoseconds
+ * (1 .. 10^9).  The wait runs out, the kernel records RA_ERR_TIMEOUT in the
+ * status word and returns normally.  Exercises the give-up path that every
+ * kernel's waits share, without faulting or hanging the device.
+ */
+ra_status ra_probe_wait_timeout(unsigned long long timeout_ns, ra_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RING_ATTN_H */

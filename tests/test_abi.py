@@ -1,0 +1,71 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads, and
+exports every function that include/ring_attn.h declares."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import context_exact_attention_gb300 as cea
+from context_exact_attention_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ring_attn.h")
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return cea.load_library()
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(cea.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(cea.library_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.ra_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert lib.ra_status_string(99) == b"unknown status"
+
+
+def test_argument_errors_are_caught_before_any_cuda_call(lib):
+    """Validation runs on the host before the runtime is touched, so these codes come
+    back even without a GPU."""
+    fake = ctypes.c_void_p(1 << 20)            # 16-byte aligned, never dereferenced
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    null = ctypes.c_void_p(0)
+    s = ctypes.c_void_p(0)
+    # null pointer
+    assert lib.ring_attn_fwd(null, fake, fake, fake, null, 1, 256, 2, 128, 4, 0, s) == 1
+    # L not divisible by P
+    assert lib.ring_attn_fwd(fake, fake, fake, ctypes.c_void_p(1 << 40), null, 1, 250, 2, 128, 4, 0, s) == 4
+    # misaligned
+    assert lib.ring_attn_fwd(odd, fake, fake, ctypes.c_void_p(1 << 40), null, 1, 256, 2, 128, 4, 0, s) == 3
+    # unsupported head dim for bf16
+    assert lib.ring_attn_fwd(fake, fake, fake, ctypes.c_void_p(1 << 40), null, 1, 256, 2, 96, 4, 0, s) == 2
+    # out overlapping q
+    assert lib.ring_attn_fwd(fake, fake, fake, fake, null, 1, 256, 2, 128, 4, 0, s) == 1
+    # permutes: H not divisible by P, and in == out
+    assert lib.ulysses_seq2head(fake, ctypes.c_void_p(1 << 40), 1, 64, 6, 128, 4, 2, s) == 4
+    assert lib.ulysses_seq2head(fake, fake, 1, 64, 8, 128, 4, 2, s) == 1
+    assert lib.ulysses_seq2head(fake, ctypes.c_void_p(1 << 40), 1, 64, 8, 128, 4, 3, s) == 2
+    # merge: zero rows is a no-op, partial overlap rejected, bad D
+    assert lib.attn_merge_partials(null, null, null, null, null, null, 0, 128, 0, s) == 0
+    assert lib.attn_merge_partials(fake, fake, fake, fake, ctypes.c_void_p((1 << 20) + 16), fake,
+                                   10, 128, 0, s) == 1
+    assert lib.attn_merge_partials(fake, fake, fake, fake, fake, fake, 10, 4, 0, s) == 2
+    assert lib.ra_probe_wait_timeout(0, s) == 1

@@ -1,0 +1,278 @@
+"""GPU parity of every kernel against the fp64 oracle, at sizes the oracle finishes
+in seconds: several tiles, ragged tails, non-power-of-two P, causal and not."""
+import numpy as np
+import pytest
+import torch
+
+import context_exact_attention_gb300 as cea
+import oracle
+from context_exact_attention_gb300.workloads import TINY, make_qkv
+from helpers import assert_bf16_close, assert_f32_close, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _dev(*ts):
+    return tuple(t.to(DEV) for t in ts)
+
+
+# ---------------------------------------------------------------- fp32 path --
+
+@pytest.mark.parametrize("P,causal", [(1, False), (4, False), (4, True), (1, True)])
+def test_f32_tiny_ring_config(P, causal):
+    """B=1, H=2, L=256, D=64, fp32 N(0,1) from seed 0: P=4 shards of 64 tokens, and P=1."""
+    w = TINY
+    q, k, v = make_qkv(w.B, w.L, w.H, w.D, seed=0, dtype=torch.float32)
+    out, lse = cea.ring_attn_fwd_f32(*_dev(q, k, v), P=P, causal=causal)
+    ref, lref = oracle.attention(q, k, v, causal=causal)
+    assert_f32_close(to_np(out), ref, "out")
+    assert_f32_close(to_np(lse), lref, "lse")
+    assert cea.check_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(2, 96, 3, 32, 3), (1, 200, 2, 128, 5), (1, 64, 1, 256, 2),
+                                   (1, 48, 2, 4, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32_shapes(shape, causal):
+    B, L, H, D, P = shape
+    q, k, v = make_qkv(B, L, H, D, seed=3, dtype=torch.float32)
+    out, lse = cea.ring_attn_fwd_f32(*_dev(q, k, v), P=P, causal=causal)
+    ref, lref, _ = oracle.ring_attention(q, k, v, P, causal=causal)
+    assert_f32_close(to_np(out), ref, "out")
+    assert_f32_close(to_np(lse), lref, "lse")
+
+
+# ---------------------------------------------------------------- bf16 path --
+
+BF16_CASES = [
+    # B, L, H, D, P
+    (1, 512, 2, 128, 1),
+    (1, 512, 2, 128, 4),      # shards of one tile
+    (2, 1024, 3, 128, 2),     # shards of 4 tiles
+    (1, 384, 2, 128, 2),      # shard of 192: ragged query pair and ragged key block
+    (1, 192, 2, 64, 3),       # shard of 64: smaller than a tile, P not a power of two
+    (1, 640, 2, 64, 5),
+    (1, 1280, 1, 128, 5),     # shard of 256
+    (1, 2048, 2, 128, 8),
+    (1, 300, 1, 128, 3),      # shard of 100
+]
+
+
+@pytest.mark.parametrize("case", BF16_CASES, ids=lambda c: "B%dL%dH%dD%dP%d" % c)
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_parity(case, causal):
+    B, L, H, D, P = case
+    q, k, v = make_qkv(B, L, H, D, seed=1, dtype=torch.bfloat16)
+    out, lse = cea.ring_attn_fwd(*_dev(q, k, v), P=P, causal=causal)
+    assert cea.check_status() == 0
+    ref, lref = oracle.attention(q, k, v, causal=causal)
+    assert_bf16_close(to_np(out), ref, "out")
+    assert_bf16_close(to_np(lse), lref, "lse")
+
+
+def test_bf16_spread_scores():
+    """Per-head scale s_h ~ U[0.5, 2] on q and k (score std up to 4): peaked softmax rows."""
+    q, k, v = make_qkv(1, 1024, 4, 128, seed=2, dtype=torch.bfloat16, head_scale=True)
+    for causal in (False, True):
+        out, lse = cea.ring_attn_fwd(*_dev(q, k, v), P=4, causal=causal)
+        ref, lref = oracle.attention(q, k, v, causal=causal)
+        assert_bf16_close(to_np(out), ref, "out")
+        assert_bf16_close(to_np(lse), lref, "lse")
+
+
+def test_bf16_large_scores_stay_finite():
+    """Shift every key by one vector: scores near 1000 ("序列并行与 Ring Attention", section 09).
+    The output is the unshifted one; bf16 inputs quantise the shifted keys, so the oracle
+    is evaluated on those same quantised values."""
+    B, L, H, D, P = 1, 512, 2, 128, 4
+    q, k, v = make_qkv(B, L, H, D, seed=4, dtype=torch.bfloat16)
+    q = q.float()
+    q[..., 0] = q[..., 0].abs() + 1.0
+    q = q.to(torch.bfloat16)
+    k = (k.float() + torch.tensor([80.0] + [0.0] * (D - 1))).to(torch.bfloat16)
+    out, lse = cea.ring_attn_fwd(*_dev(q, k, v), P=P, causal=True)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    ref, lref = oracle.attention(q, k, v, causal=True)
+    assert_bf16_close(to_np(out), ref, "out")
+    assert_bf16_close(to_np(lse), lref, "lse")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("P", [1, 3, 4, 8])
+@pytest.mark.parametrize("causal", [False, True])
+def test_schedule_trace_matches_oracle(dtype, P, causal):
+    """The K/V source of every (shard, ring step), -1 where skipped ("序列并行与 Ring
+    Attention", section 6.6): exact integers."""
+    L = 128 * P if dtype == torch.bfloat16 else 16 * P
+    D = 128 if dtype == torch.bfloat16 else 32
+    q, k, v = make_qkv(1, L, 2, D, seed=5, dtype=dtype)
+    out, lse, trace = cea.ring_attn_fwd_trace(*_dev(q, k, v), P=P, causal=causal)
+    ref, _, tref = oracle.ring_attention(q, k, v, P, causal=causal)
+    assert np.array_equal(trace.cpu().numpy(), tref)
+    if dtype == torch.bfloat16:
+        assert_bf16_close(to_np(out), ref, "out")
+        plain, _ = cea.ring_attn_fwd(*_dev(q, k, v), P=P, causal=causal)
+        assert torch.equal(plain, out)
+    else:
+        assert_f32_close(to_np(out), ref, "out")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_did_it_communicate(causal):
+    """P > 1: every shard differs from local-only attention (juejin page, section 二
+    step 4); causal shard 0 sees only itself and matches local-only."""
+    B, L, H, D, P = 1, 1024, 2, 128, 4
+    q, k, v = make_qkv(B, L, H, D, seed=6, dtype=torch.bfloat16)
+    out, _ = cea.ring_attn_fwd(*_dev(q, k, v), P=P, causal=causal)
+    got = to_np(out)
+    loc, _ = oracle.local_only(q, k, v, P, causal=causal)
+    Ls = L // P
+    for r in range(P):
+        d = np.abs(got[:, r * Ls:(r + 1) * Ls] - loc[:, r * Ls:(r + 1) * Ls]).max()
+        if causal and r == 0:
+            assert d < 2e-2
+        else:
+            assert d > 5e-2, (r, d)
+
+
+def test_poisoned_remote_shard():
+    """Large K/V in shard s (juejin page, section 六): non-causal every shard changes,
+    causal exactly the shards r >= s change."""
+    B, L, H, D, P, s = 1, 1024, 2, 128, 4, 2
+    q, k, v = make_qkv(B, L, H, D, seed=7, dtype=torch.bfloat16)
+    Ls = L // P
+    k2, v2 = k.clone(), v.clone()
+    k2[:, s * Ls:(s + 1) * Ls] = q[:, s * Ls:(s + 1) * Ls].float().mean(1, keepdim=True).to(k.dtype) * 4
+    v2[:, s * Ls:(s + 1) * Ls] = 100.0
+    for causal in (False, True):
+        a, _ = cea.ring_attn_fwd(*_dev(q, k, v), P=P, causal=causal)
+        b, _ = cea.ring_attn_fwd(*_dev(q, k2, v2), P=P, causal=causal)
+        for r in range(P):
+            d = (a[:, r * Ls:(r + 1) * Ls].float() - b[:, r * Ls:(r + 1) * Ls].float()).abs().max().item()
+            assert (d > 0.1) == (not causal or r >= s), (causal, r, d)
+
+
+def test_bf16_deterministic():
+    q, k, v = _dev(*make_qkv(1, 2048, 4, 128, seed=8, dtype=torch.bfloat16))
+    first, lfirst = cea.ring_attn_fwd(q, k, v, P=4, causal=True)
+    for _ in range(3):
+        again, lagain = cea.ring_attn_fwd(q, k, v, P=4, causal=True)
+        assert torch.equal(first, again) and torch.equal(lfirst, lagain)
+
+
+def test_without_lse_output():
+    q, k, v = _dev(*make_qkv(1, 512, 2, 128, seed=9, dtype=torch.bfloat16))
+    with_lse, _ = cea.ring_attn_fwd(q, k, v, P=2, causal=True)
+    without, none = cea.ring_attn_fwd(q, k, v, P=2, causal=True, want_lse=False)
+    assert none is None and torch.equal(with_lse, without)
+
+
+# ---------------------------------------------------------------- merge --
+
+def _partials(rows, D, dtype, seed, n_inf=0):
+    g = torch.Generator().manual_seed(seed)
+    oa = torch.randn(rows, D, generator=g).to(dtype)
+    ob = torch.randn(rows, D, generator=g).to(dtype)
+    la = torch.randn(rows, generator=g) * 3
+    lb = torch.randn(rows, generator=g) * 3
+    if n_inf:
+        la[:n_inf] = -float("inf")
+        lb[n_inf // 2:n_inf + n_inf // 2] = -float("inf")
+    return oa, la, ob, lb
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rows,D", [(1000, 128), (37, 64), (5, 8), (4096, 256)])
+def test_merge_matches_oracle(dtype, rows, D):
+    if dtype == torch.bfloat16 and D == 8:
+        D = 16
+    oa, la, ob, lb = _partials(rows, D, dtype, seed=rows, n_inf=min(8, rows))
+    o, l = cea.attn_merge_partials(*_dev(oa, la, ob, lb))
+    ref, lref = oracle.merge(oa, la, ob, lb)
+    check = assert_bf16_close if dtype == torch.bfloat16 else assert_f32_close
+    check(to_np(o), ref, "o")
+    lg = to_np(l)
+    both = np.isneginf(lref)
+    assert np.array_equal(np.isneginf(lg), both)
+    check(lg[~both], lref[~both], "lse")
+
+
+def test_merge_in_place_and_of_attention_partials():
+    """In place (o_out = o_a, lse_out = lse_a); merging the GPU results of two key halves
+    (as separate batch entries) reproduces the oracle's full attention."""
+    B, L, H, D = 1, 512, 2, 128
+    q, k, v = make_qkv(B, 2 * L, H, D, seed=10, dtype=torch.bfloat16)
+    # first half of the keys for all queries, via a batch of two independent problems
+    qa = torch.cat([q[:, :L], q[:, L:]], 0)
+    ka = torch.cat([k[:, :L], k[:, :L]], 0)
+    va = torch.cat([v[:, :L], v[:, :L]], 0)
+    kb = torch.cat([k[:, L:], k[:, L:]], 0)
+    vb = torch.cat([v[:, L:], v[:, L:]], 0)
+    oa, la = cea.ring_attn_fwd(*_dev(qa, ka, va), P=1)
+    ob, lb = cea.ring_attn_fwd(*_dev(qa, kb, vb), P=1)
+    cea.attn_merge_partials(oa, la, ob, lb, o_out=oa, lse_out=la)
+    full = oa.view(2, L, H, D)
+    merged = torch.cat([full[0:1], full[1:2]], 1)
+    ref, lref = oracle.attention(q, k, v)
+    assert_bf16_close(to_np(merged), ref, "merged")
+    assert_bf16_close(to_np(la.view(2, L, H)).reshape(1, 2 * L, H), lref, "lse")
+
+
+# ---------------------------------------------------------------- Ulysses --
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", [(4, 2, 64, 8, 16), (8, 1, 128, 32, 128), (2, 3, 30, 6, 8),
+                                   (3, 1, 10, 3, 8)])
+def test_permutes_bit_exact(dtype, shape):
+    P, B, Ls, H, D = shape
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(P, B, Ls, H, D, generator=g).to(dtype)
+    y = cea.ulysses_seq2head(x.to(DEV), P)
+    yref = oracle.seq2head(x.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy(), P)
+    ycpu = y.cpu()
+    assert np.array_equal(ycpu.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy(), yref)
+    back = cea.ulysses_head2seq(y, P)
+    assert torch.equal(back.cpu(), x)
+    xref = oracle.head2seq(yref, P)
+    assert np.array_equal(xref, x.view(torch.int16 if dtype == torch.bfloat16 else torch.int32).numpy())
+
+
+def test_ulysses_attention_end_to_end():
+    """seq->head transpose, full attention per head group, head->seq: equals full
+    attention of the global tensor, shard by shard."""
+    P, B, L, H, D = 4, 2, 512, 8, 128
+    q, k, v = make_qkv(B, L, H, D, seed=12, dtype=torch.bfloat16)
+    Ls = L // P
+    to_seq = lambda t: torch.stack([t[:, r * Ls:(r + 1) * Ls] for r in range(P)]).contiguous()
+    o_seq = cea.ulysses_attention(*_dev(to_seq(q), to_seq(k), to_seq(v)), P)
+    ref, _ = oracle.attention(q, k, v)
+    got = to_np(o_seq)                                 # [P, B, Ls, H, D]
+    glob = np.concatenate([got[r] for r in range(P)], axis=1)
+    assert_bf16_close(glob, ref, "ulysses")
+
+
+# ---------------------------------------------------------------- errors --
+
+def test_binding_reports_argument_errors():
+    q, k, v = _dev(*make_qkv(1, 250, 2, 128, seed=0, dtype=torch.bfloat16))
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ring_attn_fwd(q, k, v, P=4)
+    assert e.value.code == 4
+    q, k, v = _dev(*make_qkv(1, 256, 2, 96, seed=0, dtype=torch.bfloat16))
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ring_attn_fwd(q, k, v, P=4)
+    assert e.value.code == 2
+    assert cea.check_status() == 0
+
+
+def test_bounded_wait_reports_timeout():
+    """A wait on a barrier nothing completes gives up after its limit and the status
+    word says so; the context stays usable."""
+    assert cea.check_status() == 0
+    cea.probe_wait_timeout(2_000_000)
+    assert cea.check_status() == 6
+    assert cea.check_status() == 0
+    q, k, v = _dev(*make_qkv(1, 256, 1, 128, seed=0, dtype=torch.bfloat16))
+    cea.ring_attn_fwd(q, k, v, P=2)
+    assert cea.check_status() == 0
