@@ -1,0 +1,444 @@
+"""Benchmark: exact ring-attention forward on GB300, one JSON line on stdout.
+
+Headline workload: causal LM context-parallel forward, B=1, H=32, L=32768, D=128,
+bf16, P=8 virtual ring shards of 4096 tokens with whole-shard causal skip
+(q, k ~ N(0,1) scaled per head by s_h ~ U[0.5, 2], v ~ N(0,1)).  One step is
+one ring_attn_fwd call over that input; the metric is algorithmic TFLOP/s
+(4*D per visible query/key pair).  Inputs (3 x 256 MiB) exceed the 129 MB L2,
+so no flush is needed between steps.
+
+Also measured in the same run (the "rows" object): the diffusion-DiT full
+attention workload (40 calls), the LSE merge at the causal-LM size, the Ulysses
+transposes and pipeline, and the long-context causal workload.
+
+--impl reference times the fp64 CPU oracle (the only reference this project
+has) on the host cores, on a bounded sample of query rows of the same workload.
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU
+(independent replicas, weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from context_exact_attention_gb300.workloads import (DIT, LM, LONG, ULYSSES,  # noqa: E402
+                                                     attention_flops, make_workload_inputs,
+                                                     sample_rows)
+
+METRIC = "attention fwd TFLOP/s (bf16, full & causal) and % of GB300 dense BF16 peak"
+HEADLINE = LM
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SRC = os.path.join(ROOT, "context_exact_attention_gb300", "csrc", "attn_bf16_sm103.cu")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _rank_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def _peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _kernel_hash():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic_per_launch():
+    """DRAM bytes of one ring_attn_fwd launch from a committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        if t.get("kernel_sha256_16") == _kernel_hash():
+            return t.get("bytes_per_launch_full_workload")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "200"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and parts[1] != self.uuid:
+                    continue
+                try:
+                    rows.append((float(parts[2].split()[0]), float(parts[3].split()[0]),
+                                 parts[4], parts[5:]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for _, _, _, rs in rows:
+            for n, val in zip(names[1:], rs[1:]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        loaded = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "power_w_max": None, "reasons": sorted(reasons)}
+
+
+def _time_loop(fn, steps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop)
+
+
+def _flops_rows(L, D, causal, rows, heads):
+    per_head = sum((i + 1) if causal else L for i in rows)
+    return 4 * D * heads * per_head
+
+
+def cpu_oracle_sample(w, budget_s=15.0, seed=0):
+    """Time the fp64 oracle on the host cores on sampled query rows of workload w.
+    Returns (TFLOP/s, seconds, rows, threads)."""
+    import oracle
+
+    q, k, v = make_workload_inputs(w, seed=seed)
+    threads = oracle.default_threads()
+    probe = sample_rows(w.L, w.P, 2 * w.P, seed=1)        # shard edges only
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, causal=w.causal, rows=probe, threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    per_row = dt / len(probe)
+    n = int(max(2 * w.P, min(4 * w.L, budget_s / per_row)))
+    rows = sample_rows(w.L, w.P, n, seed=1)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, causal=w.causal, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    fl = _flops_rows(w.L, w.D, w.causal, rows, w.B * w.H)
+    return fl / dt / 1e12, dt, len(rows), threads
+
+
+def run_reference(args, rank, world):
+    """fp64 CPU oracle arm: each step is a bounded sample of query rows of the workload."""
+    if rank != 0:
+        return
+    import oracle
+
+    w = HEADLINE
+    q, k, v = make_workload_inputs(w, seed=0)
+    threads = oracle.default_threads()
+    n_rows = args.ref_rows
+    rows_all = sample_rows(w.L, w.P, n_rows * (args.warmup + args.steps), seed=1)
+    chunks = [rows_all[i::args.warmup + args.steps] for i in range(args.warmup + args.steps)]
+    for c in chunks[:args.warmup]:
+        oracle.attention(q, k, v, causal=w.causal, rows=c, threads=threads)
+    fl = 0
+    t0 = time.perf_counter()
+    for c in chunks[args.warmup:]:
+        oracle.attention(q, k, v, causal=w.causal, rows=c, threads=threads)
+        fl += _flops_rows(w.L, w.D, w.causal, c, w.B * w.H)
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "D": w.D, "P": w.P,
+                   "causal": w.causal, "sample": f"{n_rows} query rows x {w.B * w.H} heads per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_rows} sampled query rows (all heads) per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, rank, world, local_rank):
+    import context_exact_attention_gb300 as cea
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cea.load_library()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+
+    w = HEADLINE
+    qc, kc, vc = make_workload_inputs(w, seed=0)
+    q, k, v = (t.to(dev) for t in (qc, kc, vc))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.L, w.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: cea.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal, out=out, lse=lse,
+                                      stream=stream)
+    for _ in range(args.warmup):
+        step()
+    if cea.check_status(stream) != 0:
+        raise RuntimeError("kernel reported a device-side timeout during warm-up")
+    flops = attention_flops(w.B, w.L, w.H, w.D, w.causal)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    if dist is not None:
+        dist.barrier()
+    with ClockSampler(uuid) as clk:
+        ms = _time_loop(step, args.steps, stream)
+    clocks = clk.summary()
+    if cea.check_status(stream) != 0:
+        raise RuntimeError("kernel reported a device-side timeout in the timed region")
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    value = flops * world / (ms_step * 1e-3) / 1e12
+
+    # -- end to end through the public API: pinned host inputs in, result back out
+    hq, hk, hv = (t.pin_memory() for t in (qc, kc, vc))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_steps = max(3, args.steps // 4)
+    e2e_ms = _time_loop(e2e_step, e2e_steps, stream) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+    peaks, peak_src = _peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": _traffic_per_launch(),
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback 1.9 PFLOP/s bf16",
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "kernel": "ring_attn_bf16_kernel<128>"}
+
+    rows = {}
+    if not args.no_rows and rank == 0:
+        rows = measure_rows(cea, dev, stream, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, dt, n, threads = cpu_oracle_sample(w, budget_s=args.cpu_budget)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} sampled query rows x {w.B * w.H} heads of the causal-LM workload "
+                         f"({dt:.1f} s, fp64)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "D": w.D, "P": w.P,
+                       "causal": w.causal, "global_batch": w.B * world, "seq_len": w.L,
+                       "parallelism": f"replicas{world}",
+                       "l2": "inputs 805 MB per step > 129 MB L2 (no flush needed)"},
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps, "clocks": clocks, "rows": rows,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def measure_rows(cea, dev, stream, peaks):
+    """Secondary measurements: every other hot-path row, a few timed repetitions each."""
+    res = {}
+    hbm = float(peaks["hbm_gbs"])
+    peak = float(peaks["bf16_tflops"])
+
+    # diffusion-DiT full attention, 40 calls as one denoising loop
+    w = DIT
+    q, k, v = (t.to(dev) for t in make_workload_inputs(w, seed=0))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.L, w.H), dtype=torch.float32, device=dev)
+    f = lambda: cea.ring_attn_fwd(q, k, v, P=w.P, causal=False, out=out, lse=lse, stream=stream)
+    for _ in range(3):
+        f()
+    ms = _time_loop(f, w.repeats, stream)
+    fl = attention_flops(w.B, w.L, w.H, w.D, False)
+    res["dit_full_x40"] = {"ms_total": ms, "ms_per_call": ms / w.repeats,
+                           "tflops": fl * w.repeats / (ms * 1e-3) / 1e12,
+                           "frac": fl * w.repeats / (ms * 1e-3) / 1e12 / peak,
+                           "note": "inputs 72 MiB fit in L2; back-to-back calls"}
+    del q, k, v, out, lse
+
+    # LSE merge at the causal-LM size: two partials of 1,048,576 rows x 128 bf16
+    rows, D = LM.B * LM.L * LM.H, LM.D
+    g = torch.Generator(device=dev).manual_seed(0)
+    oa = torch.randn(rows, D, device=dev, generator=g).to(torch.bfloat16)
+    ob = torch.randn(rows, D, device=dev, generator=g).to(torch.bfloat16)
+    la = torch.randn(rows, device=dev, generator=g)
+    lb = torch.randn(rows, device=dev, generator=g)
+    oo, lo = torch.empty_like(oa), torch.empty_like(la)
+    f = lambda: cea.attn_merge_partials(oa, la, ob, lb, o_out=oo, lse_out=lo, stream=stream)
+    for _ in range(3):
+        f()
+    n = 20
+    ms = _time_loop(f, n, stream) / n
+    by = rows * (3 * D * 2 + 3 * 4)
+    res["merge_lm_size"] = {"ms": ms, "GB/s": by / (ms * 1e-3) / 1e9,
+                            "frac": by / (ms * 1e-3) / 1e9 / hbm, "bytes": by,
+                            "note": "working set 805 MB > L2"}
+    del oa, ob, la, lb, oo, lo
+
+    # Ulysses transposes and pipeline
+    w = ULYSSES
+    Ls, Hg = w.L // w.P, w.H // w.P
+    x = torch.randn(w.P, w.B, Ls, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
+    y = torch.empty(w.P, w.B, w.L, Hg, w.D, device=dev, dtype=torch.bfloat16)
+    f = lambda: cea.ulysses_seq2head(x, w.P, out=y, stream=stream)
+    for _ in range(3):
+        f()
+    ms = _time_loop(f, n, stream) / n
+    by = 2 * x.numel() * 2
+    res["ulysses_seq2head"] = {"ms": ms, "GB/s": by / (ms * 1e-3) / 1e9,
+                               "frac": by / (ms * 1e-3) / 1e9 / hbm, "bytes": by}
+    f = lambda: cea.ulysses_head2seq(y, w.P, out=x, stream=stream)
+    ms = _time_loop(f, n, stream) / n
+    res["ulysses_head2seq"] = {"ms": ms, "GB/s": by / (ms * 1e-3) / 1e9,
+                               "frac": by / (ms * 1e-3) / 1e9 / hbm, "bytes": by}
+    qs = x
+    ks = torch.randn_like(x, dtype=torch.float32).to(torch.bfloat16)
+    vs = torch.randn_like(x, dtype=torch.float32).to(torch.bfloat16)
+    bufs = {nm: torch.empty(w.P, w.B, w.L, Hg, w.D, device=dev, dtype=torch.bfloat16)
+            for nm in ("q", "k", "v", "o")}
+    f = lambda: cea.ulysses_attention(qs, ks, vs, w.P, stream=stream, buffers=bufs)
+    for _ in range(2):
+        f()
+    n2 = 5
+    ms = _time_loop(f, n2, stream) / n2
+    fl = attention_flops(w.B, w.L, w.H, w.D, False)
+    res["ulysses_pipeline"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                               "frac": fl / (ms * 1e-3) / 1e12 / peak,
+                               "note": "3 seq2head + attention (B'=16, H'=4, P=1) + head2seq"}
+    del x, y, qs, ks, vs, bufs
+
+    # long-context causal
+    w = LONG
+    q, k, v = (torch.randn(w.B, w.L, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.L, w.H), dtype=torch.float32, device=dev)
+    f = lambda: cea.ring_attn_fwd(q, k, v, P=w.P, causal=True, out=out, lse=lse, stream=stream)
+    f()
+    ms = _time_loop(f, 3, stream) / 3
+    fl = attention_flops(w.B, w.L, w.H, w.D, True)
+    res["long_causal"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                          "frac": fl / (ms * 1e-3) / 1e12 / peak}
+    del q, k, v, out, lse
+    if cea.check_status(stream) != 0:
+        raise RuntimeError("kernel reported a device-side timeout in the secondary rows")
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-rows", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--ref-rows", type=int, default=16,
+                    help="query rows (all heads) per reference step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = _rank_env()
+    if world != args.gpus and "RANK" in os.environ:
+        print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()
