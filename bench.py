@@ -19,6 +19,7 @@ Multi-GPU (torchrun): every rank runs the same workload on its own GPU
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -166,7 +167,7 @@ def cpu_oracle_sample(w, budget_s=15.0, seed=0):
     Returns (TFLOP/s, seconds, rows, threads)."""
     import oracle
 
-    q, k, v = make_workload_inputs(w, seed=seed)
+    q, k, v = (oracle.to_f64(t) for t in make_workload_inputs(w, seed=seed))
     threads = oracle.default_threads()
     probe = sample_rows(w.L, w.P, 2 * w.P, seed=1)        # shard edges only
     t0 = time.perf_counter()
@@ -189,7 +190,7 @@ def run_reference(args, rank, world):
     import oracle
 
     w = HEADLINE
-    q, k, v = make_workload_inputs(w, seed=0)
+    q, k, v = (oracle.to_f64(t) for t in make_workload_inputs(w, seed=0))
     threads = oracle.default_threads()
     n_rows = args.ref_rows
     rows_all = sample_rows(w.L, w.P, n_rows * (args.warmup + args.steps), seed=1)
@@ -229,6 +230,8 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("gloo")
 
     w = HEADLINE
+    if args.profile_case:
+        w = dataclasses.replace(w, H=8, name=w.name.replace("H32", "H8") + " (profile case)")
     qc, kc, vc = make_workload_inputs(w, seed=0)
     q, k, v = (t.to(dev) for t in (qc, kc, vc))
     out = torch.empty_like(q)
@@ -313,7 +316,8 @@ def run_gpu(args, rank, world, local_rank):
             "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "D": w.D, "P": w.P,
                        "causal": w.causal, "global_batch": w.B * world, "seq_len": w.L,
                        "parallelism": f"replicas{world}",
-                       "l2": "inputs 805 MB per step > 129 MB L2 (no flush needed)"},
+                       "l2": f"inputs {3 * q.numel() * 2 / 1e6:.0f} MB per step > 129 MB L2 "
+                             "(no flush needed)"},
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -426,7 +430,10 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
-    ap.add_argument("--ref-rows", type=int, default=16,
+    ap.add_argument("--profile-case", action="store_true",
+                    help="headline workload with 8 heads instead of 32 (201 MB of inputs, "
+                         "still larger than L2): the small case for profiler captures")
+    ap.add_argument("--ref-rows", type=int, default=8,
                     help="query rows (all heads) per reference step")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -80,10 +80,13 @@ def default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
 
-def _f64(x) -> np.ndarray:
-    """Any array-like (numpy, or a CPU torch tensor of any float dtype) -> contiguous fp64 numpy."""
+def to_f64(x) -> np.ndarray:
+    """Any array-like (numpy, or a CPU torch tensor of any float dtype) -> contiguous fp64 numpy.
+    Arrays that already are contiguous fp64 are returned as they are (no copy)."""
     if hasattr(x, "detach"):
         x = x.detach().cpu().double().numpy()
+    if isinstance(x, np.ndarray) and x.dtype == np.float64 and x.flags.c_contiguous:
+        return x
     return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
 
 
@@ -99,7 +102,7 @@ def attention(q, k, v, causal: bool = False, rows=None, q_pos0: int = 0, k_pos0:
     Returns ``(out [B, n_rows, H, D], lse [B, n_rows, H])`` as fp64 numpy arrays.
     """
     lib = _load()
-    q, k, v = _f64(q), _f64(k), _f64(v)
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
     B, Lq, H, D = q.shape
     Lk = k.shape[1]
     assert k.shape == (B, Lk, H, D) and v.shape == (B, Lk, H, D)
@@ -125,7 +128,7 @@ def ring_attention(q, k, v, P: int, causal: bool = False, threads: int | None = 
     Returns ``(out [B, L, H, D], lse [B, L, H], trace [P, P] int32)``.
     """
     lib = _load()
-    q, k, v = _f64(q), _f64(k), _f64(v)
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
     B, L, H, D = q.shape
     assert k.shape == q.shape and v.shape == q.shape
     out = np.empty_like(q)
@@ -144,7 +147,7 @@ def ring_attention(q, k, v, P: int, causal: bool = False, threads: int | None = 
 
 def local_only(q, k, v, P: int, causal: bool = False, threads: int | None = None):
     """Each shard attends only to its own K/V block (no exchange between shards)."""
-    q, k, v = _f64(q), _f64(k), _f64(v)
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
     B, L, H, D = q.shape
     if L % P:
         raise ValueError("L must be divisible by P")
@@ -162,8 +165,8 @@ def local_only(q, k, v, P: int, causal: bool = False, threads: int | None = None
 def merge(o_a, lse_a, o_b, lse_b):
     """LSE combine of two partials.  o_*: [..., D], lse_*: [...] (same leading shape)."""
     lib = _load()
-    o_a, o_b = _f64(o_a), _f64(o_b)
-    lse_a, lse_b = _f64(lse_a), _f64(lse_b)
+    o_a, o_b = to_f64(o_a), to_f64(o_b)
+    lse_a, lse_b = to_f64(lse_a), to_f64(lse_b)
     lead = o_a.shape[:-1]
     D = o_a.shape[-1]
     rows = int(np.prod(lead)) if lead else 1

@@ -138,13 +138,15 @@ static void attn_item(void* vctx, long item, double* w)
         w[j] = (w[j] == -INFINITY) ? 0.0 : exp(w[j] - m);
         den += w[j];
     }
-    for (long d = 0; d < D; ++d) {
-        double acc = 0.0;
-        for (long j = 0; j < c->Lk; ++j) {
-            if (w[j] != 0.0) acc += w[j] * c->v[((b * c->Lk + j) * H + h) * D + d];
-        }
-        orow[d] = acc / den;
+    /* acc[d] = sum_j w_j v[j][d], keys taken in order j = 0, 1, ... for every d */
+    double* acc = w + c->Lk;
+    for (long d = 0; d < D; ++d) acc[d] = 0.0;
+    for (long j = 0; j < c->Lk; ++j) {
+        if (w[j] == 0.0) continue;
+        const double* vrow = c->v + ((b * c->Lk + j) * H + h) * D;
+        for (long d = 0; d < D; ++d) acc[d] += w[j] * vrow[d];
     }
+    for (long d = 0; d < D; ++d) orow[d] = acc[d] / den;
     *lrow = m + log(den);
 }
 
@@ -167,7 +169,7 @@ int oracle_attention(const double* q, const double* k, const double* v,
     attn_ctx_t c = { q, k, v, out, lse, B, Lq, Lk, H, D, causal, q_pos0, k_pos0, rows, n_rows };
     long n_items = B * H * n_rows;
     if (n_items == 0) return 0;
-    return run_pool(attn_item, &c, n_items, Lk > 0 ? Lk : 1, n_threads);
+    return run_pool(attn_item, &c, n_items, (Lk > 0 ? Lk : 1) + D, n_threads);
 }
 
 /* ------------------------------------------------------------------------- */
