@@ -157,6 +157,15 @@ def _time_loop(fn, steps, stream):
     return start.elapsed_time(stop)
 
 
+def max_over_ranks(ms, dist=None):
+    """The slowest rank's time (the whole job ends when its last rank does)."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _flops_rows(L, D, causal, rows, heads):
     per_head = sum((i + 1) if causal else L for i in rows)
     return 4 * D * heads * per_head
@@ -258,11 +267,7 @@ def run_gpu(args, rank, world, local_rank):
     clocks = clk.summary()
     if cea.check_status(stream) != 0:
         raise RuntimeError("kernel reported a device-side timeout in the timed region")
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist)
     ms_step = ms_max / args.steps
     value = flops * world / (ms_step * 1e-3) / 1e12
 

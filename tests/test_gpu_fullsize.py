@@ -1,0 +1,97 @@
+"""Parity at the full sizes of the five workloads, in the launch configuration the
+benchmark times: outputs compared with the fp64 oracle on sampled query rows (the first
+and last row of every shard plus seeded uniform rows), element-wise merges and
+bit-exact transposes over the whole tensors, and determinism over repeated calls."""
+import numpy as np
+import pytest
+import torch
+
+import context_exact_attention_gb300 as cea
+import oracle
+from context_exact_attention_gb300.workloads import (DIT, LM, LONG, ULYSSES,
+                                                     make_workload_inputs, sample_rows)
+from helpers import assert_bf16_close, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _check_rows(w, out, lse, q, k, v, n_rows):
+    rows = sample_rows(w.L, w.P, n_rows, seed=1)
+    ref, lref = oracle.attention(q, k, v, causal=w.causal, rows=rows)
+    got = to_np(out[:, rows])
+    assert_bf16_close(got, ref, f"{w.name} out")
+    assert_bf16_close(to_np(lse[:, rows]), lref, f"{w.name} lse")
+
+
+def test_dit_full_attention_40_calls():
+    """Non-causal B=1 H=24 L=4096 D=128 P=4, 40 calls (denoising steps): every call
+    bit-identical to the first, and the result matches the oracle on 256 rows x 24 heads."""
+    w = DIT
+    q, k, v = make_workload_inputs(w, seed=0)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    first, lfirst = cea.ring_attn_fwd(qd, kd, vd, P=w.P, causal=False)
+    out, lse = torch.empty_like(first), torch.empty_like(lfirst)
+    for _ in range(w.repeats - 1):
+        cea.ring_attn_fwd(qd, kd, vd, P=w.P, causal=False, out=out, lse=lse)
+        assert torch.equal(out, first) and torch.equal(lse, lfirst)
+    assert cea.check_status() == 0
+    _check_rows(w, first, lfirst, q, k, v, 256)
+
+
+def test_causal_lm_full_size():
+    """Causal B=1 H=32 L=32768 D=128 P=8 with per-head score scales: 96 rows x 32 heads."""
+    w = LM
+    q, k, v = make_workload_inputs(w, seed=0)
+    out, lse = cea.ring_attn_fwd(*(t.to(DEV) for t in (q, k, v)), P=w.P, causal=True)
+    assert cea.check_status() == 0
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    _check_rows(w, out, lse, q, k, v, 96)
+
+
+def test_long_context_full_size():
+    """Causal B=1 H=8 L=131072 D=128 P=8: 512 sampled rows per head."""
+    w = LONG
+    q, k, v = make_workload_inputs(w, seed=0)
+    out, lse = cea.ring_attn_fwd(*(t.to(DEV) for t in (q, k, v)), P=w.P, causal=True)
+    assert cea.check_status() == 0
+    assert torch.isfinite(out).all()
+    _check_rows(w, out, lse, q, k, v, 512)
+
+
+def test_ulysses_full_size():
+    """B=2 L=8192 H=32 D=128 P=8: the three seq->head transposes are bit-exact against
+    the oracle, and the head->seq result of full attention per head group matches the
+    oracle's attention of the global tensors on 64 rows x 64 (batch, head) pairs."""
+    w = ULYSSES
+    q, k, v = make_workload_inputs(w, seed=0)
+    Ls = w.L // w.P
+    to_seq = lambda t: torch.stack([t[:, r * Ls:(r + 1) * Ls] for r in range(w.P)]).contiguous()
+    qs, ks, vs = (to_seq(t) for t in (q, k, v))
+    head = cea.ulysses_seq2head(qs.to(DEV), w.P)
+    ref_head = oracle.seq2head(qs.view(torch.int16).numpy(), w.P)
+    assert np.array_equal(head.cpu().view(torch.int16).numpy(), ref_head)
+    o_seq = cea.ulysses_attention(qs.to(DEV), ks.to(DEV), vs.to(DEV), w.P)
+    assert cea.check_status() == 0
+    glob = torch.cat([o_seq[r] for r in range(w.P)], dim=1)      # [B, L, H, D]
+    rows = sample_rows(w.L, w.P, 64, seed=1)
+    ref, _ = oracle.attention(q, k, v, causal=False, rows=rows)
+    assert_bf16_close(to_np(glob[:, rows]), ref, "ulysses out")
+    back = cea.ulysses_head2seq(head, w.P)
+    assert torch.equal(back.cpu(), qs)
+
+
+def test_merge_causal_lm_size():
+    """Two partials of 1,048,576 rows x 128 (bf16 o, fp32 lse): the GPU merge against the
+    oracle's, element by element over the whole tensors, and in place."""
+    rows, D = LM.B * LM.L * LM.H, LM.D
+    g = torch.Generator().manual_seed(3)
+    oa = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    ob = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    la = torch.randn(rows, generator=g) * 4
+    lb = torch.randn(rows, generator=g) * 4
+    ref, lref = oracle.merge(oa, la, ob, lb)
+    oad, lad = oa.to(DEV), la.to(DEV)
+    cea.attn_merge_partials(oad, lad, ob.to(DEV), lb.to(DEV), o_out=oad, lse_out=lad)
+    assert_bf16_close(to_np(oad), ref, "merge o")
+    assert_bf16_close(to_np(lad), lref, "merge lse")
