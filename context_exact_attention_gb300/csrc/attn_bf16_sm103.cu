@@ -14,8 +14,12 @@
 //   warp 0      TMA producer: Q tiles once, then K and V blocks through two
 //               2-deep shared-memory rings (the next block loads while the
 //               current one is used: the ring's double buffer, section 6.3).
-//   warp 1      MMA issuer (one thread): S_t = Q_t K^T into TMEM, then
-//               O_t += P_t V with P_t read from TMEM.
+//   warp 1      MMA issuer: S_t = Q_t K^T into TMEM, then O_t += P_t V with P_t
+//               read from TMEM.
+//   Both run their schedule warp-wide, so addresses and descriptors stay
+//   warp-uniform, and one elected lane issues each TMA / tcgen05 instruction
+//   (a lone-lane issuer pays register-to-uniform moves on every MMA and
+//   cannot keep the tensor pipe fed).
 //   warps 4-7   softmax of query tile 0; warps 8-11 softmax of query tile 1.
 //               One thread per query row (TMEM lane): row max, exp2, row sum,
 //               P packed to bf16 back into TMEM over S, O rescale when needed.
@@ -181,110 +185,133 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // The whole warp runs the loop (warp-uniform values); one elected lane issues.
+        const bool leader = elect_one();
+        if (leader) {
             tma_prefetch_desc(&tmap_q);
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
-            const bool tracing = p.trace != nullptr && bh == 0 && pair == 0;
-            if (tracing)
-                for (int t = 0; t < p.P; ++t) p.trace[r * p.P + t] = -1;
-            const uint64_t keep = l2_policy_evict_last();    // K/V: read by every tile pair of the head
-            const uint64_t once = l2_policy_evict_first();   // Q: read once
+        }
+        const bool tracing = p.trace != nullptr && bh == 0 && pair == 0;
+        if (tracing && leader)
+            for (int t = 0; t < p.P; ++t) p.trace[r * p.P + t] = -1;
+        const uint64_t keep = l2_policy_evict_last();    // K/V: read by every tile pair of the head
+        const uint64_t once = l2_policy_evict_first();   // Q: read once
+        if (leader) {
             mbar_arrive_expect_tx(bar(kBarQ), kTiles * Lay::kTileBytes);
             for (int tq = 0; tq < kTiles; ++tq)
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
                     tma_load_4d(sbase + Lay::kQ + tq * Lay::kTileBytes + bx * 16384, &tmap_q,
                                 bar(kBarQ), bx * 64, h, q0 + tq * kRows, b, once);
-            int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
-            for (int n = 0; n < sc.n_blocks; ++n) {
-                int s, kt, t;
-                sc.block(n, s, kt, t);
-                if (tracing && kt == 0) p.trace[r * p.P + t] = s;
-                const int st = n & 1;
-                const uint32_t ph = (n >> 1) & 1;
-                const int row = s * p.Ls + kt * kKeys;
-                if (!mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc)) break;
+        }
+        int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+        for (int n = 0; n < sc.n_blocks; ++n) {
+            int s, kt, t;
+            sc.block(n, s, kt, t);
+            if (tracing && kt == 0 && leader) p.trace[r * p.P + t] = s;
+            const int st = n & 1;
+            const uint32_t ph = (n >> 1) & 1;
+            const int row = s * p.Ls + kt * kKeys;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc))) break;
+            if (leader) {
                 mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kTileBytes);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
                     tma_load_4d(sbase + Lay::kK + st * Lay::kTileBytes + bx * 16384, &tmap_k,
                                 bar(kBarKFull + st), bx * 64, h, row, b, keep);
-                last_k[st] = n;
-                if (!mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc)) break;
+            }
+            last_k[st] = n;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc))) break;
+            if (leader) {
                 mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kTileBytes);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
                     tma_load_4d(sbase + Lay::kV + st * Lay::kTileBytes + bx * 16384, &tmap_v,
                                 bar(kBarVFull + st), bx * 64, h, row, b, keep);
-                last_v[st] = n;
             }
-            // let this CTA's own copies land before anyone leaves
-            mbar_wait_drain(bar(kBarQ), 0, wc);
-            for (int st = 0; st < 2; ++st) {
-                if (last_k[st] >= 0) mbar_wait_drain(bar(kBarKFull + st), (last_k[st] >> 1) & 1, wc);
-                if (last_v[st] >= 0) mbar_wait_drain(bar(kBarVFull + st), (last_v[st] >> 1) & 1, wc);
-            }
+            last_v[st] = n;
+        }
+        // let this CTA's own copies land before anyone leaves
+        mbar_wait_drain(bar(kBarQ), 0, wc);
+        for (int st = 0; st < 2; ++st) {
+            if (last_k[st] >= 0) mbar_wait_drain(bar(kBarKFull + st), (last_k[st] >> 1) & 1, wc);
+            if (last_v[st] >= 0) mbar_wait_drain(bar(kBarVFull + st), (last_v[st] >> 1) & 1, wc);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t kIdescQK = idesc_bf16_f32(kRows, kKeys, false);
-            constexpr uint32_t kIdescPV = idesc_bf16_f32(kRows, D, true);
-            // S_tq = Q_tq K^T: both operands K-major (head dim contiguous), 128-byte
-            // swizzled rows of 64 elements; 16-element K steps advance 32 bytes
-            // inside a swizzle row, then jump to the next 64-wide box.
-            auto issue_qk = [&](int tq, int st) {
-                const uint32_t d_t = tmem + Lay::col_s(tq);
-                const uint32_t qa = sbase + Lay::kQ + tq * Lay::kTileBytes;
-                const uint32_t ka = sbase + Lay::kK + st * Lay::kTileBytes;
+        // The whole warp runs the loop so that descriptors stay warp-uniform; one
+        // elected lane issues the tcgen05 instructions.
+        const bool leader = elect_one();
+        constexpr uint32_t kIdescQK = idesc_bf16_f32(kRows, kKeys, false);
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(kRows, D, true);
+        constexpr uint64_t kTileU = Lay::kTileBytes >> 4;   // descriptor address unit: 16 bytes
+        // S_tq = Q_tq K^T: both operands K-major (head dim contiguous), 128-byte swizzled
+        // rows of 64 elements, 8-row atoms 1024 bytes apart; 16-element K steps advance
+        // 32 bytes inside a swizzle row, then jump to the next 64-wide box (16 KiB).
+        const uint64_t dq = sdesc_sw128(sbase + Lay::kQ, 16, 1024);
+        const uint64_t dk = sdesc_sw128(sbase + Lay::kK, 16, 1024);
+        // V is the MN-major B operand (head dim contiguous): 8 key rows of 128 bytes per
+        // swizzle atom (stride 1024), the second 64-wide box 16 KiB further (leading
+        // offset); 16-key steps advance 2 KiB.
+        const uint64_t dv = sdesc_sw128(sbase + Lay::kV, 16384, 1024);
+        auto issue_qk = [&](int tq, int st) {
+            const uint32_t d_t = tmem + Lay::col_s(tq);
+            const uint64_t a0 = dq + tq * kTileU, b0 = dk + st * kTileU;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_ss(d_t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                           kIdescQK, k > 0 ? 1u : 0u);
-                }
-            };
-            // O_tq += P_tq V: P (128 x 128 keys, bf16 pairs) sits in TMEM over S_tq; V is
-            // the MN-major B operand (head dim contiguous): 8 key rows of 128 bytes per
-            // swizzle atom (stride 1024), the second 64-wide box 16 KiB further.
-            auto issue_pv = [&](int tq, int st, bool acc) {
-                const uint32_t d_t = tmem + Lay::col_o(tq);
-                const uint32_t pa = tmem + Lay::col_s(tq);
-                const uint32_t va = sbase + Lay::kV + st * Lay::kTileBytes;
+            for (int k = 0; k < D / 16; ++k) {
+                const uint64_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+                mma_ss(d_t, a0 + off, b0 + off, kIdescQK, k > 0 ? 1u : 0u);
+            }
+        };
+        // O_tq += P_tq V: P (128 x 128 keys, bf16 pairs) sits in TMEM over S_tq.
+        auto issue_pv = [&](int tq, int st, bool acc) {
+            const uint32_t d_t = tmem + Lay::col_o(tq);
+            const uint32_t pa = tmem + Lay::col_s(tq);
+            const uint64_t b0 = dv + st * kTileU;
 #pragma unroll
-                for (int k = 0; k < kKeys / 16; ++k)
-                    mma_ts(d_t, pa + k * 8, sdesc_sw128(va + k * 2048, 16384, 1024), kIdescPV,
-                           (acc || k > 0) ? 1u : 0u);
-            };
+            for (int k = 0; k < kKeys / 16; ++k)
+                mma_ts(d_t, pa + k * 8, b0 + ((k * 2048) >> 4), kIdescPV, (acc || k > 0) ? 1u : 0u);
+        };
+        auto wait_all = [&](int idx, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(bar(idx), parity, wc));
+        };
 
-            bool ok = mbar_wait(bar(kBarQ), 0, wc);
-            if (ok) ok = mbar_wait(bar(kBarKFull + 0), 0, wc);
-            if (ok) {
-                tc_fence_after();
+        bool ok = wait_all(kBarQ, 0) && wait_all(kBarKFull + 0, 0);
+        if (ok) {
+            tc_fence_after();
+            if (leader) {
                 issue_qk(0, 0);
                 tc_commit(bar(kBarSFull + 0));
                 issue_qk(1, 0);
                 tc_commit(bar(kBarSFull + 1));
                 tc_commit(bar(kBarKEmpty + 0));
             }
-            for (int n = 0; ok && n < sc.n_blocks; ++n) {
-                const int st = n & 1;
-                const uint32_t ph = (n >> 1) & 1;
-                const bool more = n + 1 < sc.n_blocks;
-                const int st1 = (n + 1) & 1;
-                const uint32_t ph1 = ((n + 1) >> 1) & 1;
-                if (!(ok = mbar_wait(bar(kBarVFull + st), ph, wc))) break;
-                if (!(ok = mbar_wait(bar(kBarPFull + 0), n & 1, wc))) break;
-                tc_fence_after();
+            __syncwarp();
+        }
+        for (int n = 0; ok && n < sc.n_blocks; ++n) {
+            const int st = n & 1;
+            const uint32_t ph = (n >> 1) & 1;
+            const bool more = n + 1 < sc.n_blocks;
+            const int st1 = (n + 1) & 1;
+            const uint32_t ph1 = ((n + 1) >> 1) & 1;
+            if (!(ok = wait_all(kBarVFull + st, ph) && wait_all(kBarPFull + 0, n & 1))) break;
+            tc_fence_after();
+            if (leader) {
                 issue_pv(0, st, n > 0);
                 if (!more) tc_commit(bar(kBarOFull + 0));
-                if (more) {
-                    if (!(ok = mbar_wait(bar(kBarKFull + st1), ph1, wc))) break;
-                    tc_fence_after();
+            }
+            __syncwarp();
+            if (more) {
+                if (!(ok = wait_all(kBarKFull + st1, ph1))) break;
+                tc_fence_after();
+                if (leader) {
                     issue_qk(0, st1);
                     tc_commit(bar(kBarSFull + 0));
                 }
-                if (!(ok = mbar_wait(bar(kBarPFull + 1), n & 1, wc))) break;
-                tc_fence_after();
+                __syncwarp();
+            }
+            if (!(ok = wait_all(kBarPFull + 1, n & 1))) break;
+            tc_fence_after();
+            if (leader) {
                 issue_pv(1, st, n > 0);
                 tc_commit(bar(kBarVEmpty + st));
                 if (!more) tc_commit(bar(kBarOFull + 1));
@@ -294,10 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_commit(bar(kBarKEmpty + st1));
                 }
             }
-            // every MMA this CTA issued has finished before TMEM is released
-            tc_commit(bar(kBarDone));
-            mbar_wait_drain(bar(kBarDone), 0, wc);
+            __syncwarp();
         }
+        // every MMA this CTA issued has finished before TMEM is released
+        if (leader) tc_commit(bar(kBarDone));
+        __syncwarp();
+        mbar_wait_drain(bar(kBarDone), 0, wc);
         __syncwarp();
     } else if (warp >= 4) {
         // ----------------------------------------------------------- softmax
@@ -337,36 +366,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 128; ++c) sv[c] = (c > lim) ? -INFINITY : sv[c];
             }
 
-            float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+            float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
+            float mx2 = fmaxf(sv[4], sv[5]), mx3 = fmaxf(sv[6], sv[7]);
 #pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-                mx0 = fmaxf(mx0, sv[c]);
-                mx1 = fmaxf(mx1, sv[c + 1]);
-                mx2 = fmaxf(mx2, sv[c + 2]);
-                mx3 = fmaxf(mx3, sv[c + 3]);
+            for (int c = 8; c < 128; c += 8) {
+                mx0 = fmax3(mx0, sv[c], sv[c + 1]);
+                mx1 = fmax3(mx1, sv[c + 2], sv[c + 3]);
+                mx2 = fmax3(mx2, sv[c + 4], sv[c + 5]);
+                mx3 = fmax3(mx3, sv[c + 6], sv[c + 7]);
             }
-            const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
             const float m_new = fmaxf(m, m_blk);
             const bool raise = m_new > m + kRescaleThreshold;   // always on the first finite block
             const float m_ref = raise ? m_new : m;
             const float alpha = raise ? ex2(m - m_ref) : 1.f;    // ex2(-inf) = 0
             const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-            float sum0 = 0.f, sum1 = 0.f;
+            // p = 2^(s * scale*log2(e) - m_ref) for column pairs (packed fp32 FMA and
+            // adds), packed to bf16 pairs and written over S as the A operand of P V.
+            const uint64_t scale2 = f2pack(sl2, sl2), negm2 = f2pack(neg_m, neg_m);
+            uint64_t sum_a = 0, sum_b = 0;
+            uint32_t pk[64];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2(fmaf(sv[64 * half + 2 * i], sl2, neg_m));
-                    const float p1 = ex2(fmaf(sv[64 * half + 2 * i + 1], sl2, neg_m));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(tS + 32 * half, pk);
+            for (int i = 0; i < 64; ++i) {
+                float x0, x1;
+                f2unpack(ffma2(f2pack(sv[2 * i], sv[2 * i + 1]), scale2, negm2), x0, x1);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                if (i & 1) sum_b = fadd2(sum_b, f2pack(p0, p1));
+                else sum_a = fadd2(sum_a, f2pack(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
             }
-            l = l * alpha + (sum0 + sum1);
+            tmem_st64(tS, pk);
+            float sa0, sa1;
+            f2unpack(fadd2(sum_a, sum_b), sa0, sa1);
+            l = l * alpha + (sa0 + sa1);
             m = m_ref;
 
             // O was last written by P V of the previous block, which finished
