@@ -22,7 +22,10 @@
 //   cannot keep the tensor pipe fed).
 //   warps 4-7   softmax of query tile 0; warps 8-11 softmax of query tile 1.
 //               One thread per query row (TMEM lane): row max, exp2, row sum,
-//               P packed to bf16 back into TMEM over S, O rescale when needed.
+//               P packed to bf16 back into TMEM over S in two 64-key halves
+//               (each half released to the MMA issuer on its own barrier, so the
+//               first half's P V overlaps the second half's exponentials), O
+//               rescale when needed.
 // The two tiles ping-pong: while one tile's softmax runs, the tensor core
 // computes the other tile's P V and next S.
 //
@@ -73,10 +76,10 @@ enum : int {
     kBarVFull = 5,   // +stage
     kBarVEmpty = 7,  // +stage
     kBarSFull = 9,   // +tile
-    kBarPFull = 11,  // +tile
-    kBarOFull = 13,  // +tile
-    kBarDone = 15,
-    kBarCount = 16
+    kBarPFull = 11,  // +2*tile +half: P columns of keys [0,64) and [64,128)
+    kBarOFull = 15,  // +tile
+    kBarDone = 17,
+    kBarCount = 18
 };
 
 struct Params {
@@ -166,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarVFull + i), 1);
             mbar_init(bar(kBarVEmpty + i), 1);
             mbar_init(bar(kBarSFull + i), 1);
-            mbar_init(bar(kBarPFull + i), kRows);
+            mbar_init(bar(kBarPFull + 2 * i), kRows);
+            mbar_init(bar(kBarPFull + 2 * i + 1), kRows);
             mbar_init(bar(kBarOFull + i), 1);
         }
         mbar_init(bar(kBarDone), 1);
@@ -262,13 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_ss(d_t, a0 + off, b0 + off, kIdescQK, k > 0 ? 1u : 0u);
             }
         };
-        // O_tq += P_tq V: P (128 x 128 keys, bf16 pairs) sits in TMEM over S_tq.
-        auto issue_pv = [&](int tq, int st, bool acc) {
+        // O_tq += P_tq V for keys [64 half, 64 half + 64): P (bf16 pairs) sits in TMEM
+        // over S_tq, 32 columns per half.
+        auto issue_pv = [&](int tq, int st, int half, bool acc) {
             const uint32_t d_t = tmem + Lay::col_o(tq);
-            const uint32_t pa = tmem + Lay::col_s(tq);
-            const uint64_t b0 = dv + st * kTileU;
+            const uint32_t pa = tmem + Lay::col_s(tq) + 32 * half;
+            const uint64_t b0 = dv + st * kTileU + ((half * 64 * 128) >> 4);
 #pragma unroll
-            for (int k = 0; k < kKeys / 16; ++k)
+            for (int k = 0; k < 4; ++k)
                 mma_ts(d_t, pa + k * 8, b0 + ((k * 2048) >> 4), kIdescPV, (acc || k > 0) ? 1u : 0u);
         };
         auto wait_all = [&](int idx, uint32_t parity) {
@@ -295,8 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph1 = ((n + 1) >> 1) & 1;
             if (!(ok = wait_all(kBarVFull + st, ph) && wait_all(kBarPFull + 0, n & 1))) break;
             tc_fence_after();
+            if (leader) issue_pv(0, st, 0, n > 0);
+            __syncwarp();
+            if (!(ok = wait_all(kBarPFull + 1, n & 1))) break;
+            tc_fence_after();
             if (leader) {
-                issue_pv(0, st, n > 0);
+                issue_pv(0, st, 1, true);
                 if (!more) tc_commit(bar(kBarOFull + 0));
             }
             __syncwarp();
@@ -309,10 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            if (!(ok = wait_all(kBarPFull + 1, n & 1))) break;
+            if (!(ok = wait_all(kBarPFull + 2, n & 1))) break;
+            tc_fence_after();
+            if (leader) issue_pv(1, st, 0, n > 0);
+            __syncwarp();
+            if (!(ok = wait_all(kBarPFull + 3, n & 1))) break;
             tc_fence_after();
             if (leader) {
-                issue_pv(1, st, n > 0);
+                issue_pv(1, st, 1, true);
                 tc_commit(bar(kBarVEmpty + st));
                 if (!more) tc_commit(bar(kBarOFull + 1));
                 if (more) {
@@ -383,39 +396,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
             // p = 2^(s * scale*log2(e) - m_ref) for column pairs (packed fp32 FMA and
-            // adds), packed to bf16 pairs and written over S as the A operand of P V.
+            // adds), packed to bf16 pairs and written over S as the A operand of P V,
+            // in two halves of 64 keys so that the first half's P V overlaps the
+            // second half's exponentials.
             const uint64_t scale2 = f2pack(sl2, sl2), negm2 = f2pack(neg_m, neg_m);
             uint64_t sum_a = 0, sum_b = 0;
-            uint32_t pk[64];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                float x0, x1;
-                f2unpack(ffma2(f2pack(sv[2 * i], sv[2 * i + 1]), scale2, negm2), x0, x1);
-                const float p0 = ex2(x0), p1 = ex2(x1);
-                if (i & 1) sum_b = fadd2(sum_b, f2pack(p0, p1));
-                else sum_a = fadd2(sum_a, f2pack(p0, p1));
-                pk[i] = pack_bf16x2(p0, p1);
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = 64 * half + 2 * i;
+                    float x0, x1;
+                    f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), scale2, negm2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    if (i & 1) sum_b = fadd2(sum_b, f2pack(p0, p1));
+                    else sum_a = fadd2(sum_a, f2pack(p0, p1));
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + 32 * half, pk);
+                // O was last written by P V of the previous block, which finished
+                // before this block's S (same issuing thread, in order); it is rescaled
+                // before this block's first P V can start accumulating into it.
+                if (half == 0 && n > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32 * c, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                        tmem_st32(tO + 32 * c, o);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(kBarPFull + 2 * tq + half));
             }
-            tmem_st64(tS, pk);
             float sa0, sa1;
             f2unpack(fadd2(sum_a, sum_b), sa0, sa1);
             l = l * alpha + (sa0 + sa1);
             m = m_ref;
-
-            // O was last written by P V of the previous block, which finished
-            // before this block's S (same issuing thread, in order).
-            if (n > 0 && __any_sync(0xffffffffu, raise)) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + 32 * c, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-                    tmem_st32(tO + 32 * c, o);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(bar(kBarPFull + tq));
         }
 
         if (ok) {
