@@ -9,12 +9,12 @@
  *   them.  All calls are asynchronous on `stream` (NULL = the legacy default
  *   stream) and never synchronise the host, except ra_check_status().
  * - Sequence tensors are contiguous row-major [B, L, H, D] (batch, sequence,
- *   head, head dim), the layout of the verify script on the juejin page
- *   "ring attention 没做通信" (section 三: "q/k/v: (B, S, H, D)").  lse tensors
- *   are fp32 [B, L, H], natural logarithm (same page, section 五).
+ *   head, head dim), the layout of the verify script in the juejin.cn article
+ *   on debugging a ring-attention library (section 三: batch, sequence, head, head dim).
+ *   lse tensors are fp32 [B, L, H], natural logarithm (same article, section 五).
  * - Virtual shard r (0 <= r < P) is the token range [r*L/P, (r+1)*L/P); L must be
- *   divisible by P ("序列并行与 Ring Attention", section 6.4; the Ulysses
- *   guideline page on aitangshan.cn, section 四, on divisibility by cp_size).
+ *   divisible by P ("序列并行与 Ring Attention", section 6.4; "Finalize
+ *   Guidelines for Ulysses based context parallel attention", section 四).
  * - Argument errors are detected on the host before anything is launched and
  *   reported through the return value; nothing is written in that case.
  *   Launch failures return RA_ERR_CUDA.  Kernels that give up waiting (a
@@ -89,7 +89,7 @@ ra_status ring_attn_fwd_trace(const void* q, const void* k, const void* v, void*
 
 /*
  * attn_merge_partials -- log-sum-exp merge of two partial attention results
- * over disjoint key sets (the `combine` of the juejin page, section 四):
+ * over disjoint key sets (the `combine` of the juejin.cn ring-attention article, section 四):
  *   lse_out = ln(e^lse_a + e^lse_b)
  *   o_out   = o_a * e^(lse_a - lse_out) + o_b * e^(lse_b - lse_out)
  * A partial with lse = -inf (it saw no key) gets weight 0; if both are -inf,

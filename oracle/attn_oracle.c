@@ -8,8 +8,8 @@
  * Every routine is the plain definition written out, in double precision,
  * with no blocking, fusion or reordering beyond what the cited passage states.
  * Tensors are contiguous row-major [B, L, H, D] (batch, sequence, head, head
- * dim), as in the verify script of "把一个扩散模型...ring attention 没做通信"
- * (juejin, section 三, "q/k/v: (B, S, H, D)"); lse is [B, L, H], natural log
+ * dim), as in the verify script of the juejin.cn ring-attention debugging
+ * article (section 三); lse is [B, L, H], natural log
  * (same page, section 五, local_attn_lse returns lse of shape (B, Sq, H)).
  *
  * Routines:
