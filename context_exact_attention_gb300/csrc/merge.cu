@@ -9,7 +9,8 @@
 // group's first lane writes the merged lse.  Reading before the warp barrier
 // and writing after it keeps in-place merges (lse_out == lse_a) race-free;
 // each output vector is written by the thread that read it, so o_out == o_a
-// is race-free as well.
+// is race-free as well.  Each lane keeps four rows' loads in flight, and the
+// grid is one resident wave (occupancy query).
 #include <cuda_bf16.h>
 
 #include "ra_device.cuh"
@@ -66,6 +67,8 @@ __device__ __forceinline__ uint4 combine_vec_f32(uint4 x, uint4 y, float wa, flo
     return res;
 }
 
+constexpr int kRowsInFlight = 4;   // row groups per lane group per iteration
+
 template <bool kBf16>
 __global__ void __launch_bounds__(kBlock)
     merge_kernel(const uint4* o_a, const float* lse_a, const uint4* o_b, const float* lse_b,
@@ -77,22 +80,94 @@ __global__ void __launch_bounds__(kBlock)
     const int sub = lane & (G - 1);
     const long long warp_global = (static_cast<long long>(blockIdx.x) * kBlock + threadIdx.x) >> 5;
     const long long n_warps = (static_cast<long long>(gridDim.x) * kBlock) >> 5;
-    for (long long base = warp_global * rows_per_warp; base < rows; base += n_warps * rows_per_warp) {
-        const long long row = base + (lane >> group_log2);
-        const bool valid = row < rows;
-        Weights w{0.f, 0.f, -INFINITY};
-        if (valid) {
-            w = merge_weights(lse_a[row], lse_b[row]);
-            const long long off = row * vpr;
-            for (int c = sub; c < vpr; c += G) {
-                const uint4 x = o_a[off + c];
-                const uint4 y = o_b[off + c];
-                o_out[off + c] = kBf16 ? combine_vec_bf16(x, y, w.wa, w.wb)
-                                       : combine_vec_f32(x, y, w.wa, w.wb);
+    const long long step = n_warps * rows_per_warp;   // rows covered by one sweep of all warps
+    for (long long base = warp_global * rows_per_warp; base < rows; base += kRowsInFlight * step) {
+        long long row[kRowsInFlight];
+        bool valid[kRowsInFlight];
+        Weights w[kRowsInFlight];
+#pragma unroll
+        for (int u = 0; u < kRowsInFlight; ++u) {
+            row[u] = base + u * step + (lane >> group_log2);
+            valid[u] = row[u] < rows;
+            w[u] = Weights{0.f, 0.f, -INFINITY};
+        }
+        // issue every load of the kRowsInFlight rows before any arithmetic
+        float la[kRowsInFlight], lb[kRowsInFlight];
+#pragma unroll
+        for (int u = 0; u < kRowsInFlight; ++u) {
+            la[u] = valid[u] ? lse_a[row[u]] : 0.f;
+            lb[u] = valid[u] ? lse_b[row[u]] : 0.f;
+        }
+        for (int c = sub; c < vpr; c += G) {
+            uint4 x[kRowsInFlight], y[kRowsInFlight];
+#pragma unroll
+            for (int u = 0; u < kRowsInFlight; ++u) {
+                if (valid[u]) {
+                    x[u] = __ldcs(o_a + row[u] * vpr + c);
+                    y[u] = __ldcs(o_b + row[u] * vpr + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kRowsInFlight; ++u) {
+                if (!valid[u]) continue;
+                if (c == sub) w[u] = merge_weights(la[u], lb[u]);
+                __stcs(o_out + row[u] * vpr + c, kBf16 ? combine_vec_bf16(x[u], y[u], w[u].wa, w[u].wb)
+                                                       : combine_vec_f32(x[u], y[u], w[u].wa, w[u].wb));
             }
         }
         __syncwarp();
-        if (valid && sub == 0) lse_out[row] = w.lse;
+#pragma unroll
+        for (int u = 0; u < kRowsInFlight; ++u)
+            if (valid[u] && sub == 0) lse_out[row[u]] = merge_weights(la[u], lb[u]).lse;
+        __syncwarp();
+    }
+}
+
+// Fast path for rows of 1, 2, 4, 8, 16 or 32 vectors: thread v of a sweep owns
+// 16-byte vector v, four sweeps in flight per thread.  Consecutive vectors of a
+// row land on consecutive lanes of one warp (sweeps start on multiples of 32),
+// so reading both lse values before the __syncwarp() and writing lse_out after
+// it keeps in-place merges race-free here too.
+constexpr int kFlatUnroll = 4;
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kBlock)
+    merge_flat_kernel(const uint4* o_a, const float* lse_a, const uint4* o_b, const float* lse_b,
+                      uint4* o_out, float* lse_out, long long n_vec, int log2_vpr)
+{
+    const long long stride = static_cast<long long>(gridDim.x) * kBlock;
+    const long long vpr_mask = (1ll << log2_vpr) - 1;
+    for (long long v0 = static_cast<long long>(blockIdx.x) * kBlock + threadIdx.x;
+         v0 - threadIdx.x % 32 < n_vec; v0 += kFlatUnroll * stride) {
+        long long v[kFlatUnroll];
+        bool valid[kFlatUnroll];
+        float la[kFlatUnroll], lb[kFlatUnroll];
+        uint4 x[kFlatUnroll], y[kFlatUnroll];
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) {
+            v[u] = v0 + u * stride;
+            valid[u] = v[u] < n_vec;
+            if (valid[u]) {
+                const long long row = v[u] >> log2_vpr;
+                la[u] = lse_a[row];
+                lb[u] = lse_b[row];
+                x[u] = __ldcs(o_a + v[u]);
+                y[u] = __ldcs(o_b + v[u]);
+            }
+        }
+        float lse_new[kFlatUnroll];
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) {
+            if (!valid[u]) continue;
+            const Weights w = merge_weights(la[u], lb[u]);
+            lse_new[u] = w.lse;
+            __stcs(o_out + v[u], kBf16 ? combine_vec_bf16(x[u], y[u], w.wa, w.wb)
+                                       : combine_vec_f32(x[u], y[u], w.wa, w.wb));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u)
+            if (valid[u] && (v[u] & vpr_mask) == 0) lse_out[v[u] >> log2_vpr] = lse_new[u];
         __syncwarp();
     }
 }
@@ -108,13 +183,40 @@ cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, c
     while ((1 << group_log2) < vpr && group_log2 < 5) ++group_log2;
     const long long rows_per_warp = 32 >> group_log2;
     const long long warps_needed = (rows + rows_per_warp - 1) / rows_per_warp;
-    int dev = 0, sms = 148;
+    int dev = 0, sms = 148, per_sm = 1;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (elem_bytes == 2)
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, merge_kernel<true>, kBlock, 0);
+    else
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, merge_kernel<false>, kBlock, 0);
     long long blocks = (warps_needed * 32 + kBlock - 1) / kBlock;
-    const long long cap = static_cast<long long>(sms) * 8;   // 8 resident blocks of 256 per SM
+    const long long cap = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);  // one resident wave
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    if (vpr <= 32 && (vpr & (vpr - 1)) == 0) {
+        int log2_vpr = 0;
+        while ((1 << log2_vpr) < vpr) ++log2_vpr;
+        const long long n_vec = rows * vpr;
+        int fast_per_sm = 1;
+        if (elem_bytes == 2)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fast_per_sm, merge_flat_kernel<true>, kBlock, 0);
+        else
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fast_per_sm, merge_flat_kernel<false>, kBlock, 0);
+        long long fblocks = (n_vec + kBlock - 1) / kBlock;
+        const long long fcap = static_cast<long long>(sms) * (fast_per_sm > 0 ? fast_per_sm : 1);
+        if (fblocks > fcap) fblocks = fcap;
+        if (fblocks < 1) fblocks = 1;
+        if (elem_bytes == 2)
+            merge_flat_kernel<true><<<static_cast<unsigned>(fblocks), kBlock, 0, stream>>>(
+                static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b), lse_b,
+                static_cast<uint4*>(o_out), lse_out, n_vec, log2_vpr);
+        else
+            merge_flat_kernel<false><<<static_cast<unsigned>(fblocks), kBlock, 0, stream>>>(
+                static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b), lse_b,
+                static_cast<uint4*>(o_out), lse_out, n_vec, log2_vpr);
+        return cudaGetLastError();
+    }
     if (elem_bytes == 2)
         merge_kernel<true><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
             static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b), lse_b,

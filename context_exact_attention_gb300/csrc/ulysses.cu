@@ -8,6 +8,8 @@
 // a time (index math once per chunk), its lanes stream each chunk's 16-byte
 // vectors: all loads of the four chunks are issued before their stores, reads
 // and writes are coalesced, and the data is touched once (streaming hints).
+// The grid is one resident wave (occupancy query); index math is 32-bit when
+// the buffer has fewer than 2^31 vectors.
 #include "ra_device.cuh"
 #include "ra_internal.h"
 
@@ -17,11 +19,12 @@ namespace {
 constexpr int kBlock = 256;
 constexpr int kBatch = 4;   // chunks in flight per warp
 
+template <typename I>
 struct PermuteGeom {
-    long long n_chunks;    // chunks in the whole buffer
-    long long cv;          // 16-byte vectors per chunk (Hg * D * elem / 16)
-    long long hv;          // vectors per position on the sequence side (H * D * elem / 16)
-    long long B, L, Ls, P;
+    I n_chunks;    // chunks in the whole buffer
+    I cv;          // 16-byte vectors per chunk (Hg * D * elem / 16)
+    I hv;          // vectors per position on the sequence side (H * D * elem / 16)
+    I B, L, Ls, P;
 };
 
 // Output chunk ch -> first vector of its source chunk.
@@ -29,45 +32,46 @@ struct PermuteGeom {
 //                        source = ((r*B + b)*Ls + l)*hv + g*cv.
 //   dir 1 (head -> seq): ch = ((r*B + b)*Ls + l)*P + g;
 //                        source = ((g*B + b)*L + r*Ls + l)*cv.
-template <int kDir>
-__device__ __forceinline__ long long source_chunk(long long ch, const PermuteGeom& g)
+template <int kDir, typename I>
+__device__ __forceinline__ I source_chunk(I ch, const PermuteGeom<I>& g)
 {
     if (kDir == 0) {
-        const long long lg = ch % g.L;
-        const long long gb = ch / g.L;
-        const long long b = gb % g.B;
-        const long long grp = gb / g.B;
-        const long long r = lg / g.Ls, l = lg - r * g.Ls;
+        const I gb = ch / g.L;
+        const I lg = ch - gb * g.L;
+        const I grp = gb / g.B;
+        const I b = gb - grp * g.B;
+        const I r = lg / g.Ls, l = lg - r * g.Ls;
         return ((r * g.B + b) * g.Ls + l) * g.hv + grp * g.cv;
     } else {
-        const long long grp = ch % g.P;
-        const long long rbl = ch / g.P;
-        const long long l = rbl % g.Ls;
-        const long long rb = rbl / g.Ls;
-        const long long b = rb % g.B;
-        const long long r = rb / g.B;
+        const I rbl = ch / g.P;
+        const I grp = ch - rbl * g.P;
+        const I rb = rbl / g.Ls;
+        const I l = rbl - rb * g.Ls;
+        const I r = rb / g.B;
+        const I b = rb - r * g.B;
         return ((grp * g.B + b) * g.L + r * g.Ls + l) * g.cv;
     }
 }
 
-template <int kDir>
+// I is the index type of vectors (32-bit when the whole buffer has < 2^31 vectors).
+template <int kDir, typename I>
 __global__ void __launch_bounds__(kBlock)
-    permute_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, PermuteGeom g)
+    permute_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, PermuteGeom<I> g)
 {
     const int lane = threadIdx.x & 31;
-    const long long warp_global = (static_cast<long long>(blockIdx.x) * kBlock + threadIdx.x) >> 5;
-    const long long n_warps = (static_cast<long long>(gridDim.x) * kBlock) >> 5;
-    for (long long ch0 = warp_global; ch0 < g.n_chunks; ch0 += kBatch * n_warps) {
-        long long src[kBatch], dst[kBatch];
+    const I warp_global = static_cast<I>((blockIdx.x * kBlock + threadIdx.x) >> 5);
+    const I n_warps = static_cast<I>((gridDim.x * kBlock) >> 5);
+    for (I ch0 = warp_global; ch0 < g.n_chunks; ch0 += kBatch * n_warps) {
+        I src[kBatch], dst[kBatch];
         bool live[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const long long ch = ch0 + u * n_warps;
+            const I ch = ch0 + u * n_warps;
             live[u] = ch < g.n_chunks;
-            src[u] = live[u] ? source_chunk<kDir>(ch, g) : 0;
+            src[u] = live[u] ? source_chunk<kDir>(ch, g) : I(0);
             dst[u] = ch * g.cv;
         }
-        for (long long c = lane; c < g.cv; c += 32) {
+        for (I c = lane; c < g.cv; c += 32) {
             uint4 x[kBatch];
 #pragma unroll
             for (int u = 0; u < kBatch; ++u)
@@ -79,34 +83,44 @@ __global__ void __launch_bounds__(kBlock)
     }
 }
 
+template <int kDir, typename I>
+cudaError_t launch_typed(const void* in, void* out, int B, int L, int H, int D, int P,
+                         int elem_bytes, cudaStream_t stream)
+{
+    PermuteGeom<I> g;
+    g.B = B;
+    g.L = L;
+    g.P = P;
+    g.Ls = L / P;
+    g.cv = static_cast<I>(static_cast<long long>(H / P) * D * elem_bytes / 16);
+    g.hv = static_cast<I>(static_cast<long long>(H) * D * elem_bytes / 16);
+    g.n_chunks = static_cast<I>(static_cast<long long>(B) * L * P);
+    int dev = 0, sms = 148, per_sm = 1;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_kernel<kDir, I>, kBlock, 0);
+    const long long warps_needed = (static_cast<long long>(g.n_chunks) + kBatch - 1) / kBatch;
+    long long blocks = (warps_needed * 32 + kBlock - 1) / kBlock;
+    const long long cap = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);  // one resident wave
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    permute_kernel<kDir, I><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
+        static_cast<const uint4*>(in), static_cast<uint4*>(out), g);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_ulysses_permute(const void* in, void* out, int B, int L, int H, int D, int P,
                                    int elem_bytes, int dir, cudaStream_t stream)
 {
-    PermuteGeom g;
-    g.B = B;
-    g.L = L;
-    g.P = P;
-    g.Ls = L / P;
-    g.cv = static_cast<long long>(H / P) * D * elem_bytes / 16;
-    g.hv = static_cast<long long>(H) * D * elem_bytes / 16;
-    g.n_chunks = static_cast<long long>(B) * L * P;   // B*L positions x P groups, either side
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long warps_needed = (g.n_chunks + kBatch - 1) / kBatch;
-    long long blocks = (warps_needed * 32 + kBlock - 1) / kBlock;
-    const long long cap = static_cast<long long>(sms) * 8;   // 8 resident blocks of 256 per SM
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+    const long long total_vec = static_cast<long long>(B) * L * H * D * elem_bytes / 16;
+    const bool small = total_vec < (1ll << 30);   // headroom for the grid-stride steps
     if (dir == 0)
-        permute_kernel<0><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
-            static_cast<const uint4*>(in), static_cast<uint4*>(out), g);
-    else
-        permute_kernel<1><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
-            static_cast<const uint4*>(in), static_cast<uint4*>(out), g);
-    return cudaGetLastError();
+        return small ? launch_typed<0, int>(in, out, B, L, H, D, P, elem_bytes, stream)
+                     : launch_typed<0, long long>(in, out, B, L, H, D, P, elem_bytes, stream);
+    return small ? launch_typed<1, int>(in, out, B, L, H, D, P, elem_bytes, stream)
+                 : launch_typed<1, long long>(in, out, B, L, H, D, P, elem_bytes, stream);
 }
 
 }  // namespace ra

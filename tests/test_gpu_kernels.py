@@ -183,7 +183,7 @@ def _partials(rows, D, dtype, seed, n_inf=0):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("rows,D", [(1000, 128), (37, 64), (5, 8), (4096, 256)])
+@pytest.mark.parametrize("rows,D", [(1000, 128), (37, 64), (5, 8), (4096, 256), (99, 40)])
 def test_merge_matches_oracle(dtype, rows, D):
     if dtype == torch.bfloat16 and D == 8:
         D = 16
