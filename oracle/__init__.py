@@ -21,6 +21,8 @@ computes, and the passage it follows:
   section 四).
 * :func:`seq2head` / :func:`head2seq` -- Ulysses all-to-all layout transposes
   (section 3.5), as byte copies.
+* :func:`attention_bwd` -- gradients dQ, dK, dV of the attention output by the
+  chain rule (the backward of sections 3.3 and 6.2, summed on one device).
 
 Every pin of these routines is in ``tests/test_oracle.py``.
 """
@@ -68,6 +70,9 @@ def _load():
             lib.oracle_ring_attention.restype = ctypes.c_int
             lib.oracle_merge.argtypes = [dp, dp, dp, dp, dp, dp, L, L]
             lib.oracle_merge.restype = ctypes.c_int
+            lib.oracle_attention_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, L, L, L, L,
+                                                 ctypes.c_int, ctypes.c_int]
+            lib.oracle_attention_bwd.restype = ctypes.c_int
             for name in ("oracle_seq2head", "oracle_head2seq"):
                 fn = getattr(lib, name)
                 fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, L, L, L, L, L, L]
@@ -160,6 +165,23 @@ def local_only(q, k, v, P: int, causal: bool = False, threads: int | None = None
                          k_pos0=r * Ls, threads=threads)
         out[:, sl], lse[:, sl] = o, l
     return out, lse
+
+
+def attention_bwd(q, k, v, dout, causal: bool = False, threads: int | None = None):
+    """Gradients (dq, dk, dv) of O = attention(q, k, v) for the upstream gradient dout.
+
+    All [B, L, H, D]; small L only (two L x L matrices per (batch, head)).
+    """
+    lib = _load()
+    q, k, v, dout = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    B, L, H, D = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and dout.shape == q.shape
+    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    rc = lib.oracle_attention_bwd(_dp(q), _dp(k), _dp(v), _dp(dout), _dp(dq), _dp(dk), _dp(dv),
+                                  B, L, H, D, int(bool(causal)), threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd failed ({rc})")
+    return dq, dk, dv
 
 
 def merge(o_a, lse_a, o_b, lse_b):

@@ -352,3 +352,93 @@ int oracle_head2seq(const void* in, void* out, long B, long L, long H, long D,
                     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* backward: gradients of the attention output                               */
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    double *dq, *dk, *dv;
+    long B, L, H, D;
+    int causal;
+} bwd_ctx_t;
+
+/*
+ * One (batch, head): the chain rule through O = softmax(S) V with
+ * S = Q K^T / sqrt(D) (masked entries excluded):
+ *   dV = P^T dO,  dP = dO V^T,  dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik),
+ *   dQ = dS K / sqrt(D),  dK = dS^T Q / sqrt(D).
+ * The backward that "序列并行与 Ring Attention" (sections 3.3 and 6.2) describes
+ * recomputes the probabilities from the saved row statistics and returns dK, dV
+ * to the shard that owns K, V; on one device that is this same sum.
+ * scratch: P (L*L) then dP (L*L).
+ */
+static void bwd_item(void* vctx, long item, double* scratch)
+{
+    const bwd_ctx_t* c = (const bwd_ctx_t*)vctx;
+    const long L = c->L, H = c->H, D = c->D;
+    const long h = item % H, b = item / H;
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+    double* P = scratch;
+    double* dP = scratch + L * L;
+#define AT(t, i) ((t) + ((b * L + (i)) * H + h) * D)
+    for (long i = 0; i < L; ++i) {
+        double m = -INFINITY;
+        for (long j = 0; j < L; ++j) {
+            if (c->causal && j > i) { P[i * L + j] = -INFINITY; continue; }
+            double s = 0.0;
+            for (long d = 0; d < D; ++d) s += AT(c->q, i)[d] * AT(c->k, j)[d];
+            s *= inv_sqrt_d;
+            P[i * L + j] = s;
+            if (s > m) m = s;
+        }
+        double den = 0.0;
+        for (long j = 0; j < L; ++j) {
+            P[i * L + j] = (P[i * L + j] == -INFINITY) ? 0.0 : exp(P[i * L + j] - m);
+            den += P[i * L + j];
+        }
+        for (long j = 0; j < L; ++j) P[i * L + j] /= den;
+    }
+    for (long i = 0; i < L; ++i)
+        for (long j = 0; j < L; ++j) {
+            double s = 0.0;
+            for (long d = 0; d < D; ++d) s += AT(c->dout, i)[d] * AT(c->v, j)[d];
+            dP[i * L + j] = s;
+        }
+    /* dS overwrites dP */
+    for (long i = 0; i < L; ++i) {
+        double rowdot = 0.0;
+        for (long j = 0; j < L; ++j) rowdot += P[i * L + j] * dP[i * L + j];
+        for (long j = 0; j < L; ++j) dP[i * L + j] = P[i * L + j] * (dP[i * L + j] - rowdot);
+    }
+    for (long i = 0; i < L; ++i)
+        for (long d = 0; d < D; ++d) {
+            double s = 0.0;
+            for (long j = 0; j < L; ++j) s += dP[i * L + j] * AT(c->k, j)[d];
+            AT(c->dq, i)[d] = s * inv_sqrt_d;
+        }
+    for (long j = 0; j < L; ++j)
+        for (long d = 0; d < D; ++d) {
+            double sk = 0.0, sv = 0.0;
+            for (long i = 0; i < L; ++i) {
+                sk += dP[i * L + j] * AT(c->q, i)[d];
+                sv += P[i * L + j] * AT(c->dout, i)[d];
+            }
+            AT(c->dk, j)[d] = sk * inv_sqrt_d;
+            AT(c->dv, j)[d] = sv;
+        }
+#undef AT
+}
+
+/* Gradients of O = attention(Q, K, V) against an upstream gradient dO.
+ * All tensors [B, L, H, D]; meant for small L (keeps two L x L matrices per thread). */
+int oracle_attention_bwd(const double* q, const double* k, const double* v, const double* dout,
+                         double* dq, double* dk, double* dv,
+                         long B, long L, long H, long D, int causal, int n_threads)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 0 || L < 0 || H < 0 || D <= 0) return -1;
+    bwd_ctx_t c = { q, k, v, dout, dq, dk, dv, B, L, H, D, causal };
+    long n_items = B * H;
+    if (n_items == 0 || L == 0) return 0;
+    return run_pool(bwd_item, &c, n_items, 2 * L * L, n_threads);
+}

@@ -372,3 +372,68 @@ def test_divisibility_errors():
                               np.zeros((1, 10, 1, 2)), 3)
     with pytest.raises(ValueError):
         oracle.seq2head(np.zeros((4, 1, 2, 6, 2)), 4)
+
+
+# -- backward (gradients) ----------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences(causal):
+    """dq, dk, dv are the gradient of the scalar sum(O * dO): central differences on a
+    tiny problem (brute force, independent of the chain-rule code)."""
+    B, L, H, D = 1, 5, 2, 3
+    q, k, v, do = (_rand((B, L, H, D), 60 + i) for i in range(4))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal=causal)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attention(q_, k_, v_, causal=causal, threads=1)
+        return float((o * do).sum())
+
+    eps = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (loss(**{k_ + "_": a for k_, a in args_p.items()})
+                        - loss(**{k_ + "_": a for k_, a in args_m.items()})) / (2 * eps)
+        np.testing.assert_allclose(g, num, rtol=0, atol=1e-7, err_msg=name)
+
+
+def test_backward_matches_torch_autograd():
+    """fp64 torch autograd of softmax(q k^T / sqrt(D)) v (a library route)."""
+    torch = pytest.importorskip("torch")
+    B, L, H, D = 2, 13, 3, 8
+    q, k, v, do = (_rand((B, L, H, D), 70 + i) for i in range(4))
+    for causal in (False, True):
+        tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+        s = torch.einsum("bihd,bjhd->bhij", tq, tk) / math.sqrt(D)
+        if causal:
+            s = s.masked_fill(torch.ones(L, L, dtype=torch.bool).triu(1), float("-inf"))
+        o = torch.einsum("bhij,bjhd->bihd", torch.softmax(s, dim=-1), tv)
+        o.backward(torch.tensor(do))
+        dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal=causal)
+        np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_closed_forms(causal):
+    """Rows of P sum to 1, so sum_j dV_j = sum_i dO_i; rows of dS sum to 0, so
+    sum_j dK_j = 0; dO = 0 gives zero gradients."""
+    B, L, H, D = 1, 11, 2, 4
+    q, k, v, do = (_rand((B, L, H, D), 80 + i) for i in range(4))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal=causal)
+    np.testing.assert_allclose(dv.sum(axis=1), do.sum(axis=1), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, rtol=0, atol=1e-12)
+    z = oracle.attention_bwd(q, k, v, np.zeros_like(do), causal=causal)
+    assert all(np.all(g == 0) for g in z)
+    if causal:
+        # the last key is visible to the last query only, so its dv is a multiple of dO
+        # of that query (the multiple is that query's weight on it)
+        cross = np.cross(dv[0, L - 1, 0, :3], do[0, L - 1, 0, :3])
+        assert np.abs(cross).max() < 1e-12
