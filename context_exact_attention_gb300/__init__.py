@@ -21,7 +21,8 @@ from . import workloads  # noqa: F401  (seeded inputs; no attention arithmetic)
 __all__ = [
     "RingAttnError", "library_path", "load_library", "ring_attn_fwd", "ring_attn_fwd_f32",
     "ring_attn_fwd_trace", "attn_merge_partials", "ulysses_seq2head", "ulysses_head2seq",
-    "ulysses_attention", "check_status", "probe_wait_timeout", "EXPORTED_SYMBOLS",
+    "ulysses_attention", "ring_attn_bwd", "check_status", "probe_wait_timeout",
+    "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -36,7 +37,7 @@ _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned",
 EXPORTED_SYMBOLS = (
     "ring_attn_fwd", "ring_attn_fwd_f32", "ring_attn_fwd_trace", "attn_merge_partials",
     "ulysses_seq2head", "ulysses_head2seq", "ra_check_status", "ra_status_string",
-    "ra_probe_wait_timeout",
+    "ra_probe_wait_timeout", "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
 )
 
 
@@ -74,11 +75,15 @@ def load_library(build_if_missing: bool = False):
             "ulysses_head2seq": [vp, vp, i, i, i, i, i, i, vp],
             "ra_check_status": [vp],
             "ra_probe_wait_timeout": [ctypes.c_ulonglong, vp],
+            "ring_attn_bwd": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
+                              i, i, i, i, i, i, vp],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        lib.ring_attn_bwd_workspace_bytes.argtypes = [i, i, i]
+        lib.ring_attn_bwd_workspace_bytes.restype = ctypes.c_ulonglong
         lib.ra_status_string.argtypes = [ctypes.c_int]
         lib.ra_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -223,6 +228,32 @@ def ulysses_attention(q_seq, k_seq, v_seq, P: int, stream=None, buffers=None):
     ring_attn_fwd(qh.view(shape), kh.view(shape), vh.view(shape), P=1, causal=False,
                   out=buffers["o"].view(shape), want_lse=False, stream=stream)
     return ulysses_head2seq(buffers["o"], P, stream=stream)
+
+
+def ring_attn_bwd(q, k, v, out, lse, dout, P: int = 1, causal: bool = False, dq=None, dk=None,
+                  dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of ring_attn_fwd for the upstream gradient dout (bf16).
+
+    out and lse are the forward's results for the same q, k, v, P, causal.  The
+    workspace (fp32, one value per query row) is allocated with torch if not given."""
+    _check_qkv(q, k, v, torch.bfloat16)
+    for name, t in (("out", out), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    B, L, H, D = q.shape
+    if lse is None or lse.dtype != torch.float32 or tuple(lse.shape) != (B, L, H):
+        raise ValueError("lse must be the forward's fp32 [B, L, H] tensor")
+    lib = load_library()
+    need = lib.ring_attn_bwd_workspace_bytes(B, L, H)
+    if workspace is None:
+        workspace = torch.empty(max(1, need // 4), dtype=torch.float32, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _call("ring_attn_bwd", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+          _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, L,
+          H, D, P, int(bool(causal)), _stream(stream))
+    return dq, dk, dv
 
 
 def check_status(stream=None) -> int:

@@ -269,6 +269,63 @@ ra_status ulysses_head2seq(const void* in, void* out, int B, int L, int H, int D
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+unsigned long long ring_attn_bwd_workspace_bytes(int B, int L, int H)
+{
+    if (B < 1 || L < 1 || H < 1) return 0;
+    return static_cast<unsigned long long>(B) * L * H * sizeof(float);
+}
+
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        void* workspace, unsigned long long workspace_bytes, int B, int L, int H,
+                        int D, int P, int causal, ra_stream_t stream)
+{
+    unsigned long long n = 0;
+    ra_status st = check_attn(q, k, v, out, lse, B, L, H, D, P, 2, &n);
+    if (st != RA_OK) return st;
+    if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
+    if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+        !aligned(workspace, 16))
+        return RA_ERR_MISALIGNED;
+    const unsigned long long ws = ring_attn_bwd_workspace_bytes(B, L, H);
+    if (workspace_bytes < ws) return RA_ERR_INVALID_ARG;
+    const unsigned long long bytes = n * 2;
+    const void* ins[6] = {q, k, v, out, dout, lse};
+    const unsigned long long in_bytes[6] = {bytes, bytes, bytes, bytes, bytes, ws};
+    void* outs[4] = {dq, dk, dv, workspace};
+    const unsigned long long out_bytes[4] = {bytes, bytes, bytes, ws};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 6; ++j)
+            if (overlap(outs[i], out_bytes[i], ins[j], in_bytes[j])) return RA_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(outs[i], out_bytes[i], outs[j], out_bytes[j])) return RA_ERR_INVALID_ARG;
+    }
+    ra::BwdArgs a;
+    a.out = out;
+    a.dout = dout;
+    a.lse = lse;
+    a.dvec = static_cast<float*>(workspace);
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.L = L;
+    a.H = H;
+    a.D = D;
+    a.P = P;
+    a.causal = causal ? 1 : 0;
+    a.timeout_ns = kWaitLimitNs;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    st = status_word(&a.status);
+    if (st != RA_OK) return st;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, H, D) ||
+        !encode_qkv_map(&tv, v, B, L, H, D) || !encode_qkv_map(&tdo, dout, B, L, H, D))
+        return RA_ERR_CUDA;
+    return from_cuda(ra::launch_attn_bwd_bf16(a, tq, tk, tv, tdo));
+}
+
 ra_status ra_check_status(ra_stream_t stream)
 {
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -31,6 +31,24 @@ cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tmap_q,
 // fp32 SIMT kernel.
 cudaError_t launch_attn_f32(const AttnArgs& a);
 
+// Backward (bf16): Dvec into the workspace, then the dK/dV and dQ kernels.
+struct BwdArgs {
+    const void* out;     // forward output O
+    const void* dout;    // upstream gradient dO
+    const float* lse;    // forward lse [B, L, H]
+    float* dvec;         // workspace [B, L, H]
+    void* dq;
+    void* dk;
+    void* dv;
+    int B, L, H, D, P, causal;
+    unsigned int* status;
+    unsigned long long timeout_ns;
+    cudaStream_t stream;
+};
+cudaError_t launch_attn_bwd_bf16(const BwdArgs& a, const CUtensorMap& tmap_q,
+                                 const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                 const CUtensorMap& tmap_do);
+
 cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                          void* o_out, float* lse_out, long long rows, int D, int elem_bytes,
                          cudaStream_t stream);

@@ -129,6 +129,36 @@ ra_status ulysses_head2seq(const void* in, void* out, int B, int L, int H, int D
                            int elem_bytes, ra_stream_t stream);
 
 /*
+ * ring_attn_bwd_workspace_bytes -- bytes of device workspace ring_attn_bwd needs
+ * for a [B, L, H] problem (one fp32 per query row); 0 for invalid sizes.
+ */
+unsigned long long ring_attn_bwd_workspace_bytes(int B, int L, int H);
+
+/*
+ * ring_attn_bwd -- gradients of ring_attn_fwd (bf16).  With S = q k^T / sqrt(D),
+ * P = softmax(S) under the same visibility rule as the forward, and the upstream
+ * gradient dout:
+ *   dv = P^T dout,  dS = P o (dout v^T - rowsum(dout o out)),
+ *   dq = dS k / sqrt(D),  dk = dS^T q / sqrt(D).
+ * P is recomputed from the forward's lse rather than stored; each K/V block meets
+ * the query shards in ring order (r = (s + t) mod P, shards before s skipped under
+ * causal masking) and its dk, dv are written once, to the rows of the shard that
+ * owns it ("序列并行与 Ring Attention", sections 3.3 and 6.2).
+ *
+ * q, k, v, out, dout: device bf16 [B, L, H, D] (out and lse as ring_attn_fwd
+ *                     produced them for these q, k, v, P, causal);
+ * lse:                device fp32 [B, L, H];
+ * dq, dk, dv:         device bf16 [B, L, H, D] outputs, overlapping nothing;
+ * workspace:          device scratch of at least ring_attn_bwd_workspace_bytes
+ *                     (contents need no initialisation; overwritten).
+ * D must be 64 or 128; all pointers 16-byte aligned.  Deterministic (no atomics).
+ */
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        void* workspace, unsigned long long workspace_bytes, int B, int L, int H,
+                        int D, int P, int causal, ra_stream_t stream);
+
+/*
  * ra_check_status -- synchronise `stream`, then read and clear the status word
  * of the current device.  Returns RA_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last check, RA_ERR_CUDA if the stream reports an

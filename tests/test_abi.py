@@ -16,7 +16,7 @@ HEADER = os.path.join(ROOT, "include", "ring_attn.h")
 def declared_functions():
     text = open(HEADER, encoding="utf-8").read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w \t*]*?[ \t*](\w+)\s*\(", text, flags=re.M)))
 
 
 @pytest.fixture(scope="module")
