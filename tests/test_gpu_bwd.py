@@ -1,12 +1,19 @@
 """GPU parity of the backward (dq, dk, dv) against the fp64 gradient oracle.
 
-Tolerance.  Each gradient element is an fp32-accumulated sum whose terms carry
-one bf16 rounding of P or dS (unit roundoff u = 2^-9) plus the bf16 rounding of
-the stored forward output inside Dvec, and the result is rounded to bf16 once
-more; errors of independent terms add in quadrature while a gradient can cancel
-to far below its terms (dk sums to zero over the keys).  So the bar is
-norm-wise: ||got - ref|| <= 4u ||ref|| per tensor (u = 2^-9), cosine > 0.9999,
-and element-wise |got - ref| <= 4u |ref| + 8u rms(ref).
+Tolerance.  A first-order rounding bound, element by element.  Every gradient
+element is a sum of terms whose bf16 operands carry one rounding each (unit
+roundoff u = 2^-9): dq_i = sum_j dS_ij k_j / sqrt(D) and dk_j = sum_i dS_ij q_i /
+sqrt(D) with dS rounded; dv_j = sum_i P_ij dO_i with P rounded; and every dS_ij
+of row i also carries the error of Dvec_i = dO_i . O_i computed from the bf16
+output O, |dDvec_i| <= u sum_d |dO_id O_id|.  Accumulation is fp32 (negligible)
+and the result is rounded to bf16 once.  So, with magnitudes taken from exact
+fp64 quantities,
+  |err(dq_id)| <= u |dq_id| + u sum_j (|dS_ij| + P_ij u^-1 |dDvec_i|) |k_jd| / sqrt(D)
+and likewise for dk (sum over queries, q) and dv (sum_i P_ij |dO_id|).  The test
+allows twice that, plus 1e-6.  Early causal query rows, which sum a few large
+and cancelling terms, are where the term magnitudes matter: there an error of
+several times the result's own rounding is still exact arithmetic on bf16
+operands.  Norm-wise, ||got - ref|| <= 4u ||ref|| and cosine > 0.9999.
 """
 import numpy as np
 import pytest
@@ -22,14 +29,39 @@ DEV = "cuda:0"
 U = 2.0 ** -9
 
 
-def _grad_close(got, ref, what):
+def _term_scales(q, k, v, do, causal):
+    """Magnitude sums of the terms behind each gradient element (see the module
+    docstring), from fp64 copies of the inputs: an error scale, not a reference."""
+    q, k, v, do = (np.asarray(t.float().numpy(), np.float64) for t in (q, k, v, do))
+    B, L, H, D = q.shape
+    sq, sk, sv = np.zeros_like(q), np.zeros_like(q), np.zeros_like(q)
+    c = 1.0 / np.sqrt(D)
+    for b in range(B):
+        for h in range(H):
+            qq, kk, vv, dd = q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h]
+            s = qq @ kk.T * c
+            if causal:
+                s = np.where(np.tril(np.ones((L, L), bool)), s, -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            dp = dd @ vv.T
+            o = p @ vv
+            ds = p * (dp - (dd * o).sum(axis=1, keepdims=True))
+            ddvec = np.abs(dd * o).sum(axis=1, keepdims=True)          # |dDvec_i| / u
+            w = np.abs(ds) + p * ddvec
+            sq[b, :, h] = w @ np.abs(kk) * c
+            sk[b, :, h] = w.T @ np.abs(qq) * c
+            sv[b, :, h] = p.T @ np.abs(dd)
+    return sq, sk, sv
+
+
+def _grad_close(got, ref, what, scale):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert np.isfinite(got).all(), what
     err = np.abs(got - ref)
-    rms = np.sqrt((ref * ref).mean())
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
-    worst = (err / (4 * U * np.abs(ref) + 8 * U * rms)).max()
+    worst = (err / (2 * U * (np.abs(ref) + scale) + 1e-6)).max()
     print(f"{what}: rel_l2 {rel:.2e} cos {cosine(got, ref):.7f} worst/bound {worst:.3f}")
     assert rel <= 4 * U, (what, rel)
     assert cosine(got, ref) > 0.9999, what
@@ -59,9 +91,10 @@ def test_bwd_parity(case, causal):
     dq, dk, dv = cea.ring_attn_bwd(qd, kd, vd, out, lse, dod, P=P, causal=causal)
     assert cea.check_status() == 0
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=causal)
-    _grad_close(to_np(dq), rq, "dq")
-    _grad_close(to_np(dk), rk, "dk")
-    _grad_close(to_np(dv), rv, "dv")
+    sq, sk, sv = _term_scales(q, k, v, do, causal)
+    _grad_close(to_np(dq), rq, "dq", sq)
+    _grad_close(to_np(dk), rk, "dk", sk)
+    _grad_close(to_np(dv), rv, "dv", sv)
 
 
 def test_bwd_deterministic_and_spread_scores():
@@ -76,8 +109,9 @@ def test_bwd_deterministic_and_spread_scores():
     for a, b in zip(first, again):
         assert torch.equal(a, b)
     ref = oracle.attention_bwd(q, k, v, do, causal=True)
-    for name, got, r in zip(("dq", "dk", "dv"), first, ref):
-        _grad_close(to_np(got), r, name)
+    scales = _term_scales(q, k, v, do, True)
+    for name, got, r, sc in zip(("dq", "dk", "dv"), first, ref, scales):
+        _grad_close(to_np(got), r, name, sc)
 
 
 def test_bwd_argument_errors():
