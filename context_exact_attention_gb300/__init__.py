@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_fwd", "ring_attn_fwd_f32", "ring_attn_fwd_trace", "attn_merge_partials",
     "ulysses_seq2head", "ulysses_head2seq", "ra_check_status", "ra_status_string",
     "ra_probe_wait_timeout", "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
+    "ring_attn_bwd_noalloc",
 )
 
 
@@ -77,6 +78,7 @@ def load_library(build_if_missing: bool = False):
             "ra_probe_wait_timeout": [ctypes.c_ulonglong, vp],
             "ring_attn_bwd": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
                               i, i, i, i, i, i, vp],
+            "ring_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)

@@ -159,6 +159,31 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
                         int D, int P, int causal, ra_stream_t stream);
 
 /*
+ * ring_attn_bwd_noalloc -- ring_attn_bwd for callers that cannot allocate device
+ * memory (no counterpart on the pages: an addition of this library).
+ *
+ * Same operation, arguments, layout and errors as ring_attn_bwd, minus the
+ * workspace: it uses a fixed array compiled into the library instead, so it
+ * never calls cudaMalloc, cudaFree or any other allocating routine.  Meant for
+ * code that is handed only its tensors (plugins), runs inside a runtime that owns
+ * all device memory, or must not allocate after warm-up.
+ *
+ * Limits and sharing:
+ * - B*L*H must not exceed RA_BWD_NOALLOC_MAX_ROWS; larger problems return
+ *   RA_ERR_INVALID_ARG without launching anything (use ring_attn_bwd for them).
+ * - The array holds 4 MiB on every GPU that loads the library, until exit.
+ * - The first call on each device looks up the array's device address (with
+ *   that device current); later calls reuse it.
+ * - All calls on a device share the array; calls whose GPU work overlaps (for
+ *   example on different streams) race and must be ordered by the caller.
+ *   Nothing in it needs clearing: each call writes every row before reading it.
+ */
+#define RA_BWD_NOALLOC_MAX_ROWS 1048576ull
+ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                int B, int L, int H, int D, int P, int causal, ra_stream_t stream);
+
+/*
  * ra_check_status -- synchronise `stream`, then read and clear the status word
  * of the current device.  Returns RA_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last check, RA_ERR_CUDA if the stream reports an
