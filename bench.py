@@ -9,7 +9,8 @@ so no flush is needed between steps.
 
 Also measured in the same run (the "rows" object): the diffusion-DiT full
 attention workload (40 calls), the LSE merge at the causal-LM size, the Ulysses
-transposes and pipeline, and the long-context causal workload.
+transposes and pipeline, the backward of the causal-LM workload, and the
+long-context causal workload.
 
 --impl reference times the fp64 CPU oracle (the only reference this project
 has) on the host cores, on a bounded sample of query rows of the same workload.
@@ -407,6 +408,24 @@ def measure_rows(cea, dev, stream, peaks):
                                "frac": fl / (ms * 1e-3) / 1e12 / peak,
                                "note": "3 seq2head + attention (B'=16, H'=4, P=1) + head2seq"}
     del x, y, qs, ks, vs, bufs
+
+    # backward of the headline workload (dq, dk, dv): algorithmic FLOPs are 2.5x the
+    # forward's (five D-length products per visible pair)
+    w = LM
+    q, k, v = (t.to(dev) for t in make_workload_inputs(w, seed=0))
+    do = torch.randn(q.shape, device=dev, generator=g).to(torch.bfloat16)
+    out, lse = cea.ring_attn_fwd(q, k, v, P=w.P, causal=True)
+    ws = torch.empty(w.B * w.L * w.H, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    f = lambda: cea.ring_attn_bwd(q, k, v, out, lse, do, P=w.P, causal=True, dq=dq, dk=dk, dv=dv,
+                                  workspace=ws, stream=stream)
+    f()
+    ms = _time_loop(f, 3, stream) / 3
+    fl = 2.5 * attention_flops(w.B, w.L, w.H, w.D, True)
+    res["lm_backward"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                          "frac": fl / (ms * 1e-3) / 1e12 / peak,
+                          "note": "row dots + dK/dV kernel + dQ kernel; 2.5x forward FLOPs"}
+    del q, k, v, do, out, lse, ws, dq, dk, dv
 
     # long-context causal
     w = LONG
