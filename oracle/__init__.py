@@ -65,6 +65,9 @@ def _load():
             lib.oracle_attention.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, ctypes.c_int,
                                              L, L, lp, L, ctypes.c_int]
             lib.oracle_attention.restype = ctypes.c_int
+            lib.oracle_attention_gqa.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, L,
+                                                 ctypes.c_int, L, L, lp, L, ctypes.c_int]
+            lib.oracle_attention_gqa.restype = ctypes.c_int
             lib.oracle_ring_attention.argtypes = [dp, dp, dp, dp, dp, L, L, L, L, L, ctypes.c_int,
                                                   ip, ctypes.c_int]
             lib.oracle_ring_attention.restype = ctypes.c_int
@@ -101,7 +104,9 @@ def _dp(a: np.ndarray):
 
 def attention(q, k, v, causal: bool = False, rows=None, q_pos0: int = 0, k_pos0: int = 0,
               threads: int | None = None):
-    """Naive attention.  q: [B, Lq, H, D], k/v: [B, Lk, H, D] (any float type, computed in fp64).
+    """Naive attention.  q: [B, Lq, H, D], k/v: [B, Lk, Hk, D] (any float type, computed in
+    fp64).  Hk may be smaller than H (grouped key/value heads): H must be a multiple of
+    Hk, and query head h reads key/value head h // (H // Hk).
 
     ``rows``: optional 1-D list of query rows to evaluate (the rest are not computed).
     Returns ``(out [B, n_rows, H, D], lse [B, n_rows, H])`` as fp64 numpy arrays.
@@ -109,8 +114,10 @@ def attention(q, k, v, causal: bool = False, rows=None, q_pos0: int = 0, k_pos0:
     lib = _load()
     q, k, v = to_f64(q), to_f64(k), to_f64(v)
     B, Lq, H, D = q.shape
-    Lk = k.shape[1]
-    assert k.shape == (B, Lk, H, D) and v.shape == (B, Lk, H, D)
+    Lk, Hk = k.shape[1], k.shape[2]
+    assert k.shape == (B, Lk, Hk, D) and v.shape == (B, Lk, Hk, D)
+    if H % Hk:
+        raise ValueError("query heads must be a multiple of key/value heads")
     if rows is None:
         n_rows, rows_p = Lq, None
     else:
@@ -119,9 +126,9 @@ def attention(q, k, v, causal: bool = False, rows=None, q_pos0: int = 0, k_pos0:
         rows_p = rows_a.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
     out = np.empty((B, n_rows, H, D), dtype=np.float64)
     lse = np.empty((B, n_rows, H), dtype=np.float64)
-    rc = lib.oracle_attention(_dp(q), _dp(k), _dp(v), _dp(out), _dp(lse), B, Lq, Lk, H, D,
-                              int(bool(causal)), q_pos0, k_pos0, rows_p, n_rows,
-                              threads or default_threads())
+    rc = lib.oracle_attention_gqa(_dp(q), _dp(k), _dp(v), _dp(out), _dp(lse), B, Lq, Lk, H, Hk,
+                                  D, int(bool(causal)), q_pos0, k_pos0, rows_p, n_rows,
+                                  threads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_attention failed ({rc})")
     return out, lse

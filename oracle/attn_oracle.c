@@ -96,6 +96,7 @@ typedef struct {
     const double *q, *k, *v;
     double *out, *lse;
     long B, Lq, Lk, H, D;
+    long Hk;                 /* key/value heads; query head h reads key/value head h / (H / Hk) */
     int causal;
     long q_pos0, k_pos0;     /* global position of q row 0 / key 0 */
     const long* rows;        /* query rows to evaluate (indices into Lq), or NULL for all */
@@ -112,6 +113,7 @@ static void attn_item(void* vctx, long item, double* w)
     const long bh = item / c->n_rows;
     const long h = bh % H, b = bh / H;
     const long i = c->rows ? c->rows[ri] : ri;
+    const long hk = h / (H / c->Hk);
     const long q_pos = c->q_pos0 + i;
     const double inv_sqrt_d = 1.0 / sqrt((double)D);
     const double* qrow = c->q + ((b * c->Lq + i) * H + h) * D;
@@ -119,7 +121,7 @@ static void attn_item(void* vctx, long item, double* w)
     double m = -INFINITY;
     for (long j = 0; j < c->Lk; ++j) {
         if (c->causal && c->k_pos0 + j > q_pos) { w[j] = -INFINITY; continue; }
-        const double* krow = c->k + ((b * c->Lk + j) * H + h) * D;
+        const double* krow = c->k + ((b * c->Lk + j) * c->Hk + hk) * D;
         double s = 0.0;
         for (long d = 0; d < D; ++d) s += qrow[d] * krow[d];
         s *= inv_sqrt_d;
@@ -143,7 +145,7 @@ static void attn_item(void* vctx, long item, double* w)
     for (long d = 0; d < D; ++d) acc[d] = 0.0;
     for (long j = 0; j < c->Lk; ++j) {
         if (w[j] == 0.0) continue;
-        const double* vrow = c->v + ((b * c->Lk + j) * H + h) * D;
+        const double* vrow = c->v + ((b * c->Lk + j) * c->Hk + hk) * D;
         for (long d = 0; d < D; ++d) acc[d] += w[j] * vrow[d];
     }
     for (long d = 0; d < D; ++d) orow[d] = acc[d] / den;
@@ -151,25 +153,40 @@ static void attn_item(void* vctx, long item, double* w)
 }
 
 /*
- * out: [B, n_rows, H, D]; lse: [B, n_rows, H].
+ * out: [B, n_rows, H, D]; lse: [B, n_rows, H].  q: [B, Lq, H, D]; k, v: [B, Lk, Hk, D].
  * rows == NULL means every query row (n_rows must equal Lq).
  * Query row i sits at global position q_pos0 + i, key j at k_pos0 + j; under
  * causal masking key j is visible to row i iff its position <= the row's.
+ * Grouped key/value heads ("序列并行与 Ring Attention", sections 3.5 and 6.4 count
+ * them apart from the query heads): H must be a multiple of Hk, and the H / Hk
+ * consecutive query heads h = g*(H/Hk) .. (g+1)*(H/Hk) - 1 share key/value head g.
  */
+int oracle_attention_gqa(const double* q, const double* k, const double* v,
+                         double* out, double* lse,
+                         long B, long Lq, long Lk, long H, long Hk, long D, int causal,
+                         long q_pos0, long k_pos0,
+                         const long* rows, long n_rows, int n_threads)
+{
+    if (!q || !k || !v || !out || !lse || B < 0 || Lq < 0 || Lk < 0 || H < 0 || D <= 0) return -1;
+    if (Hk <= 0 || (H > 0 && H % Hk != 0)) return -2;
+    if (!rows) n_rows = Lq;
+    if (n_rows < 0) return -1;
+    if (rows) for (long i = 0; i < n_rows; ++i) if (rows[i] < 0 || rows[i] >= Lq) return -1;
+    attn_ctx_t c = { q, k, v, out, lse, B, Lq, Lk, H, D, Hk, causal, q_pos0, k_pos0, rows, n_rows };
+    long n_items = B * H * n_rows;
+    if (n_items == 0) return 0;
+    return run_pool(attn_item, &c, n_items, (Lk > 0 ? Lk : 1) + D, n_threads);
+}
+
+/* The same with as many key/value heads as query heads. */
 int oracle_attention(const double* q, const double* k, const double* v,
                      double* out, double* lse,
                      long B, long Lq, long Lk, long H, long D, int causal,
                      long q_pos0, long k_pos0,
                      const long* rows, long n_rows, int n_threads)
 {
-    if (!q || !k || !v || !out || !lse || B < 0 || Lq < 0 || Lk < 0 || H < 0 || D <= 0) return -1;
-    if (!rows) n_rows = Lq;
-    if (n_rows < 0) return -1;
-    if (rows) for (long i = 0; i < n_rows; ++i) if (rows[i] < 0 || rows[i] >= Lq) return -1;
-    attn_ctx_t c = { q, k, v, out, lse, B, Lq, Lk, H, D, causal, q_pos0, k_pos0, rows, n_rows };
-    long n_items = B * H * n_rows;
-    if (n_items == 0) return 0;
-    return run_pool(attn_item, &c, n_items, (Lk > 0 ? Lk : 1) + D, n_threads);
+    return oracle_attention_gqa(q, k, v, out, lse, B, Lq, Lk, H, H > 0 ? H : 1, D, causal,
+                                q_pos0, k_pos0, rows, n_rows, n_threads);
 }
 
 /* ------------------------------------------------------------------------- */

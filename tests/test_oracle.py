@@ -437,3 +437,33 @@ def test_backward_closed_forms(causal):
         # of that query (the multiple is that query's weight on it)
         cross = np.cross(dv[0, L - 1, 0, :3], do[0, L - 1, 0, :3])
         assert np.abs(cross).max() < 1e-12
+
+
+# -- grouped key/value heads (GQA / MQA) ---------------------------------------------------------
+
+@pytest.mark.parametrize("Hk", [1, 2, 3, 6])
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_kv_heads_equal_repeated_heads(Hk, causal):
+    """H query heads over Hk key/value heads equal ordinary attention with each key/value
+    head repeated for its H/Hk consecutive query heads (numpy repeat); Hk = H is plain
+    attention and Hk = 1 is multi-query attention."""
+    B, L, H, D = 2, 19, 6, 5
+    q = _rand((B, L, H, D), 90)
+    k, v = _rand((B, L, Hk, D), 91), _rand((B, L, Hk, D), 92)
+    got, lg = oracle.attention(q, k, v, causal=causal)
+    rep = H // Hk
+    ref, lr = oracle.attention(q, np.repeat(k, rep, axis=2), np.repeat(v, rep, axis=2),
+                               causal=causal)
+    assert np.abs(got - ref).max() < 1e-15 and np.abs(lg - lr).max() < 1e-15
+    # each query head really uses its own group: scipy on head h with key head h // rep
+    for h in (0, H - 1):
+        s = q[0, :, h] @ k[0, :, h // rep].T / math.sqrt(D)
+        if causal:
+            s = np.where(np.tril(np.ones((L, L), bool)), s, -np.inf)
+        np.testing.assert_allclose(got[0, :, h], scipy.special.softmax(s, 1) @ v[0, :, h // rep],
+                                   rtol=1e-13, atol=1e-13)
+
+
+def test_grouped_kv_heads_must_divide():
+    with pytest.raises(ValueError):
+        oracle.attention(np.zeros((1, 4, 6, 2)), np.zeros((1, 4, 4, 2)), np.zeros((1, 4, 4, 2)))
