@@ -409,6 +409,22 @@ def measure_rows(cea, dev, stream, peaks):
                                "note": "3 seq2head + attention (B'=16, H'=4, P=1) + head2seq"}
     del x, y, qs, ks, vs, bufs
 
+    # grouped key/value heads at the headline shape: 32 query heads over 8 key/value heads
+    w = LM
+    q, _, _ = (t.to(dev) for t in make_workload_inputs(w, seed=0))
+    kk = torch.randn(w.B, w.L, 8, w.D, device=dev, generator=g).to(torch.bfloat16)
+    vv = torch.randn(w.B, w.L, 8, w.D, device=dev, generator=g).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.L, w.H), dtype=torch.float32, device=dev)
+    f = lambda: cea.ring_attn_fwd_gqa(q, kk, vv, P=w.P, causal=True, out=out, lse=lse,
+                                      stream=stream)
+    f()
+    ms = _time_loop(f, 5, stream) / 5
+    fl = attention_flops(w.B, w.L, w.H, w.D, True)
+    res["lm_gqa_32q_8kv"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                             "frac": fl / (ms * 1e-3) / 1e12 / peak}
+    del q, kk, vv, out, lse
+
     # backward of the headline workload (dq, dk, dv): algorithmic FLOPs are 2.5x the
     # forward's (five D-length products per visible pair)
     w = LM

@@ -21,7 +21,8 @@ from . import workloads  # noqa: F401  (seeded inputs; no attention arithmetic)
 __all__ = [
     "RingAttnError", "library_path", "load_library", "ring_attn_fwd", "ring_attn_fwd_f32",
     "ring_attn_fwd_trace", "attn_merge_partials", "ulysses_seq2head", "ulysses_head2seq",
-    "ulysses_attention", "ring_attn_bwd", "check_status", "probe_wait_timeout",
+    "ulysses_attention", "ring_attn_bwd", "ring_attn_fwd_gqa", "check_status",
+    "probe_wait_timeout",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -38,7 +39,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_fwd", "ring_attn_fwd_f32", "ring_attn_fwd_trace", "attn_merge_partials",
     "ulysses_seq2head", "ulysses_head2seq", "ra_check_status", "ra_status_string",
     "ra_probe_wait_timeout", "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
-    "ring_attn_bwd_noalloc",
+    "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa",
 )
 
 
@@ -79,6 +80,7 @@ def load_library(build_if_missing: bool = False):
             "ring_attn_bwd": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
                               i, i, i, i, i, i, vp],
             "ring_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
+            "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -107,7 +109,7 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _check_qkv(q, k, v, dtype):
+def _check_qkv(q, k, v, dtype, grouped=False):
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
@@ -115,7 +117,11 @@ def _check_qkv(q, k, v, dtype):
             raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
         if t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous [B, L, H, D] tensor")
-    if not (q.shape == k.shape == v.shape):
+    if grouped:
+        if k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[1] != q.shape[1] \
+                or k.shape[3] != q.shape[3]:
+            raise ValueError("k, v must be [B, L, H_kv, D] matching q's B, L, D")
+    elif not (q.shape == k.shape == v.shape):
         raise ValueError("q, k, v must have the same shape")
 
 
@@ -150,6 +156,26 @@ def ring_attn_fwd_f32(q, k, v, P: int = 1, causal: bool = False, out=None, lse=N
     """fp32 ring attention forward (SIMT path).  Returns (out, lse)."""
     return _attn("ring_attn_fwd_f32", q, k, v, P, causal, out, lse, want_lse, torch.float32,
                  stream)
+
+
+def ring_attn_fwd_gqa(q, k, v, P: int = 1, causal: bool = False, out=None, lse=None,
+                      want_lse: bool = True, stream=None):
+    """Ring attention forward with grouped key/value heads: q [B, L, H, D], k and v
+    [B, L, H_kv, D] (bf16 or fp32), query head h reading key/value head h // (H // H_kv).
+    Returns (out, lse)."""
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q must be bf16 or fp32")
+    _check_qkv(q, k, v, dtype, grouped=True)
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, L, H), dtype=torch.float32, device=q.device)
+    _call("ring_attn_fwd_gqa", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, H, Hkv, D,
+          P, int(bool(causal)), RA_BF16 if dtype == torch.bfloat16 else RA_F32, _stream(stream))
+    return out, lse
 
 
 def ring_attn_fwd_trace(q, k, v, P: int = 1, causal: bool = False, stream=None):
@@ -217,18 +243,27 @@ def ulysses_head2seq(x, P: int, out=None, stream=None):
 def ulysses_attention(q_seq, k_seq, v_seq, P: int, stream=None, buffers=None):
     """Ulysses path: seq->head transpose of q, k, v; full non-causal attention per head
     group (the head-sharded buffer is a [P*B, L, H/P, D] batch); head->seq transpose of
-    the output.  Inputs [P, B, L/P, H, D] bf16.  Returns the output in the same layout."""
+    the output.  Inputs [P, B, L/P, H, D] bf16 (k, v may have H_kv < H heads, with
+    H_kv divisible by P as well).  Returns the output in the same layout."""
     Pp, B, Ls, H, D = q_seq.shape
-    L, Hg = Ls * P, H // P
+    Hkv = k_seq.shape[3]
+    L, Hg, Hkg = Ls * P, H // P, Hkv // P
+    if Hkv % P:
+        raise ValueError("key/value heads must be divisible by P for the Ulysses transpose")
     if buffers is None:
-        buffers = {n: torch.empty((P, B, L, Hg, D), dtype=q_seq.dtype, device=q_seq.device)
-                   for n in ("q", "k", "v", "o")}
+        buffers = {n: torch.empty((P, B, L, Hkg if n in ("k", "v") else Hg, D), dtype=q_seq.dtype,
+                                  device=q_seq.device) for n in ("q", "k", "v", "o")}
     qh = ulysses_seq2head(q_seq, P, out=buffers["q"], stream=stream)
     kh = ulysses_seq2head(k_seq, P, out=buffers["k"], stream=stream)
     vh = ulysses_seq2head(v_seq, P, out=buffers["v"], stream=stream)
-    shape = (P * B, L, Hg, D)
-    ring_attn_fwd(qh.view(shape), kh.view(shape), vh.view(shape), P=1, causal=False,
-                  out=buffers["o"].view(shape), want_lse=False, stream=stream)
+    shape, kv_shape = (P * B, L, Hg, D), (P * B, L, Hkg, D)
+    if Hkv == H:
+        ring_attn_fwd(qh.view(shape), kh.view(shape), vh.view(shape), P=1, causal=False,
+                      out=buffers["o"].view(shape), want_lse=False, stream=stream)
+    else:
+        ring_attn_fwd_gqa(qh.view(shape), kh.view(kv_shape), vh.view(kv_shape), P=1,
+                          causal=False, out=buffers["o"].view(shape), want_lse=False,
+                          stream=stream)
     return ulysses_head2seq(buffers["o"], P, stream=stream)
 
 

@@ -86,26 +86,30 @@ bool overlap(const void* a, unsigned long long na, const void* b, unsigned long 
 
 ra_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
 
-// Shared checks of the attention entry points.  elem: element bytes.
+// Shared checks of the attention entry points.  elem: element bytes; Hkv: key/value
+// heads (k and v are [B, L, Hkv, D]; H must be a multiple of Hkv).
 ra_status check_attn(const void* q, const void* k, const void* v, const void* out,
                      const float* lse, int B, int L, int H, int D, int P, int elem,
-                     unsigned long long* elems)
+                     unsigned long long* elems, int Hkv = -1)
 {
+    if (Hkv < 0) Hkv = H;
     if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
-    if (B < 1 || L < 1 || H < 1 || D < 1 || P < 1) return RA_ERR_INVALID_ARG;
+    if (B < 1 || L < 1 || H < 1 || D < 1 || P < 1 || Hkv < 1) return RA_ERR_INVALID_ARG;
     const unsigned long long n = static_cast<unsigned long long>(B) * L * H * D;
     if (n >= (1ull << 40)) return RA_ERR_INVALID_ARG;
-    if (L % P != 0) return RA_ERR_NOT_DIVISIBLE;
+    if (L % P != 0 || H % Hkv != 0) return RA_ERR_NOT_DIVISIBLE;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
         return RA_ERR_MISALIGNED;
     if (lse && !aligned(lse, 4)) return RA_ERR_MISALIGNED;
     const unsigned long long bytes = n * elem;
-    if (overlap(out, bytes, q, bytes) || overlap(out, bytes, k, bytes) || overlap(out, bytes, v, bytes))
+    const unsigned long long kv_bytes = static_cast<unsigned long long>(B) * L * Hkv * D * elem;
+    if (overlap(out, bytes, q, bytes) || overlap(out, bytes, k, kv_bytes) ||
+        overlap(out, bytes, v, kv_bytes))
         return RA_ERR_INVALID_ARG;
     if (lse) {
         const unsigned long long lb = static_cast<unsigned long long>(B) * L * H * 4;
-        if (overlap(lse, lb, q, bytes) || overlap(lse, lb, k, bytes) || overlap(lse, lb, v, bytes) ||
-            overlap(lse, lb, out, bytes))
+        if (overlap(lse, lb, q, bytes) || overlap(lse, lb, k, kv_bytes) ||
+            overlap(lse, lb, v, kv_bytes) || overlap(lse, lb, out, bytes))
             return RA_ERR_INVALID_ARG;
     }
     *elems = n;
@@ -114,12 +118,13 @@ ra_status check_attn(const void* q, const void* k, const void* v, const void* ou
 
 ra_status attn_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                     int L, int H, int D, int P, int causal, ra_dtype dtype, int* trace,
-                    cudaStream_t stream)
+                    cudaStream_t stream, int Hkv = -1)
 {
+    if (Hkv < 0) Hkv = H;
     if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_UNSUPPORTED;
     const int elem = dtype == RA_BF16 ? 2 : 4;
     unsigned long long n = 0;
-    ra_status st = check_attn(q, k, v, out, lse, B, L, H, D, P, elem, &n);
+    ra_status st = check_attn(q, k, v, out, lse, B, L, H, D, P, elem, &n, Hkv);
     if (st != RA_OK) return st;
     if (dtype == RA_BF16 && D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
     if (dtype == RA_F32 && (D % 4 != 0 || D > 256)) return RA_ERR_UNSUPPORTED;
@@ -141,14 +146,15 @@ ra_status attn_impl(const void* q, const void* k, const void* v, void* out, floa
     a.D = D;
     a.P = P;
     a.causal = causal ? 1 : 0;
+    a.Hkv = Hkv;
     a.timeout_ns = kWaitLimitNs;
     a.stream = stream;
     st = status_word(&a.status);
     if (st != RA_OK) return st;
     if (dtype == RA_F32) return from_cuda(ra::launch_attn_f32(a));
     CUtensorMap tq, tk, tv;
-    if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, H, D) ||
-        !encode_qkv_map(&tv, v, B, L, H, D))
+    if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, Hkv, D) ||
+        !encode_qkv_map(&tv, v, B, L, Hkv, D))
         return RA_ERR_CUDA;
     return from_cuda(ra::launch_attn_bf16(a, tq, tk, tv));
 }
@@ -224,6 +230,15 @@ ra_status ring_attn_fwd_trace(const void* q, const void* k, const void* v, void*
     if (!trace) return RA_ERR_INVALID_ARG;
     return attn_impl(q, k, v, out, lse, B, L, H, D, P, causal, dtype, trace,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* lse,
+                            int B, int L, int H, int H_kv, int D, int P, int causal,
+                            ra_dtype dtype, ra_stream_t stream)
+{
+    if (H_kv < 1) return RA_ERR_INVALID_ARG;
+    return attn_impl(q, k, v, out, lse, B, L, H, D, P, causal, dtype, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), H_kv);
 }
 
 ra_status attn_merge_partials(const void* o_a, const float* lse_a, const void* o_b,

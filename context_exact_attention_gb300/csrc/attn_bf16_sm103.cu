@@ -89,6 +89,7 @@ struct Params {
     unsigned int* status;
     unsigned long long timeout_ns;
     int B, L, H, P, Ls, causal;
+    int group;       // query heads per key/value head
     int n_kt;        // K/V blocks per shard
     int n_pair;      // query-tile pairs per shard
     float scale_log2;
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pair = p.n_pair - 1 - (u - (u / p.n_pair) * p.n_pair);
     const int b = bh / p.H;
     const int h = bh - b * p.H;
+    const int hk = h / p.group;                       // key/value head of this query head
     const int q0_local = pair * (kTiles * kRows);     // first query row of the pair, within shard
     const int q0 = r * p.Ls + q0_local;               // global
 
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kTileBytes);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
                     tma_load_4d(sbase + Lay::kK + st * Lay::kTileBytes + bx * 16384, &tmap_k,
-                                bar(kBarKFull + st), bx * 64, h, row, b, keep);
+                                bar(kBarKFull + st), bx * 64, hk, row, b, keep);
             }
             last_k[st] = n;
             if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc))) break;
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kTileBytes);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
                     tma_load_4d(sbase + Lay::kV + st * Lay::kTileBytes + bx * 16384, &tmap_v,
-                                bar(kBarVFull + st), bx * 64, h, row, b, keep);
+                                bar(kBarVFull + st), bx * 64, hk, row, b, keep);
             }
             last_v[st] = n;
         }
@@ -502,6 +504,7 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     p.P = a.P;
     p.Ls = a.L / a.P;
     p.causal = a.causal;
+    p.group = a.H / a.Hkv;
     p.n_kt = (p.Ls + kKeys - 1) / kKeys;
     p.n_pair = (p.n_kt + kTiles - 1) / kTiles;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     ring_attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                          const float* __restrict__ v, float* __restrict__ out,
                          float* __restrict__ lse, int* __restrict__ trace, int B, int L, int H,
-                         int D, int P, int causal, float scale)
+                         int Hkv, int D, int P, int causal, float scale)
 {
     __shared__ float qs[kWarps][kMaxD];
     const int warp = threadIdx.x >> 5;
@@ -64,8 +64,11 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int c = 0; c < kMaxD / 32; ++c) acc[c] = 0.f;
 
-    const float* kb = k + static_cast<size_t>(b) * L * row_stride + static_cast<size_t>(h) * D;
-    const float* vb = v + static_cast<size_t>(b) * L * row_stride + static_cast<size_t>(h) * D;
+    // key/value rows: Hkv heads per position; query head h reads head h / (H / Hkv)
+    const size_t kv_stride = static_cast<size_t>(Hkv) * D;
+    const int hk = h / (H / Hkv);
+    const float* kb = k + static_cast<size_t>(b) * L * kv_stride + static_cast<size_t>(hk) * D;
+    const float* vb = v + static_cast<size_t>(b) * L * kv_stride + static_cast<size_t>(hk) * D;
 
     for (int t = 0; t < P; ++t) {
         int s = r - t;
@@ -79,7 +82,7 @@ __global__ void __launch_bounds__(kWarps * 32)
             const int j = j0 + lane;
             float sc = -INFINITY;
             if (j < j_end) {
-                const float* krow = kb + static_cast<size_t>(j) * row_stride;
+                const float* krow = kb + static_cast<size_t>(j) * kv_stride;
                 float dot = 0.f;
                 for (int d = 0; d < D; d += 4) {
                     const float4 kk = *reinterpret_cast<const float4*>(krow + d);
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kWarps * 32)
             for (int c = 0; c < kMaxD / 32; ++c) acc[c] *= alpha;
             for (int jj = 0; jj < n_here; ++jj) {
                 const float pw = __shfl_sync(0xffffffffu, pj, jj);
-                const float* vrow = vb + static_cast<size_t>(j0 + jj) * row_stride;
+                const float* vrow = vb + static_cast<size_t>(j0 + jj) * kv_stride;
 #pragma unroll
                 for (int c = 0; c < kMaxD / 32; ++c) {
                     const int d = lane + 32 * c;
@@ -130,7 +133,7 @@ cudaError_t launch_attn_f32(const AttnArgs& a)
     ring_attn_f32_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, a.stream>>>(
         static_cast<const float*>(a.q), static_cast<const float*>(a.k),
         static_cast<const float*>(a.v), static_cast<float*>(a.out), a.lse, a.trace, a.B, a.L,
-        a.H, a.D, a.P, a.causal, 1.0f / sqrtf(static_cast<float>(a.D)));
+        a.H, a.Hkv, a.D, a.P, a.causal, 1.0f / sqrtf(static_cast<float>(a.D)));
     return cudaGetLastError();
 }
 

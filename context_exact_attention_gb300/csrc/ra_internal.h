@@ -18,6 +18,7 @@ struct AttnArgs {
     float* lse;      // may be null
     int* trace;      // may be null
     int B, L, H, D, P, causal;
+    int Hkv;                       // key/value heads (H for plain attention)
     unsigned int* status;          // device status word
     unsigned long long timeout_ns; // limit of one bounded wait
     cudaStream_t stream;

@@ -88,6 +88,19 @@ ra_status ring_attn_fwd_trace(const void* q, const void* k, const void* v, void*
                               int* trace, ra_stream_t stream);
 
 /*
+ * ring_attn_fwd_gqa -- ring_attn_fwd (dtype RA_BF16) or ring_attn_fwd_f32
+ * (RA_F32) with grouped key/value heads (GQA; MQA when H_kv == 1): q and out are
+ * [B, L, H, D], k and v are [B, L, H_kv, D], and the H / H_kv consecutive query
+ * heads h = g*(H/H_kv) .. (g+1)*(H/H_kv) - 1 all attend with key/value head g.
+ * "序列并行与 Ring Attention" (sections 3.5 and 6.4) counts key/value heads apart
+ * from query heads; the consecutive grouping is this library's reading.
+ * H % H_kv != 0 returns RA_ERR_NOT_DIVISIBLE.  Otherwise as ring_attn_fwd.
+ */
+ra_status ring_attn_fwd_gqa(const void* q, const void* k, const void* v, void* out, float* lse,
+                            int B, int L, int H, int H_kv, int D, int P, int causal,
+                            ra_dtype dtype, ra_stream_t stream);
+
+/*
  * attn_merge_partials -- log-sum-exp merge of two partial attention results
  * over disjoint key sets (the `combine` of the juejin.cn ring-attention article, section 四):
  *   lse_out = ln(e^lse_a + e^lse_b)

@@ -276,3 +276,59 @@ def test_bounded_wait_reports_timeout():
     q, k, v = _dev(*make_qkv(1, 256, 1, 128, seed=0, dtype=torch.bfloat16))
     cea.ring_attn_fwd(q, k, v, P=2)
     assert cea.check_status() == 0
+
+
+# ---------------------------------------------------------------- grouped K/V heads --
+
+GQA_CASES = [
+    # B, L, H, Hkv, D, P, dtype
+    (1, 512, 8, 1, 128, 4, torch.bfloat16),    # multi-query
+    (1, 512, 8, 2, 128, 4, torch.bfloat16),
+    (1, 1024, 8, 4, 128, 8, torch.bfloat16),
+    (2, 384, 6, 3, 64, 2, torch.bfloat16),     # shard of 192
+    (1, 96, 4, 2, 32, 3, torch.float32),
+    (2, 64, 6, 1, 16, 2, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", GQA_CASES, ids=lambda c: "B%dL%dH%dHkv%dD%dP%d" % c[:6])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_parity(case, causal):
+    B, L, H, Hkv, D, P, dtype = case
+    q, _, _ = make_qkv(B, L, H, D, seed=50, dtype=dtype)
+    _, k, v = make_qkv(B, L, Hkv, D, seed=51, dtype=dtype)
+    out, lse = cea.ring_attn_fwd_gqa(*_dev(q, k, v), P=P, causal=causal)
+    assert cea.check_status() == 0
+    ref, lref = oracle.attention(q, k, v, causal=causal)
+    check = assert_bf16_close if dtype == torch.bfloat16 else assert_f32_close
+    check(to_np(out), ref, "out")
+    check(to_np(lse), lref, "lse")
+    if Hkv == H or dtype == torch.float32:
+        return
+    # with every key/value head repeated for its query heads, plain attention agrees
+    rep = H // Hkv
+    full, _ = cea.ring_attn_fwd(*_dev(q, k.repeat_interleave(rep, 2).contiguous(),
+                                      v.repeat_interleave(rep, 2).contiguous()), P=P, causal=causal)
+    assert torch.equal(full, out)
+
+
+def test_gqa_ulysses_end_to_end():
+    """Ulysses with fewer key/value heads (H_kv divisible by P): the head-sharded key/value
+    buffer keeps H_kv/P heads per rank and each rank runs grouped attention."""
+    P, B, L, H, Hkv, D = 4, 2, 512, 8, 4, 128
+    q, _, _ = make_qkv(B, L, H, D, seed=52, dtype=torch.bfloat16)
+    _, k, v = make_qkv(B, L, Hkv, D, seed=53, dtype=torch.bfloat16)
+    Ls = L // P
+    to_seq = lambda t: torch.stack([t[:, r * Ls:(r + 1) * Ls] for r in range(P)]).contiguous()
+    o_seq = cea.ulysses_attention(*_dev(to_seq(q), to_seq(k), to_seq(v)), P)
+    ref, _ = oracle.attention(q, k, v)
+    got = to_np(o_seq)
+    assert_bf16_close(np.concatenate([got[r] for r in range(P)], axis=1), ref, "ulysses gqa")
+
+
+def test_gqa_argument_errors():
+    q, _, _ = (t.to(DEV) for t in make_qkv(1, 256, 6, 128, seed=0, dtype=torch.bfloat16))
+    _, k, v = (t.to(DEV) for t in make_qkv(1, 256, 4, 128, seed=0, dtype=torch.bfloat16))
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ring_attn_fwd_gqa(q, k, v, P=2)
+    assert e.value.code == 4
