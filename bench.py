@@ -425,6 +425,19 @@ def measure_rows(cea, dev, stream, peaks):
                              "frac": fl / (ms * 1e-3) / 1e12 / peak}
     del q, kk, vv, out, lse
 
+    # zigzag layout of the headline workload (shard r holds chunks r and 2P-1-r)
+    w = LM
+    q, k, v = (t.to(dev) for t in make_workload_inputs(w, seed=0))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.L, w.H), dtype=torch.float32, device=dev)
+    f = lambda: cea.ring_attn_fwd_zigzag(q, k, v, P=w.P, out=out, lse=lse, stream=stream)
+    f()
+    ms = _time_loop(f, 5, stream) / 5
+    fl = attention_flops(w.B, w.L, w.H, w.D, True)
+    res["lm_zigzag"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                        "frac": fl / (ms * 1e-3) / 1e12 / peak}
+    del q, k, v, out, lse
+
     # backward of the headline workload (dq, dk, dv): algorithmic FLOPs are 2.5x the
     # forward's (five D-length products per visible pair)
     w = LM

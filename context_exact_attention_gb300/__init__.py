@@ -21,7 +21,8 @@ from . import workloads  # noqa: F401  (seeded inputs; no attention arithmetic)
 __all__ = [
     "RingAttnError", "library_path", "load_library", "ring_attn_fwd", "ring_attn_fwd_f32",
     "ring_attn_fwd_trace", "attn_merge_partials", "ulysses_seq2head", "ulysses_head2seq",
-    "ulysses_attention", "ring_attn_bwd", "ring_attn_fwd_gqa", "check_status",
+    "ulysses_attention", "ring_attn_bwd", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
+    "zigzag_positions", "check_status",
     "probe_wait_timeout",
     "EXPORTED_SYMBOLS",
 ]
@@ -39,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_fwd", "ring_attn_fwd_f32", "ring_attn_fwd_trace", "attn_merge_partials",
     "ulysses_seq2head", "ulysses_head2seq", "ra_check_status", "ra_status_string",
     "ra_probe_wait_timeout", "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
-    "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa",
+    "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
 )
 
 
@@ -81,6 +82,7 @@ def load_library(build_if_missing: bool = False):
                               i, i, i, i, i, i, vp],
             "ring_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
             "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
+            "ring_attn_fwd_zigzag": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp, vp],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -176,6 +178,36 @@ def ring_attn_fwd_gqa(q, k, v, P: int = 1, causal: bool = False, out=None, lse=N
     _call("ring_attn_fwd_gqa", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, H, Hkv, D,
           P, int(bool(causal)), RA_BF16 if dtype == torch.bfloat16 else RA_F32, _stream(stream))
     return out, lse
+
+
+def zigzag_positions(L: int, P: int):
+    """Global position of every row of the zigzag layout (shard r holds chunks r and
+    2P-1-r of 2P chunks): a list of L ints.  Index bookkeeping only."""
+    c = L // (2 * P)
+    pos = []
+    for r in range(P):
+        pos.extend(range(r * c, (r + 1) * c))
+        pos.extend(range((2 * P - 1 - r) * c, (2 * P - r) * c))
+    return pos
+
+
+def ring_attn_fwd_zigzag(q, k, v, P: int = 1, out=None, lse=None, want_lse: bool = True,
+                         trace: bool = False, stream=None):
+    """Causal ring attention over the zigzag shard layout (rows in zigzag order, see
+    zigzag_positions).  bf16 or fp32.  Returns (out, lse) or (out, lse, trace)."""
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q must be bf16 or fp32")
+    _check_qkv(q, k, v, dtype)
+    B, L, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, L, H), dtype=torch.float32, device=q.device)
+    tr = torch.full((P, P), -7, dtype=torch.int32, device=q.device) if trace else None
+    _call("ring_attn_fwd_zigzag", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, H, D, P,
+          RA_BF16 if dtype == torch.bfloat16 else RA_F32, _ptr(tr), _stream(stream))
+    return (out, lse, tr) if trace else (out, lse)
 
 
 def ring_attn_fwd_trace(q, k, v, P: int = 1, causal: bool = False, stream=None):

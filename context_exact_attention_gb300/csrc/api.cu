@@ -118,7 +118,7 @@ ra_status check_attn(const void* q, const void* k, const void* v, const void* ou
 
 ra_status attn_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                     int L, int H, int D, int P, int causal, ra_dtype dtype, int* trace,
-                    cudaStream_t stream, int Hkv = -1)
+                    cudaStream_t stream, int Hkv = -1, int zigzag = 0)
 {
     if (Hkv < 0) Hkv = H;
     if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_UNSUPPORTED;
@@ -147,6 +147,7 @@ ra_status attn_impl(const void* q, const void* k, const void* v, void* out, floa
     a.P = P;
     a.causal = causal ? 1 : 0;
     a.Hkv = Hkv;
+    a.zigzag = zigzag;
     a.timeout_ns = kWaitLimitNs;
     a.stream = stream;
     st = status_word(&a.status);
@@ -239,6 +240,18 @@ ra_status ring_attn_fwd_gqa(const void* q, const void* k, const void* v, void* o
     if (H_kv < 1) return RA_ERR_INVALID_ARG;
     return attn_impl(q, k, v, out, lse, B, L, H, D, P, causal, dtype, nullptr,
                      reinterpret_cast<cudaStream_t>(stream), H_kv);
+}
+
+ra_status ring_attn_fwd_zigzag(const void* q, const void* k, const void* v, void* out,
+                               float* lse, int B, int L, int H, int D, int P, ra_dtype dtype,
+                               int* trace, ra_stream_t stream)
+{
+    if (P < 1 || L < 1) return RA_ERR_INVALID_ARG;
+    if (L % (2 * P) != 0) return RA_ERR_NOT_DIVISIBLE;
+    // bf16 key/query tiles of 128 must not straddle the two chunks of a shard
+    if (dtype == RA_BF16 && (L / (2 * P)) % 128 != 0) return RA_ERR_UNSUPPORTED;
+    return attn_impl(q, k, v, out, lse, B, L, H, D, P, 1, dtype, trace,
+                     reinterpret_cast<cudaStream_t>(stream), H, 1);
 }
 
 ra_status attn_merge_partials(const void* o_a, const float* lse_a, const void* o_b,

@@ -38,6 +38,8 @@
 // p by 256, well inside fp32 and bf16 range.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "ra_device.cuh"
 #include "ra_internal.h"
 
@@ -89,38 +91,157 @@ struct Params {
     unsigned int* status;
     unsigned long long timeout_ns;
     int B, L, H, P, Ls, causal;
+    int zigzag;      // shard r holds chunks r and 2P-1-r of 2P chunks (causal only)
     int group;       // query heads per key/value head
     int n_kt;        // K/V blocks per shard
     int n_pair;      // query-tile pairs per shard
     float scale_log2;
 };
 
-// Ring schedule of one CTA: the n-th K/V block it visits is block kt of shard
-// s, met at ring step t.  Step 0 is the CTA's own shard r; under causal
-// masking only blocks up to the diagonal are listed there, and steps whose
-// source lies in the future (s > r, i.e. t > r) are absent.
-struct Sched {
-    int r, P, n_kt, n_first, n_blocks;
-    __device__ __forceinline__ void block(int n, int& s, int& kt, int& t) const
+// Global position of local row i of shard `shard`.  Contiguous layout: shard r
+// holds positions [r Ls, (r+1) Ls).  Zigzag layout ("序列并行与 Ring Attention",
+// section 3.4: each rank holds an early and a late part so causal work is even):
+// with 2P chunks of c = Ls/2 positions, shard r holds chunk r, then chunk 2P-1-r.
+__device__ __forceinline__ int position(int shard, int i, int P, int Ls, int zig)
+{
+    if (!zig) return shard * Ls + i;
+    const int c = Ls >> 1;
+    return i < c ? shard * c + i : (2 * P - 1 - shard) * c + (i - c);
+}
+
+// Ring walk of one CTA: at step t = 0..P-1 the queries of shard r meet shard
+// s = (r - t) mod P (section 3.3).  Of shard s only the key tiles whose first key
+// position does not exceed the CTA's last query position are visited (all of
+// them without causal masking): in the contiguous layout that is all of a past
+// shard, a prefix of the diagonal one and none of a future one (section 3.4's
+// whole-block skip); in the zigzag layout a prefix of each of the shard's two
+// chunks.  Every role walks the same sequence.
+struct RingWalk {
+    int r, P, n_kt, Ls, zig, causal, maxq;
+    int t, s, idx, cnt_a, cnt_b;
+    __device__ __forceinline__ int prefix(int first_pos, int n) const
+    {
+        if (!causal) return n;
+        if (maxq < first_pos) return 0;
+        return min(n, (maxq - first_pos) / kKeys + 1);
+    }
+    __device__ __forceinline__ void enter()
+    {
+        s = r - t;
+        if (s < 0) s += P;
+        if (!zig) {
+            cnt_a = prefix(s * Ls, n_kt);
+            cnt_b = 0;
+        } else {
+            const int c = Ls >> 1, nh = n_kt >> 1;
+            cnt_a = prefix(s * c, nh);
+            cnt_b = prefix((2 * P - 1 - s) * c, nh);
+        }
+        idx = 0;
+    }
+    __device__ __forceinline__ void settle()
+    {
+        while (t < P && idx >= cnt_a + cnt_b) {
+            ++t;
+            if (t < P) enter();
+        }
+    }
+    __device__ __forceinline__ void begin()
+    {
+        t = 0;
+        enter();
+        settle();
+    }
+    __device__ __forceinline__ void next()
+    {
+        ++idx;
+        settle();
+    }
+    __device__ __forceinline__ int total()
+    {
+        int n = 0;
+        for (t = 0; t < P; ++t) {
+            enter();
+            n += cnt_a + cnt_b;
+        }
+        return n;
+    }
+    // key tile within shard s, and the position of its first key
+    __device__ __forceinline__ int kt() const { return idx < cnt_a ? idx : (n_kt >> 1) + (idx - cnt_a); }
+    __device__ __forceinline__ int pos0() const { return position(s, kt() * kKeys, P, Ls, zig); }
+};
+
+// The contiguous layout's schedule in closed form (same sequence as RingWalk
+// gives for it): step 0 is the own shard r (under causal masking only the tiles
+// up to the diagonal), then shards r-1, r-2, ... (causal: down to 0; otherwise
+// all of them, wrapping around).
+struct ContigSched {
+    int r, P, n_kt, Ls, n_first, n_blocks;
+    int s, kt_, t;
+    __device__ __forceinline__ void init(int r_, int P_, int n_kt_, int Ls_, int causal, int q_last)
+    {
+        r = r_;
+        P = P_;
+        n_kt = n_kt_;
+        Ls = Ls_;
+        if (causal) {
+            n_first = min(n_kt, q_last / kKeys + 1);
+            n_blocks = n_first + r * n_kt;
+        } else {
+            n_first = n_kt;
+            n_blocks = P * n_kt;
+        }
+    }
+    __device__ __forceinline__ void at(int n)
     {
         if (n < n_first) {
             t = 0;
             s = r;
-            kt = n;
+            kt_ = n;
             return;
         }
         const int m = n - n_first;
         t = 1 + m / n_kt;
-        kt = m - (t - 1) * n_kt;
+        kt_ = m - (t - 1) * n_kt;
         s = r - t;
         if (s < 0) s += P;
     }
+    __device__ __forceinline__ int kt() const { return kt_; }
+    __device__ __forceinline__ bool first_of_shard() const { return kt_ == 0; }
+    __device__ __forceinline__ int pos0() const { return s * Ls + kt_ * kKeys; }
+};
+
+// The zigzag layout's schedule, walked in order (at(n) must see n = 0, 1, 2, ...).
+struct ZigzagSched {
+    RingWalk w;
+    int n_blocks, s, t;
+    __device__ __forceinline__ void init(int r_, int P_, int n_kt_, int Ls_, int causal, int maxq)
+    {
+        w.r = r_;
+        w.P = P_;
+        w.n_kt = n_kt_;
+        w.Ls = Ls_;
+        w.zig = 1;
+        w.causal = causal;
+        w.maxq = maxq;
+        n_blocks = w.total();
+    }
+    __device__ __forceinline__ void at(int n)
+    {
+        if (n == 0) w.begin();
+        else w.next();
+        s = w.s;
+        t = w.t;
+    }
+    __device__ __forceinline__ int kt() const { return w.kt(); }
+    __device__ __forceinline__ bool first_of_shard() const { return w.idx == 0; }
+    __device__ __forceinline__ int pos0() const { return w.pos0(); }
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-template <int D>
+template <int D, bool kZig>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                           const __grid_constant__ CUtensorMap tmap_k,
@@ -150,18 +271,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q0_local = pair * (kTiles * kRows);     // first query row of the pair, within shard
     const int q0 = r * p.Ls + q0_local;               // global
 
-    Sched sc;
-    sc.r = r;
-    sc.P = p.P;
-    sc.n_kt = p.n_kt;
-    if (p.causal) {
-        const int q_last = min(p.Ls - 1, q0_local + kTiles * kRows - 1);
-        sc.n_first = min(p.n_kt, q_last / kKeys + 1);
-        sc.n_blocks = sc.n_first + r * p.n_kt;
-    } else {
-        sc.n_first = p.n_kt;
-        sc.n_blocks = p.P * p.n_kt;
+    using Sched = typename std::conditional<kZig, ZigzagSched, ContigSched>::type;
+    Sched walk;
+    {
+        const int last = min(p.Ls - 1, q0_local + kTiles * kRows - 1);
+        if (kZig) {
+            // last query position of the pair (positions rise within each chunk, and
+            // the late chunk lies after the early one)
+            const int mid = min(p.Ls - 1, q0_local + kRows - 1);
+            walk.init(r, p.P, p.n_kt, p.Ls, p.causal,
+                      max(position(r, last, p.P, p.Ls, 1), position(r, mid, p.P, p.Ls, 1)));
+        } else {
+            walk.init(r, p.P, p.n_kt, p.Ls, p.causal, last);
+        }
     }
+    const int n_blocks = walk.n_blocks;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQ), 1);
@@ -198,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
         }
-        const bool tracing = p.trace != nullptr && bh == 0 && pair == 0;
+        // the shard's last query pair meets every shard the shard visits, in either layout
+        const bool tracing = p.trace != nullptr && bh == 0 && pair == p.n_pair - 1;
         if (tracing && leader)
             for (int t = 0; t < p.P; ++t) p.trace[r * p.P + t] = -1;
         const uint64_t keep = l2_policy_evict_last();    // K/V: read by every tile pair of the head
@@ -211,13 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 bar(kBarQ), bx * 64, h, q0 + tq * kRows, b, once);
         }
         int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
-        for (int n = 0; n < sc.n_blocks; ++n) {
-            int s, kt, t;
-            sc.block(n, s, kt, t);
-            if (tracing && kt == 0 && leader) p.trace[r * p.P + t] = s;
+        for (int n = 0; n < n_blocks; ++n) {
+            walk.at(n);
+            if (tracing && walk.first_of_shard() && leader) p.trace[r * p.P + walk.t] = walk.s;
             const int st = n & 1;
             const uint32_t ph = (n >> 1) & 1;
-            const int row = s * p.Ls + kt * kKeys;
+            const int row = walk.s * p.Ls + walk.kt() * kKeys;   // physical row of the tile
             if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc))) break;
             if (leader) {
                 mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kTileBytes);
@@ -294,10 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
-        for (int n = 0; ok && n < sc.n_blocks; ++n) {
+        for (int n = 0; ok && n < n_blocks; ++n) {
             const int st = n & 1;
             const uint32_t ph = (n >> 1) & 1;
-            const bool more = n + 1 < sc.n_blocks;
+            const bool more = n + 1 < n_blocks;
             const int st1 = (n + 1) & 1;
             const uint32_t ph1 = ((n + 1) >> 1) & 1;
             if (!(ok = wait_all(kBarVFull + st, ph) && wait_all(kBarPFull + 0, n & 1))) break;
@@ -352,15 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + Lay::col_s(tq);
         const uint32_t tO = tmem + lane_off + Lay::col_o(tq);
         const int row_local = q0_local + tq * kRows + row;   // within shard r
-        const int row_glob = r * p.Ls + row_local;
+        const int row_glob = r * p.Ls + row_local;           // physical row
+        const int row_pos = position(r, row_local, p.P, p.Ls, kZig ? 1 : 0);
         const float sl2 = p.scale_log2;
 
         float m = -INFINITY;   // running max of scaled scores, base-2 units
         float l = 0.f;         // running denominator, relative to m
         bool ok = true;
-        for (int n = 0; n < sc.n_blocks; ++n) {
-            int s, kt, t;
-            sc.block(n, s, kt, t);
+        for (int n = 0; n < n_blocks; ++n) {
+            walk.at(n);
             ok = mbar_wait(bar(kBarSFull + tq), n & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -372,10 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 128; ++c) sv[c] = u2f(sraw[c]);
 
-            // visible columns: inside the shard, and under causal masking on the
-            // diagonal shard, key position <= query position (global positions)
-            int lim = min(kKeys - 1, p.Ls - kt * kKeys - 1);
-            if (p.causal && s == r) lim = min(lim, row_local - kt * kKeys);
+            // visible columns: inside the shard, and under causal masking key
+            // position <= query position (global positions)
+            int lim = min(kKeys - 1, p.Ls - walk.kt() * kKeys - 1);
+            if (p.causal) lim = min(lim, row_pos - walk.pos0());
             if (lim < kKeys - 1) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) sv[c] = (c > lim) ? -INFINITY : sv[c];
@@ -476,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool kZig>
 cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv)
 {
@@ -487,7 +611,7 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(ring_attn_bf16_kernel<D>,
+        e = cudaFuncSetAttribute(ring_attn_bf16_kernel<D, kZig>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
@@ -504,13 +628,14 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     p.P = a.P;
     p.Ls = a.L / a.P;
     p.causal = a.causal;
+    p.zigzag = a.zigzag;
     p.group = a.H / a.Hkv;
     p.n_kt = (p.Ls + kKeys - 1) / kKeys;
     p.n_pair = (p.n_kt + kTiles - 1) / kTiles;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
     const long long grid = static_cast<long long>(a.B) * a.H * a.P * p.n_pair;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    ring_attn_bf16_kernel<D><<<static_cast<unsigned>(grid), kThreads, Lay::kSmem, a.stream>>>(
+    ring_attn_bf16_kernel<D, kZig><<<static_cast<unsigned>(grid), kThreads, Lay::kSmem, a.stream>>>(
         tq, tk, tv, p);
     return cudaGetLastError();
 }
@@ -520,8 +645,13 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
 cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv)
 {
-    if (a.D == 64) return launch_d<64>(a, tq, tk, tv);
-    if (a.D == 128) return launch_d<128>(a, tq, tk, tv);
+    if (a.zigzag) {
+        if (a.D == 64) return launch_d<64, true>(a, tq, tk, tv);
+        if (a.D == 128) return launch_d<128, true>(a, tq, tk, tv);
+    } else {
+        if (a.D == 64) return launch_d<64, false>(a, tq, tk, tv);
+        if (a.D == 128) return launch_d<128, false>(a, tq, tk, tv);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     ring_attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                          const float* __restrict__ v, float* __restrict__ out,
                          float* __restrict__ lse, int* __restrict__ trace, int B, int L, int H,
-                         int Hkv, int D, int P, int causal, float scale)
+                         int Hkv, int D, int P, int causal, int zig, float scale)
 {
     __shared__ float qs[kWarps][kMaxD];
     const int warp = threadIdx.x >> 5;
@@ -53,12 +53,21 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int b = static_cast<int>(bh / H);
     const int Ls = L / P;
     const int r = i / Ls;
+    // global positions: contiguous shards, or zigzag (shard r holds chunks r and
+    // 2P-1-r of 2P chunks of Ls/2 positions)
+    auto position = [&](int shard, int local) {
+        if (!zig) return shard * Ls + local;
+        const int c = Ls / 2;
+        return local < c ? shard * c + local : (2 * P - 1 - shard) * c + (local - c);
+    };
+    const int q_pos = position(r, i - r * Ls);
     const size_t row_stride = static_cast<size_t>(H) * D;   // between consecutive positions
     const float* qrow = q + (static_cast<size_t>(b) * L + i) * row_stride + static_cast<size_t>(h) * D;
     for (int d = lane; d < D; d += 32) qs[warp][d] = qrow[d];
     __syncwarp();
 
-    const bool tracing = trace != nullptr && b == 0 && h == 0 && i == r * Ls;
+    // the shard's last row meets every shard the shard visits, in either layout
+    const bool tracing = trace != nullptr && b == 0 && h == 0 && i == r * Ls + Ls - 1;
     float m = -INFINITY, l = 0.f;
     float acc[kMaxD / 32];
 #pragma unroll
@@ -73,15 +82,16 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int t = 0; t < P; ++t) {
         int s = r - t;
         if (s < 0) s += P;
-        const bool skip = causal && s > r;
+        // whole shard in the future of this query: skipped
+        const bool skip = causal && position(s, 0) > q_pos;
         if (tracing && lane == 0) trace[r * P + t] = skip ? -1 : s;
         if (skip) continue;
         const int j_begin = s * Ls;
-        const int j_end = (causal && s == r) ? i + 1 : j_begin + Ls;   // keys j <= i on the diagonal
+        const int j_end = j_begin + Ls;
         for (int j0 = j_begin; j0 < j_end; j0 += 32) {
             const int j = j0 + lane;
             float sc = -INFINITY;
-            if (j < j_end) {
+            if (j < j_end && (!causal || position(s, j - j_begin) <= q_pos)) {
                 const float* krow = kb + static_cast<size_t>(j) * kv_stride;
                 float dot = 0.f;
                 for (int d = 0; d < D; d += 4) {
@@ -133,7 +143,7 @@ cudaError_t launch_attn_f32(const AttnArgs& a)
     ring_attn_f32_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, a.stream>>>(
         static_cast<const float*>(a.q), static_cast<const float*>(a.k),
         static_cast<const float*>(a.v), static_cast<float*>(a.out), a.lse, a.trace, a.B, a.L,
-        a.H, a.Hkv, a.D, a.P, a.causal, 1.0f / sqrtf(static_cast<float>(a.D)));
+        a.H, a.Hkv, a.D, a.P, a.causal, a.zigzag, 1.0f / sqrtf(static_cast<float>(a.D)));
     return cudaGetLastError();
 }
 

@@ -19,6 +19,7 @@ struct AttnArgs {
     int* trace;      // may be null
     int B, L, H, D, P, causal;
     int Hkv;                       // key/value heads (H for plain attention)
+    int zigzag;                    // zigzag shard layout (causal)
     unsigned int* status;          // device status word
     unsigned long long timeout_ns; // limit of one bounded wait
     cudaStream_t stream;

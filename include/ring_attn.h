@@ -101,6 +101,25 @@ ra_status ring_attn_fwd_gqa(const void* q, const void* k, const void* v, void* o
                             ra_dtype dtype, ra_stream_t stream);
 
 /*
+ * ring_attn_fwd_zigzag -- causal ring attention (dtype RA_BF16 or RA_F32) over
+ * the zigzag shard layout that balances causal work across shards
+ * ("序列并行与 Ring Attention", section 3.4).  The sequence is cut into 2P
+ * chunks of c = L/(2P) positions and virtual shard r holds chunk r followed by
+ * chunk 2P-1-r: row i of q, k, v, out (and lse) sits at global position
+ *   r*c + i'            for i' = i - r*L/P < c, and
+ *   (2P-1-r)*c + i' - c otherwise,
+ * and the causal rule compares those global positions.  The result is causal
+ * attention of the sequence in position order, returned in the zigzag row order.
+ * Every ring step now meets a shard with visible keys, and every shard does the
+ * same amount of work.  trace, if not NULL, is filled as by ring_attn_fwd_trace.
+ * Requires L % (2P) == 0 (RA_ERR_NOT_DIVISIBLE), and for bf16 c % 128 == 0
+ * (RA_ERR_UNSUPPORTED).  Otherwise as ring_attn_fwd.
+ */
+ra_status ring_attn_fwd_zigzag(const void* q, const void* k, const void* v, void* out,
+                               float* lse, int B, int L, int H, int D, int P, ra_dtype dtype,
+                               int* trace, ra_stream_t stream);
+
+/*
  * attn_merge_partials -- log-sum-exp merge of two partial attention results
  * over disjoint key sets (the `combine` of the juejin.cn ring-attention article, section 四):
  *   lse_out = ln(e^lse_a + e^lse_b)

@@ -69,3 +69,21 @@ def test_argument_errors_are_caught_before_any_cuda_call(lib):
                                    10, 128, 0, s) == 1
     assert lib.attn_merge_partials(fake, fake, fake, fake, fake, fake, 10, 4, 0, s) == 2
     assert lib.ra_probe_wait_timeout(0, s) == 1
+
+
+def test_zigzag_positions_layout_and_balance():
+    """Shard r of the zigzag layout holds chunks r and 2P-1-r; every shard then has the
+    same number of visible causal (query, key) pairs, while contiguous shards grow
+    with r ("序列并行与 Ring Attention", section 3.4)."""
+    for L, P in ((16, 2), (48, 3), (64, 4)):
+        pos = cea.zigzag_positions(L, P)
+        assert sorted(pos) == list(range(L))
+        c, Ls = L // (2 * P), L // P
+        for r in range(P):
+            shard = pos[r * Ls:(r + 1) * Ls]
+            assert shard[:c] == list(range(r * c, (r + 1) * c))
+            assert shard[c:] == list(range((2 * P - 1 - r) * c, (2 * P - r) * c))
+        work_zig = [sum(p + 1 for p in pos[r * Ls:(r + 1) * Ls]) for r in range(P)]
+        work_contig = [sum(p + 1 for p in range(r * Ls, (r + 1) * Ls)) for r in range(P)]
+        assert len(set(work_zig)) == 1
+        assert work_contig == sorted(work_contig) and work_contig[0] < work_contig[-1]

@@ -332,3 +332,59 @@ def test_gqa_argument_errors():
     with pytest.raises(cea.RingAttnError) as e:
         cea.ring_attn_fwd_gqa(q, k, v, P=2)
     assert e.value.code == 4
+
+
+# ---------------------------------------------------------------- zigzag layout --
+
+ZIGZAG_CASES = [
+    # B, L, H, D, P, dtype
+    (1, 512, 2, 128, 2, torch.bfloat16),
+    (2, 1024, 2, 128, 4, torch.bfloat16),
+    (1, 768, 2, 64, 3, torch.bfloat16),
+    (1, 2048, 1, 128, 8, torch.bfloat16),
+    (1, 96, 2, 32, 3, torch.float32),
+    (2, 64, 1, 16, 4, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", ZIGZAG_CASES, ids=lambda c: "B%dL%dH%dD%dP%d" % c[:5])
+def test_zigzag_parity(case):
+    """Causal attention of the position-ordered sequence, returned in zigzag row order:
+    the oracle runs on the position-ordered tensors and its rows are permuted."""
+    B, L, H, D, P, dtype = case
+    qg, kg, vg = make_qkv(B, L, H, D, seed=60, dtype=dtype)    # row = global position
+    pos = torch.tensor(cea.zigzag_positions(L, P))
+    q, k, v = (t[:, pos].contiguous() for t in (qg, kg, vg))     # row i holds position pos[i]
+    out, lse, trace = cea.ring_attn_fwd_zigzag(*_dev(q, k, v), P=P, trace=True)
+    assert cea.check_status() == 0
+    ref, lref = oracle.attention(qg, kg, vg, causal=True)
+    check = assert_bf16_close if dtype == torch.bfloat16 else assert_f32_close
+    check(to_np(out), ref[:, pos.numpy()], "out")
+    check(to_np(lse), lref[:, pos.numpy()], "lse")
+    # no ring step is skipped any more: every shard meets every shard, its own first,
+    # and at step t shard r holds what shard r-1 held at step t-1
+    tr = trace.cpu().numpy()
+    for r in range(P):
+        assert sorted(tr[r].tolist()) == list(range(P)) and tr[r, 0] == r
+        for t in range(1, P):
+            assert tr[r, t] == tr[(r - 1) % P, t - 1]
+
+
+def test_zigzag_matches_contiguous_layout():
+    B, L, H, D, P = 1, 1024, 4, 128, 4
+    qg, kg, vg = make_qkv(B, L, H, D, seed=61, dtype=torch.bfloat16)
+    pos = torch.tensor(cea.zigzag_positions(L, P))
+    contig, _ = cea.ring_attn_fwd(*_dev(qg, kg, vg), P=P, causal=True)
+    zig, _ = cea.ring_attn_fwd_zigzag(*_dev(*(t[:, pos].contiguous() for t in (qg, kg, vg))), P=P)
+    assert_bf16_close(to_np(zig), to_np(contig)[:, pos.numpy()], "zigzag vs contiguous")
+
+
+def test_zigzag_argument_errors():
+    q, k, v = _dev(*make_qkv(1, 516, 1, 128, seed=0, dtype=torch.bfloat16))
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ring_attn_fwd_zigzag(q, k, v, P=4)            # 516 % 4 == 0 but 516 % 8 != 0
+    assert e.value.code == 4
+    q, k, v = _dev(*make_qkv(1, 256, 1, 128, seed=0, dtype=torch.bfloat16))
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ring_attn_fwd_zigzag(q, k, v, P=2)            # chunks of 64 rows: not 128-aligned
+    assert e.value.code == 2
