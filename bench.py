@@ -438,6 +438,31 @@ def measure_rows(cea, dev, stream, peaks):
                         "frac": fl / (ms * 1e-3) / 1e12 / peak}
     del q, k, v, out, lse
 
+    # packed variable-length sequences filling the headline length (causal)
+    w = LM
+    gl = torch.Generator().manual_seed(5)
+    lengths = []
+    while sum(lengths) < w.L:
+        lengths.append(int(torch.randint(256, 8192, (1,), generator=gl)))
+    lengths[-1] -= sum(lengths) - w.L
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=dev)
+    q, k, v = (torch.randn(w.L, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.L, w.H), dtype=torch.float32, device=dev)
+    f = lambda: cea.ring_attn_fwd_varlen(q, k, v, cu_d, P=w.P, causal=True, out=out, lse=lse,
+                                         stream=stream)
+    f()
+    ms = _time_loop(f, 5, stream) / 5
+    fl = sum(attention_flops(1, n, w.H, w.D, True) for n in lengths)
+    res["lm_varlen_causal"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                               "frac": fl / (ms * 1e-3) / 1e12 / peak, "n_seqs": len(lengths),
+                               "note": "lengths U[256, 8192) packed to 32768 tokens, 32 heads"}
+    del q, k, v, out, lse, cu_d
+
     # backward of the headline workload (dq, dk, dv): algorithmic FLOPs are 2.5x the
     # forward's (five D-length products per visible pair)
     w = LM

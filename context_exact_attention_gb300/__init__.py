@@ -22,7 +22,7 @@ __all__ = [
     "RingAttnError", "library_path", "load_library", "ring_attn_fwd", "ring_attn_fwd_f32",
     "ring_attn_fwd_trace", "attn_merge_partials", "ulysses_seq2head", "ulysses_head2seq",
     "ulysses_attention", "ring_attn_bwd", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
-    "zigzag_positions", "check_status",
+    "zigzag_positions", "ring_attn_fwd_varlen", "varlen_padded_length", "check_status",
     "probe_wait_timeout",
     "EXPORTED_SYMBOLS",
 ]
@@ -41,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "ulysses_seq2head", "ulysses_head2seq", "ra_check_status", "ra_status_string",
     "ra_probe_wait_timeout", "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
     "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
+    "ring_attn_fwd_varlen",
 )
 
 
@@ -83,6 +84,7 @@ def load_library(build_if_missing: bool = False):
             "ring_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
             "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
             "ring_attn_fwd_zigzag": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp, vp],
+            "ring_attn_fwd_varlen": [vp, vp, vp, vp, f_p, vp, i, i, i, i, i, i, i, vp, vp],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -206,6 +208,39 @@ def ring_attn_fwd_zigzag(q, k, v, P: int = 1, out=None, lse=None, want_lse: bool
         lse = torch.empty((B, L, H), dtype=torch.float32, device=q.device)
     tr = torch.full((P, P), -7, dtype=torch.int32, device=q.device) if trace else None
     _call("ring_attn_fwd_zigzag", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, L, H, D, P,
+          RA_BF16 if dtype == torch.bfloat16 else RA_F32, _ptr(tr), _stream(stream))
+    return (out, lse, tr) if trace else (out, lse)
+
+
+def varlen_padded_length(total: int, P: int, multiple: int = 1) -> int:
+    """Smallest length >= total that P shards of a multiple of `multiple` rows divide:
+    ceil(total / (P * multiple)) * P * multiple (the Ulysses guideline page's
+    padded_seq_len rule, e.g. 3000 tokens, 4 shards, multiple 8 -> 3008)."""
+    step = P * multiple
+    return -(-total // step) * step
+
+
+def ring_attn_fwd_varlen(q, k, v, cu_seqlens, P: int = 1, causal: bool = False, out=None,
+                         lse=None, want_lse: bool = True, trace: bool = False, stream=None):
+    """Ring attention over packed sequences.  q, k, v: [L, H, D] (bf16 or fp32);
+    cu_seqlens: int32 CUDA tensor [n_seqs + 1] of sequence starts ending with L.
+    Returns (out, lse) or (out, lse, trace)."""
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q must be bf16 or fp32")
+    if q.dim() != 3:
+        raise ValueError("packed q, k, v are [L, H, D]")
+    _check_qkv(q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), dtype)
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    L, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((L, H), dtype=torch.float32, device=q.device)
+    tr = torch.full((P, P), -7, dtype=torch.int32, device=q.device) if trace else None
+    _call("ring_attn_fwd_varlen", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+          _ptr(cu_seqlens), cu_seqlens.numel() - 1, L, H, D, P, int(bool(causal)),
           RA_BF16 if dtype == torch.bfloat16 else RA_F32, _ptr(tr), _stream(stream))
     return (out, lse, tr) if trace else (out, lse)
 

@@ -118,7 +118,8 @@ ra_status check_attn(const void* q, const void* k, const void* v, const void* ou
 
 ra_status attn_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                     int L, int H, int D, int P, int causal, ra_dtype dtype, int* trace,
-                    cudaStream_t stream, int Hkv = -1, int zigzag = 0)
+                    cudaStream_t stream, int Hkv = -1, int zigzag = 0,
+                    const int* cu_seqlens = nullptr, int n_seqs = 0)
 {
     if (Hkv < 0) Hkv = H;
     if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_UNSUPPORTED;
@@ -148,6 +149,8 @@ ra_status attn_impl(const void* q, const void* k, const void* v, void* out, floa
     a.causal = causal ? 1 : 0;
     a.Hkv = Hkv;
     a.zigzag = zigzag;
+    a.cu_seqlens = cu_seqlens;
+    a.n_seqs = n_seqs;
     a.timeout_ns = kWaitLimitNs;
     a.stream = stream;
     st = status_word(&a.status);
@@ -252,6 +255,16 @@ ra_status ring_attn_fwd_zigzag(const void* q, const void* k, const void* v, void
     if (dtype == RA_BF16 && (L / (2 * P)) % 128 != 0) return RA_ERR_UNSUPPORTED;
     return attn_impl(q, k, v, out, lse, B, L, H, D, P, 1, dtype, trace,
                      reinterpret_cast<cudaStream_t>(stream), H, 1);
+}
+
+ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                               float* lse, const int* cu_seqlens, int n_seqs, int L, int H, int D,
+                               int P, int causal, ra_dtype dtype, int* trace, ra_stream_t stream)
+{
+    if (!cu_seqlens || n_seqs < 1) return RA_ERR_INVALID_ARG;
+    if (!aligned(cu_seqlens, 4)) return RA_ERR_MISALIGNED;
+    return attn_impl(q, k, v, out, lse, 1, L, H, D, P, causal, dtype, trace,
+                     reinterpret_cast<cudaStream_t>(stream), H, 0, cu_seqlens, n_seqs);
 }
 
 ra_status attn_merge_partials(const void* o_a, const float* lse_a, const void* o_b,

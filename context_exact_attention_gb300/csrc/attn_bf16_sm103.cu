@@ -92,6 +92,8 @@ struct Params {
     unsigned long long timeout_ns;
     int B, L, H, P, Ls, causal;
     int zigzag;      // shard r holds chunks r and 2P-1-r of 2P chunks (causal only)
+    const int* cu_seqlens;   // packed sequences: starts of n_seqs sequences, then L
+    int n_seqs;
     int group;       // query heads per key/value head
     int n_kt;        // K/V blocks per shard
     int n_pair;      // query-tile pairs per shard
@@ -238,10 +240,80 @@ struct ZigzagSched {
     __device__ __forceinline__ int pos0() const { return w.pos0(); }
 };
 
+// Packed sequences: sequence g covers positions [cu[g], cu[g+1]); a query sees
+// only keys of its own sequence (and, causal, not after itself).  Returns the
+// first and last visible key position of the query at `pos`.
+__device__ __forceinline__ void seq_bounds(const int* cu, int n_seqs, int pos, int causal, int& lo,
+                                           int& hi)
+{
+    int a = 0, b = n_seqs;                       // invariant: cu[a] <= pos < cu[b]
+    while (b - a > 1) {
+        const int mid = (a + b) >> 1;
+        if (__ldg(cu + mid) <= pos) a = mid;
+        else b = mid;
+    }
+    lo = __ldg(cu + a);
+    hi = causal ? pos : __ldg(cu + a + 1) - 1;
+}
+
+// Packed-sequence schedule: ring order as always; of shard s the key tiles that
+// intersect the CTA's visible position range [lo, hi] (a contiguous run of tiles,
+// possibly none).
+struct VarlenSched {
+    int r, P, n_kt, Ls, lo, hi;
+    int n_blocks, s, t, idx, k_first, k_count;
+    __device__ __forceinline__ void enter()
+    {
+        s = r - t;
+        if (s < 0) s += P;
+        const int base = s * Ls;
+        const int a = max(lo, base), b = min(hi, base + Ls - 1);
+        if (a > b) {
+            k_first = 0;
+            k_count = 0;
+        } else {
+            k_first = (a - base) / kKeys;
+            k_count = (b - base) / kKeys - k_first + 1;
+        }
+        idx = 0;
+    }
+    __device__ __forceinline__ void init(int r_, int P_, int n_kt_, int Ls_, int lo_, int hi_)
+    {
+        r = r_;
+        P = P_;
+        n_kt = n_kt_;
+        Ls = Ls_;
+        lo = lo_;
+        hi = hi_;
+        n_blocks = 0;
+        for (t = 0; t < P; ++t) {
+            enter();
+            n_blocks += k_count;
+        }
+    }
+    __device__ __forceinline__ void at(int n)
+    {
+        if (n == 0) {
+            t = 0;
+            enter();
+        } else {
+            ++idx;
+        }
+        while (idx >= k_count && t < P) {
+            ++t;
+            if (t < P) enter();
+        }
+    }
+    __device__ __forceinline__ int kt() const { return k_first + idx; }
+    __device__ __forceinline__ bool first_of_shard() const { return idx == 0; }
+    __device__ __forceinline__ int pos0() const { return s * Ls + kt() * kKeys; }
+};
+
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-template <int D, bool kZig>
+// kMode: 0 contiguous shards, 1 zigzag shards, 2 packed sequences (contiguous shards).
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                           const __grid_constant__ CUtensorMap tmap_k,
@@ -271,11 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q0_local = pair * (kTiles * kRows);     // first query row of the pair, within shard
     const int q0 = r * p.Ls + q0_local;               // global
 
-    using Sched = typename std::conditional<kZig, ZigzagSched, ContigSched>::type;
+    constexpr bool kZig = kMode == 1;
+    constexpr bool kVarlen = kMode == 2;
+    using Sched = typename std::conditional<
+        kZig, ZigzagSched, typename std::conditional<kVarlen, VarlenSched, ContigSched>::type>::type;
     Sched walk;
     {
         const int last = min(p.Ls - 1, q0_local + kTiles * kRows - 1);
-        if (kZig) {
+        if constexpr (kVarlen) {
+            // visible positions of the pair: from the first row's sequence start to the
+            // last row's (causal) position or sequence end
+            int lo0, hi0, lo1, hi1;
+            seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + q0_local, p.causal, lo0, hi0);
+            seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + last, p.causal, lo1, hi1);
+            walk.init(r, p.P, p.n_kt, p.Ls, lo0, hi1);
+        } else if constexpr (kZig) {
             // last query position of the pair (positions rise within each chunk, and
             // the late chunk lies after the early one)
             const int mid = min(p.Ls - 1, q0_local + kRows - 1);
@@ -478,6 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_local = q0_local + tq * kRows + row;   // within shard r
         const int row_glob = r * p.Ls + row_local;           // physical row
         const int row_pos = position(r, row_local, p.P, p.Ls, kZig ? 1 : 0);
+        int seq_lo = 0, seq_hi = 0;                            // packed sequences only
+        if constexpr (kVarlen) {
+            if (row_local < p.Ls) seq_bounds(p.cu_seqlens, p.n_seqs, row_pos, p.causal, seq_lo, seq_hi);
+            else seq_hi = -1;
+        }
         const float sl2 = p.scale_log2;
 
         float m = -INFINITY;   // running max of scaled scores, base-2 units
@@ -499,10 +586,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // visible columns: inside the shard, and under causal masking key
             // position <= query position (global positions)
             int lim = min(kKeys - 1, p.Ls - walk.kt() * kKeys - 1);
-            if (p.causal) lim = min(lim, row_pos - walk.pos0());
-            if (lim < kKeys - 1) {
+            int lo_lim = 0;
+            if constexpr (kVarlen) {
+                lim = min(lim, seq_hi - walk.pos0());
+                lo_lim = seq_lo - walk.pos0();
+            } else if (p.causal) {
+                lim = min(lim, row_pos - walk.pos0());
+            }
+            if (lim < kKeys - 1 || lo_lim > 0) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) sv[c] = (c > lim) ? -INFINITY : sv[c];
+                for (int c = 0; c < 128; ++c) sv[c] = (c > lim || c < lo_lim) ? -INFINITY : sv[c];
             }
 
             float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
@@ -570,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             tc_fence_after();
             const bool valid = row_local < p.Ls;
-            const float inv_l = 1.f / l;
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;        // a row that saw no key: 0
             __nv_bfloat16* dst =
                 p.out + ((static_cast<size_t>(b) * p.L + row_glob) * p.H + h) * static_cast<size_t>(D);
 #pragma unroll
@@ -589,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (valid && p.lse != nullptr)
-                p.lse[(static_cast<size_t>(b) * p.L + row_glob) * p.H + h] = (m + log2f(l)) * kLn2;
+                p.lse[(static_cast<size_t>(b) * p.L + row_glob) * p.H + h] =
+                    l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
     }
 
@@ -600,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool kZig>
+template <int D, int kMode>
 cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv)
 {
@@ -611,7 +705,7 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(ring_attn_bf16_kernel<D, kZig>,
+        e = cudaFuncSetAttribute(ring_attn_bf16_kernel<D, kMode>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
@@ -629,13 +723,15 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     p.Ls = a.L / a.P;
     p.causal = a.causal;
     p.zigzag = a.zigzag;
+    p.cu_seqlens = a.cu_seqlens;
+    p.n_seqs = a.n_seqs;
     p.group = a.H / a.Hkv;
     p.n_kt = (p.Ls + kKeys - 1) / kKeys;
     p.n_pair = (p.n_kt + kTiles - 1) / kTiles;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
     const long long grid = static_cast<long long>(a.B) * a.H * a.P * p.n_pair;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    ring_attn_bf16_kernel<D, kZig><<<static_cast<unsigned>(grid), kThreads, Lay::kSmem, a.stream>>>(
+    ring_attn_bf16_kernel<D, kMode><<<static_cast<unsigned>(grid), kThreads, Lay::kSmem, a.stream>>>(
         tq, tk, tv, p);
     return cudaGetLastError();
 }
@@ -645,12 +741,15 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
 cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv)
 {
-    if (a.zigzag) {
-        if (a.D == 64) return launch_d<64, true>(a, tq, tk, tv);
-        if (a.D == 128) return launch_d<128, true>(a, tq, tk, tv);
+    if (a.cu_seqlens != nullptr) {
+        if (a.D == 64) return launch_d<64, 2>(a, tq, tk, tv);
+        if (a.D == 128) return launch_d<128, 2>(a, tq, tk, tv);
+    } else if (a.zigzag) {
+        if (a.D == 64) return launch_d<64, 1>(a, tq, tk, tv);
+        if (a.D == 128) return launch_d<128, 1>(a, tq, tk, tv);
     } else {
-        if (a.D == 64) return launch_d<64, false>(a, tq, tk, tv);
-        if (a.D == 128) return launch_d<128, false>(a, tq, tk, tv);
+        if (a.D == 64) return launch_d<64, 0>(a, tq, tk, tv);
+        if (a.D == 128) return launch_d<128, 0>(a, tq, tk, tv);
     }
     return cudaErrorInvalidValue;
 }

@@ -35,11 +35,21 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-__global__ void __launch_bounds__(kWarps * 32)
+// Global position of local row i of a shard: contiguous shards, or zigzag (shard
+// r holds chunks r and 2P-1-r of 2P chunks of Ls/2 positions).
+__device__ __forceinline__ int position_of(int shard, int i, int P, int Ls, int zig)
+{
+    if (!zig) return shard * Ls + i;
+    const int c = Ls / 2;
+    return i < c ? shard * c + i : (2 * P - 1 - shard) * c + (i - c);
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 1)
     ring_attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                          const float* __restrict__ v, float* __restrict__ out,
                          float* __restrict__ lse, int* __restrict__ trace, int B, int L, int H,
-                         int Hkv, int D, int P, int causal, int zig, float scale)
+                         int Hkv, int D, int P, int causal, int zig, const int* cu_seqlens,
+                         int n_seqs, float scale)
 {
     __shared__ float qs[kWarps][kMaxD];
     const int warp = threadIdx.x >> 5;
@@ -53,14 +63,20 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int b = static_cast<int>(bh / H);
     const int Ls = L / P;
     const int r = i / Ls;
-    // global positions: contiguous shards, or zigzag (shard r holds chunks r and
-    // 2P-1-r of 2P chunks of Ls/2 positions)
-    auto position = [&](int shard, int local) {
-        if (!zig) return shard * Ls + local;
-        const int c = Ls / 2;
-        return local < c ? shard * c + local : (2 * P - 1 - shard) * c + (local - c);
-    };
-    const int q_pos = position(r, i - r * Ls);
+    const int q_pos = position_of(r, i - r * Ls, P, Ls, zig);
+    // visible key positions [lo, hi]: everything (or up to the query, causal), or for
+    // packed sequences the query's own sequence (up to the query, causal)
+    int lo = 0, hi = causal ? q_pos : L - 1;
+    if (cu_seqlens != nullptr) {
+        int a = 0, bb = n_seqs;
+        while (bb - a > 1) {
+            const int mid = (a + bb) >> 1;
+            if (cu_seqlens[mid] <= q_pos) a = mid;
+            else bb = mid;
+        }
+        lo = cu_seqlens[a];
+        hi = causal ? q_pos : cu_seqlens[a + 1] - 1;
+    }
     const size_t row_stride = static_cast<size_t>(H) * D;   // between consecutive positions
     const float* qrow = q + (static_cast<size_t>(b) * L + i) * row_stride + static_cast<size_t>(h) * D;
     for (int d = lane; d < D; d += 32) qs[warp][d] = qrow[d];
@@ -82,8 +98,9 @@ __global__ void __launch_bounds__(kWarps * 32)
     for (int t = 0; t < P; ++t) {
         int s = r - t;
         if (s < 0) s += P;
-        // whole shard in the future of this query: skipped
-        const bool skip = causal && position(s, 0) > q_pos;
+        // whole shard outside the visible keys of this query: skipped
+        const bool skip = cu_seqlens != nullptr ? (s * Ls > hi || s * Ls + Ls - 1 < lo)
+                                                : (causal && position_of(s, 0, P, Ls, zig) > q_pos);
         if (tracing && lane == 0) trace[r * P + t] = skip ? -1 : s;
         if (skip) continue;
         const int j_begin = s * Ls;
@@ -91,7 +108,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         for (int j0 = j_begin; j0 < j_end; j0 += 32) {
             const int j = j0 + lane;
             float sc = -INFINITY;
-            if (j < j_end && (!causal || position(s, j - j_begin) <= q_pos)) {
+            const int kpos = position_of(s, j - j_begin, P, Ls, zig);
+            if (j < j_end && kpos >= lo && kpos <= hi) {
                 const float* krow = kb + static_cast<size_t>(j) * kv_stride;
                 float dot = 0.f;
                 for (int d = 0; d < D; d += 4) {
@@ -123,14 +141,14 @@ __global__ void __launch_bounds__(kWarps * 32)
         }
     }
     float* orow = out + (static_cast<size_t>(b) * L + i) * row_stride + static_cast<size_t>(h) * D;
-    const float inv_l = 1.f / l;
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;          // a row that saw no key: 0
 #pragma unroll
     for (int c = 0; c < kMaxD / 32; ++c) {
         const int d = lane + 32 * c;
         if (d < D) orow[d] = acc[c] * inv_l;
     }
     if (lse != nullptr && lane == 0)
-        lse[(static_cast<size_t>(b) * L + i) * H + h] = m + logf(l);
+        lse[(static_cast<size_t>(b) * L + i) * H + h] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
 }  // namespace
@@ -143,7 +161,8 @@ cudaError_t launch_attn_f32(const AttnArgs& a)
     ring_attn_f32_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, a.stream>>>(
         static_cast<const float*>(a.q), static_cast<const float*>(a.k),
         static_cast<const float*>(a.v), static_cast<float*>(a.out), a.lse, a.trace, a.B, a.L,
-        a.H, a.Hkv, a.D, a.P, a.causal, a.zigzag, 1.0f / sqrtf(static_cast<float>(a.D)));
+        a.H, a.Hkv, a.D, a.P, a.causal, a.zigzag, a.cu_seqlens, a.n_seqs,
+        1.0f / sqrtf(static_cast<float>(a.D)));
     return cudaGetLastError();
 }
 

@@ -20,6 +20,8 @@ struct AttnArgs {
     int B, L, H, D, P, causal;
     int Hkv;                       // key/value heads (H for plain attention)
     int zigzag;                    // zigzag shard layout (causal)
+    const int* cu_seqlens;         // packed sequences (device), or null
+    int n_seqs;
     unsigned int* status;          // device status word
     unsigned long long timeout_ns; // limit of one bounded wait
     cudaStream_t stream;

@@ -120,6 +120,26 @@ ra_status ring_attn_fwd_zigzag(const void* q, const void* k, const void* v, void
                                int* trace, ra_stream_t stream);
 
 /*
+ * ring_attn_fwd_varlen -- ring attention (dtype RA_BF16 or RA_F32) over packed
+ * variable-length sequences: q, k, v, out are [L, H, D] (one batch), lse [L, H],
+ * and sequence g occupies rows [cu_seqlens[g], cu_seqlens[g+1]).  A query sees
+ * only keys of its own sequence (causal: not after itself), so no sample attends
+ * to another ("序列并行与 Ring Attention", section 6.5, packed sequences must
+ * carry their boundaries).  The P virtual shards still split the packed rows
+ * evenly (L % P == 0); a sequence may span shards.  Padding to a multiple of P:
+ * add the padding rows as one more sequence and ignore its output (the
+ * Ulysses guideline page's padded_seq_len rule, section 四/六).
+ *
+ * cu_seqlens: DEVICE int32 [n_seqs + 1] with cu_seqlens[0] == 0, non-decreasing,
+ *             cu_seqlens[n_seqs] == L.  The kernels read it as given; other
+ *             contents give undefined results (never out-of-bounds accesses).
+ * A query row that sees no key (only with malformed cu_seqlens) gets 0 and -inf.
+ */
+ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                               float* lse, const int* cu_seqlens, int n_seqs, int L, int H, int D,
+                               int P, int causal, ra_dtype dtype, int* trace, ra_stream_t stream);
+
+/*
  * attn_merge_partials -- log-sum-exp merge of two partial attention results
  * over disjoint key sets (the `combine` of the juejin.cn ring-attention article, section 四):
  *   lse_out = ln(e^lse_a + e^lse_b)

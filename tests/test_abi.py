@@ -87,3 +87,15 @@ def test_zigzag_positions_layout_and_balance():
         work_contig = [sum(p + 1 for p in range(r * Ls, (r + 1) * Ls)) for r in range(P)]
         assert len(set(work_zig)) == 1
         assert work_contig == sorted(work_contig) and work_contig[0] < work_contig[-1]
+
+
+def test_varlen_padded_length_rule():
+    """ceil(total / (P * multiple)) * P * multiple: the Ulysses guideline page's example
+    of 3000 tokens over 4 shards padded to 3008 (multiple 8), and no-ops when divisible."""
+    assert cea.varlen_padded_length(3000, 4, 8) == 3008
+    assert cea.varlen_padded_length(3008, 4, 8) == 3008
+    assert cea.varlen_padded_length(1, 8) == 8
+    for total in range(1, 200):
+        for P in (1, 3, 4):
+            n = cea.varlen_padded_length(total, P, 2)
+            assert n >= total and n % (2 * P) == 0 and n - total < 2 * P

@@ -388,3 +388,58 @@ def test_zigzag_argument_errors():
     with pytest.raises(cea.RingAttnError) as e:
         cea.ring_attn_fwd_zigzag(q, k, v, P=2)            # chunks of 64 rows: not 128-aligned
     assert e.value.code == 2
+
+
+# ---------------------------------------------------------------- packed sequences --
+
+def _packed(lengths, H, D, dtype, seed):
+    L = sum(lengths)
+    q, k, v = make_qkv(1, L, H, D, seed=seed, dtype=dtype)
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    return q[0], k[0], v[0], cu
+
+
+VARLEN_CASES = [
+    # lengths, H, D, P, dtype
+    ([37, 263, 1, 399, 324], 2, 128, 2, torch.bfloat16),        # sequences cross the shard edge
+    ([1024], 2, 128, 4, torch.bfloat16),                        # one sequence = plain attention
+    ([5, 600, 130, 7, 200, 1, 593, 512], 2, 64, 4, torch.bfloat16),
+    ([100, 412, 252, 300], 1, 128, 1, torch.bfloat16),
+    ([5, 40, 1, 50], 2, 32, 3, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=lambda c: "n%d_P%d_%s" % (len(c[0]), c[3], str(c[4])[6:]))
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_parity(case, causal):
+    """Every sequence attends only within itself: each output slice equals the oracle run
+    on that sequence alone."""
+    lengths, H, D, P, dtype = case
+    q, k, v, cu = _packed(lengths, H, D, dtype, seed=70)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    out, lse = cea.ring_attn_fwd_varlen(*_dev(q, k, v), cu_d, P=P, causal=causal)
+    assert cea.check_status() == 0
+    check = assert_bf16_close if dtype == torch.bfloat16 else assert_f32_close
+    got, lg = to_np(out), to_np(lse)
+    for a, b in zip(cu[:-1], cu[1:]):
+        ref, lref = oracle.attention(q[None, a:b], k[None, a:b], v[None, a:b], causal=causal)
+        check(got[a:b], ref[0], f"rows {a}:{b}")
+        check(lg[a:b], lref[0], f"lse {a}:{b}")
+
+
+def test_varlen_samples_do_not_see_each_other():
+    """Replace one sequence's keys and values by huge values: every other sequence's
+    output is bit-for-bit unchanged (masked scores contribute exactly zero)."""
+    lengths = [300, 200, 524]
+    q, k, v, cu = _packed(lengths, 2, 128, torch.bfloat16, seed=71)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    for causal in (False, True):
+        a, _ = cea.ring_attn_fwd_varlen(*_dev(q, k, v), cu_d, P=4, causal=causal)
+        k2, v2 = k.clone(), v.clone()
+        k2[300:500] = 30.0
+        v2[300:500] = 1e4
+        b, _ = cea.ring_attn_fwd_varlen(*_dev(q, k2, v2), cu_d, P=4, causal=causal)
+        assert torch.equal(a[:300], b[:300]) and torch.equal(a[500:], b[500:])
+        assert not torch.equal(a[300:500], b[300:500])
