@@ -76,6 +76,9 @@ def _load():
             lib.oracle_attention_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, L, L, L, L,
                                                  ctypes.c_int, ctypes.c_int]
             lib.oracle_attention_bwd.restype = ctypes.c_int
+            lib.oracle_attention_bwd_dq_rows.argtypes = [dp, dp, dp, dp, dp, L, L, L, L,
+                                                         ctypes.c_int, lp, L, ctypes.c_int]
+            lib.oracle_attention_bwd_dq_rows.restype = ctypes.c_int
             for name in ("oracle_seq2head", "oracle_head2seq"):
                 fn = getattr(lib, name)
                 fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, L, L, L, L, L, L]
@@ -189,6 +192,23 @@ def attention_bwd(q, k, v, dout, causal: bool = False, threads: int | None = Non
     if rc != 0:
         raise ValueError(f"oracle_attention_bwd failed ({rc})")
     return dq, dk, dv
+
+
+def attention_bwd_dq_rows(q, k, v, dout, rows, causal: bool = False, threads: int | None = None):
+    """dq of the listed query rows only (each row needs only its own scores): works at
+    any sequence length.  Returns [B, len(rows), H, D]."""
+    lib = _load()
+    q, k, v, dout = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    B, L, H, D = q.shape
+    rows_a = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    out = np.empty((B, rows_a.shape[0], H, D), dtype=np.float64)
+    rc = lib.oracle_attention_bwd_dq_rows(_dp(q), _dp(k), _dp(v), _dp(dout), _dp(out), B, L, H, D,
+                                          int(bool(causal)),
+                                          rows_a.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
+                                          rows_a.shape[0], threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd_dq_rows failed ({rc})")
+    return out
 
 
 def merge(o_a, lse_a, o_b, lse_b):

@@ -459,3 +459,72 @@ int oracle_attention_bwd(const double* q, const double* k, const double* v, cons
     if (n_items == 0 || L == 0) return 0;
     return run_pool(bwd_item, &c, n_items, 2 * L * L, n_threads);
 }
+
+/* ------------------------------------------------------------------------- */
+/* backward for chosen query rows: dq of row i needs only row i's scores     */
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    double* dq;
+    long B, L, H, D;
+    int causal;
+    const long* rows;
+    long n_rows;
+} bwd_rows_ctx_t;
+
+/* dq_i = sum_j P_ij (dP_ij - sum_k P_ik dP_ik) k_j / sqrt(D) with P_i. = softmax of
+ * row i's scores and dP_ij = dO_i . v_j: the same chain rule as bwd_item, one row.
+ * scratch: P (L) then dP (L). */
+static void bwd_rows_item(void* vctx, long item, double* scratch)
+{
+    const bwd_rows_ctx_t* c = (const bwd_rows_ctx_t*)vctx;
+    const long L = c->L, H = c->H, D = c->D;
+    const long ri = item % c->n_rows;
+    const long bh = item / c->n_rows;
+    const long h = bh % H, b = bh / H;
+    const long i = c->rows[ri];
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+    const long n = c->causal ? i + 1 : L;     /* visible keys 0..n-1 */
+    double* P = scratch;
+    double* dP = scratch + L;
+#define AT(t, r) ((t) + ((b * L + (r)) * H + h) * D)
+    double m = -INFINITY;
+    for (long j = 0; j < n; ++j) {
+        double s = 0.0;
+        for (long d = 0; d < D; ++d) s += AT(c->q, i)[d] * AT(c->k, j)[d];
+        P[j] = s * inv_sqrt_d;
+        if (P[j] > m) m = P[j];
+    }
+    double den = 0.0;
+    for (long j = 0; j < n; ++j) { P[j] = exp(P[j] - m); den += P[j]; }
+    double rowdot = 0.0;
+    for (long j = 0; j < n; ++j) {
+        P[j] /= den;
+        double s = 0.0;
+        for (long d = 0; d < D; ++d) s += AT(c->dout, i)[d] * AT(c->v, j)[d];
+        dP[j] = s;
+        rowdot += P[j] * s;
+    }
+    double* out = c->dq + ((b * c->n_rows + ri) * H + h) * D;
+    for (long d = 0; d < D; ++d) out[d] = 0.0;
+    for (long j = 0; j < n; ++j) {
+        const double ds = P[j] * (dP[j] - rowdot);
+        for (long d = 0; d < D; ++d) out[d] += ds * AT(c->k, j)[d];
+    }
+    for (long d = 0; d < D; ++d) out[d] *= inv_sqrt_d;
+#undef AT
+}
+
+/* dq of the listed query rows only: dq_rows [B, n_rows, H, D]. */
+int oracle_attention_bwd_dq_rows(const double* q, const double* k, const double* v,
+                                 const double* dout, double* dq_rows,
+                                 long B, long L, long H, long D, int causal,
+                                 const long* rows, long n_rows, int n_threads)
+{
+    if (!q || !k || !v || !dout || !dq_rows || !rows || B < 0 || L <= 0 || H < 0 || D <= 0) return -1;
+    for (long r = 0; r < n_rows; ++r) if (rows[r] < 0 || rows[r] >= L) return -1;
+    bwd_rows_ctx_t c = { q, k, v, dout, dq_rows, B, L, H, D, causal, rows, n_rows };
+    long n_items = B * H * n_rows;
+    if (n_items == 0) return 0;
+    return run_pool(bwd_rows_item, &c, n_items, 2 * L, n_threads);
+}

@@ -8,7 +8,7 @@ import torch
 
 import context_exact_attention_gb300 as cea
 import oracle
-from context_exact_attention_gb300.workloads import (DIT, LM, LONG, ULYSSES,
+from context_exact_attention_gb300.workloads import (DIT, LM, LONG, ULYSSES, make_qkv,
                                                      make_workload_inputs, sample_rows)
 from helpers import assert_bf16_close, to_np
 
@@ -95,3 +95,87 @@ def test_merge_causal_lm_size():
     cea.attn_merge_partials(oad, lad, ob.to(DEV), lb.to(DEV), o_out=oad, lse_out=lad)
     assert_bf16_close(to_np(oad), ref, "merge o")
     assert_bf16_close(to_np(lad), lref, "merge lse")
+
+
+def test_variants_at_causal_lm_size():
+    """The causal-LM size (L=32768, D=128, P=8) through the grouped-head, zigzag and
+    packed-sequence entry points, on sampled query rows."""
+    w = LM
+    rows = sample_rows(w.L, w.P, 48, seed=1)
+    # grouped key/value heads: 16 query heads over 4 key/value heads
+    q, _, _ = make_qkv(1, w.L, 16, w.D, seed=3, dtype=torch.bfloat16)
+    _, k, v = make_qkv(1, w.L, 4, w.D, seed=4, dtype=torch.bfloat16)
+    out, lse = cea.ring_attn_fwd_gqa(*(t.to(DEV) for t in (q, k, v)), P=w.P, causal=True)
+    ref, lref = oracle.attention(q, k, v, causal=True, rows=rows)
+    assert_bf16_close(to_np(out[:, rows]), ref, "gqa out")
+    assert_bf16_close(to_np(lse[:, rows]), lref, "gqa lse")
+    # zigzag: rows are in zigzag order, the oracle sees position order
+    qg, kg, vg = make_qkv(1, w.L, 8, w.D, seed=5, dtype=torch.bfloat16)
+    pos = torch.tensor(cea.zigzag_positions(w.L, w.P))
+    out, lse = cea.ring_attn_fwd_zigzag(*(t[:, pos].contiguous().to(DEV) for t in (qg, kg, vg)),
+                                        P=w.P)
+    ref, lref = oracle.attention(qg, kg, vg, causal=True, rows=pos[rows].tolist())
+    assert_bf16_close(to_np(out[:, rows]), ref, "zigzag out")
+    assert_bf16_close(to_np(lse[:, rows]), lref, "zigzag lse")
+    # packed sequences
+    g = torch.Generator().manual_seed(6)
+    lengths = []
+    while sum(lengths) < w.L:
+        lengths.append(int(torch.randint(1, 9000, (1,), generator=g)))
+    lengths[-1] -= sum(lengths) - w.L
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    q, k, v = (t[0] for t in make_qkv(1, w.L, 8, w.D, seed=7, dtype=torch.bfloat16))
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    out, lse = cea.ring_attn_fwd_varlen(*(t.to(DEV) for t in (q, k, v)), cu_d, P=w.P, causal=True)
+    assert cea.check_status() == 0
+    got, lg = to_np(out), to_np(lse)
+    for a, b in zip(cu[:-1], cu[1:]):
+        pick = [i - a for i in rows if a <= i < b]
+        if not pick:
+            continue
+        ref, lref = oracle.attention(q[None, a:b], k[None, a:b], v[None, a:b], causal=True,
+                                     rows=pick)
+        assert_bf16_close(got[[a + i for i in pick]], ref[0], f"varlen rows in {a}:{b}")
+        assert_bf16_close(lg[[a + i for i in pick]], lref[0], f"varlen lse in {a}:{b}")
+
+
+def test_backward_at_causal_lm_size():
+    """Backward at the causal-LM size (8 heads): identities that hold at any size -- the
+    sum of dv over keys equals the sum of dout over queries, the sum of dk over keys is
+    zero -- within the accumulated bf16 rounding, and dq on sampled rows against the fp64
+    chain rule for those rows (one query row needs only its own scores)."""
+    w = LM
+    H = 8
+    q, k, v = make_qkv(1, w.L, H, w.D, seed=8, dtype=torch.bfloat16, head_scale=True)
+    do = torch.randn(1, w.L, H, w.D, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = cea.ring_attn_fwd(qd, kd, vd, P=w.P, causal=True)
+    dq, dk, dv = cea.ring_attn_bwd(qd, kd, vd, out, lse, dod, P=w.P, causal=True)
+    assert cea.check_status() == 0
+    u = 2.0 ** -9
+    sdv = dv.double().sum(1).cpu().numpy()
+    sdo = do.double().sum(1).numpy()
+    bound = 4 * u * dv.double().abs().sum(1).cpu().numpy() + 1e-3
+    assert (np.abs(sdv - sdo) <= bound).all()
+    sdk = dk.double().sum(1).cpu().numpy()
+    assert (np.abs(sdk) <= 4 * u * dk.double().abs().sum(1).cpu().numpy() + 1e-3).all()
+    # sampled dq rows against the oracle; the error scale is the first-order rounding bound
+    # of tests/test_gpu_bwd.py (term magnitudes of each element), from fp64 quantities
+    rows = sample_rows(w.L, w.P, 24, seed=2)
+    ref = oracle.attention_bwd_dq_rows(q, k, v, do, rows, causal=True)
+    qf, kf, vf, dof = (t.double().numpy()[0] for t in (q, k, v, do))
+    c = 1.0 / np.sqrt(w.D)
+    for ri, i in enumerate(rows):
+        for h in range(H):
+            s = kf[:i + 1, h] @ qf[i, h] * c
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            dp = vf[:i + 1, h] @ dof[i, h]
+            ds = p * (dp - (p * dp).sum())
+            dvec_err = np.abs(dof[i, h] * (p @ vf[:i + 1, h])).sum()
+            scale = (np.abs(ds) + p * dvec_err) @ np.abs(kf[:i + 1, h]) * c
+            got = dq[0, i, h].double().cpu().numpy()
+            r = ref[0, ri, h]
+            assert (np.abs(got - r) <= 2 * u * (np.abs(r) + scale) + 1e-6).all(), (i, h)

@@ -467,3 +467,15 @@ def test_grouped_kv_heads_equal_repeated_heads(Hk, causal):
 def test_grouped_kv_heads_must_divide():
     with pytest.raises(ValueError):
         oracle.attention(np.zeros((1, 4, 6, 2)), np.zeros((1, 4, 4, 2)), np.zeros((1, 4, 4, 2)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_dq_rows_match_full_backward(causal):
+    """The per-row dq routine (for long sequences) reproduces the rows of the full
+    backward, which the finite-difference and autograd pins tie down."""
+    B, L, H, D = 2, 29, 2, 6
+    q, k, v, do = (_rand((B, L, H, D), 100 + i) for i in range(4))
+    dq, _, _ = oracle.attention_bwd(q, k, v, do, causal=causal)
+    rows = [0, 1, 13, 28]
+    part = oracle.attention_bwd_dq_rows(q, k, v, do, rows, causal=causal)
+    np.testing.assert_allclose(part, dq[:, rows], rtol=0, atol=1e-14)
