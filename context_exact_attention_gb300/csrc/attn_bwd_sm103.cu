@@ -14,15 +14,25 @@
 // once; the query side (dQ) is one CTA per 128-row query tile walking the K/V
 // shards in the forward's order.  No atomics: results are deterministic.
 //
-// Kernels (256 threads: warp 0 TMA producer, warp 1 MMA issuer, warps 4-7 one
-// thread per TMEM lane for the elementwise step; warp-uniform schedules with one
-// elected lane issuing):
+// Kernels (384 threads: warp 0 TMA producer, warp 1 MMA issuer, warps 4-11 the
+// elementwise step -- two warps per TMEM lane quarter, warps 4-7 taking columns
+// [0,64) and warps 8-11 columns [64,128) of the same rows, each writing its bf16
+// results inside its own column range; warp-uniform schedules with one elected
+// lane issuing):
 //   bwd_rowdot_kernel   Dvec = rowsum(dO o O), fp32 workspace [B, L, H]
 //   bwd_dkdv_kernel<D>  TMEM: S^T [0,128), dP^T [128,256), dV, dK (D columns each)
 //       S^T = K Q^T, dP^T = V dO^T (SS); P^T, dS^T (bf16) written over them;
 //       dV += P^T dO, dK += dS^T Q (A from TMEM, B = dO / Q as MN-major SMEM).
-//   bwd_dq_kernel<D>    TMEM: S [0,128), dP [128,256), dQ (D columns)
-//       S = Q K^T, dP = dO V^T (SS); dS (bf16) written over S; dQ += dS K.
+//       Tensor-pipe order per block: dV(n) S^T(n+1) dK(n) dP^T(n+1), so that
+//       P^T(n) is computed while dP^T(n) runs, dS^T(n) while dV(n) and S^T(n+1) run.
+//   bwd_dq_kernel<D>    TMEM: three 128-column regions rotating between S, dP and dS,
+//       then dQ (D columns).  S = Q K^T, dP = dO V^T (SS); dS (bf16) written over S;
+//       dQ += dS K.  Block n uses regions n mod 3 (S, then dS) and (n+1) mod 3 (dP), so
+//       S and dP of block n+1 are issued as soon as block n's dP has been read, ahead
+//       of block n's dQ: the elementwise step of one block overlaps the products of
+//       the next.
+//   Elementwise arithmetic runs on packed fp32 pairs (f32x2 fma/add/mul); the causal
+//   and ragged-tail mask is applied only in the blocks that need one.
 #include <cuda_bf16.h>
 
 #include "ra_device.cuh"
@@ -32,7 +42,7 @@ namespace ra {
 namespace {
 
 constexpr int kRows = 128;     // rows per tile (TMEM lanes), both queries and keys
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;   // warps 0-3: producer, MMA issuer, idle; 4-11: elementwise
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -99,13 +109,17 @@ __global__ void __launch_bounds__(256)
 
 enum : int {
     kKVFull = 0,
-    kQFull = 1,      // +stage: Q, dO tiles (TMA) and the stats (32 producer lanes)
-    kQEmpty = 3,     // +stage
-    kKVSFull = 5,    // S^T, dP^T ready
-    kKVPFull = 6,    // P^T, dS^T written
-    kKVOFull = 7,    // dK, dV final
-    kKVDone = 8,
-    kKVBars = 9
+    kQFull = 1,      // +stage: Q tile (TMA) and the query statistics (32 producer lanes)
+    kQEmpty = 3,     // +stage: released after dK, the last reader of Q and the statistics
+    kKVDOFull = 5,     // +stage: dO tile
+    kKVDOEmpty = 7,    // +stage: released after dV, the last reader of dO
+    kKVSFull = 9,    // S^T ready
+    kKVDPFull = 10,  // dP^T ready
+    kKVPFull = 11,   // P^T written (all elementwise threads)
+    kKVDSFull = 12,  // dS^T written
+    kKVOFull = 13,   // dK, dV final
+    kKVDone = 14,
+    kKVBars = 15
 };
 
 template <int D>
@@ -126,8 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBar + kKVBars * 8);
     int* abort_flag = reinterpret_cast<int*>(smem + kBar + kKVBars * 8 + 4);
     auto bar = [&](int i) -> uint32_t { return sbase + kBar + 8u * i; };
-    auto stats_lse2 = [&](int st) { return reinterpret_cast<float*>(smem + kStats + st * 1024); };
-    auto stats_dvec = [&](int st) { return reinterpret_cast<float*>(smem + kStats + st * 1024 + 512); };
+    // per-query statistics of a stage, negated for the packed adds: -lse log2(e), -Dvec
+    auto stats_nlse2 = [&](int st) { return reinterpret_cast<float*>(smem + kStats + st * 1024); };
+    auto stats_ndvec = [&](int st) { return reinterpret_cast<float*>(smem + kStats + st * 1024 + 512); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -164,9 +179,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kQFull + i), 1 + 32);
             mbar_init(bar(kQEmpty + i), 1);
+            mbar_init(bar(kKVDOFull + i), 1);
+            mbar_init(bar(kKVDOEmpty + i), 1);
         }
         mbar_init(bar(kKVSFull), 1);
-        mbar_init(bar(kKVPFull), kRows);
+        mbar_init(bar(kKVDPFull), 1);
+        mbar_init(bar(kKVPFull), 2 * kRows);
+        mbar_init(bar(kKVDSFull), 2 * kRows);
         mbar_init(bar(kKVOFull), 1);
         mbar_init(bar(kKVDone), 1);
         *abort_flag = 0;
@@ -195,39 +214,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(sbase + kV + bx * 16384, &tmap_v, bar(kKVFull), bx * 64, h, key0, b, keep);
             }
         }
-        int last[2] = {-1, -1};
+        int last_q[2] = {-1, -1}, last_do[2] = {-1, -1};
         for (int n = 0; n < n_blocks; ++n) {
             int r, qt;
             block(n, r, qt);
             const int st = n & 1;
             const uint32_t ph = (n >> 1) & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(kQEmpty + st), ph ^ 1, wc))) break;
             const int qrow = r * p.Ls + qt * kRows;
+            // dO first: its stage is released a product earlier than the Q stage
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kKVDOEmpty + st), ph ^ 1, wc))) break;
             if (leader) {
-                mbar_arrive_expect_tx(bar(kQFull + st), 2 * T);
-                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                mbar_arrive_expect_tx(bar(kKVDOFull + st), T);
+                for (int bx = 0; bx < Lay::kBoxes; ++bx)
+                    tma_load_4d(sbase + kDO + st * T + bx * 16384, &tmap_do, bar(kKVDOFull + st), bx * 64,
+                                h, qrow, b, keep);
+            }
+            last_do[st] = n;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kQEmpty + st), ph ^ 1, wc))) break;
+            if (leader) {
+                mbar_arrive_expect_tx(bar(kQFull + st), T);
+                for (int bx = 0; bx < Lay::kBoxes; ++bx)
                     tma_load_4d(sbase + kQ + st * T + bx * 16384, &tmap_q, bar(kQFull + st), bx * 64,
                                 h, qrow, b, keep);
-                    tma_load_4d(sbase + kDO + st * T + bx * 16384, &tmap_do, bar(kQFull + st), bx * 64,
-                                h, qrow, b, keep);
-                }
             }
-            // per-query statistics of this tile: lse in base-2 units, Dvec
-            float* l2 = stats_lse2(st);
-            float* dvs = stats_dvec(st);
+            // per-query statistics of this tile: -lse in base-2 units, -Dvec
+            float* l2 = stats_nlse2(st);
+            float* dvs = stats_ndvec(st);
             for (int c = lane; c < kRows; c += 32) {
                 const int q_local = qt * kRows + c;
                 const bool valid = q_local < p.Ls;
                 const size_t idx = (static_cast<size_t>(b) * p.L + qrow + c) * p.H + h;
-                l2[c] = valid ? p.lse[idx] * kLog2e : 0.f;
-                dvs[c] = valid ? p.dvec[idx] : 0.f;
+                l2[c] = valid ? -p.lse[idx] * kLog2e : 0.f;
+                dvs[c] = valid ? -p.dvec[idx] : 0.f;
             }
             mbar_arrive(bar(kQFull + st));
-            last[st] = n;
+            last_q[st] = n;
         }
         mbar_wait_drain(bar(kKVFull), 0, wc);
-        for (int st = 0; st < 2; ++st)
-            if (last[st] >= 0) mbar_wait_drain(bar(kQFull + st), (last[st] >> 1) & 1, wc);
+        for (int st = 0; st < 2; ++st) {
+            if (last_q[st] >= 0) mbar_wait_drain(bar(kQFull + st), (last_q[st] >> 1) & 1, wc);
+            if (last_do[st] >= 0) mbar_wait_drain(bar(kKVDOFull + st), (last_do[st] >> 1) & 1, wc);
+        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -247,33 +274,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_ss(tmem + dcol, a0 + off, b0 + off, kIdescS, k > 0 ? 1u : 0u);
             }
         };
+        // A operand in TMEM: query columns [64 h, 64 h + 64) as bf16 pairs sit in columns
+        // [acol + 64 h, acol + 64 h + 32)
         auto ts = [&](uint32_t dcol, uint32_t acol, uint64_t b0, bool acc) {
 #pragma unroll
             for (int k = 0; k < kRows / 16; ++k)
-                mma_ts(tmem + dcol, tmem + acol + k * 8, b0 + ((k * 2048) >> 4), kIdescAcc,
-                       (acc || k > 0) ? 1u : 0u);
+                mma_ts(tmem + dcol, tmem + acol + 64 * (k >> 2) + (k & 3) * 8,
+                       b0 + ((k * 2048) >> 4), kIdescAcc, (acc || k > 0) ? 1u : 0u);
         };
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVFull), 0, wc));
-        for (int n = 0; ok && n < n_blocks; ++n) {
-            const int st = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kQFull + st), ph, wc)))) break;
+        auto wait_q = [&](int n) {
+            return __all_sync(0xffffffffu, mbar_wait(bar(kQFull + (n & 1)), (n >> 1) & 1, wc));
+        };
+        auto wait_do = [&](int n) {
+            return __all_sync(0xffffffffu, mbar_wait(bar(kKVDOFull + (n & 1)), (n >> 1) & 1, wc));
+        };
+        // Tensor-pipe order: S(0) dP(0) | dV(0) S(1) dK(0) dP(1) | dV(1) S(2) dK(1) dP(2) | ...
+        // so P^T(n) is computed while dP^T(n) runs and dS^T(n) while dV(n), S(n+1) run.
+        // Each product overwrites TMEM only after the products reading it were issued.
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVFull), 0, wc)) && wait_q(0);
+        if (ok) {
             tc_fence_after();
             if (leader) {
-                ss(0, dK_A, dQ_B + st * Lay::kTileU);       // S^T = K Q^T
-                ss(128, dV_A, dDO_B + st * Lay::kTileU);    // dP^T = V dO^T
+                ss(0, dK_A, dQ_B);          // S^T = K Q^T
                 tc_commit(bar(kKVSFull));
             }
             __syncwarp();
+        }
+        if (ok && (ok = wait_do(0))) {
+            tc_fence_after();
+            if (leader) {
+                ss(128, dV_A, dDO_B);       // dP^T = V dO^T
+                tc_commit(bar(kKVDPFull));
+            }
+            __syncwarp();
+        }
+        for (int n = 0; ok && n < n_blocks; ++n) {
+            const int st = n & 1;
+            const bool more = n + 1 < n_blocks;
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVPFull), n & 1, wc)))) break;
             tc_fence_after();
             if (leader) {
-                ts(256, 0, dDO_MN + st * Lay::kTileU, n > 0);          // dV += P^T dO
-                ts(256 + D, 128, dQ_MN + st * Lay::kTileU, n > 0);     // dK += dS^T Q
-                tc_commit(bar(kQEmpty + st));
-                if (n + 1 == n_blocks) tc_commit(bar(kKVOFull));
+                ts(256, 0, dDO_MN + st * Lay::kTileU, n > 0);                   // dV += P^T dO
+                tc_commit(bar(kKVDOEmpty + st));
             }
             __syncwarp();
+            if (more) {
+                if (!(ok = wait_q(n + 1))) break;
+                tc_fence_after();
+                if (leader) {
+                    ss(0, dK_A, dQ_B + (st ^ 1) * Lay::kTileU);
+                    tc_commit(bar(kKVSFull));
+                }
+                __syncwarp();
+            }
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVDSFull), n & 1, wc)))) break;
+            tc_fence_after();
+            if (leader) {
+                ts(256 + D, 128, dQ_MN + st * Lay::kTileU, n > 0);             // dK += dS^T Q
+                tc_commit(bar(kQEmpty + st));
+                if (!more) tc_commit(bar(kKVOFull));
+            }
+            __syncwarp();
+            if (more) {
+                if (!(ok = wait_do(n + 1))) break;
+                tc_fence_after();
+                if (leader) {
+                    ss(128, dV_A, dDO_B + (st ^ 1) * Lay::kTileU);
+                    tc_commit(bar(kKVDPFull));
+                }
+                __syncwarp();
+            }
         }
         if (leader) tc_commit(bar(kKVDone));
         __syncwarp();
@@ -282,13 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------------ elementwise
         const int quarter = warp & 3;
+        const int half = (warp - 4) >> 2;                 // query columns [64 half, 64 half + 64)
         const int row = quarter * 32 + lane;              // key row of the tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off;              // S^T, then P^T
-        const uint32_t tP = tmem + lane_off + 128;        // dP^T, then dS^T
+        const uint32_t tS = tmem + lane_off + 64 * half;        // S^T, then P^T
+        const uint32_t tP = tmem + lane_off + 128 + 64 * half;  // dP^T, then dS^T
         const int key_local = kt * kRows + row;           // within shard s
         const bool key_valid = key_local < p.Ls;
-        const float sl2 = p.scale_log2;
+        const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
         bool ok = true;
         for (int n = 0; n < n_blocks; ++n) {
             int r, qt;
@@ -304,66 +375,89 @@ __global__ void __launch_bounds__(kThreads, 1)
             int lo = 0;
             if (p.causal && r == s) lo = max(0, key_local - qt * kRows);
             if (!key_valid) lo = kRows;
-            const float* l2 = stats_lse2(st);
-            const float* dvs = stats_dvec(st);
+            const bool masked = __any_sync(0xffffffffu, lo > 0 || hi < kRows - 1);
+            const float* nl2 = stats_nlse2(st) + 64 * half;
+            const float* ndv = stats_ndvec(st) + 64 * half;
+            // P^T = exp2(S^T scale log2(e) - lse log2(e)); kept in fp32 for dS^T
+            uint64_t pp[32];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sr[64], dr[64];
-                tmem_ld64(tS + 64 * half, sr);
-                tmem_ld64(tP + 64 * half, dr);
-                uint32_t pk_p[32], pk_ds[32];
+            for (int chunk = 0; chunk < 2; ++chunk) {
+                uint32_t sr[32];
+                tmem_ld32(tS + 32 * chunk, sr);
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = 64 * half + 4 * i;
-                    const float4 lse4 = *reinterpret_cast<const float4*>(l2 + c);
-                    const float4 dv4 = *reinterpret_cast<const float4*>(dvs + c);
-                    const float la[4] = {lse4.x, lse4.y, lse4.z, lse4.w};
-                    const float da[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
-                    float pv[4], dsv[4];
+                for (int i = 0; i < 8; ++i) {
+                    const ulonglong2 nl = *reinterpret_cast<const ulonglong2*>(nl2 + 32 * chunk + 4 * i);
+                    const uint64_t x0 = ffma2(f2pack(u2f(sr[4 * i]), u2f(sr[4 * i + 1])), sl2, nl.x);
+                    const uint64_t x1 = ffma2(f2pack(u2f(sr[4 * i + 2]), u2f(sr[4 * i + 3])), sl2, nl.y);
+                    float a0, a1, a2, a3;
+                    f2unpack(x0, a0, a1);
+                    f2unpack(x1, a2, a3);
+                    float e[4] = {ex2(a0), ex2(a1), ex2(a2), ex2(a3)};
+                    if (masked) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int cc = c + j;
-                        const bool vis = cc >= lo && cc <= hi;
-                        const float pr = vis ? ex2(fmaf(u2f(sr[4 * i + j]), sl2, -la[j])) : 0.f;
-                        pv[j] = pr;
-                        dsv[j] = pr * (u2f(dr[4 * i + j]) - da[j]);
+                        for (int j = 0; j < 4; ++j) {
+                            const int c = 64 * half + 32 * chunk + 4 * i + j;
+                            e[j] = (c >= lo && c <= hi) ? e[j] : 0.f;
+                        }
                     }
-                    pk_p[2 * i] = pack_bf16x2(pv[0], pv[1]);
-                    pk_p[2 * i + 1] = pack_bf16x2(pv[2], pv[3]);
-                    pk_ds[2 * i] = pack_bf16x2(dsv[0], dsv[1]);
-                    pk_ds[2 * i + 1] = pack_bf16x2(dsv[2], dsv[3]);
+                    pp[16 * chunk + 2 * i] = f2pack(e[0], e[1]);
+                    pp[16 * chunk + 2 * i + 1] = f2pack(e[2], e[3]);
+                    pk[2 * i] = pack_bf16x2(e[0], e[1]);
+                    pk[2 * i + 1] = pack_bf16x2(e[2], e[3]);
                 }
-                tmem_st32(tS + 32 * half, pk_p);
-                tmem_st32(tP + 32 * half, pk_ds);
+                // 32 query columns as bf16 pairs: 16 columns, inside the ones just read
+                tmem_st16(tS + 16 * chunk, pk);
             }
             tc_fence_before();
             mbar_arrive(bar(kKVPFull));
+            // dS^T = P^T (dP^T - Dvec)
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVDPFull), n & 1, wc)))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int chunk = 0; chunk < 2; ++chunk) {
+                uint32_t dr[32];
+                tmem_ld32(tP + 32 * chunk, dr);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const ulonglong2 nd = *reinterpret_cast<const ulonglong2*>(ndv + 32 * chunk + 4 * i);
+                    const uint64_t d0 = fadd2(f2pack(u2f(dr[4 * i]), u2f(dr[4 * i + 1])), nd.x);
+                    const uint64_t d1 = fadd2(f2pack(u2f(dr[4 * i + 2]), u2f(dr[4 * i + 3])), nd.y);
+                    float g0, g1, g2, g3;
+                    f2unpack(fmul2(pp[16 * chunk + 2 * i], d0), g0, g1);
+                    f2unpack(fmul2(pp[16 * chunk + 2 * i + 1], d1), g2, g3);
+                    pk[2 * i] = pack_bf16x2(g0, g1);
+                    pk[2 * i + 1] = pack_bf16x2(g2, g3);
+                }
+                tmem_st16(tP + 16 * chunk, pk);
+            }
+            tc_fence_before();
+            mbar_arrive(bar(kKVDSFull));
         }
         if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVOFull), 0, wc));
         }
         if (ok) {
             tc_fence_after();
+            // half 0 writes dV, half 1 writes dK
             const size_t base = ((static_cast<size_t>(b) * p.L + key0 + row) * p.H + h) * D;
+            const uint32_t tA = tmem + lane_off + 256 + half * D;
+            const float mul = half ? p.scale : 1.f;
+            __nv_bfloat16* dst = (half ? p.dk : p.dv) + base;
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {       // 0: dV, 1: dK
-                const uint32_t tA = tmem + lane_off + 256 + which * D;
-                const float mul = which ? p.scale : 1.f;
-                __nv_bfloat16* dst = (which ? p.dk : p.dv) + base;
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tA + 32 * c, o);
+                uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tA + 32 * c, o);
-                    uint32_t pk[16];
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(u2f(o[2 * i]) * mul, u2f(o[2 * i + 1]) * mul);
+                if (key_valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[i] = pack_bf16x2(u2f(o[2 * i]) * mul, u2f(o[2 * i + 1]) * mul);
-                    if (key_valid) {
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                    }
+                    for (int j = 0; j < 4; ++j)
+                        d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
             }
         }
@@ -380,16 +474,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 enum : int {
     kQDFull = 0,     // Q and dO of the tile
-    kDKFull = 1,     // +stage
-    kDKEmpty = 3,    // +stage
-    kDVFull = 5,     // +stage
-    kDVEmpty = 7,    // +stage
-    kDSFull = 9,     // S, dP ready
-    kDDSFull = 10,   // dS written
-    kDOFull = 11,    // dQ final
-    kDDone = 12,
-    kDBars = 13
+    kDKFull = 1,     // +stage (three K stages: K is read last by dQ, late in a block)
+    kDKEmpty = 4,    // +stage
+    kDVFull = 7,     // +stage (two V stages)
+    kDVEmpty = 9,    // +stage
+    kDSFull = 11,    // S, dP ready
+    kDDSFull = 12,   // dS written
+    kDOFull = 13,    // dQ final
+    kDDone = 14,
+    kDFree = 15,     // dP of the current block read by the elementwise step
+    kDBars = 16
 };
+constexpr int kKStages = 3;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -400,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using Lay = BwdLayout<D>;
     constexpr int T = Lay::kTileBytes;
-    constexpr int kQ = 0, kDO = T, kK = 2 * T, kV = 4 * T, kBar = 6 * T;
+    constexpr int kQ = 0, kDO = T, kK = 2 * T, kV = (2 + kKStages) * T, kBar = (4 + kKStages) * T;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -447,16 +543,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kQDFull), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(bar(kDKFull + i), 1);
             mbar_init(bar(kDKEmpty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kDVFull + i), 1);
             mbar_init(bar(kDVEmpty + i), 1);
         }
         mbar_init(bar(kDSFull), 1);
-        mbar_init(bar(kDDSFull), kRows);
+        mbar_init(bar(kDDSFull), 2 * kRows);
         mbar_init(bar(kDOFull), 1);
         mbar_init(bar(kDDone), 1);
+        mbar_init(bar(kDFree), 2 * kRows);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -484,21 +583,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(sbase + kDO + bx * 16384, &tmap_do, bar(kQDFull), bx * 64, h, q0, b, once);
             }
         }
-        int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+        int last_k[kKStages] = {-1, -1, -1}, last_v[2] = {-1, -1};
         for (int n = 0; n < n_blocks; ++n) {
             int s, kt;
             block(n, s, kt);
             const int st = n & 1;
             const uint32_t ph = (n >> 1) & 1;
+            const int kst = n % kKStages;
+            const uint32_t kph = (n / kKStages) & 1;
             const int row = s * p.Ls + kt * kRows;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(kDKEmpty + st), ph ^ 1, wc))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kDKEmpty + kst), kph ^ 1, wc))) break;
             if (leader) {
-                mbar_arrive_expect_tx(bar(kDKFull + st), T);
+                mbar_arrive_expect_tx(bar(kDKFull + kst), T);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
-                    tma_load_4d(sbase + kK + st * T + bx * 16384, &tmap_k, bar(kDKFull + st), bx * 64,
-                                h, row, b, keep);
+                    tma_load_4d(sbase + kK + kst * T + bx * 16384, &tmap_k, bar(kDKFull + kst),
+                                bx * 64, h, row, b, keep);
             }
-            last_k[st] = n;
+            last_k[kst] = n;
             if (!__all_sync(0xffffffffu, mbar_wait(bar(kDVEmpty + st), ph ^ 1, wc))) break;
             if (leader) {
                 mbar_arrive_expect_tx(bar(kDVFull + st), T);
@@ -509,10 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             last_v[st] = n;
         }
         mbar_wait_drain(bar(kQDFull), 0, wc);
-        for (int st = 0; st < 2; ++st) {
-            if (last_k[st] >= 0) mbar_wait_drain(bar(kDKFull + st), (last_k[st] >> 1) & 1, wc);
+        for (int st = 0; st < kKStages; ++st)
+            if (last_k[st] >= 0) mbar_wait_drain(bar(kDKFull + st), (last_k[st] / kKStages) & 1, wc);
+        for (int st = 0; st < 2; ++st)
             if (last_v[st] >= 0) mbar_wait_drain(bar(kDVFull + st), (last_v[st] >> 1) & 1, wc);
-        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -531,30 +632,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_ss(tmem + dcol, a0 + off, b0 + off, kIdescS, k > 0 ? 1u : 0u);
             }
         };
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kQDFull), 0, wc));
-        for (int n = 0; ok && n < n_blocks; ++n) {
+        constexpr uint32_t kDQCol = 384;
+        auto region = [](int i) -> uint32_t { return 128u * static_cast<uint32_t>(i % 3); };
+        // S(n) = Q K_n^T into region n, dP(n) = dO V_n^T into region n+1 (mod 3)
+        auto issue_s_dp = [&](int n) {
+            const int st = n & 1;
+            ss(region(n), dQ_A, dK_B + (n % kKStages) * Lay::kTileU);
+            ss(region(n + 1), dDO_A, dV_B + st * Lay::kTileU);
+            tc_commit(bar(kDSFull));
+            tc_commit(bar(kDVEmpty + st));
+        };
+        auto wait_kv = [&](int n) {
             const int st = n & 1;
             const uint32_t ph = (n >> 1) & 1;
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kDKFull + st), ph, wc) &&
-                                                   mbar_wait(bar(kDVFull + st), ph, wc))))
-                break;
+            return __all_sync(0xffffffffu,
+                              mbar_wait(bar(kDKFull + n % kKStages), (n / kKStages) & 1, wc) &&
+                                  mbar_wait(bar(kDVFull + st), ph, wc));
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kQDFull), 0, wc));
+        if (ok && (ok = wait_kv(0))) {
             tc_fence_after();
-            if (leader) {
-                ss(0, dQ_A, dK_B + st * Lay::kTileU);      // S = Q K^T
-                ss(128, dDO_A, dV_B + st * Lay::kTileU);   // dP = dO V^T
-                tc_commit(bar(kDSFull));
-                tc_commit(bar(kDVEmpty + st));
-            }
+            if (leader) issue_s_dp(0);
             __syncwarp();
+        }
+        for (int n = 0; ok && n < n_blocks; ++n) {
+            if (n + 1 < n_blocks) {
+                // block n's dP has been read: its region is free, and the third region's
+                // dS (block n-1) was consumed by dQ(n-1), issued before
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kDFree), n & 1, wc)))) break;
+                if (!(ok = wait_kv(n + 1))) break;
+                tc_fence_after();
+                if (leader) issue_s_dp(n + 1);
+                __syncwarp();
+            }
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kDDSFull), n & 1, wc)))) break;
             tc_fence_after();
             if (leader) {
-                const uint64_t b0 = dK_MN + st * Lay::kTileU;
+                const uint64_t b0 = dK_MN + (n % kKStages) * Lay::kTileU;
+                const uint32_t a0 = tmem + region(n);
+                // dQ += dS K; dS of keys [64 h, 64 h + 64) sits in columns [64 h, 64 h + 32)
 #pragma unroll
-                for (int k = 0; k < kRows / 16; ++k)             // dQ += dS K
-                    mma_ts(tmem + 256, tmem + k * 8, b0 + ((k * 2048) >> 4), kIdescAcc,
-                           (n > 0 || k > 0) ? 1u : 0u);
-                tc_commit(bar(kDKEmpty + st));
+                for (int k = 0; k < kRows / 16; ++k)
+                    mma_ts(tmem + kDQCol, a0 + 64 * (k >> 2) + (k & 3) * 8, b0 + ((k * 2048) >> 4),
+                           kIdescAcc, (n > 0 || k > 0) ? 1u : 0u);
+                tc_commit(bar(kDKEmpty + n % kKStages));
                 if (n + 1 == n_blocks) tc_commit(bar(kDOFull));
             }
             __syncwarp();
@@ -566,16 +687,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------------ elementwise
         const int quarter = warp & 3;
+        const int half = (warp - 4) >> 2;                   // key columns [64 half, 64 half + 64)
         const int row = quarter * 32 + lane;                // query row of the tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off;                // S, then dS
-        const uint32_t tP = tmem + lane_off + 128;          // dP
+        auto region = [](int i) -> uint32_t { return 128u * static_cast<uint32_t>(i % 3); };
         const int row_local = q_local0 + row;
         const bool row_valid = row_local < p.Ls;
         const size_t sidx = (static_cast<size_t>(b) * p.L + q0 + row) * p.H + h;
-        const float lse2 = row_valid ? p.lse[sidx] * kLog2e : 0.f;
-        const float dvr = row_valid ? p.dvec[sidx] : 0.f;
-        const float sl2 = p.scale_log2;
+        const float nl2 = row_valid ? -p.lse[sidx] * kLog2e : 0.f;
+        const float ndv = row_valid ? -p.dvec[sidx] : 0.f;
+        const uint64_t nl2x2 = f2pack(nl2, nl2);
+        const uint64_t ndvx2 = f2pack(ndv, ndv);
+        const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
         bool ok = true;
         for (int n = 0; n < n_blocks; ++n) {
             int s, kt;
@@ -586,20 +709,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             int lim = min(kRows - 1, p.Ls - kt * kRows - 1);
             if (p.causal && s == r) lim = min(lim, row_local - kt * kRows);
             if (!row_valid) lim = -1;
+            const bool masked = __any_sync(0xffffffffu, lim < kRows - 1);
+            const uint32_t tS = tmem + lane_off + region(n) + 64 * half;        // S, then dS
+            const uint32_t tP = tmem + lane_off + region(n + 1) + 64 * half;    // dP
+            // dP - Dvec of this warp's 64 columns; once both halves have read dP, the MMA
+            // issuer may reuse its region for the next block's S
+            uint64_t dd[32];
+            {
+                uint32_t dr[64];
+                tmem_ld64(tP, dr);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sr[64], dr[64];
-                tmem_ld64(tS + 64 * half, sr);
-                tmem_ld64(tP + 64 * half, dr);
-                uint32_t pk[32];
+                for (int i = 0; i < 32; ++i) dd[i] = fadd2(f2pack(u2f(dr[2 * i]), u2f(dr[2 * i + 1])), ndvx2);
+            }
+            tc_fence_before();
+            mbar_arrive(bar(kDFree));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = 64 * half + 2 * i;
-                    const float p0 = (c <= lim) ? ex2(fmaf(u2f(sr[2 * i]), sl2, -lse2)) : 0.f;
-                    const float p1 = (c + 1 <= lim) ? ex2(fmaf(u2f(sr[2 * i + 1]), sl2, -lse2)) : 0.f;
-                    pk[i] = pack_bf16x2(p0 * (u2f(dr[2 * i]) - dvr), p1 * (u2f(dr[2 * i + 1]) - dvr));
+            for (int chunk = 0; chunk < 2; ++chunk) {
+                uint32_t sr[32];
+                tmem_ld32(tS + 32 * chunk, sr);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float a0, a1;
+                    f2unpack(ffma2(f2pack(u2f(sr[2 * i]), u2f(sr[2 * i + 1])), sl2, nl2x2), a0, a1);
+                    float e0 = ex2(a0), e1 = ex2(a1);
+                    if (masked) {
+                        const int c = 64 * half + 32 * chunk + 2 * i;
+                        e0 = (c <= lim) ? e0 : 0.f;
+                        e1 = (c + 1 <= lim) ? e1 : 0.f;
+                    }
+                    float g0, g1;
+                    f2unpack(fmul2(f2pack(e0, e1), dd[16 * chunk + i]), g0, g1);
+                    pk[i] = pack_bf16x2(g0, g1);
                 }
-                tmem_st32(tS + 32 * half, pk);
+                // dS of 32 keys as bf16 pairs: 16 columns, inside the ones already read
+                tmem_st16(tS + 16 * chunk, pk);
             }
             tc_fence_before();
             mbar_arrive(bar(kDDSFull));
@@ -607,17 +751,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kDOFull), 0, wc));
         if (ok) {
             tc_fence_after();
+            // each half writes half of the D output columns
             __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(b) * p.L + q0 + row) * p.H + h) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
+                const int col = half * (D / 2) + 32 * c;
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + 256 + 32 * c, o);
+                tmem_ld32(tmem + lane_off + 384 + col, o);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack_bf16x2(u2f(o[2 * i]) * p.scale, u2f(o[2 * i + 1]) * p.scale);
                 if (row_valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
@@ -639,7 +785,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
 {
     using Lay = BwdLayout<D>;
     constexpr int kSmemKV = 6 * Lay::kTileBytes + 2048 + 256 + 1024;
-    constexpr int kSmemQ = 6 * Lay::kTileBytes + 256 + 1024;
+    constexpr int kSmemQ = (4 + kKStages) * Lay::kTileBytes + 256 + 1024;
     static int configured[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
