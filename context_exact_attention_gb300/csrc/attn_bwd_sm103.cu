@@ -14,8 +14,9 @@
 // once; the query side (dQ) is one CTA per 128-row query tile walking the K/V
 // shards in the forward's order.  No atomics: results are deterministic.
 //
-// Kernels (384 threads: warp 0 TMA producer, warp 1 MMA issuer, warps 4-11 the
-// elementwise step -- two warps per TMEM lane quarter, warps 4-7 taking columns
+// Kernels (384 threads: warp 0 TMA producer, warp 1 MMA issuer, in the dK/dV kernel
+// warps 2-3 the per-query statistics, warps 4-11 the elementwise step -- two warps per
+// TMEM lane quarter, warps 4-7 taking columns
 // [0,64) and warps 8-11 columns [64,128) of the same rows, each writing its bf16
 // results inside its own column range; warp-uniform schedules with one elected
 // lane issuing):
@@ -42,7 +43,7 @@ namespace ra {
 namespace {
 
 constexpr int kRows = 128;     // rows per tile (TMEM lanes), both queries and keys
-constexpr int kThreads = 384;   // warps 0-3: producer, MMA issuer, idle; 4-11: elementwise
+constexpr int kThreads = 384;   // warps 0-3: producer, MMA issuer, statistics (dK/dV); 4-11: elementwise
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -107,19 +108,38 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------------ dK, dV --
 
+constexpr int kQStages = 3;          // Q is read last by dK, late in a block: three stages
+constexpr int kMaxSmem = 232448;     // opt-in shared memory limit of one block (227 KiB)
+
 enum : int {
     kKVFull = 0,
-    kQFull = 1,      // +stage: Q tile (TMA) and the query statistics (32 producer lanes)
-    kQEmpty = 3,     // +stage: released after dK, the last reader of Q and the statistics
-    kKVDOFull = 5,     // +stage: dO tile
-    kKVDOEmpty = 7,    // +stage: released after dV, the last reader of dO
-    kKVSFull = 9,    // S^T ready
-    kKVDPFull = 10,  // dP^T ready
-    kKVPFull = 11,   // P^T written (all elementwise threads)
-    kKVDSFull = 12,  // dS^T written
-    kKVOFull = 13,   // dK, dV final
-    kKVDone = 14,
-    kKVBars = 15
+    kQFull = 1,        // +stage (3): Q tile (TMA) and its -lse statistics (warp 2)
+    kQEmpty = 4,       // +stage: released after dK, the last reader of Q
+    kKVDOFull = 7,     // +stage (2): dO tile and its -Dvec statistics (warp 3)
+    kKVDOEmpty = 9,    // +stage: released after dK too (the dS^T step reads -Dvec)
+    kKVSFull = 11,     // S^T ready
+    kKVDPFull = 12,    // dP^T ready
+    kKVPFull = 13,     // P^T written (all elementwise threads)
+    kKVDSFull = 14,    // dS^T written
+    kKVOFull = 15,     // dK, dV final
+    kKVDone = 16,
+    kKVBars = 17
+};
+
+// Shared memory of the dK/dV kernel from a 1024-aligned base: K, V, three Q stages, two dO
+// stages, the statistics (128 fp32 per stage), barriers.  The allocation adds what is left
+// of the 227 KiB limit for aligning the base; the kernel checks that this was enough.
+template <int D>
+struct KVSmem {
+    static constexpr int T = kRows * D * 2;
+    static constexpr int kK = 0, kV = T, kQ = 2 * T, kDO = (2 + kQStages) * T;
+    static constexpr int kNlse = (4 + kQStages) * T;
+    static constexpr int kNdvec = kNlse + kQStages * kRows * 4;
+    static constexpr int kBar = kNdvec + 2 * kRows * 4;
+    static constexpr int kNeed = kBar + 256;
+    static constexpr int kAlloc = kNeed + 1023 < kMaxSmem ? kNeed + 1023 : kMaxSmem;
+    static_assert(kNeed <= kMaxSmem, "dK/dV shared memory layout exceeds the limit");
+    static_assert(kKVBars * 8 + 8 <= 256, "barrier area");
 };
 
 template <int D>
@@ -130,19 +150,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmap_do, const BwdParams p)
 {
     using Lay = BwdLayout<D>;
+    using Sm = KVSmem<D>;
     constexpr int T = Lay::kTileBytes;
-    constexpr int kK = 0, kV = T, kQ = 2 * T, kDO = 4 * T, kStats = 6 * T;   // stats: 2 x 1 KiB
-    constexpr int kBar = kStats + 2048;
+    constexpr int kK = Sm::kK, kV = Sm::kV, kQ = Sm::kQ, kDO = Sm::kDO, kBar = Sm::kBar;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_addr(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+    if (pad + Sm::kNeed > static_cast<uint32_t>(Sm::kAlloc)) {
+        // the dynamic shared memory base leaves too little room to align the tiles
+        if (threadIdx.x == 0) atomicOr(p.status, RA_STATUS_LAYOUT);
+        return;
+    }
+    uint8_t* smem = smem_raw + pad;
     const uint32_t sbase = smem_addr(smem);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBar + kKVBars * 8);
     int* abort_flag = reinterpret_cast<int*>(smem + kBar + kKVBars * 8 + 4);
     auto bar = [&](int i) -> uint32_t { return sbase + kBar + 8u * i; };
-    // per-query statistics of a stage, negated for the packed adds: -lse log2(e), -Dvec
-    auto stats_nlse2 = [&](int st) { return reinterpret_cast<float*>(smem + kStats + st * 1024); };
-    auto stats_ndvec = [&](int st) { return reinterpret_cast<float*>(smem + kStats + st * 1024 + 512); };
+    // per-query statistics, negated for the packed adds: -lse log2(e) with the Q stage,
+    // -Dvec with the dO stage
+    auto stats_nlse2 = [&](int qs) { return reinterpret_cast<float*>(smem + Sm::kNlse + qs * 512); };
+    auto stats_ndvec = [&](int ds) { return reinterpret_cast<float*>(smem + Sm::kNdvec + ds * 512); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -176,10 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kKVFull), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQStages; ++i) {
             mbar_init(bar(kQFull + i), 1 + 32);
             mbar_init(bar(kQEmpty + i), 1);
-            mbar_init(bar(kKVDOFull + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kKVDOFull + i), 1 + 32);
             mbar_init(bar(kKVDOEmpty + i), 1);
         }
         mbar_init(bar(kKVSFull), 1);
@@ -214,47 +243,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(sbase + kV + bx * 16384, &tmap_v, bar(kKVFull), bx * 64, h, key0, b, keep);
             }
         }
-        int last_q[2] = {-1, -1}, last_do[2] = {-1, -1};
+        int last_q[kQStages] = {-1, -1, -1}, last_do[2] = {-1, -1};
         for (int n = 0; n < n_blocks; ++n) {
             int r, qt;
             block(n, r, qt);
-            const int st = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
+            const int qs = n % kQStages, ds = n & 1;
             const int qrow = r * p.Ls + qt * kRows;
-            // dO first: its stage is released a product earlier than the Q stage
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(kKVDOEmpty + st), ph ^ 1, wc))) break;
+            // Q first: its stage frees a block earlier than the dO stage, and S^T needs it first
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kQEmpty + qs), ((n / kQStages) & 1) ^ 1, wc)))
+                break;
             if (leader) {
-                mbar_arrive_expect_tx(bar(kKVDOFull + st), T);
+                mbar_arrive_expect_tx(bar(kQFull + qs), T);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
-                    tma_load_4d(sbase + kDO + st * T + bx * 16384, &tmap_do, bar(kKVDOFull + st), bx * 64,
+                    tma_load_4d(sbase + kQ + qs * T + bx * 16384, &tmap_q, bar(kQFull + qs), bx * 64,
                                 h, qrow, b, keep);
             }
-            last_do[st] = n;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(kQEmpty + st), ph ^ 1, wc))) break;
+            last_q[qs] = n;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kKVDOEmpty + ds), ((n >> 1) & 1) ^ 1, wc))) break;
             if (leader) {
-                mbar_arrive_expect_tx(bar(kQFull + st), T);
+                mbar_arrive_expect_tx(bar(kKVDOFull + ds), T);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
-                    tma_load_4d(sbase + kQ + st * T + bx * 16384, &tmap_q, bar(kQFull + st), bx * 64,
-                                h, qrow, b, keep);
+                    tma_load_4d(sbase + kDO + ds * T + bx * 16384, &tmap_do, bar(kKVDOFull + ds),
+                                bx * 64, h, qrow, b, keep);
             }
-            // per-query statistics of this tile: -lse in base-2 units, -Dvec
-            float* l2 = stats_nlse2(st);
-            float* dvs = stats_ndvec(st);
-            for (int c = lane; c < kRows; c += 32) {
-                const int q_local = qt * kRows + c;
-                const bool valid = q_local < p.Ls;
-                const size_t idx = (static_cast<size_t>(b) * p.L + qrow + c) * p.H + h;
-                l2[c] = valid ? -p.lse[idx] * kLog2e : 0.f;
-                dvs[c] = valid ? -p.dvec[idx] : 0.f;
-            }
-            mbar_arrive(bar(kQFull + st));
-            last_q[st] = n;
+            last_do[ds] = n;
         }
         mbar_wait_drain(bar(kKVFull), 0, wc);
-        for (int st = 0; st < 2; ++st) {
-            if (last_q[st] >= 0) mbar_wait_drain(bar(kQFull + st), (last_q[st] >> 1) & 1, wc);
-            if (last_do[st] >= 0) mbar_wait_drain(bar(kKVDOFull + st), (last_do[st] >> 1) & 1, wc);
-        }
+        for (int i = 0; i < kQStages; ++i)
+            if (last_q[i] >= 0) mbar_wait_drain(bar(kQFull + i), (last_q[i] / kQStages) & 1, wc);
+        for (int i = 0; i < 2; ++i)
+            if (last_do[i] >= 0) mbar_wait_drain(bar(kKVDOFull + i), (last_do[i] >> 1) & 1, wc);
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -283,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        b0 + ((k * 2048) >> 4), kIdescAcc, (acc || k > 0) ? 1u : 0u);
         };
         auto wait_q = [&](int n) {
-            return __all_sync(0xffffffffu, mbar_wait(bar(kQFull + (n & 1)), (n >> 1) & 1, wc));
+            return __all_sync(0xffffffffu,
+                              mbar_wait(bar(kQFull + n % kQStages), (n / kQStages) & 1, wc));
         };
         auto wait_do = [&](int n) {
             return __all_sync(0xffffffffu, mbar_wait(bar(kKVDOFull + (n & 1)), (n >> 1) & 1, wc));
@@ -313,16 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool more = n + 1 < n_blocks;
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVPFull), n & 1, wc)))) break;
             tc_fence_after();
-            if (leader) {
-                ts(256, 0, dDO_MN + st * Lay::kTileU, n > 0);                   // dV += P^T dO
-                tc_commit(bar(kKVDOEmpty + st));
-            }
+            if (leader) ts(256, 0, dDO_MN + st * Lay::kTileU, n > 0);           // dV += P^T dO
             __syncwarp();
             if (more) {
                 if (!(ok = wait_q(n + 1))) break;
                 tc_fence_after();
                 if (leader) {
-                    ss(0, dK_A, dQ_B + (st ^ 1) * Lay::kTileU);
+                    ss(0, dK_A, dQ_B + ((n + 1) % kQStages) * Lay::kTileU);
                     tc_commit(bar(kKVSFull));
                 }
                 __syncwarp();
@@ -330,8 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVDSFull), n & 1, wc)))) break;
             tc_fence_after();
             if (leader) {
-                ts(256 + D, 128, dQ_MN + st * Lay::kTileU, n > 0);             // dK += dS^T Q
-                tc_commit(bar(kQEmpty + st));
+                ts(256 + D, 128, dQ_MN + (n % kQStages) * Lay::kTileU, n > 0);  // dK += dS^T Q
+                tc_commit(bar(kQEmpty + n % kQStages));
+                tc_commit(bar(kKVDOEmpty + st));
                 if (!more) tc_commit(bar(kKVOFull));
             }
             __syncwarp();
@@ -349,6 +366,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         mbar_wait_drain(bar(kKVDone), 0, wc);
         __syncwarp();
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------------------------ statistics
+        // Warp 2 writes -lse log2(e) into the Q stage, warp 3 -Dvec into the dO stage, each
+        // lane four query rows; the global loads of a block are issued before waiting for
+        // its stage, so their latency overlaps the wait.
+        const bool is_lse = warp == 2;
+        const float* src = is_lse ? p.lse : p.dvec;
+        const float mul = is_lse ? -kLog2e : -1.f;
+        auto fetch = [&](int n, float (&v)[4]) {
+            int r, qt;
+            block(n, r, qt);
+            const int qrow = r * p.Ls + qt * kRows;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = lane + 32 * j;
+                const size_t idx = (static_cast<size_t>(b) * p.L + qrow + c) * p.H + h;
+                v[j] = (qt * kRows + c < p.Ls) ? src[idx] * mul : 0.f;
+            }
+        };
+        float v[4];
+        fetch(0, v);
+        for (int n = 0; n < n_blocks; ++n) {
+            float nxt[4] = {0.f, 0.f, 0.f, 0.f};
+            if (n + 1 < n_blocks) fetch(n + 1, nxt);
+            float* dst;
+            uint32_t full;
+            bool ok;
+            if (is_lse) {
+                const int qs = n % kQStages;
+                ok = mbar_wait(bar(kQEmpty + qs), ((n / kQStages) & 1) ^ 1, wc);
+                dst = stats_nlse2(qs);
+                full = bar(kQFull + qs);
+            } else {
+                const int ds = n & 1;
+                ok = mbar_wait(bar(kKVDOEmpty + ds), ((n >> 1) & 1) ^ 1, wc);
+                dst = stats_ndvec(ds);
+                full = bar(kKVDOFull + ds);
+            }
+            if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[lane + 32 * j] = v[j];
+            mbar_arrive(full);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = nxt[j];
+        }
     } else if (warp >= 4) {
         // ------------------------------------------------------ elementwise
         const int quarter = warp & 3;
@@ -366,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             block(n, r, qt);
             const int st = n & 1;
             ok = mbar_wait(bar(kKVSFull), n & 1, wc);
-            ok = ok && mbar_wait(bar(kQFull + st), (n >> 1) & 1, wc);
+            ok = ok && mbar_wait(bar(kQFull + n % kQStages), (n / kQStages) & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -376,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.causal && r == s) lo = max(0, key_local - qt * kRows);
             if (!key_valid) lo = kRows;
             const bool masked = __any_sync(0xffffffffu, lo > 0 || hi < kRows - 1);
-            const float* nl2 = stats_nlse2(st) + 64 * half;
+            const float* nl2 = stats_nlse2(n % kQStages) + 64 * half;
             const float* ndv = stats_ndvec(st) + 64 * half;
             // P^T = exp2(S^T scale log2(e) - lse log2(e)); kept in fp32 for dS^T
             uint64_t pp[32];
@@ -412,7 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(kKVPFull));
             // dS^T = P^T (dP^T - Dvec)
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVDPFull), n & 1, wc)))) break;
+            ok = mbar_wait(bar(kKVDPFull), n & 1, wc);
+            ok = ok && mbar_wait(bar(kKVDOFull + st), (n >> 1) & 1, wc);    // -Dvec statistics
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;
             tc_fence_after();
 #pragma unroll
             for (int chunk = 0; chunk < 2; ++chunk) {
@@ -784,7 +848,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
                          const CUtensorMap& tv, const CUtensorMap& tdo)
 {
     using Lay = BwdLayout<D>;
-    constexpr int kSmemKV = 6 * Lay::kTileBytes + 2048 + 256 + 1024;
+    constexpr int kSmemKV = KVSmem<D>::kAlloc;
     constexpr int kSmemQ = (4 + kKStages) * Lay::kTileBytes + 256 + 1024;
     static int configured[64] = {0};
     int dev = 0;

@@ -11,6 +11,7 @@
 
 // Bits of the per-device status word.
 #define RA_STATUS_TIMEOUT 1u
+#define RA_STATUS_LAYOUT 2u   // a kernel could not lay out its shared memory and did nothing
 
 namespace ra {
 

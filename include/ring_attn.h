@@ -19,7 +19,9 @@
  *   reported through the return value; nothing is written in that case.
  *   Launch failures return RA_ERR_CUDA.  Kernels that give up waiting (a
  *   bounded wait ran out) record RA_ERR_TIMEOUT in a per-device status word
- *   that ra_check_status() reads and clears; they never trap.
+ *   that ra_check_status() reads and clears; they never trap.  A kernel that
+ *   finds its dynamic shared memory too misaligned to lay out its tiles writes
+ *   nothing and records an error that ra_check_status() reports as RA_ERR_CUDA.
  */
 #ifndef RING_ATTN_H
 #define RING_ATTN_H
