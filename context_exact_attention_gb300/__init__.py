@@ -23,7 +23,7 @@ __all__ = [
     "ring_attn_fwd_trace", "attn_merge_partials", "ulysses_seq2head", "ulysses_head2seq",
     "ulysses_attention", "ring_attn_bwd", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
     "zigzag_positions", "ring_attn_fwd_varlen", "varlen_padded_length", "check_status",
-    "probe_wait_timeout",
+    "probe_wait_timeout", "ring_attn_fwd_host", "host_workspace_bytes",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "ulysses_seq2head", "ulysses_head2seq", "ra_check_status", "ra_status_string",
     "ra_probe_wait_timeout", "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
     "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
-    "ring_attn_fwd_varlen",
+    "ring_attn_fwd_varlen", "ring_attn_fwd_host", "ring_attn_fwd_host_workspace_bytes",
 )
 
 
@@ -85,11 +85,15 @@ def load_library(build_if_missing: bool = False):
             "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
             "ring_attn_fwd_zigzag": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp, vp],
             "ring_attn_fwd_varlen": [vp, vp, vp, vp, f_p, vp, i, i, i, i, i, i, i, vp, vp],
+            "ring_attn_fwd_host": [vp, vp, vp, vp, f_p, vp, ctypes.c_ulonglong, i, i, i, i, i, i,
+                                   i, vp],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        lib.ring_attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.ring_attn_fwd_host_workspace_bytes.restype = ctypes.c_ulonglong
         lib.ring_attn_bwd_workspace_bytes.argtypes = [i, i, i]
         lib.ring_attn_bwd_workspace_bytes.restype = ctypes.c_ulonglong
         lib.ra_status_string.argtypes = [ctypes.c_int]
@@ -153,6 +157,51 @@ def ring_attn_fwd(q, k, v, P: int = 1, causal: bool = False, out=None, lse=None,
                   want_lse: bool = True, stream=None):
     """bf16 ring attention forward over P virtual shards.  Returns (out, lse)."""
     return _attn("ring_attn_fwd", q, k, v, P, causal, out, lse, want_lse, torch.bfloat16, stream)
+
+
+def host_workspace_bytes(B: int, L: int, H: int, D: int, heads_per_group: int) -> int:
+    """Device workspace bytes ring_attn_fwd_host needs (0 for invalid sizes)."""
+    return int(load_library().ring_attn_fwd_host_workspace_bytes(B, L, H, D, heads_per_group))
+
+
+def ring_attn_fwd_host(q, k, v, P: int = 1, causal: bool = False, out=None, lse=None,
+                       want_lse: bool = True, heads_per_group: int | None = None,
+                       workspace=None, device=None, stream=None):
+    """ring_attn_fwd on HOST bf16 [B, L, H, D] tensors (pin them for overlap): the
+    library copies head groups in, runs the attention and copies the results back,
+    overlapping the three.  Returns host (out, lse) once the work is enqueued on
+    `stream`; synchronize the stream before reading them."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 [B, L, H, D] host tensor")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k, v must have the same shape")
+    B, L, H, D = q.shape
+    if heads_per_group is None:
+        heads_per_group = next(g for g in (4, 2, 1) if H % g == 0)
+    dev = torch.device(device) if device is not None else torch.device(
+        "cuda", torch.cuda.current_device())
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin)
+    if lse is None and want_lse:
+        lse = torch.empty((B, L, H), dtype=torch.float32, pin_memory=pin)
+    if out.is_cuda or (lse is not None and lse.is_cuda):
+        raise ValueError("out and lse must be host tensors")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, L, H)
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [B, L, H] tensor")
+    need = host_workspace_bytes(B, L, H, D, heads_per_group)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a device tensor")
+    _call("ring_attn_fwd_host", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace),
+          ctypes.c_ulonglong(workspace.numel() * workspace.element_size()), B, L, H, D, P,
+          int(bool(causal)), int(heads_per_group), _stream(stream))
+    return out, lse
 
 
 def ring_attn_fwd_f32(q, k, v, P: int = 1, causal: bool = False, out=None, lse=None,

@@ -142,6 +142,44 @@ ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void
                                int P, int causal, ra_dtype dtype, int* trace, ra_stream_t stream);
 
 /*
+ * ring_attn_fwd_host -- ring_attn_fwd (bf16) on tensors in HOST memory, with the
+ * host<->device copies overlapped with the attention (no counterpart on the pages:
+ * an addition of this library for callers whose activations live on the host).
+ *
+ * The operation and the result are exactly those of ring_attn_fwd on the same
+ * values (bit-identical: attention is independent per head, and each head goes
+ * through the same kernel).  Heads are processed in groups of heads_per_group:
+ * group g's q, k, v are copied to the device while group g-1 computes, and its
+ * output is copied back while later groups compute.
+ *
+ * q_host, k_host, v_host, out_host: host bf16 [B, L, H, D]; lse_host: host fp32
+ *     [B, L, H] or NULL.  Page-locked memory (cudaHostAlloc, torch pin_memory) is
+ *     needed for the copies to overlap anything; pageable memory gives correct
+ *     results with copies the runtime stages and serialises.  out_host and
+ *     lse_host must not overlap the inputs.
+ * workspace: device memory of at least
+ *     ring_attn_fwd_host_workspace_bytes(B, L, H, D, heads_per_group) bytes,
+ *     256-byte aligned, owned by the caller; no other work may use it until the
+ *     call's work on `stream` has completed.  Contents need no initialisation.
+ * heads_per_group: 1 <= heads_per_group <= H, H % heads_per_group == 0
+ *     (RA_ERR_NOT_DIVISIBLE otherwise).  Smaller groups overlap more of the copies;
+ *     each group is one kernel launch over B * heads_per_group heads.
+ * Streams: the work starts after the caller's earlier work on `stream`, and later
+ * work on `stream` (or cudaStreamSynchronize(stream)) sees out_host and lse_host
+ * complete.  The library runs the copies and the groups' kernels on its own
+ * streams (two copy streams and two compute streams per device, created on first
+ * use and kept until exit); enqueueing holds a per-device lock.
+ * Errors: as ring_attn_fwd, plus RA_ERR_INVALID_ARG for a short workspace and
+ * RA_ERR_MISALIGNED for a workspace not 256-byte aligned.
+ */
+unsigned long long ring_attn_fwd_host_workspace_bytes(int B, int L, int H, int D,
+                                                      int heads_per_group);
+ra_status ring_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                             void* out_host, float* lse_host, void* workspace,
+                             unsigned long long workspace_bytes, int B, int L, int H, int D, int P,
+                             int causal, int heads_per_group, ra_stream_t stream);
+
+/*
  * attn_merge_partials -- log-sum-exp merge of two partial attention results
  * over disjoint key sets (the `combine` of the juejin.cn ring-attention article, section 四):
  *   lse_out = ln(e^lse_a + e^lse_b)

@@ -99,3 +99,41 @@ def test_varlen_padded_length_rule():
         for P in (1, 3, 4):
             n = cea.varlen_padded_length(total, P, 2)
             assert n >= total and n % (2 * P) == 0 and n - total < 2 * P
+
+
+def test_host_entry_argument_errors(lib):
+    """ring_attn_fwd_host checks its arguments on the host before touching the runtime."""
+    fake = ctypes.c_void_p(1 << 20)
+    out = ctypes.c_void_p(1 << 40)
+    ws = ctypes.c_void_p(1 << 44)
+    null = ctypes.c_void_p(0)
+    s = ctypes.c_void_p(0)
+    B, L, H, D, P = 1, 256, 8, 128, 4
+    need = lib.ring_attn_fwd_host_workspace_bytes(B, L, H, D, 2)
+    big = ctypes.c_ulonglong(need)
+    f = lib.ring_attn_fwd_host
+    # group size must divide H
+    assert f(fake, fake, fake, out, null, ws, big, B, L, H, D, P, 1, 3, s) == 4
+    assert f(fake, fake, fake, out, null, ws, big, B, L, H, D, P, 1, 0, s) == 1
+    assert f(fake, fake, fake, out, null, ws, big, B, L, H, D, P, 1, 9, s) == 1
+    # short or misaligned workspace, missing pointers
+    assert f(fake, fake, fake, out, null, ws, ctypes.c_ulonglong(need - 1), B, L, H, D, P, 1, 2, s) == 1
+    assert f(fake, fake, fake, out, null, ctypes.c_void_p((1 << 44) + 16), big, B, L, H, D, P, 1, 2, s) == 3
+    assert f(fake, fake, fake, out, null, null, big, B, L, H, D, P, 1, 2, s) == 1
+    # head dim, shard divisibility, output overlapping an input
+    assert f(fake, fake, fake, out, null, ws, big, B, L, H, 96, P, 1, 2, s) == 2
+    assert f(fake, fake, fake, out, null, ws, ctypes.c_ulonglong(1 << 30), B, 250, H, D, P, 1, 2, s) == 4
+    assert f(fake, fake, fake, fake, null, ws, big, B, L, H, D, P, 1, 2, s) == 1
+
+
+def test_host_workspace_size():
+    """Three slots of (q, k, v, out, lse) for one head group plus the full lse, each
+    rounded up to 256 bytes; 0 for sizes that cannot be grouped."""
+    lib = cea.load_library()
+    r = lambda x: (x + 255) // 256 * 256
+    for (B, L, H, D, g) in [(1, 256, 8, 128, 2), (2, 1000, 6, 64, 3), (1, 32768, 32, 128, 4)]:
+        rows = B * L
+        slot = 4 * r(rows * g * D * 2) + r(rows * g * 4)
+        assert lib.ring_attn_fwd_host_workspace_bytes(B, L, H, D, g) == 3 * slot + r(rows * H * 4)
+    assert lib.ring_attn_fwd_host_workspace_bytes(1, 256, 8, 128, 3) == 0
+    assert lib.ring_attn_fwd_host_workspace_bytes(1, 256, 8, 128, 16) == 0
