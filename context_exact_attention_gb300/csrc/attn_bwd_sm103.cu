@@ -26,12 +26,10 @@
 //       dV += P^T dO, dK += dS^T Q (A from TMEM, B = dO / Q as MN-major SMEM).
 //       Tensor-pipe order per block: dV(n) S^T(n+1) dK(n) dP^T(n+1), so that
 //       P^T(n) is computed while dP^T(n) runs, dS^T(n) while dV(n) and S^T(n+1) run.
-//   bwd_dq_kernel<D>    TMEM: three 128-column regions rotating between S, dP and dS,
-//       then dQ (D columns).  S = Q K^T, dP = dO V^T (SS); dS (bf16) written over S;
-//       dQ += dS K.  Block n uses regions n mod 3 (S, then dS) and (n+1) mod 3 (dP), so
-//       S and dP of block n+1 are issued as soon as block n's dP has been read, ahead
-//       of block n's dQ: the elementwise step of one block overlaps the products of
-//       the next.
+//   bwd_dq_kernel<D>    TMEM: S, then dS, alternating between [0,128) and [128,256) by
+//       block parity; dP in [256,384); dQ (D columns) at 384.  S = Q K^T, dP = dO V^T
+//       (SS); dS (bf16) written over S; dQ += dS K.  Tensor-pipe order per block:
+//       S(n+1) dP(n+1) dQ(n), so block n+1's elementwise step overlaps dQ(n).
 //   Elementwise arithmetic runs on packed fp32 pairs (f32x2 fma/add/mul); the causal
 //   and ragged-tail mask is applied only in the blocks that need one.
 #include <cuda_bf16.h>
@@ -330,37 +328,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = 0; ok && n < n_blocks; ++n) {
             const int st = n & 1;
             const bool more = n + 1 < n_blocks;
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVPFull), n & 1, wc)))) break;
+            // P^T(n) written and (if another block follows) Q(n+1) loaded: dV(n), S^T(n+1)
+            const int q1 = (n + 1) % kQStages;
+            ok = more ? mbar_wait2(bar(kKVPFull), n & 1, bar(kQFull + q1), ((n + 1) / kQStages) & 1, wc)
+                      : mbar_wait(bar(kKVPFull), n & 1, wc);
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;
             tc_fence_after();
-            if (leader) ts(256, 0, dDO_MN + st * Lay::kTileU, n > 0);           // dV += P^T dO
-            __syncwarp();
-            if (more) {
-                if (!(ok = wait_q(n + 1))) break;
-                tc_fence_after();
-                if (leader) {
-                    ss(0, dK_A, dQ_B + ((n + 1) % kQStages) * Lay::kTileU);
+            if (leader) {
+                ts(256, 0, dDO_MN + st * Lay::kTileU, n > 0);                   // dV += P^T dO
+                if (more) {
+                    ss(0, dK_A, dQ_B + q1 * Lay::kTileU);
                     tc_commit(bar(kKVSFull));
                 }
-                __syncwarp();
             }
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kKVDSFull), n & 1, wc)))) break;
+            __syncwarp();
+            // dS^T(n) written and dO(n+1) loaded: dK(n), dP^T(n+1)
+            ok = more ? mbar_wait2(bar(kKVDSFull), n & 1, bar(kKVDOFull + (st ^ 1)), ((n + 1) >> 1) & 1, wc)
+                      : mbar_wait(bar(kKVDSFull), n & 1, wc);
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;
             tc_fence_after();
             if (leader) {
                 ts(256 + D, 128, dQ_MN + (n % kQStages) * Lay::kTileU, n > 0);  // dK += dS^T Q
                 tc_commit(bar(kQEmpty + n % kQStages));
                 tc_commit(bar(kKVDOEmpty + st));
                 if (!more) tc_commit(bar(kKVOFull));
-            }
-            __syncwarp();
-            if (more) {
-                if (!(ok = wait_do(n + 1))) break;
-                tc_fence_after();
-                if (leader) {
+                if (more) {
                     ss(128, dV_A, dDO_B + (st ^ 1) * Lay::kTileU);
                     tc_commit(bar(kKVDPFull));
                 }
-                __syncwarp();
             }
+            __syncwarp();
         }
         if (leader) tc_commit(bar(kKVDone));
         __syncwarp();
@@ -542,12 +539,12 @@ enum : int {
     kDKEmpty = 4,    // +stage
     kDVFull = 7,     // +stage (two V stages)
     kDVEmpty = 9,    // +stage
-    kDSFull = 11,    // S, dP ready
-    kDDSFull = 12,   // dS written
-    kDOFull = 13,    // dQ final
-    kDDone = 14,
-    kDFree = 15,     // dP of the current block read by the elementwise step
-    kDBars = 16
+    kDSFull = 11,    // +(block parity): S ready
+    kDDSFull = 13,   // +(block parity): dS written
+    kDOFull = 15,    // dQ final
+    kDDone = 16,
+    kDPFull = 17,    // dP ready
+    kDBars = 18
 };
 constexpr int kKStages = 3;
 
@@ -615,11 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kDVFull + i), 1);
             mbar_init(bar(kDVEmpty + i), 1);
         }
-        mbar_init(bar(kDSFull), 1);
-        mbar_init(bar(kDDSFull), 2 * kRows);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kDSFull + i), 1);
+            mbar_init(bar(kDDSFull + i), 2 * kRows);
+        }
         mbar_init(bar(kDOFull), 1);
         mbar_init(bar(kDDone), 1);
-        mbar_init(bar(kDFree), 2 * kRows);
+        mbar_init(bar(kDPFull), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -696,51 +695,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_ss(tmem + dcol, a0 + off, b0 + off, kIdescS, k > 0 ? 1u : 0u);
             }
         };
-        constexpr uint32_t kDQCol = 384;
-        auto region = [](int i) -> uint32_t { return 128u * static_cast<uint32_t>(i % 3); };
-        // S(n) = Q K_n^T into region n, dP(n) = dO V_n^T into region n+1 (mod 3)
-        auto issue_s_dp = [&](int n) {
-            const int st = n & 1;
-            ss(region(n), dQ_A, dK_B + (n % kKStages) * Lay::kTileU);
-            ss(region(n + 1), dDO_A, dV_B + st * Lay::kTileU);
-            tc_commit(bar(kDSFull));
-            tc_commit(bar(kDVEmpty + st));
-        };
+        // TMEM: S, then dS, alternate between columns [0,128) and [128,256) by block parity;
+        // dP always in [256,384); dQ in [384, 384 + D).  Per block the issuer waits twice:
+        // for K(n+1) and V(n+1), then queues S(n+1); for dS(n), then queues dP(n+1) and
+        // dQ(n).  Tensor-pipe order S(n+1) dP(n+1) dQ(n): block n+1's P is computed while
+        // dP(n+1) and dQ(n) run.  Why each product may overwrite what it does:
+        //  - S(n+1) goes over dS(n-1), which dQ(n-1) (issued before it) consumed;
+        //  - dP(n+1) goes over dP(n), which every elementwise thread read before writing
+        //    dS(n).
+        // No barrier phase can be produced twice ahead of its consumer: S and dS use one
+        // barrier per block parity, S(n+2)/dP(n+2) are queued only after dS(n+1) was
+        // consumed, and dP has one barrier whose next phase follows dS of this block.
+        constexpr uint32_t kDPCol = 256, kDQCol = 384;
         auto wait_kv = [&](int n) {
-            const int st = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
             return __all_sync(0xffffffffu,
-                              mbar_wait(bar(kDKFull + n % kKStages), (n / kKStages) & 1, wc) &&
-                                  mbar_wait(bar(kDVFull + st), ph, wc));
+                              mbar_wait2(bar(kDKFull + n % kKStages), (n / kKStages) & 1,
+                                         bar(kDVFull + (n & 1)), (n >> 1) & 1, wc));
         };
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kQDFull), 0, wc));
-        if (ok && (ok = wait_kv(0))) {
+        auto issue_s = [&](int n) {     // S(n) = Q K_n^T
+            ss(128u * (n & 1), dQ_A, dK_B + (n % kKStages) * Lay::kTileU);
+            tc_commit(bar(kDSFull + (n & 1)));
+        };
+        auto issue_dp = [&](int n) {    // dP(n) = dO V_n^T
+            ss(kDPCol, dDO_A, dV_B + (n & 1) * Lay::kTileU);
+            tc_commit(bar(kDPFull));
+            tc_commit(bar(kDVEmpty + (n & 1)));
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kQDFull), 0, wc)) && wait_kv(0);
+        if (ok) {
             tc_fence_after();
-            if (leader) issue_s_dp(0);
+            if (leader) {
+                issue_s(0);
+                issue_dp(0);
+            }
             __syncwarp();
         }
         for (int n = 0; ok && n < n_blocks; ++n) {
-            if (n + 1 < n_blocks) {
-                // block n's dP has been read: its region is free, and the third region's
-                // dS (block n-1) was consumed by dQ(n-1), issued before
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kDFree), n & 1, wc)))) break;
+            const bool more = n + 1 < n_blocks;
+            if (more) {
                 if (!(ok = wait_kv(n + 1))) break;
                 tc_fence_after();
-                if (leader) issue_s_dp(n + 1);
+                if (leader) issue_s(n + 1);
                 __syncwarp();
             }
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kDDSFull), n & 1, wc)))) break;
+            if (!(ok = __all_sync(0xffffffffu,
+                                  mbar_wait(bar(kDDSFull + (n & 1)), (n >> 1) & 1, wc))))
+                break;
             tc_fence_after();
             if (leader) {
+                if (more) issue_dp(n + 1);
                 const uint64_t b0 = dK_MN + (n % kKStages) * Lay::kTileU;
-                const uint32_t a0 = tmem + region(n);
+                const uint32_t a0 = tmem + 128u * (n & 1);
                 // dQ += dS K; dS of keys [64 h, 64 h + 64) sits in columns [64 h, 64 h + 32)
 #pragma unroll
                 for (int k = 0; k < kRows / 16; ++k)
                     mma_ts(tmem + kDQCol, a0 + 64 * (k >> 2) + (k & 3) * 8, b0 + ((k * 2048) >> 4),
                            kIdescAcc, (n > 0 || k > 0) ? 1u : 0u);
                 tc_commit(bar(kDKEmpty + n % kKStages));
-                if (n + 1 == n_blocks) tc_commit(bar(kDOFull));
+                if (!more) tc_commit(bar(kDOFull));
             }
             __syncwarp();
         }
@@ -754,7 +766,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = (warp - 4) >> 2;                   // key columns [64 half, 64 half + 64)
         const int row = quarter * 32 + lane;                // query row of the tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        auto region = [](int i) -> uint32_t { return 128u * static_cast<uint32_t>(i % 3); };
         const int row_local = q_local0 + row;
         const bool row_valid = row_local < p.Ls;
         const size_t sidx = (static_cast<size_t>(b) * p.L + q0 + row) * p.H + h;
@@ -763,35 +774,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t nl2x2 = f2pack(nl2, nl2);
         const uint64_t ndvx2 = f2pack(ndv, ndv);
         const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
+        const uint32_t tP = tmem + lane_off + 256 + 64 * half;                  // dP
         bool ok = true;
         for (int n = 0; n < n_blocks; ++n) {
             int s, kt;
             block(n, s, kt);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kDSFull), n & 1, wc));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kDSFull + (n & 1)), (n >> 1) & 1, wc));
             if (!ok) break;
             tc_fence_after();
             int lim = min(kRows - 1, p.Ls - kt * kRows - 1);
             if (p.causal && s == r) lim = min(lim, row_local - kt * kRows);
             if (!row_valid) lim = -1;
             const bool masked = __any_sync(0xffffffffu, lim < kRows - 1);
-            const uint32_t tS = tmem + lane_off + region(n) + 64 * half;        // S, then dS
-            const uint32_t tP = tmem + lane_off + region(n + 1) + 64 * half;    // dP
-            // dP - Dvec of this warp's 64 columns; once both halves have read dP, the MMA
-            // issuer may reuse its region for the next block's S
-            uint64_t dd[32];
-            {
-                uint32_t dr[64];
-                tmem_ld64(tP, dr);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dd[i] = fadd2(f2pack(u2f(dr[2 * i]), u2f(dr[2 * i + 1])), ndvx2);
-            }
-            tc_fence_before();
-            mbar_arrive(bar(kDFree));
+            const uint32_t tS = tmem + lane_off + 128u * (n & 1) + 64 * half;  // S, then dS
+            // P = exp2(S scale log2(e) - lse log2(e)) of this warp's 64 columns, in fp32
+            uint64_t pp[32];
 #pragma unroll
             for (int chunk = 0; chunk < 2; ++chunk) {
                 uint32_t sr[32];
                 tmem_ld32(tS + 32 * chunk, sr);
-                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float a0, a1;
@@ -802,15 +803,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         e0 = (c <= lim) ? e0 : 0.f;
                         e1 = (c + 1 <= lim) ? e1 : 0.f;
                     }
+                    pp[16 * chunk + i] = f2pack(e0, e1);
+                }
+            }
+            // dS = P (dP - Dvec), bf16, written over this warp's S columns
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kDPFull), n & 1, wc)))) break;
+            tc_fence_after();
+            uint32_t dr[64];
+            tmem_ld64(tP, dr);
+#pragma unroll
+            for (int chunk = 0; chunk < 2; ++chunk) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int j = 16 * chunk + i;
+                    const uint64_t d = fadd2(f2pack(u2f(dr[2 * j]), u2f(dr[2 * j + 1])), ndvx2);
                     float g0, g1;
-                    f2unpack(fmul2(f2pack(e0, e1), dd[16 * chunk + i]), g0, g1);
+                    f2unpack(fmul2(pp[j], d), g0, g1);
                     pk[i] = pack_bf16x2(g0, g1);
                 }
-                // dS of 32 keys as bf16 pairs: 16 columns, inside the ones already read
+                // 32 keys as bf16 pairs: 16 columns inside the ones already read
                 tmem_st16(tS + 16 * chunk, pk);
             }
             tc_fence_before();
-            mbar_arrive(bar(kDDSFull));
+            mbar_arrive(bar(kDDSFull + (n & 1)));
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kDOFull), 0, wc));
         if (ok) {
