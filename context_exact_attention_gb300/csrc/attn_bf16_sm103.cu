@@ -506,26 +506,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool more = n + 1 < n_blocks;
             const int st1 = (n + 1) & 1;
             const uint32_t ph1 = ((n + 1) >> 1) & 1;
-            if (!(ok = wait_all(kBarVFull + st, ph) && wait_all(kBarPFull + 0, n & 1))) break;
+            // Each wait between MMA batches costs the tensor pipe ~100 cycles even when the
+            // barrier is already complete, so barriers that gate the same batch are checked
+            // together: V and the first P half of tile 0, then its second P half and the
+            // next K block.
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait2(bar(kBarVFull + st), ph,
+                                                          bar(kBarPFull + 0), n & 1, wc))))
+                break;
             tc_fence_after();
             if (leader) issue_pv(0, st, 0, n > 0);
             __syncwarp();
-            if (!(ok = wait_all(kBarPFull + 1, n & 1))) break;
+            ok = more ? mbar_wait2(bar(kBarPFull + 1), n & 1, bar(kBarKFull + st1), ph1, wc)
+                      : mbar_wait(bar(kBarPFull + 1), n & 1, wc);
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;
             tc_fence_after();
             if (leader) {
                 issue_pv(0, st, 1, true);
                 if (!more) tc_commit(bar(kBarOFull + 0));
-            }
-            __syncwarp();
-            if (more) {
-                if (!(ok = wait_all(kBarKFull + st1, ph1))) break;
-                tc_fence_after();
-                if (leader) {
+                if (more) {
                     issue_qk(0, st1);
                     tc_commit(bar(kBarSFull + 0));
                 }
-                __syncwarp();
             }
+            __syncwarp();
             if (!(ok = wait_all(kBarPFull + 2, n & 1))) break;
             tc_fence_after();
             if (leader) issue_pv(1, st, 0, n > 0);
