@@ -437,16 +437,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool masked = __any_sync(0xffffffffu, lo > 0 || hi < kRows - 1);
             const float* nl2 = stats_nlse2(n % kQStages) + 64 * half;
             const float* ndv = stats_ndvec(st) + 64 * half;
-            // P^T = exp2(S^T scale log2(e) - lse log2(e)); kept in fp32 for dS^T
+            // P^T = exp2(S^T scale log2(e) - lse log2(e)); kept in fp32 for dS^T.  One TMEM
+            // load and one store for the warp's 64 columns (fewer dependent round trips).
             uint64_t pp[32];
+            {
+                uint32_t sr[64];
+                tmem_ld64(tS, sr);
+                uint32_t pk[32];
 #pragma unroll
-            for (int chunk = 0; chunk < 2; ++chunk) {
-                uint32_t sr[32];
-                tmem_ld32(tS + 32 * chunk, sr);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const ulonglong2 nl = *reinterpret_cast<const ulonglong2*>(nl2 + 32 * chunk + 4 * i);
+                for (int i = 0; i < 16; ++i) {
+                    const ulonglong2 nl = *reinterpret_cast<const ulonglong2*>(nl2 + 4 * i);
                     const uint64_t x0 = ffma2(f2pack(u2f(sr[4 * i]), u2f(sr[4 * i + 1])), sl2, nl.x);
                     const uint64_t x1 = ffma2(f2pack(u2f(sr[4 * i + 2]), u2f(sr[4 * i + 3])), sl2, nl.y);
                     float a0, a1, a2, a3;
@@ -456,17 +456,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (masked) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const int c = 64 * half + 32 * chunk + 4 * i + j;
+                            const int c = 64 * half + 4 * i + j;
                             e[j] = (c >= lo && c <= hi) ? e[j] : 0.f;
                         }
                     }
-                    pp[16 * chunk + 2 * i] = f2pack(e[0], e[1]);
-                    pp[16 * chunk + 2 * i + 1] = f2pack(e[2], e[3]);
+                    pp[2 * i] = f2pack(e[0], e[1]);
+                    pp[2 * i + 1] = f2pack(e[2], e[3]);
                     pk[2 * i] = pack_bf16x2(e[0], e[1]);
                     pk[2 * i + 1] = pack_bf16x2(e[2], e[3]);
                 }
-                // 32 query columns as bf16 pairs: 16 columns, inside the ones just read
-                tmem_st16(tS + 16 * chunk, pk);
+                // 64 query columns as bf16 pairs: 32 columns, inside the ones just read
+                tmem_st32(tS, pk);
             }
             tc_fence_before();
             mbar_arrive(bar(kKVPFull));
@@ -475,23 +475,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ok && mbar_wait(bar(kKVDOFull + st), (n >> 1) & 1, wc);    // -Dvec statistics
             if (!(ok = __all_sync(0xffffffffu, ok))) break;
             tc_fence_after();
+            {
+                uint32_t dr[64];
+                tmem_ld64(tP, dr);
+                uint32_t pk[32];
 #pragma unroll
-            for (int chunk = 0; chunk < 2; ++chunk) {
-                uint32_t dr[32];
-                tmem_ld32(tP + 32 * chunk, dr);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const ulonglong2 nd = *reinterpret_cast<const ulonglong2*>(ndv + 32 * chunk + 4 * i);
+                for (int i = 0; i < 16; ++i) {
+                    const ulonglong2 nd = *reinterpret_cast<const ulonglong2*>(ndv + 4 * i);
                     const uint64_t d0 = fadd2(f2pack(u2f(dr[4 * i]), u2f(dr[4 * i + 1])), nd.x);
                     const uint64_t d1 = fadd2(f2pack(u2f(dr[4 * i + 2]), u2f(dr[4 * i + 3])), nd.y);
                     float g0, g1, g2, g3;
-                    f2unpack(fmul2(pp[16 * chunk + 2 * i], d0), g0, g1);
-                    f2unpack(fmul2(pp[16 * chunk + 2 * i + 1], d1), g2, g3);
+                    f2unpack(fmul2(pp[2 * i], d0), g0, g1);
+                    f2unpack(fmul2(pp[2 * i + 1], d1), g2, g3);
                     pk[2 * i] = pack_bf16x2(g0, g1);
                     pk[2 * i + 1] = pack_bf16x2(g2, g3);
                 }
-                tmem_st16(tP + 16 * chunk, pk);
+                tmem_st32(tP, pk);
             }
             tc_fence_before();
             mbar_arrive(bar(kKVDSFull));
@@ -789,41 +788,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tS = tmem + lane_off + 128u * (n & 1) + 64 * half;  // S, then dS
             // P = exp2(S scale log2(e) - lse log2(e)) of this warp's 64 columns, in fp32
             uint64_t pp[32];
+            {
+                uint32_t sr[64];
+                tmem_ld64(tS, sr);
 #pragma unroll
-            for (int chunk = 0; chunk < 2; ++chunk) {
-                uint32_t sr[32];
-                tmem_ld32(tS + 32 * chunk, sr);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     float a0, a1;
                     f2unpack(ffma2(f2pack(u2f(sr[2 * i]), u2f(sr[2 * i + 1])), sl2, nl2x2), a0, a1);
                     float e0 = ex2(a0), e1 = ex2(a1);
                     if (masked) {
-                        const int c = 64 * half + 32 * chunk + 2 * i;
+                        const int c = 64 * half + 2 * i;
                         e0 = (c <= lim) ? e0 : 0.f;
                         e1 = (c + 1 <= lim) ? e1 : 0.f;
                     }
-                    pp[16 * chunk + i] = f2pack(e0, e1);
+                    pp[i] = f2pack(e0, e1);
                 }
             }
             // dS = P (dP - Dvec), bf16, written over this warp's S columns
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kDPFull), n & 1, wc)))) break;
             tc_fence_after();
-            uint32_t dr[64];
-            tmem_ld64(tP, dr);
+            {
+                uint32_t dr[64];
+                tmem_ld64(tP, dr);
+                uint32_t pk[32];
 #pragma unroll
-            for (int chunk = 0; chunk < 2; ++chunk) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int j = 16 * chunk + i;
-                    const uint64_t d = fadd2(f2pack(u2f(dr[2 * j]), u2f(dr[2 * j + 1])), ndvx2);
+                for (int i = 0; i < 32; ++i) {
+                    const uint64_t d = fadd2(f2pack(u2f(dr[2 * i]), u2f(dr[2 * i + 1])), ndvx2);
                     float g0, g1;
-                    f2unpack(fmul2(pp[j], d), g0, g1);
+                    f2unpack(fmul2(pp[i], d), g0, g1);
                     pk[i] = pack_bf16x2(g0, g1);
                 }
-                // 32 keys as bf16 pairs: 16 columns inside the ones already read
-                tmem_st16(tS + 16 * chunk, pk);
+                // 64 keys as bf16 pairs: 32 columns inside the ones already read
+                tmem_st32(tS, pk);
             }
             tc_fence_before();
             mbar_arrive(bar(kDDSFull + (n & 1)));
