@@ -503,6 +503,33 @@ def measure_rows(cea, dev, stream, peaks):
     return res
 
 
+def run_profile_backward(args):
+    """The backward of the causal-LM workload with 8 heads (the small case for profiler
+    captures of the row-dot, dK/dV and dQ kernels): `warmup` + `steps` calls, one line out."""
+    import context_exact_attention_gb300 as cea
+
+    dev = torch.device("cuda", 0)
+    cea.load_library()
+    w = dataclasses.replace(LM, H=8)
+    q, k, v = (t.to(dev) for t in make_workload_inputs(w, seed=0))
+    g = torch.Generator(device=dev).manual_seed(9)
+    do = torch.randn(q.shape, device=dev, generator=g).to(torch.bfloat16)
+    stream = torch.cuda.current_stream(dev)
+    out, lse = cea.ring_attn_fwd(q, k, v, P=w.P, causal=True, stream=stream)
+    ws = torch.empty(w.B * w.L * w.H, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    f = lambda: cea.ring_attn_bwd(q, k, v, out, lse, do, P=w.P, causal=True, dq=dq, dk=dk, dv=dv,
+                                  workspace=ws, stream=stream)
+    for _ in range(args.warmup):
+        f()
+    ms = _time_loop(f, args.steps, stream) / args.steps
+    if cea.check_status(stream) != 0:
+        raise RuntimeError("kernel reported a device-side timeout")
+    fl = 2.5 * attention_flops(w.B, w.L, w.H, w.D, True)
+    print(json.dumps({"case": "causal LM backward, B1 H8 L32768 D128 P8 bf16", "ms": ms,
+                      "tflops": fl / (ms * 1e-3) / 1e12}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -515,6 +542,8 @@ def main():
     ap.add_argument("--profile-case", action="store_true",
                     help="headline workload with 8 heads instead of 32 (201 MB of inputs, "
                          "still larger than L2): the small case for profiler captures")
+    ap.add_argument("--profile-backward", action="store_true",
+                    help="only the backward of the headline workload with 8 heads (profiler case)")
     ap.add_argument("--ref-rows", type=int, default=8,
                     help="query rows (all heads) per reference step")
     args = ap.parse_args()
@@ -523,7 +552,9 @@ def main():
     rank, world, local_rank = _rank_env()
     if world != args.gpus and "RANK" in os.environ:
         print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
-    if args.impl == "reference":
+    if args.profile_backward:
+        run_profile_backward(args)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_gpu(args, rank, world, local_rank)
