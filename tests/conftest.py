@@ -13,8 +13,8 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # GPU tests are skipped, not failed, when no GPU is present; the driver
-    # selects them explicitly with -m gpu on a GPU machine.
+    # GPU tests are skipped, not failed, when no GPU is present; on a machine with a
+    # GPU they are selected with -m gpu.
     try:
         import torch
         has_gpu = torch.cuda.is_available()
