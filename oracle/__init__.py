@@ -194,6 +194,29 @@ def attention_bwd(q, k, v, dout, causal: bool = False, threads: int | None = Non
     return dq, dk, dv
 
 
+def attention_bwd_gqa(q, k, v, dout, causal: bool = False, threads: int | None = None):
+    """Gradients with grouped key/value heads: q, dout [B, L, H, D]; k, v [B, L, Hk, D],
+    query head h reading key/value head h // (H // Hk) (the forward oracle's rule).
+
+    The grouped attention is ordinary attention on k, v with each key/value head repeated
+    for its H // Hk query heads; the gradient of a repeated tensor is the sum of the
+    gradients of its copies (chain rule of the copy), so dk, dv of head g sum the
+    per-query-head gradients over the group.  Returns (dq [B,L,H,D], dk, dv [B,L,Hk,D])."""
+    q, k, v, dout = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    B, L, H, D = q.shape
+    Hk = k.shape[2]
+    assert k.shape == (B, L, Hk, D) and v.shape == k.shape and dout.shape == q.shape
+    if H % Hk:
+        raise ValueError("query heads must be a multiple of key/value heads")
+    G = H // Hk
+    kr = np.ascontiguousarray(np.repeat(k, G, axis=2))
+    vr = np.ascontiguousarray(np.repeat(v, G, axis=2))
+    dq, dkr, dvr = attention_bwd(q, kr, vr, dout, causal=causal, threads=threads)
+    dk = dkr.reshape(B, L, Hk, G, D).sum(axis=3)
+    dv = dvr.reshape(B, L, Hk, G, D).sum(axis=3)
+    return dq, dk, dv
+
+
 def attention_bwd_dq_rows(q, k, v, dout, rows, causal: bool = False, threads: int | None = None):
     """dq of the listed query rows only (each row needs only its own scores): works at
     any sequence length.  Returns [B, len(rows), H, D]."""

@@ -479,3 +479,45 @@ def test_backward_dq_rows_match_full_backward(causal):
     rows = [0, 1, 13, 28]
     part = oracle.attention_bwd_dq_rows(q, k, v, do, rows, causal=causal)
     np.testing.assert_allclose(part, dq[:, rows], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("Hk", [1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_backward_matches_finite_differences(Hk, causal):
+    """Gradients with grouped key/value heads are the gradient of sum(O * dO) where O is
+    the grouped forward oracle itself: central differences (independent of the repeat
+    and sum inside attention_bwd_gqa)."""
+    B, L, H, D = 1, 4, 4, 3
+    q, do = _rand((B, L, H, D), 90), _rand((B, L, H, D), 91)
+    k, v = _rand((B, L, Hk, D), 92), _rand((B, L, Hk, D), 93)
+    dq, dk, dv = oracle.attention_bwd_gqa(q, k, v, do, causal=causal)
+    assert dk.shape == k.shape and dv.shape == v.shape and dq.shape == q.shape
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attention(q_, k_, v_, causal=causal, threads=1)
+        return float((o * do).sum())
+
+    eps = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (loss(**{k_ + "_": a for k_, a in args_p.items()})
+                        - loss(**{k_ + "_": a for k_, a in args_m.items()})) / (2 * eps)
+        np.testing.assert_allclose(g, num, rtol=0, atol=1e-7, err_msg=name)
+
+
+def test_grouped_backward_with_one_group_per_head_is_plain_backward():
+    """Hk = H: every group has one query head, the plain backward."""
+    B, L, H, D = 2, 9, 3, 4
+    q, k, v, do = (_rand((B, L, H, D), 94 + i) for i in range(4))
+    for causal in (False, True):
+        a = oracle.attention_bwd_gqa(q, k, v, do, causal=causal)
+        b = oracle.attention_bwd(q, k, v, do, causal=causal)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
