@@ -485,6 +485,24 @@ def measure_rows(cea, dev, stream, peaks):
                           "note": "row dots + dK/dV kernel + dQ kernel; 2.5x forward FLOPs"}
     del q, k, v, do, out, lse, ws, dq, dk, dv
 
+    # backward with grouped key/value heads: 32 query heads over 8 key/value heads at the
+    # headline length (same algorithmic FLOPs as the plain backward of 32 heads)
+    q = torch.randn(w.B, w.L, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
+    k, v = (torch.randn(w.B, w.L, 8, w.D, device=dev, generator=g).to(torch.bfloat16)
+            for _ in range(2))
+    do = torch.randn(q.shape, device=dev, generator=g).to(torch.bfloat16)
+    out, lse = cea.ring_attn_fwd_gqa(q, k, v, P=w.P, causal=True)
+    ws = torch.empty(w.B * w.L * w.H, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    f = lambda: cea.ring_attn_bwd_gqa(q, k, v, out, lse, do, P=w.P, causal=True, dq=dq, dk=dk,
+                                      dv=dv, workspace=ws, stream=stream)
+    f()
+    ms = _time_loop(f, 3, stream) / 3
+    res["lm_gqa_backward"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                              "frac": fl / (ms * 1e-3) / 1e12 / peak,
+                              "note": "32 query heads over 8 key/value heads; 2.5x forward FLOPs"}
+    del q, k, v, do, out, lse, ws, dq, dk, dv
+
     # long-context causal
     w = LONG
     q, k, v = (torch.randn(w.B, w.L, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)

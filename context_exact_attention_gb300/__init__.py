@@ -23,7 +23,7 @@ __all__ = [
     "ring_attn_fwd_trace", "attn_merge_partials", "ulysses_seq2head", "ulysses_head2seq",
     "ulysses_attention", "ring_attn_bwd", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
     "zigzag_positions", "ring_attn_fwd_varlen", "varlen_padded_length", "check_status",
-    "probe_wait_timeout", "ring_attn_fwd_host", "host_workspace_bytes",
+    "probe_wait_timeout", "ring_attn_fwd_host", "host_workspace_bytes", "ring_attn_bwd_gqa",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "ra_probe_wait_timeout", "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
     "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
     "ring_attn_fwd_varlen", "ring_attn_fwd_host", "ring_attn_fwd_host_workspace_bytes",
+    "ring_attn_bwd_gqa",
 )
 
 
@@ -82,6 +83,8 @@ def load_library(build_if_missing: bool = False):
             "ring_attn_bwd": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
                               i, i, i, i, i, i, vp],
             "ring_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
+            "ring_attn_bwd_gqa": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
+                                  i, i, i, i, i, i, i, vp],
             "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
             "ring_attn_fwd_zigzag": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp, vp],
             "ring_attn_fwd_varlen": [vp, vp, vp, vp, f_p, vp, i, i, i, i, i, i, i, vp, vp],
@@ -406,6 +409,32 @@ def ring_attn_bwd(q, k, v, out, lse, dout, P: int = 1, causal: bool = False, dq=
     _call("ring_attn_bwd", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
           _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, L,
           H, D, P, int(bool(causal)), _stream(stream))
+    return dq, dk, dv
+
+
+def ring_attn_bwd_gqa(q, k, v, out, lse, dout, P: int = 1, causal: bool = False, dq=None,
+                      dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of ring_attn_fwd_gqa: q, out, dout [B, L, H, D]; k, v [B, L, H_kv, D];
+    returns dq like q and dk, dv like k (summed over each key/value head's query heads)."""
+    _check_qkv(q, k, v, torch.bfloat16, grouped=True)
+    for name, t in (("out", out), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    B, L, H, D = q.shape
+    Hkv = k.shape[2]
+    if lse is None or lse.dtype != torch.float32 or tuple(lse.shape) != (B, L, H):
+        raise ValueError("lse must be the forward's fp32 [B, L, H] tensor")
+    lib = load_library()
+    need = lib.ring_attn_bwd_workspace_bytes(B, L, H)
+    if workspace is None:
+        workspace = torch.empty(max(1, need // 4), dtype=torch.float32, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _call("ring_attn_bwd_gqa", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+          _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), B, L, H, Hkv, D, P, int(bool(causal)),
+          _stream(stream))
     return dq, dk, dv
 
 

@@ -316,13 +316,17 @@ unsigned long long ring_attn_bwd_workspace_bytes(int B, int L, int H)
     return static_cast<unsigned long long>(B) * L * H * sizeof(float);
 }
 
-ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
-                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                        void* workspace, unsigned long long workspace_bytes, int B, int L, int H,
-                        int D, int P, int causal, ra_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                   unsigned long long workspace_bytes, int B, int L, int H, int Hkv, int D, int P,
+                   int causal, ra_stream_t stream)
 {
     unsigned long long n = 0;
-    ra_status st = check_attn(q, k, v, out, lse, B, L, H, D, P, 2, &n);
+    ra_status st = check_attn(q, k, v, out, lse, B, L, H, D, P, 2, &n, Hkv);
     if (st != RA_OK) return st;
     if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
@@ -331,11 +335,12 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
         return RA_ERR_MISALIGNED;
     const unsigned long long ws = ring_attn_bwd_workspace_bytes(B, L, H);
     if (workspace_bytes < ws) return RA_ERR_INVALID_ARG;
-    const unsigned long long bytes = n * 2;
+    const unsigned long long bytes = n * 2;                       // q, out, dout, dq
+    const unsigned long long kv_bytes = bytes / H * Hkv;          // k, v, dk, dv
     const void* ins[6] = {q, k, v, out, dout, lse};
-    const unsigned long long in_bytes[6] = {bytes, bytes, bytes, bytes, bytes, ws};
+    const unsigned long long in_bytes[6] = {bytes, kv_bytes, kv_bytes, bytes, bytes, ws};
     void* outs[4] = {dq, dk, dv, workspace};
-    const unsigned long long out_bytes[4] = {bytes, bytes, bytes, ws};
+    const unsigned long long out_bytes[4] = {bytes, kv_bytes, kv_bytes, ws};
     for (int i = 0; i < 4; ++i) {
         for (int j = 0; j < 6; ++j)
             if (overlap(outs[i], out_bytes[i], ins[j], in_bytes[j])) return RA_ERR_INVALID_ARG;
@@ -353,6 +358,7 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
     a.B = B;
     a.L = L;
     a.H = H;
+    a.Hkv = Hkv;
     a.D = D;
     a.P = P;
     a.causal = causal ? 1 : 0;
@@ -361,10 +367,33 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
     st = status_word(&a.status);
     if (st != RA_OK) return st;
     CUtensorMap tq, tk, tv, tdo;
-    if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, H, D) ||
-        !encode_qkv_map(&tv, v, B, L, H, D) || !encode_qkv_map(&tdo, dout, B, L, H, D))
+    if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, Hkv, D) ||
+        !encode_qkv_map(&tv, v, B, L, Hkv, D) || !encode_qkv_map(&tdo, dout, B, L, H, D))
         return RA_ERR_CUDA;
     return from_cuda(ra::launch_attn_bwd_bf16(a, tq, tk, tv, tdo));
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        void* workspace, unsigned long long workspace_bytes, int B, int L, int H,
+                        int D, int P, int causal, ra_stream_t stream)
+{
+    return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, L, H, H, D,
+                    P, causal, stream);
+}
+
+ra_status ring_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* out,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            void* workspace, unsigned long long workspace_bytes, int B, int L,
+                            int H, int H_kv, int D, int P, int causal, ra_stream_t stream)
+{
+    if (H_kv < 1) return RA_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, L, H, H_kv,
+                    D, P, causal, stream);
 }
 
 ra_status ra_check_status(ra_stream_t stream)

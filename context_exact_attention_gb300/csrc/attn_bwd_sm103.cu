@@ -62,6 +62,7 @@ struct BwdParams {
     unsigned int* status;
     unsigned long long timeout_ns;
     int B, L, H, P, Ls, causal;
+    int Hkv, group;          // key/value heads; query heads per key/value head (H / Hkv)
     int n_t;                 // 128-row tiles per shard
     float scale_log2;        // log2(e) / sqrt(D)
     float scale;             // 1 / sqrt(D)
@@ -172,21 +173,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // unit: (b, h) outer; inside, heaviest key tile first (low shard, low tile)
+    // unit: (b, key/value head hk) outer; inside, heaviest key tile first (low shard,
+    // low tile).  With grouped heads the unit's keys meet the queries of every query head
+    // of its group (h = hk * group + g), one head after the other, and dK, dV accumulate
+    // over all of them.
     const int units_per_bh = p.P * p.n_t;
     const int bh = blockIdx.x / units_per_bh;
     const int u = blockIdx.x - bh * units_per_bh;
     const int s = u / p.n_t;          // shard owning these keys
     const int kt = u - s * p.n_t;     // key tile within the shard
-    const int b = bh / p.H;
-    const int h = bh - b * p.H;
+    const int b = bh / p.Hkv;
+    const int hk = bh - b * p.Hkv;
     const int key0 = s * p.Ls + kt * kRows;
     // ring schedule from the owner's side: query shard r = (s + t) mod P at step t;
     // step 0 is the own shard (causal: query tiles from the diagonal on)
     const int q_begin = p.causal ? kt : 0;
     const int n_first = p.n_t - q_begin;
-    const int n_blocks = n_first + (p.causal ? (p.P - 1 - s) : (p.P - 1)) * p.n_t;
-    auto block = [&](int n, int& r, int& qt) {
+    const int n_head = n_first + (p.causal ? (p.P - 1 - s) : (p.P - 1)) * p.n_t;
+    const int n_blocks = n_head * p.group;
+    // block n: query head h, query shard r, query tile qt
+    auto block = [&](int n, int& r, int& qt, int& h) {
+        const int g = p.group == 1 ? 0 : n / n_head;
+        h = hk * p.group + g;
+        n -= g * n_head;
         if (n < n_first) {
             r = s;
             qt = q_begin + n;
@@ -237,14 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmap_do);
             mbar_arrive_expect_tx(bar(kKVFull), 2 * T);
             for (int bx = 0; bx < Lay::kBoxes; ++bx) {
-                tma_load_4d(sbase + kK + bx * 16384, &tmap_k, bar(kKVFull), bx * 64, h, key0, b, keep);
-                tma_load_4d(sbase + kV + bx * 16384, &tmap_v, bar(kKVFull), bx * 64, h, key0, b, keep);
+                tma_load_4d(sbase + kK + bx * 16384, &tmap_k, bar(kKVFull), bx * 64, hk, key0, b, keep);
+                tma_load_4d(sbase + kV + bx * 16384, &tmap_v, bar(kKVFull), bx * 64, hk, key0, b, keep);
             }
         }
         int last_q[kQStages] = {-1, -1, -1}, last_do[2] = {-1, -1};
         for (int n = 0; n < n_blocks; ++n) {
-            int r, qt;
-            block(n, r, qt);
+            int r, qt, h;
+            block(n, r, qt, h);
             const int qs = n % kQStages, ds = n & 1;
             const int qrow = r * p.Ls + qt * kRows;
             // Q first: its stage frees a block earlier than the dO stage, and S^T needs it first
@@ -372,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* src = is_lse ? p.lse : p.dvec;
         const float mul = is_lse ? -kLog2e : -1.f;
         auto fetch = [&](int n, float (&v)[4]) {
-            int r, qt;
-            block(n, r, qt);
+            int r, qt, h;
+            block(n, r, qt, h);
             const int qrow = r * p.Ls + qt * kRows;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -421,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
         bool ok = true;
         for (int n = 0; n < n_blocks; ++n) {
-            int r, qt;
-            block(n, r, qt);
+            int r, qt, h;
+            block(n, r, qt, h);
             const int st = n & 1;
             ok = mbar_wait(bar(kKVSFull), n & 1, wc);
             ok = ok && mbar_wait(bar(kQFull + n % kQStages), (n / kQStages) & 1, wc);
@@ -501,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             tc_fence_after();
             // half 0 writes dV, half 1 writes dK
-            const size_t base = ((static_cast<size_t>(b) * p.L + key0 + row) * p.H + h) * D;
+            const size_t base = ((static_cast<size_t>(b) * p.L + key0 + row) * p.Hkv + hk) * D;
             const uint32_t tA = tmem + lane_off + 256 + half * D;
             const float mul = half ? p.scale : 1.f;
             __nv_bfloat16* dst = (half ? p.dk : p.dv) + base;
@@ -576,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qt = p.n_t - 1 - (u - (u / p.n_t) * p.n_t);
     const int b = bh / p.H;
     const int h = bh - b * p.H;
+    const int hk = h / p.group;                       // key/value head of this query head
     const int q_local0 = qt * kRows;
     const int q0 = r * p.Ls + q_local0;
     // the forward's ring order: K/V shard (r - t) mod P at step t, future shards skipped
@@ -659,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(kDKFull + kst), T);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
                     tma_load_4d(sbase + kK + kst * T + bx * 16384, &tmap_k, bar(kDKFull + kst),
-                                bx * 64, h, row, b, keep);
+                                bx * 64, hk, row, b, keep);
             }
             last_k[kst] = n;
             if (!__all_sync(0xffffffffu, mbar_wait(bar(kDVEmpty + st), ph ^ 1, wc))) break;
@@ -667,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(kDVFull + st), T);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
                     tma_load_4d(sbase + kV + st * T + bx * 16384, &tmap_v, bar(kDVFull + st), bx * 64,
-                                h, row, b, keep);
+                                hk, row, b, keep);
             }
             last_v[st] = n;
         }
@@ -897,15 +907,20 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     p.B = a.B;
     p.L = a.L;
     p.H = a.H;
+    p.Hkv = a.Hkv;
+    p.group = a.H / a.Hkv;
     p.P = a.P;
     p.Ls = a.L / a.P;
     p.causal = a.causal;
     p.n_t = (p.Ls + kRows - 1) / kRows;
     p.scale = 1.0f / sqrtf(static_cast<float>(D));
     p.scale_log2 = kLog2e * p.scale;
+    // dK/dV: one CTA per key tile of each key/value head; dQ: per query tile of each head
+    const long long grid_kv = static_cast<long long>(a.B) * a.Hkv * a.P * p.n_t;
     const long long grid = static_cast<long long>(a.B) * a.H * a.P * p.n_t;
-    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid), kThreads, kSmemKV, a.stream>>>(tq, tk, tv, tdo, p);
+    if (grid <= 0 || grid > 0x7fffffffLL || grid_kv <= 0) return cudaErrorInvalidConfiguration;
+    bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid_kv), kThreads, kSmemKV, a.stream>>>(tq, tk, tv,
+                                                                                       tdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_dq_kernel<D><<<static_cast<unsigned>(grid), kThreads, kSmemQ, a.stream>>>(tq, tk, tv, tdo, p);

@@ -45,6 +45,7 @@ struct BwdArgs {
     void* dk;
     void* dv;
     int B, L, H, D, P, causal;
+    int Hkv;             // key/value heads (H % Hkv == 0); dk, dv are [B, L, Hkv, D]
     unsigned int* status;
     unsigned long long timeout_ns;
     cudaStream_t stream;

@@ -251,6 +251,23 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
                         int D, int P, int causal, ra_stream_t stream);
 
 /*
+ * ring_attn_bwd_gqa -- ring_attn_bwd with grouped key/value heads (the backward of
+ * ring_attn_fwd_gqa): q, out, dout, dq are [B, L, H, D]; k, v, dk, dv are
+ * [B, L, H_kv, D]; query head h reads key/value head h / (H / H_kv).  K/V head g is
+ * used by the H / H_kv query heads of its group, so its gradients are the sums over
+ * them: dk_g = sum over h in the group of dS_h^T q_h / sqrt(D), dv_g = sum of P_h^T dout_h
+ * ("序列并行与 Ring Attention", sections 3.5 and 6.4 count key/value heads apart from query
+ * heads; the chain rule through the shared head gives the sums).  H % H_kv != 0 returns
+ * RA_ERR_NOT_DIVISIBLE.  The workspace is ring_attn_bwd_workspace_bytes(B, L, H).
+ * Otherwise as ring_attn_bwd (deterministic, no atomics: each dk/dv row is written once by
+ * the CTA that owns its key tile, after walking every query head of the group).
+ */
+ra_status ring_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* out,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            void* workspace, unsigned long long workspace_bytes, int B, int L,
+                            int H, int H_kv, int D, int P, int causal, ra_stream_t stream);
+
+/*
  * ring_attn_bwd_noalloc -- ring_attn_bwd for callers that cannot allocate device
  * memory (no counterpart on the pages: an addition of this library).
  *

@@ -126,3 +126,62 @@ def test_bwd_argument_errors():
     with pytest.raises(cea.RingAttnError) as e:
         cea.ring_attn_bwd(q, k, v, out, lse, q.clone(), P=3)
     assert e.value.code == 4
+
+
+# ------------------------------------------------- grouped key/value heads --
+
+GQA_CASES = [
+    # B, L, H, H_kv, D, P
+    (1, 512, 4, 2, 128, 4),
+    (2, 384, 6, 3, 64, 2),      # shards of 192: ragged tiles
+    (1, 256, 4, 1, 128, 1),     # one key/value head (multi-query)
+    (1, 640, 8, 2, 64, 5),
+]
+
+
+@pytest.mark.parametrize("case", GQA_CASES, ids=lambda c: "B%dL%dH%dHkv%dD%dP%d" % c)
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_gqa_parity(case, causal):
+    """dk, dv of each key/value head sum the gradients of its query heads: against the
+    grouped fp64 oracle, with the rounding bound of each query head's terms summed over
+    the group."""
+    B, L, H, Hkv, D, P = case
+    q, _, _ = make_qkv(B, L, H, D, seed=40, dtype=torch.bfloat16)
+    _, k, v = make_qkv(B, L, Hkv, D, seed=41, dtype=torch.bfloat16)
+    do = torch.randn(B, L, H, D, generator=torch.Generator().manual_seed(42)).to(torch.bfloat16)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = cea.ring_attn_fwd_gqa(qd, kd, vd, P=P, causal=causal)
+    dq, dk, dv = cea.ring_attn_bwd_gqa(qd, kd, vd, out, lse, dod, P=P, causal=causal)
+    assert cea.check_status() == 0
+    assert dk.shape == k.shape and dv.shape == v.shape
+    rq, rk, rv = oracle.attention_bwd_gqa(q, k, v, do, causal=causal)
+    G = H // Hkv
+    kr, vr = k.repeat_interleave(G, dim=2), v.repeat_interleave(G, dim=2)
+    sq, sk, sv = _term_scales(q, kr, vr, do, causal)
+    sk = sk.reshape(B, L, Hkv, G, D).sum(axis=3)
+    sv = sv.reshape(B, L, Hkv, G, D).sum(axis=3)
+    _grad_close(to_np(dq), rq, "dq", sq)
+    _grad_close(to_np(dk), rk, "dk", sk)
+    _grad_close(to_np(dv), rv, "dv", sv)
+
+
+def test_bwd_gqa_with_h_kv_equal_h_is_plain_backward():
+    """H_kv = H through the grouped entry point gives the plain backward's bits."""
+    B, L, H, D, P = 1, 512, 2, 128, 4
+    q, k, v = (t.to(DEV) for t in make_qkv(B, L, H, D, seed=43, dtype=torch.bfloat16))
+    do = torch.randn(B, L, H, D, generator=torch.Generator().manual_seed(44)).to(torch.bfloat16).to(DEV)
+    out, lse = cea.ring_attn_fwd(q, k, v, P=P, causal=True)
+    a = cea.ring_attn_bwd(q, k, v, out, lse, do, P=P, causal=True)
+    b = cea.ring_attn_bwd_gqa(q, k, v, out, lse, do, P=P, causal=True)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_bwd_gqa_argument_errors():
+    q, _, _ = (t.to(DEV) for t in make_qkv(1, 256, 6, 128, seed=0, dtype=torch.bfloat16))
+    _, k, v = (t.to(DEV) for t in make_qkv(1, 256, 4, 128, seed=0, dtype=torch.bfloat16))
+    out = torch.empty_like(q)
+    lse = torch.empty(1, 256, 6, device=DEV)
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ring_attn_bwd_gqa(q, k, v, out, lse, torch.empty_like(q), P=2)
+    assert e.value.code == 4          # 6 query heads over 4 key/value heads

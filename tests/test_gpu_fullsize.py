@@ -179,3 +179,35 @@ def test_backward_at_causal_lm_size():
             got = dq[0, i, h].double().cpu().numpy()
             r = ref[0, ri, h]
             assert (np.abs(got - r) <= 2 * u * (np.abs(r) + scale) + 1e-6).all(), (i, h)
+
+
+def test_grouped_backward_at_causal_lm_size():
+    """Grouped backward at the causal-LM length (8 query heads over 2 key/value heads):
+    sum of dv over keys per key/value head equals the sum of dout over queries and the
+    group's query heads, sum of dk over keys is zero, and dq on sampled rows matches the
+    fp64 chain rule through the repeated heads."""
+    w = LM
+    H, Hkv = 8, 2
+    G = H // Hkv
+    q, _, _ = make_qkv(1, w.L, H, w.D, seed=50, dtype=torch.bfloat16, head_scale=True)
+    _, k, v = make_qkv(1, w.L, Hkv, w.D, seed=51, dtype=torch.bfloat16)
+    do = torch.randn(1, w.L, H, w.D, generator=torch.Generator().manual_seed(52)).to(torch.bfloat16)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = cea.ring_attn_fwd_gqa(qd, kd, vd, P=w.P, causal=True)
+    dq, dk, dv = cea.ring_attn_bwd_gqa(qd, kd, vd, out, lse, dod, P=w.P, causal=True)
+    assert cea.check_status() == 0
+    u = 2.0 ** -9
+    sdv = dv.double().sum(1).cpu().numpy()                                   # [1, Hkv, D]
+    sdo = do.double().sum(1).numpy().reshape(1, Hkv, G, w.D).sum(axis=2)
+    assert (np.abs(sdv - sdo) <= 4 * u * dv.double().abs().sum(1).cpu().numpy() + 1e-3).all()
+    sdk = dk.double().sum(1).cpu().numpy()
+    assert (np.abs(sdk) <= 4 * u * dk.double().abs().sum(1).cpu().numpy() + 1e-3).all()
+    rows = sample_rows(w.L, w.P, 12, seed=3)
+    kr, vr = k.repeat_interleave(G, dim=2), v.repeat_interleave(G, dim=2)
+    ref = oracle.attention_bwd_dq_rows(q, kr, vr, do, rows, causal=True)
+    got = to_np(dq[:, rows]).astype(np.float64)
+    scale = np.abs(ref).max(axis=-1, keepdims=True)
+    assert np.isfinite(got).all()
+    # relative to each row's largest component: the first-order bound of the plain
+    # backward's full-size test, taken conservatively per row
+    assert (np.abs(got - ref) <= 4 * u * (np.abs(ref) + scale) + 1e-5).all()
