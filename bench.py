@@ -465,7 +465,7 @@ def measure_rows(cea, dev, stream, peaks):
     res["lm_varlen_causal"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                                "frac": fl / (ms * 1e-3) / 1e12 / peak, "n_seqs": len(lengths),
                                "note": "lengths U[256, 8192) packed to 32768 tokens, 32 heads"}
-    del q, k, v, out, lse, cu_d
+    del q, k, v, out, lse
 
     # backward of the headline workload (dq, dk, dv): algorithmic FLOPs are 2.5x the
     # forward's (five D-length products per visible pair)
@@ -502,6 +502,38 @@ def measure_rows(cea, dev, stream, peaks):
                               "frac": fl / (ms * 1e-3) / 1e12 / peak,
                               "note": "32 query heads over 8 key/value heads; 2.5x forward FLOPs"}
     del q, k, v, do, out, lse, ws, dq, dk, dv
+
+    # backward over zigzag shards (same causal problem and FLOPs as the plain backward)
+    q, k, v, do = (torch.randn(w.B, w.L, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
+                   for _ in range(4))
+    out, lse = cea.ring_attn_fwd_zigzag(q, k, v, P=w.P)
+    ws = torch.empty(w.B * w.L * w.H, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    f = lambda: cea.ring_attn_bwd_zigzag(q, k, v, out, lse, do, P=w.P, dq=dq, dk=dk, dv=dv,
+                                         workspace=ws, stream=stream)
+    f()
+    ms = _time_loop(f, 3, stream) / 3
+    fl = 2.5 * attention_flops(w.B, w.L, w.H, w.D, True)
+    res["lm_zigzag_backward"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                                 "frac": fl / (ms * 1e-3) / 1e12 / peak,
+                                 "note": "zigzag shards; 2.5x forward FLOPs"}
+    del q, k, v, do, out, lse, ws, dq, dk, dv
+
+    # backward of the packed sequences of the forward row above (same lengths)
+    q, k, v, do = (torch.randn(w.L, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
+                   for _ in range(4))
+    out, lse = cea.ring_attn_fwd_varlen(q, k, v, cu_d, P=w.P, causal=True)
+    ws = torch.empty(w.L * w.H, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    f = lambda: cea.ring_attn_bwd_varlen(q, k, v, out, lse, do, cu_d, P=w.P, causal=True, dq=dq,
+                                         dk=dk, dv=dv, workspace=ws, stream=stream)
+    f()
+    ms = _time_loop(f, 5, stream) / 5
+    fl = 2.5 * sum(attention_flops(1, n, w.H, w.D, True) for n in lengths)
+    res["lm_varlen_backward"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                                 "frac": fl / (ms * 1e-3) / 1e12 / peak, "n_seqs": len(lengths),
+                                 "note": "packed sequences of the forward row; 2.5x forward FLOPs"}
+    del q, k, v, do, out, lse, ws, dq, dk, dv, cu_d
 
     # long-context causal
     w = LONG

@@ -24,7 +24,7 @@ __all__ = [
     "ulysses_attention", "ring_attn_bwd", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
     "zigzag_positions", "ring_attn_fwd_varlen", "varlen_padded_length", "check_status",
     "probe_wait_timeout", "ring_attn_fwd_host", "host_workspace_bytes", "ring_attn_bwd_gqa",
-    "EXPORTED_SYMBOLS",
+    "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +42,7 @@ EXPORTED_SYMBOLS = (
     "ra_probe_wait_timeout", "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
     "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
     "ring_attn_fwd_varlen", "ring_attn_fwd_host", "ring_attn_fwd_host_workspace_bytes",
-    "ring_attn_bwd_gqa",
+    "ring_attn_bwd_gqa", "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen",
 )
 
 
@@ -85,6 +85,10 @@ def load_library(build_if_missing: bool = False):
             "ring_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
             "ring_attn_bwd_gqa": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
                                   i, i, i, i, i, i, i, vp],
+            "ring_attn_bwd_zigzag": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
+                                     i, i, i, i, i, vp],
+            "ring_attn_bwd_varlen": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
+                                     vp, i, i, i, i, i, i, vp],
             "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
             "ring_attn_fwd_zigzag": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp, vp],
             "ring_attn_fwd_varlen": [vp, vp, vp, vp, f_p, vp, i, i, i, i, i, i, i, vp, vp],
@@ -435,6 +439,53 @@ def ring_attn_bwd_gqa(q, k, v, out, lse, dout, P: int = 1, causal: bool = False,
           _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
           workspace.numel() * workspace.element_size(), B, L, H, Hkv, D, P, int(bool(causal)),
           _stream(stream))
+    return dq, dk, dv
+
+
+def _bwd_outputs(q, k, v, out, lse, dout, lse_shape, dq, dk, dv, workspace, rows):
+    for name, t in (("out", out), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if lse is None or lse.dtype != torch.float32 or tuple(lse.shape) != lse_shape:
+        raise ValueError(f"lse must be the forward's fp32 {list(lse_shape)} tensor")
+    if workspace is None:
+        workspace = torch.empty(max(1, rows), dtype=torch.float32, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    return dq, dk, dv, workspace
+
+
+def ring_attn_bwd_zigzag(q, k, v, out, lse, dout, P: int = 1, dq=None, dk=None, dv=None,
+                         workspace=None, stream=None):
+    """Gradients of ring_attn_fwd_zigzag (bf16, causal): every tensor in the zigzag row
+    order of the forward (see zigzag_positions); returns (dq, dk, dv) in that order."""
+    _check_qkv(q, k, v, torch.bfloat16)
+    B, L, H, D = q.shape
+    dq, dk, dv, workspace = _bwd_outputs(q, k, v, out, lse, dout, (B, L, H), dq, dk, dv,
+                                         workspace, B * L * H)
+    _call("ring_attn_bwd_zigzag", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+          _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), B, L, H, D, P, _stream(stream))
+    return dq, dk, dv
+
+
+def ring_attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, P: int = 1, causal: bool = False,
+                         dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of ring_attn_fwd_varlen (bf16): q, k, v, out, dout [L, H, D], lse [L, H],
+    cu_seqlens the forward's int32 CUDA tensor.  Returns (dq, dk, dv), each [L, H, D]."""
+    if q.dim() != 3:
+        raise ValueError("packed q, k, v are [L, H, D]")
+    _check_qkv(q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), torch.bfloat16)
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    L, H, D = q.shape
+    dq, dk, dv, workspace = _bwd_outputs(q, k, v, out, lse, dout, (L, H), dq, dk, dv, workspace,
+                                         L * H)
+    _call("ring_attn_bwd_varlen", _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+          _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+          L, H, D, P, int(bool(causal)), _stream(stream))
     return dq, dk, dv
 
 

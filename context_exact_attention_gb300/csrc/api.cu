@@ -323,7 +323,8 @@ namespace {
 ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse,
                    const void* dout, void* dq, void* dk, void* dv, void* workspace,
                    unsigned long long workspace_bytes, int B, int L, int H, int Hkv, int D, int P,
-                   int causal, ra_stream_t stream)
+                   int causal, ra_stream_t stream, int zigzag = 0, const int* cu_seqlens = nullptr,
+                   int n_seqs = 0)
 {
     unsigned long long n = 0;
     ra_status st = check_attn(q, k, v, out, lse, B, L, H, D, P, 2, &n, Hkv);
@@ -362,6 +363,9 @@ ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     a.D = D;
     a.P = P;
     a.causal = causal ? 1 : 0;
+    a.zigzag = zigzag;
+    a.cu_seqlens = cu_seqlens;
+    a.n_seqs = n_seqs;
     a.timeout_ns = kWaitLimitNs;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     st = status_word(&a.status);
@@ -394,6 +398,31 @@ ra_status ring_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     if (H_kv < 1) return RA_ERR_INVALID_ARG;
     return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, L, H, H_kv,
                     D, P, causal, stream);
+}
+
+ra_status ring_attn_bwd_zigzag(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               void* workspace, unsigned long long workspace_bytes, int B, int L,
+                               int H, int D, int P, ra_stream_t stream)
+{
+    if (P < 1 || L < 1) return RA_ERR_INVALID_ARG;
+    if (L % (2 * P) != 0) return RA_ERR_NOT_DIVISIBLE;
+    // 128-row tiles must not straddle the two chunks of a shard
+    if ((L / (2 * P)) % 128 != 0) return RA_ERR_UNSUPPORTED;
+    return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, L, H, H, D,
+                    P, 1, stream, 1);
+}
+
+ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               void* workspace, unsigned long long workspace_bytes,
+                               const int* cu_seqlens, int n_seqs, int L, int H, int D, int P,
+                               int causal, ra_stream_t stream)
+{
+    if (!cu_seqlens || n_seqs < 1) return RA_ERR_INVALID_ARG;
+    if (!aligned(cu_seqlens, 4)) return RA_ERR_MISALIGNED;
+    return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, 1, L, H, H, D,
+                    P, causal, stream, 0, cu_seqlens, n_seqs);
 }
 
 ra_status ra_check_status(ra_stream_t stream)

@@ -12,7 +12,10 @@
 // one CTA per 128-key block that walks the query shards in ring order
 // (r = (s + t) mod P, skipping r < s under causal masking) and writes dK, dV
 // once; the query side (dQ) is one CTA per 128-row query tile walking the K/V
-// shards in the forward's order.  No atomics: results are deterministic.
+// shards in the forward's order.  No atomics: results are deterministic.  The same
+// kernels serve the zigzag shard layout and packed variable-length sequences
+// (template parameter kMode; see "shard layouts" below): only the walk over tiles
+// and the visibility masks change.
 //
 // Kernels (384 threads: warp 0 TMA producer, warp 1 MMA issuer, in the dK/dV kernel
 // warps 2-3 the per-query statistics, warps 4-11 the elementwise step -- two warps per
@@ -21,12 +24,12 @@
 // results inside its own column range; warp-uniform schedules with one elected
 // lane issuing):
 //   bwd_rowdot_kernel   Dvec = rowsum(dO o O), fp32 workspace [B, L, H]
-//   bwd_dkdv_kernel<D>  TMEM: S^T [0,128), dP^T [128,256), dV, dK (D columns each)
+//   bwd_dkdv_kernel<D, kMode>  TMEM: S^T [0,128), dP^T [128,256), dV, dK (D columns each)
 //       S^T = K Q^T, dP^T = V dO^T (SS); P^T, dS^T (bf16) written over them;
 //       dV += P^T dO, dK += dS^T Q (A from TMEM, B = dO / Q as MN-major SMEM).
 //       Tensor-pipe order per block: dV(n) S^T(n+1) dK(n) dP^T(n+1), so that
 //       P^T(n) is computed while dP^T(n) runs, dS^T(n) while dV(n) and S^T(n+1) run.
-//   bwd_dq_kernel<D>    TMEM: S, then dS, alternating between [0,128) and [128,256) by
+//   bwd_dq_kernel<D, kMode>    TMEM: S, then dS, alternating between [0,128) and [128,256) by
 //       block parity; dP in [256,384); dQ (D columns) at 384.  S = Q K^T, dP = dO V^T
 //       (SS); dS (bf16) written over S; dQ += dS K.  Tensor-pipe order per block:
 //       S(n+1) dP(n+1) dQ(n), so block n+1's elementwise step overlaps dQ(n).
@@ -66,7 +69,138 @@ struct BwdParams {
     int n_t;                 // 128-row tiles per shard
     float scale_log2;        // log2(e) / sqrt(D)
     float scale;             // 1 / sqrt(D)
+    const int* cu_seqlens;   // packed sequences: starts of n_seqs sequences, then L
+    int n_seqs;
 };
+
+// ------------------------------------------------------- shard layouts --
+//
+// kMode 0: contiguous shards (shard x holds positions [x Ls, (x+1) Ls)), with the
+// closed-form schedules below.  kMode 1: zigzag shards ("序列并行与 Ring Attention",
+// section 3.4: 2P chunks of Ls/2 positions, shard x holds chunk x, then chunk 2P-1-x;
+// causal).  kMode 2: packed sequences over contiguous shards (section 6.5: a query sees
+// only keys of its own sequence).  Modes 1 and 2 walk the ring with PosWalk.
+
+constexpr int kFar = 1 << 30;    // a position bound that never binds
+
+__device__ __forceinline__ int layout_position(int x, int i, int Ls, int P, bool zig)
+{
+    if (!zig) return x * Ls + i;
+    const int c = Ls >> 1;
+    return i < c ? x * c + i : (2 * P - 1 - x) * c + (i - c);
+}
+
+// First and last position of the packed sequence that holds position pos
+// (cu: n_seqs starts, then the total; cu[a] <= pos < cu[a+1] for exactly one
+// non-empty sequence a).
+__device__ __forceinline__ void seq_range(const int* cu, int n_seqs, int pos, int& first, int& last)
+{
+    int a = 0, b = n_seqs;
+    while (b - a > 1) {
+        const int mid = (a + b) >> 1;
+        if (__ldg(cu + mid) <= pos) a = mid;
+        else b = mid;
+    }
+    first = __ldg(cu + a);
+    last = __ldg(cu + a + 1) - 1;
+}
+
+// Ring walk over the 128-row tiles that hold positions in [lo, hi]: at step t the
+// shard x = (own + dir t) mod P (dir = -1: the queries of shard `own` meet K/V shard
+// (own - t) mod P, the forward's order; dir = +1: the keys of shard `own` meet query
+// shard (own + t) mod P, the owner's side of the same exchange), and of shard x the
+// tiles whose positions intersect [lo, hi] -- one run of tiles in a contiguous shard,
+// one run in each chunk of a zigzag shard (chunks are whole tiles).  Every role of a
+// CTA walks the same sequence, each with its own copy, in order.
+struct PosWalk {
+    int own, dir, P, Ls, n_half, zig, lo, hi;
+    int t, x, idx, first_a, cnt_a, first_b, cnt_b;
+    __device__ __forceinline__ void init(int own_, int dir_, int P_, int Ls_, int zig_, int lo_,
+                                         int hi_)
+    {
+        own = own_;
+        dir = dir_;
+        P = P_;
+        Ls = Ls_;
+        zig = zig_;
+        n_half = (Ls_ >> 1) / kRows;
+        lo = lo_;
+        hi = hi_;
+    }
+    __device__ __forceinline__ void run(int base, int len, int& first, int& cnt) const
+    {
+        const int a = max(lo, base), b = min(hi, base + len - 1);
+        if (a > b) {
+            first = 0;
+            cnt = 0;
+        } else {
+            first = (a - base) / kRows;
+            cnt = (b - base) / kRows - first + 1;
+        }
+    }
+    __device__ __forceinline__ void enter()
+    {
+        x = own + dir * t;
+        if (x >= P) x -= P;
+        if (x < 0) x += P;
+        first_b = 0;
+        cnt_b = 0;
+        if (!zig) {
+            run(x * Ls, Ls, first_a, cnt_a);
+        } else {
+            const int c = Ls >> 1;
+            run(x * c, c, first_a, cnt_a);
+            run((2 * P - 1 - x) * c, c, first_b, cnt_b);
+        }
+        idx = 0;
+    }
+    __device__ __forceinline__ void settle()
+    {
+        while (t < P && idx >= cnt_a + cnt_b) {
+            ++t;
+            if (t < P) enter();
+        }
+    }
+    __device__ __forceinline__ int total()
+    {
+        int n = 0;
+        for (t = 0; t < P; ++t) {
+            enter();
+            n += cnt_a + cnt_b;
+        }
+        return n;
+    }
+    // n = 0, 1, 2, ... in order
+    __device__ __forceinline__ void at(int n)
+    {
+        if (n == 0) {
+            t = 0;
+            enter();
+        } else {
+            ++idx;
+        }
+        settle();
+    }
+    // tile within shard x
+    __device__ __forceinline__ int tile() const
+    {
+        return idx < cnt_a ? first_a + idx : n_half + first_b + (idx - cnt_a);
+    }
+};
+
+// Zero rows [row0, row0 + n) of a [B, L, heads, D] bf16 tensor's head `head` (gradients of
+// a tile that no pair reaches: possible only with malformed sequence boundaries).
+template <int D>
+__device__ void zero_tile_rows(__nv_bfloat16* t, int b, int L, int heads, int head, int row0, int n)
+{
+    constexpr int kVec = D / 8;     // 16-byte vectors per row
+    for (int i = threadIdx.x; i < n * kVec; i += blockDim.x) {
+        const int row = row0 + i / kVec;
+        uint4* dst = reinterpret_cast<uint4*>(
+            t + ((static_cast<size_t>(b) * L + row) * heads + head) * static_cast<size_t>(D));
+        dst[i % kVec] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
 
 // ------------------------------------------------------------------ row dot --
 
@@ -141,7 +275,7 @@ struct KVSmem {
     static_assert(kKVBars * 8 + 8 <= 256, "barrier area");
 };
 
-template <int D>
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_k,
@@ -189,10 +323,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     // step 0 is the own shard (causal: query tiles from the diagonal on)
     const int q_begin = p.causal ? kt : 0;
     const int n_first = p.n_t - q_begin;
-    const int n_head = n_first + (p.causal ? (p.P - 1 - s) : (p.P - 1)) * p.n_t;
+    int n_head = n_first + (p.causal ? (p.P - 1 - s) : (p.P - 1)) * p.n_t;
+    // zigzag shards and packed sequences: the query tiles that hold positions some key
+    // of this tile is visible to (causal: from the tile's first key position on; packed:
+    // within the sequences of its first and last key), walked in the same ring order
+    constexpr bool kZig = kMode == 1;
+    PosWalk walk;
+    if constexpr (kMode != 0) {
+        const int kp0 = layout_position(s, kt * kRows, p.Ls, p.P, kZig);
+        int lo = kp0, hi = kFar;
+        if constexpr (kMode == 2) {
+            const int kp1 = s * p.Ls + min(p.Ls - 1, kt * kRows + kRows - 1);
+            int f0, l0, f1, l1;
+            seq_range(p.cu_seqlens, p.n_seqs, kp0, f0, l0);
+            seq_range(p.cu_seqlens, p.n_seqs, kp1, f1, l1);
+            lo = p.causal ? kp0 : f0;
+            hi = l1;
+        }
+        walk.init(s, +1, p.P, p.Ls, kZig ? 1 : 0, lo, hi);
+        n_head = walk.total();
+        if (n_head == 0) {          // every key of a tile sees at least its own query
+            const int n = min(kRows, p.Ls - kt * kRows);
+            zero_tile_rows<D>(p.dk, b, p.L, p.Hkv, hk, key0, n);
+            zero_tile_rows<D>(p.dv, b, p.L, p.Hkv, hk, key0, n);
+            return;
+        }
+    }
     const int n_blocks = n_head * p.group;
-    // block n: query head h, query shard r, query tile qt
+    // block n: query head h, query shard r, query tile qt (modes 1 and 2: n = 0, 1, ...
+    // in order, one head)
     auto block = [&](int n, int& r, int& qt, int& h) {
+        if constexpr (kMode != 0) {
+            walk.at(n);
+            r = walk.x;
+            qt = walk.tile();
+            h = hk;
+            return;
+        }
         const int g = p.group == 1 ? 0 : n / n_head;
         h = hk * p.group + g;
         n -= g * n_head;
@@ -428,6 +595,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key_local = kt * kRows + row;           // within shard s
         const bool key_valid = key_local < p.Ls;
         const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
+        // modes 1 and 2: the positions of the queries that see this key, [vis_lo, vis_hi]
+        int vis_lo = 0, vis_hi = kFar;
+        if constexpr (kMode != 0) {
+            if (key_valid) {
+                const int kp = layout_position(s, key_local, p.Ls, p.P, kZig);
+                vis_lo = kp;
+                if constexpr (kMode == 2) {
+                    int f, l;
+                    seq_range(p.cu_seqlens, p.n_seqs, kp, f, l);
+                    if (!p.causal) vis_lo = f;
+                    vis_hi = l;
+                }
+            }
+        }
         bool ok = true;
         for (int n = 0; n < n_blocks; ++n) {
             int r, qt, h;
@@ -439,9 +620,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             // visible query columns [lo, hi] of this tile for this key row
-            const int hi = min(kRows - 1, p.Ls - qt * kRows - 1);
+            int hi = min(kRows - 1, p.Ls - qt * kRows - 1);
             int lo = 0;
-            if (p.causal && r == s) lo = max(0, key_local - qt * kRows);
+            if constexpr (kMode == 0) {
+                if (p.causal && r == s) lo = max(0, key_local - qt * kRows);
+            } else {
+                // a query tile holds consecutive positions in every layout
+                const int qp0 = layout_position(r, qt * kRows, p.Ls, p.P, kZig);
+                lo = max(0, vis_lo - qp0);
+                hi = min(hi, vis_hi - qp0);
+            }
             if (!key_valid) lo = kRows;
             const bool masked = __any_sync(0xffffffffu, lo > 0 || hi < kRows - 1);
             const float* nl2 = stats_nlse2(n % kQStages) + 64 * half;
@@ -556,7 +744,7 @@ enum : int {
 };
 constexpr int kKStages = 3;
 
-template <int D>
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
@@ -598,7 +786,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_first = p.n_t;
         n_blocks = p.P * p.n_t;
     }
+    // zigzag shards and packed sequences: the K/V tiles holding positions that some
+    // query of this tile sees (causal: up to its last query; packed: within the
+    // sequences of its first and last query), in the same ring order
+    constexpr bool kZig = kMode == 1;
+    PosWalk walk;
+    if constexpr (kMode != 0) {
+        const int q_last = min(p.Ls - 1, q_local0 + kRows - 1);
+        const int qp0 = layout_position(r, q_local0, p.Ls, p.P, kZig);
+        const int qp1 = layout_position(r, q_last, p.Ls, p.P, kZig);
+        int lo = 0, hi = qp1;
+        if constexpr (kMode == 2) {
+            int f0, l0, f1, l1;
+            seq_range(p.cu_seqlens, p.n_seqs, qp0, f0, l0);
+            seq_range(p.cu_seqlens, p.n_seqs, qp1, f1, l1);
+            lo = f0;
+            if (!p.causal) hi = l1;
+        }
+        walk.init(r, -1, p.P, p.Ls, kZig ? 1 : 0, lo, hi);
+        n_blocks = walk.total();
+        if (n_blocks == 0) {        // every query of a tile sees at least its own key
+            zero_tile_rows<D>(p.dq, b, p.L, p.H, h, q0, min(kRows, p.Ls - q_local0));
+            return;
+        }
+    }
     auto block = [&](int n, int& s, int& kt) {
+        if constexpr (kMode != 0) {
+            walk.at(n);
+            s = walk.x;
+            kt = walk.tile();
+            return;
+        }
         if (n < n_first) {
             s = r;
             kt = n;
@@ -784,6 +1002,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t ndvx2 = f2pack(ndv, ndv);
         const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
         const uint32_t tP = tmem + lane_off + 256 + 64 * half;                  // dP
+        // modes 1 and 2: the positions of the keys this query sees, [vis_lo, vis_hi]
+        int vis_lo = 0, vis_hi = kFar;
+        if constexpr (kMode != 0) {
+            if (row_valid) {
+                const int qp = layout_position(r, row_local, p.Ls, p.P, kZig);
+                vis_hi = qp;
+                if constexpr (kMode == 2) {
+                    int f, l;
+                    seq_range(p.cu_seqlens, p.n_seqs, qp, f, l);
+                    vis_lo = f;
+                    if (!p.causal) vis_hi = l;
+                }
+            }
+        }
         bool ok = true;
         for (int n = 0; n < n_blocks; ++n) {
             int s, kt;
@@ -792,9 +1024,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             int lim = min(kRows - 1, p.Ls - kt * kRows - 1);
-            if (p.causal && s == r) lim = min(lim, row_local - kt * kRows);
+            int lo = 0;
+            if constexpr (kMode == 0) {
+                if (p.causal && s == r) lim = min(lim, row_local - kt * kRows);
+            } else {
+                // a K/V tile holds consecutive positions in every layout
+                const int kp0 = layout_position(s, kt * kRows, p.Ls, p.P, kZig);
+                lim = min(lim, vis_hi - kp0);
+                lo = vis_lo - kp0;
+            }
             if (!row_valid) lim = -1;
-            const bool masked = __any_sync(0xffffffffu, lim < kRows - 1);
+            const bool masked = __any_sync(0xffffffffu, lim < kRows - 1 || lo > 0);
             const uint32_t tS = tmem + lane_off + 128u * (n & 1) + 64 * half;  // S, then dS
             // P = exp2(S scale log2(e) - lse log2(e)) of this warp's 64 columns, in fp32
             uint64_t pp[32];
@@ -808,8 +1048,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float e0 = ex2(a0), e1 = ex2(a1);
                     if (masked) {
                         const int c = 64 * half + 2 * i;
-                        e0 = (c <= lim) ? e0 : 0.f;
-                        e1 = (c + 1 <= lim) ? e1 : 0.f;
+                        e0 = (c <= lim && c >= lo) ? e0 : 0.f;
+                        e1 = (c + 1 <= lim && c + 1 >= lo) ? e1 : 0.f;
                     }
                     pp[i] = f2pack(e0, e1);
                 }
@@ -865,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, int kMode>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo)
 {
@@ -878,9 +1118,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKV);
+        e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemKV);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ);
+        e = cudaFuncSetAttribute(bwd_dq_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemQ);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
@@ -915,16 +1157,28 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     p.n_t = (p.Ls + kRows - 1) / kRows;
     p.scale = 1.0f / sqrtf(static_cast<float>(D));
     p.scale_log2 = kLog2e * p.scale;
+    p.cu_seqlens = a.cu_seqlens;
+    p.n_seqs = a.n_seqs;
     // dK/dV: one CTA per key tile of each key/value head; dQ: per query tile of each head
     const long long grid_kv = static_cast<long long>(a.B) * a.Hkv * a.P * p.n_t;
     const long long grid = static_cast<long long>(a.B) * a.H * a.P * p.n_t;
     if (grid <= 0 || grid > 0x7fffffffLL || grid_kv <= 0) return cudaErrorInvalidConfiguration;
-    bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid_kv), kThreads, kSmemKV, a.stream>>>(tq, tk, tv,
-                                                                                       tdo, p);
+    bwd_dkdv_kernel<D, kMode><<<static_cast<unsigned>(grid_kv), kThreads, kSmemKV, a.stream>>>(
+        tq, tk, tv, tdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D><<<static_cast<unsigned>(grid), kThreads, kSmemQ, a.stream>>>(tq, tk, tv, tdo, p);
+    bwd_dq_kernel<D, kMode><<<static_cast<unsigned>(grid), kThreads, kSmemQ, a.stream>>>(tq, tk, tv,
+                                                                                       tdo, p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_layout(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const CUtensorMap& tdo)
+{
+    if (a.cu_seqlens != nullptr) return launch_bwd_d<D, 2>(a, tq, tk, tv, tdo);
+    if (a.zigzag) return launch_bwd_d<D, 1>(a, tq, tk, tv, tdo);
+    return launch_bwd_d<D, 0>(a, tq, tk, tv, tdo);
 }
 
 }  // namespace
@@ -932,8 +1186,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_attn_bwd_bf16(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo)
 {
-    if (a.D == 64) return launch_bwd_d<64>(a, tq, tk, tv, tdo);
-    if (a.D == 128) return launch_bwd_d<128>(a, tq, tk, tv, tdo);
+    if (a.D == 64) return launch_bwd_layout<64>(a, tq, tk, tv, tdo);
+    if (a.D == 128) return launch_bwd_layout<128>(a, tq, tk, tv, tdo);
     return cudaErrorInvalidValue;
 }
 

@@ -46,6 +46,9 @@ struct BwdArgs {
     void* dv;
     int B, L, H, D, P, causal;
     int Hkv;             // key/value heads (H % Hkv == 0); dk, dv are [B, L, Hkv, D]
+    int zigzag;          // zigzag shard layout (causal; Hkv == H)
+    const int* cu_seqlens;   // packed sequences (device; B == 1, Hkv == H), or null
+    int n_seqs;
     unsigned int* status;
     unsigned long long timeout_ns;
     cudaStream_t stream;

@@ -268,6 +268,44 @@ ra_status ring_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
                             int H, int H_kv, int D, int P, int causal, ra_stream_t stream);
 
 /*
+ * ring_attn_bwd_zigzag -- gradients of ring_attn_fwd_zigzag (bf16, causal): the
+ * backward of causal attention over the zigzag shard layout ("序列并行与 Ring
+ * Attention", section 3.4: shard r holds chunks r and 2P-1-r of 2P chunks; the causal
+ * rule compares global positions), with the exchange of sections 3.3 and 6.2: each
+ * K/V tile meets the query tiles of every shard in ring order from its owner's side,
+ * (s + t) mod P, and its dk, dv are written once to the owner's rows.
+ *
+ * q, k, v, out, dout, dq, dk, dv: device bf16 [B, L, H, D] in the zigzag row order
+ * (row i of shard r at the global position ring_attn_fwd_zigzag states); lse: the
+ * forward's fp32 [B, L, H].  Requires L % (2P) == 0 (RA_ERR_NOT_DIVISIBLE) and
+ * L/(2P) % 128 == 0 (RA_ERR_UNSUPPORTED).  Workspace, alignment, D and errors as
+ * ring_attn_bwd.  The result equals ring_attn_bwd of the position-ordered causal
+ * problem with its rows permuted into the zigzag order.
+ */
+ra_status ring_attn_bwd_zigzag(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               void* workspace, unsigned long long workspace_bytes, int B, int L,
+                               int H, int D, int P, ra_stream_t stream);
+
+/*
+ * ring_attn_bwd_varlen -- gradients of ring_attn_fwd_varlen (bf16): packed
+ * variable-length sequences, where a query sees only keys of its own sequence
+ * (causal: not after itself; "序列并行与 Ring Attention", section 6.5), so every
+ * gradient row depends only on its own sequence.  q, k, v, out, dout, dq, dk, dv:
+ * device bf16 [L, H, D]; lse: the forward's fp32 [L, H]; cu_seqlens: the forward's
+ * DEVICE int32 [n_seqs + 1] (0, ..., L; non-decreasing).  The P virtual shards split
+ * the packed rows evenly (L % P == 0); tiles are walked in ring order as in
+ * ring_attn_bwd.  Workspace: ring_attn_bwd_workspace_bytes(1, L, H).  With malformed
+ * cu_seqlens the results are undefined, but every access stays in bounds.  Alignment,
+ * D and errors as ring_attn_bwd.
+ */
+ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               void* workspace, unsigned long long workspace_bytes,
+                               const int* cu_seqlens, int n_seqs, int L, int H, int D, int P,
+                               int causal, ra_stream_t stream);
+
+/*
  * ring_attn_bwd_noalloc -- ring_attn_bwd for callers that cannot allocate device
  * memory (no counterpart on the pages: an addition of this library).
  *

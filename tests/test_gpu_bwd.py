@@ -185,3 +185,163 @@ def test_bwd_gqa_argument_errors():
     with pytest.raises(cea.RingAttnError) as e:
         cea.ring_attn_bwd_gqa(q, k, v, out, lse, torch.empty_like(q), P=2)
     assert e.value.code == 4          # 6 query heads over 4 key/value heads
+
+
+# ---------------------------------------------------------------- zigzag layout --
+
+ZIGZAG_CASES = [
+    # B, L, H, D, P
+    (1, 512, 2, 128, 2),
+    (2, 1024, 2, 128, 4),
+    (1, 768, 2, 64, 3),
+    (1, 2048, 1, 128, 8),
+    (1, 256, 2, 128, 1),
+]
+
+
+@pytest.mark.parametrize("case", ZIGZAG_CASES, ids=lambda c: "B%dL%dH%dD%dP%d" % c)
+def test_bwd_zigzag_parity(case):
+    """Causal backward of the position-ordered sequence, returned in zigzag row order:
+    the oracle's gradients (and the error scales) are computed in position order and
+    their rows permuted."""
+    B, L, H, D, P = case
+    qg, kg, vg = make_qkv(B, L, H, D, seed=80, dtype=torch.bfloat16)      # row = position
+    dog = torch.randn(B, L, H, D, generator=torch.Generator().manual_seed(81)).to(torch.bfloat16)
+    pos = torch.tensor(cea.zigzag_positions(L, P))
+    q, k, v, do = (t[:, pos].contiguous().to(DEV) for t in (qg, kg, vg, dog))
+    out, lse = cea.ring_attn_fwd_zigzag(q, k, v, P=P)
+    dq, dk, dv = cea.ring_attn_bwd_zigzag(q, k, v, out, lse, do, P=P)
+    assert cea.check_status() == 0
+    rq, rk, rv = oracle.attention_bwd(qg, kg, vg, dog, causal=True)
+    sq, sk, sv = _term_scales(qg, kg, vg, dog, True)
+    pz = pos.numpy()
+    _grad_close(to_np(dq), rq[:, pz], "dq", sq[:, pz])
+    _grad_close(to_np(dk), rk[:, pz], "dk", sk[:, pz])
+    _grad_close(to_np(dv), rv[:, pz], "dv", sv[:, pz])
+
+
+def test_bwd_zigzag_matches_contiguous_layout():
+    """The same causal problem through both layouts: gradients agree row for row after
+    the zigzag permutation (to the rounding of two summation orders), and each layout
+    is deterministic."""
+    B, L, H, D, P = 1, 1024, 4, 128, 4
+    qg, kg, vg = (t.to(DEV) for t in make_qkv(B, L, H, D, seed=82, dtype=torch.bfloat16,
+                                              head_scale=True))
+    dog = torch.randn(B, L, H, D, generator=torch.Generator().manual_seed(83)).to(torch.bfloat16)
+    dog = dog.to(DEV)
+    out, lse = cea.ring_attn_fwd(qg, kg, vg, P=P, causal=True)
+    contig = cea.ring_attn_bwd(qg, kg, vg, out, lse, dog, P=P, causal=True)
+    pos = torch.tensor(cea.zigzag_positions(L, P), device=DEV)
+    q, k, v, do = (t[:, pos].contiguous() for t in (qg, kg, vg, dog))
+    oz, lz = cea.ring_attn_fwd_zigzag(q, k, v, P=P)
+    zig = cea.ring_attn_bwd_zigzag(q, k, v, oz, lz, do, P=P)
+    again = cea.ring_attn_bwd_zigzag(q, k, v, oz, lz, do, P=P)
+    assert cea.check_status() == 0
+    for name, a, z, z2 in zip(("dq", "dk", "dv"), contig, zig, again):
+        assert torch.equal(z, z2), name
+        a = to_np(a)[:, pos.cpu().numpy()]
+        z = to_np(z)
+        rel = np.linalg.norm(a - z) / np.linalg.norm(a)
+        assert rel <= 4 * U and cosine(a, z) > 0.9999, (name, rel)
+
+
+def test_bwd_zigzag_argument_errors():
+    q, k, v = (t.to(DEV) for t in make_qkv(1, 256, 1, 128, seed=0, dtype=torch.bfloat16))
+    out, lse = cea.ring_attn_fwd(q, k, v, P=1)
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ring_attn_bwd_zigzag(q, k, v, out, lse, q.clone(), P=2)   # chunks of 64 rows
+    assert e.value.code == 2
+    q, k, v = (t.to(DEV) for t in make_qkv(1, 516, 1, 128, seed=0, dtype=torch.bfloat16))
+    out, lse = cea.ring_attn_fwd(q, k, v, P=1)
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ring_attn_bwd_zigzag(q, k, v, out, lse, q.clone(), P=4)   # 516 % 8 != 0
+    assert e.value.code == 4
+
+
+# ---------------------------------------------------------------- packed sequences --
+
+VARLEN_CASES = [
+    # lengths, H, D, P
+    ([37, 263, 1, 399, 324], 2, 128, 2),        # sequences cross the shard edge
+    ([1024], 2, 128, 4),                        # one sequence = plain attention
+    ([5, 600, 130, 7, 200, 1, 593, 512], 2, 64, 4),
+    ([100, 412, 252, 300], 1, 128, 1),
+    ([129, 127, 256, 1, 255, 256, 128], 2, 128, 3),  # boundaries one row off tile edges
+]
+
+
+def _packed_bwd_inputs(lengths, H, D, seed):
+    L = sum(lengths)
+    q, k, v = (t[0] for t in make_qkv(1, L, H, D, seed=seed, dtype=torch.bfloat16))
+    do = torch.randn(L, H, D, generator=torch.Generator().manual_seed(seed + 1)).to(torch.bfloat16)
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    return q, k, v, do, cu
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=lambda c: "n%d_H%d_D%d_P%d" % (len(c[0]), *c[1:]))
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_varlen_parity(case, causal):
+    """Every sequence is its own attention problem: each gradient slice equals the fp64
+    oracle's backward of that sequence alone."""
+    lengths, H, D, P = case
+    q, k, v, do, cu = _packed_bwd_inputs(lengths, H, D, seed=90)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = cea.ring_attn_fwd_varlen(qd, kd, vd, cu_d, P=P, causal=causal)
+    dq, dk, dv = cea.ring_attn_bwd_varlen(qd, kd, vd, out, lse, dod, cu_d, P=P, causal=causal)
+    assert cea.check_status() == 0
+    got = [to_np(t) for t in (dq, dk, dv)]
+    refs = [np.empty_like(g) for g in got]
+    scales = [np.empty_like(g) for g in got]
+    for a, b in zip(cu[:-1], cu[1:]):
+        if a == b:
+            continue
+        seg = [t[None, a:b] for t in (q, k, v, do)]
+        for i, (r, s) in enumerate(zip(oracle.attention_bwd(*seg, causal=causal),
+                                       _term_scales(*seg, causal))):
+            refs[i][a:b], scales[i][a:b] = r[0], s[0]
+    for name, g, r, s in zip(("dq", "dk", "dv"), got, refs, scales):
+        _grad_close(g, r, name, s)
+
+
+def test_bwd_varlen_samples_do_not_see_each_other():
+    """Replace one sequence's queries, keys, values and upstream gradient by other values:
+    the other sequences' gradients keep their bits (masked pairs contribute exactly
+    zero), the replaced sequence's change."""
+    lengths = [300, 200, 524]
+    q, k, v, do, cu = _packed_bwd_inputs(lengths, 2, 128, seed=92)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    for causal in (False, True):
+        res = []
+        for variant in range(2):
+            tq, tk, tv, tdo = (t.clone() for t in (q, k, v, do))
+            if variant:
+                tq[300:500] *= 3.0
+                tk[300:500] = 2.0
+                tv[300:500] = 40.0
+                tdo[300:500] = -tdo[300:500]
+            qd, kd, vd, dod = (t.to(DEV) for t in (tq, tk, tv, tdo))
+            out, lse = cea.ring_attn_fwd_varlen(qd, kd, vd, cu_d, P=4, causal=causal)
+            res.append(cea.ring_attn_bwd_varlen(qd, kd, vd, out, lse, dod, cu_d, P=4,
+                                                causal=causal))
+        for a, b in zip(*res):
+            assert torch.equal(a[:300], b[:300]) and torch.equal(a[500:], b[500:])
+            assert not torch.equal(a[300:500], b[300:500])
+
+
+def test_bwd_varlen_one_sequence_is_plain_backward():
+    """A single packed sequence is the plain backward with P shards: identical bits."""
+    L, H, D, P = 1024, 2, 128, 4
+    q, k, v = (t.to(DEV) for t in make_qkv(1, L, H, D, seed=94, dtype=torch.bfloat16))
+    do = torch.randn(1, L, H, D, generator=torch.Generator().manual_seed(95)).to(torch.bfloat16)
+    do = do.to(DEV)
+    cu_d = torch.tensor([0, L], dtype=torch.int32, device=DEV)
+    for causal in (False, True):
+        out, lse = cea.ring_attn_fwd(q, k, v, P=P, causal=causal)
+        a = cea.ring_attn_bwd(q, k, v, out, lse, do, P=P, causal=causal)
+        b = cea.ring_attn_bwd_varlen(q[0], k[0], v[0], out[0], lse[0], do[0], cu_d, P=P,
+                                     causal=causal)
+        for x, y in zip(a, b):
+            assert torch.equal(x[0], y)

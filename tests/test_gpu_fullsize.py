@@ -211,3 +211,101 @@ def test_grouped_backward_at_causal_lm_size():
     # relative to each row's largest component: the first-order bound of the plain
     # backward's full-size test, taken conservatively per row
     assert (np.abs(got - ref) <= 4 * u * (np.abs(ref) + scale) + 1e-5).all()
+
+
+def _dq_row_bound(q, k, v, do, i, h, keys, D):
+    """First-order rounding scale of dq[i, h] (term magnitudes, fp64), over the key rows
+    `keys` that query row i sees."""
+    c = 1.0 / np.sqrt(D)
+    kk, vv = k[keys, h], v[keys, h]
+    s = kk @ q[i, h] * c
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    dp = vv @ do[i, h]
+    ds = p * (dp - (p * dp).sum())
+    dvec_err = np.abs(do[i, h] * (p @ vv)).sum()
+    return (np.abs(ds) + p * dvec_err) @ np.abs(kk) * c
+
+
+def test_zigzag_backward_at_causal_lm_size():
+    """Zigzag backward at the causal-LM size (8 heads): the sum identities over all rows,
+    agreement with the contiguous layout's backward after the permutation, and dq on
+    sampled rows against the fp64 chain rule in position order."""
+    w = LM
+    H = 8
+    u = 2.0 ** -9
+    qg, kg, vg = make_qkv(1, w.L, H, w.D, seed=60, dtype=torch.bfloat16, head_scale=True)
+    dog = torch.randn(1, w.L, H, w.D, generator=torch.Generator().manual_seed(61)).to(torch.bfloat16)
+    pos = torch.tensor(cea.zigzag_positions(w.L, w.P))
+    q, k, v, do = (t[:, pos].contiguous().to(DEV) for t in (qg, kg, vg, dog))
+    out, lse = cea.ring_attn_fwd_zigzag(q, k, v, P=w.P)
+    dq, dk, dv = cea.ring_attn_bwd_zigzag(q, k, v, out, lse, do, P=w.P)
+    assert cea.check_status() == 0
+    sdv = dv.double().sum(1).cpu().numpy()
+    assert (np.abs(sdv - dog.double().sum(1).numpy())
+            <= 4 * u * dv.double().abs().sum(1).cpu().numpy() + 1e-3).all()
+    assert (np.abs(dk.double().sum(1).cpu().numpy())
+            <= 4 * u * dk.double().abs().sum(1).cpu().numpy() + 1e-3).all()
+    # the contiguous layout's backward of the same problem, rows permuted
+    gd = [t.to(DEV) for t in (qg, kg, vg, dog)]
+    o2, l2 = cea.ring_attn_fwd(*gd[:3], P=w.P, causal=True)
+    ref_layout = cea.ring_attn_bwd(*gd[:3], o2, l2, gd[3], P=w.P, causal=True)
+    pd = pos.to(DEV)
+    for name, a, z in zip(("dq", "dk", "dv"), ref_layout, (dq, dk, dv)):
+        a, z = a[:, pd].double(), z.double()
+        rel = float((a - z).norm() / a.norm())
+        assert rel <= 4 * u, (name, rel)
+    # sampled dq rows (zigzag row index -> position) against the oracle
+    rows = sample_rows(w.L, w.P, 12, seed=4)
+    prow = pos[rows].tolist()
+    ref = oracle.attention_bwd_dq_rows(qg, kg, vg, dog, prow, causal=True)
+    qf, kf, vf, dof = (t.double().numpy()[0] for t in (qg, kg, vg, dog))
+    for ri, (i, pi) in enumerate(zip(rows, prow)):
+        for h in range(H):
+            scale = _dq_row_bound(qf, kf, vf, dof, pi, h, slice(0, pi + 1), w.D)
+            got = dq[0, i, h].double().cpu().numpy()
+            r = ref[0, ri, h]
+            assert (np.abs(got - r) <= 2 * u * (np.abs(r) + scale) + 1e-6).all(), (i, h)
+
+
+def test_packed_backward_at_causal_lm_size():
+    """Packed-sequence backward at the causal-LM length (8 heads, lengths as in the
+    forward's full-size test): per sequence, the sum of dv over its keys equals the sum
+    of dout over its queries and the sum of dk is zero; dq on sampled rows of every
+    sequence against the fp64 chain rule of that sequence alone."""
+    w = LM
+    H = 8
+    u = 2.0 ** -9
+    g = torch.Generator().manual_seed(6)
+    lengths = []
+    while sum(lengths) < w.L:
+        lengths.append(int(torch.randint(1, 9000, (1,), generator=g)))
+    lengths[-1] -= sum(lengths) - w.L
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    q, k, v = (t[0] for t in make_qkv(1, w.L, H, w.D, seed=62, dtype=torch.bfloat16,
+                                      head_scale=True))
+    do = torch.randn(w.L, H, w.D, generator=torch.Generator().manual_seed(63)).to(torch.bfloat16)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = cea.ring_attn_fwd_varlen(qd, kd, vd, cu_d, P=w.P, causal=True)
+    dq, dk, dv = cea.ring_attn_bwd_varlen(qd, kd, vd, out, lse, dod, cu_d, P=w.P, causal=True)
+    assert cea.check_status() == 0
+    dqn, dkn, dvn = (t.double().cpu().numpy() for t in (dq, dk, dv))
+    qf, kf, vf, dof = (t.double().numpy() for t in (q, k, v, do))
+    rows = sample_rows(w.L, w.P, 24, seed=5)
+    for a, b in zip(cu[:-1], cu[1:]):
+        sdv, sdo = dvn[a:b].sum(0), dof[a:b].sum(0)
+        assert (np.abs(sdv - sdo) <= 4 * u * np.abs(dvn[a:b]).sum(0) + 1e-3).all(), (a, b)
+        assert (np.abs(dkn[a:b].sum(0)) <= 4 * u * np.abs(dkn[a:b]).sum(0) + 1e-3).all(), (a, b)
+        pick = [i for i in rows if a <= i < b]
+        if not pick:
+            continue
+        ref = oracle.attention_bwd_dq_rows(q[None, a:b], k[None, a:b], v[None, a:b],
+                                           do[None, a:b], [i - a for i in pick], causal=True)
+        for ri, i in enumerate(pick):
+            for h in range(H):
+                scale = _dq_row_bound(qf, kf, vf, dof, i, h, slice(a, i + 1), w.D)
+                r = ref[0, ri, h]
+                assert (np.abs(dqn[i, h] - r) <= 2 * u * (np.abs(r) + scale) + 1e-6).all(), (i, h)
