@@ -580,6 +580,40 @@ def run_profile_backward(args):
                       "tflops": fl / (ms * 1e-3) / 1e12}), flush=True)
 
 
+def run_profile_hbm(args):
+    """The HBM-stream kernels alone, for profiler captures: the LSE merge at the causal-LM
+    size (1,048,576 rows x 128, bf16) and the two Ulysses transposes at the Ulysses size
+    (B=2, L=8192, H=32, D=128, P=8).  `warmup` rounds of the three, then `steps` calls of
+    each kernel in turn (merge, seq2head, head2seq), one JSON line out."""
+    import context_exact_attention_gb300 as cea
+
+    dev = torch.device("cuda", 0)
+    cea.load_library()
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    rows, D = LM.B * LM.L * LM.H, LM.D
+    oa, ob = (torch.randn(rows, D, device=dev, generator=g).to(torch.bfloat16) for _ in range(2))
+    la, lb = (torch.randn(rows, device=dev, generator=g) for _ in range(2))
+    oo, lo = torch.empty_like(oa), torch.empty_like(la)
+    w = ULYSSES
+    x = torch.randn(w.P, w.B, w.L // w.P, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
+    y = torch.empty(w.P, w.B, w.L, w.H // w.P, w.D, device=dev, dtype=torch.bfloat16)
+    calls = {
+        "merge": (lambda: cea.attn_merge_partials(oa, la, ob, lb, o_out=oo, lse_out=lo,
+                                                  stream=stream), rows * (3 * D * 2 + 3 * 4)),
+        "seq2head": (lambda: cea.ulysses_seq2head(x, w.P, out=y, stream=stream), 4 * x.numel()),
+        "head2seq": (lambda: cea.ulysses_head2seq(y, w.P, out=x, stream=stream), 4 * x.numel()),
+    }
+    for _ in range(args.warmup):
+        for f, _ in calls.values():
+            f()
+    res = {"case": "merge at causal-LM size; Ulysses transposes at B2 L8192 H32 D128 P8"}
+    for name, (f, by) in calls.items():
+        ms = _time_loop(f, args.steps, stream) / args.steps
+        res[name] = {"ms": ms, "GB/s": by / (ms * 1e-3) / 1e9, "bytes": by}
+    print(json.dumps(res), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -594,6 +628,8 @@ def main():
                          "still larger than L2): the small case for profiler captures")
     ap.add_argument("--profile-backward", action="store_true",
                     help="only the backward of the headline workload with 8 heads (profiler case)")
+    ap.add_argument("--profile-hbm", action="store_true",
+                    help="only the merge and Ulysses transpose kernels (profiler case)")
     ap.add_argument("--ref-rows", type=int, default=8,
                     help="query rows (all heads) per reference step")
     args = ap.parse_args()
@@ -604,6 +640,8 @@ def main():
         print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
     if args.profile_backward:
         run_profile_backward(args)
+    elif args.profile_hbm:
+        run_profile_hbm(args)
     elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
