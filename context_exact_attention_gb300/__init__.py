@@ -24,7 +24,8 @@ __all__ = [
     "ulysses_attention", "ring_attn_bwd", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
     "zigzag_positions", "ring_attn_fwd_varlen", "varlen_padded_length", "check_status",
     "probe_wait_timeout", "ring_attn_fwd_host", "host_workspace_bytes", "ring_attn_bwd_gqa",
-    "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "EXPORTED_SYMBOLS",
+    "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "ring_attn_fwd_ex", "ring_attn_bwd_ex",
+    "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -42,8 +43,21 @@ EXPORTED_SYMBOLS = (
     "ra_probe_wait_timeout", "ring_attn_bwd", "ring_attn_bwd_workspace_bytes",
     "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
     "ring_attn_fwd_varlen", "ring_attn_fwd_host", "ring_attn_fwd_host_workspace_bytes",
-    "ring_attn_bwd_gqa", "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen",
+    "ring_attn_bwd_gqa", "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "ring_attn_fwd_ex",
+    "ring_attn_bwd_ex",
 )
+
+
+LAYOUTS = {"contiguous": 0, "zigzag": 1, "packed": 2}
+
+
+class AttnDesc(ctypes.Structure):
+    """Mirror of ra_attn_desc (include/ring_attn.h)."""
+    _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("H", ctypes.c_int),
+                ("H_kv", ctypes.c_int), ("D", ctypes.c_int), ("P", ctypes.c_int),
+                ("causal", ctypes.c_int), ("layout", ctypes.c_int),
+                ("cu_seqlens", ctypes.c_void_p), ("n_seqs", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
 
 
 class RingAttnError(RuntimeError):
@@ -89,6 +103,9 @@ def load_library(build_if_missing: bool = False):
                                      i, i, i, i, i, vp],
             "ring_attn_bwd_varlen": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
                                      vp, i, i, i, i, i, i, vp],
+            "ring_attn_fwd_ex": [vp, vp, vp, vp, vp, f_p, vp, vp],
+            "ring_attn_bwd_ex": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                 ctypes.c_ulonglong, vp],
             "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
             "ring_attn_fwd_zigzag": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp, vp],
             "ring_attn_fwd_varlen": [vp, vp, vp, vp, f_p, vp, i, i, i, i, i, i, i, vp, vp],
@@ -486,6 +503,68 @@ def ring_attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, P: int = 1, causal
           _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
           workspace.numel() * workspace.element_size(), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
           L, H, D, P, int(bool(causal)), _stream(stream))
+    return dq, dk, dv
+
+
+def _desc(q, k, P, causal, layout, cu_seqlens):
+    """Descriptor and the [B, L, H, D] view of q for ring_attn_fwd_ex / ring_attn_bwd_ex."""
+    if layout not in LAYOUTS:
+        raise ValueError(f"layout must be one of {sorted(LAYOUTS)}")
+    packed = layout == "packed"
+    if packed:
+        if q.dim() != 3 or k.dim() != 3:
+            raise ValueError("packed q, k, v are [L, H, D] / [L, H_kv, D]")
+        if (cu_seqlens is None or cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda
+                or cu_seqlens.dim() != 1):
+            raise ValueError("packed layout needs cu_seqlens, a 1-D int32 CUDA tensor")
+        B, (L, H, D) = 1, q.shape
+    else:
+        if cu_seqlens is not None:
+            raise ValueError("cu_seqlens belongs to the packed layout only")
+        B, L, H, D = q.shape
+    d = AttnDesc(B=B, L=L, H=H, H_kv=k.shape[-2], D=D, P=P, causal=int(bool(causal)),
+                 layout=LAYOUTS[layout], cu_seqlens=cu_seqlens.data_ptr() if packed else None,
+                 n_seqs=cu_seqlens.numel() - 1 if packed else 0,
+                 dtype=RA_BF16 if q.dtype == torch.bfloat16 else RA_F32)
+    return d, (B, L, H, D)
+
+
+def ring_attn_fwd_ex(q, k, v, P: int = 1, causal: bool = False, layout: str = "contiguous",
+                     cu_seqlens=None, out=None, lse=None, want_lse: bool = True,
+                     trace: bool = False, stream=None):
+    """The forward for any combination of options: grouped key/value heads (k, v with
+    fewer heads than q) with the contiguous, zigzag or packed layout.  q, k, v: [B, L, H, D]
+    / [B, L, H_kv, D], or [L, H, D] / [L, H_kv, D] for layout="packed" (with cu_seqlens).
+    bf16 or fp32.  Returns (out, lse) or (out, lse, trace); lse is [B, L, H] or [L, H]."""
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q must be bf16 or fp32")
+    d, (B, L, H, D) = _desc(q, k, P, causal, layout, cu_seqlens)
+    view = (lambda t: t.unsqueeze(0)) if layout == "packed" else (lambda t: t)
+    _check_qkv(view(q), view(k), view(v), dtype, grouped=True)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    tr = torch.full((P, P), -7, dtype=torch.int32, device=q.device) if trace else None
+    _call("ring_attn_fwd_ex", ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+          _ptr(tr), _stream(stream))
+    return (out, lse, tr) if trace else (out, lse)
+
+
+def ring_attn_bwd_ex(q, k, v, out, lse, dout, P: int = 1, causal: bool = False,
+                     layout: str = "contiguous", cu_seqlens=None, dq=None, dk=None, dv=None,
+                     workspace=None, stream=None):
+    """Gradients of ring_attn_fwd_ex (bf16) for the same options: returns (dq, dk, dv),
+    dq shaped like q and dk, dv like k (summed over each key/value head's query heads)."""
+    d, (B, L, H, D) = _desc(q, k, P, causal, layout, cu_seqlens)
+    view = (lambda t: t.unsqueeze(0)) if layout == "packed" else (lambda t: t)
+    _check_qkv(view(q), view(k), view(v), torch.bfloat16, grouped=True)
+    dq, dk, dv, workspace = _bwd_outputs(q, k, v, out, lse, dout, tuple(q.shape[:-1]), dq, dk,
+                                         dv, workspace, B * L * H)
+    _call("ring_attn_bwd_ex", ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+          _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), _stream(stream))
     return dq, dk, dv
 
 

@@ -425,6 +425,64 @@ ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
                     P, causal, stream, 0, cu_seqlens, n_seqs);
 }
 
+// The layout part of a descriptor, checked: zigzag flag, packed boundaries, batch.
+static ra_status desc_layout(const ra_attn_desc* d, int bf16, int* zig, const int** cu,
+                             int* n_seqs)
+{
+    if (!d) return RA_ERR_INVALID_ARG;
+    if (d->B < 1 || d->L < 1 || d->H < 1 || d->H_kv < 1 || d->D < 1 || d->P < 1)
+        return RA_ERR_INVALID_ARG;
+    *zig = 0;
+    *cu = nullptr;
+    *n_seqs = 0;
+    switch (d->layout) {
+    case RA_LAYOUT_CONTIGUOUS:
+        if (d->cu_seqlens) return RA_ERR_INVALID_ARG;
+        return RA_OK;
+    case RA_LAYOUT_ZIGZAG:
+        if (d->cu_seqlens) return RA_ERR_INVALID_ARG;
+        if (!d->causal) return RA_ERR_UNSUPPORTED;            // the layout exists for causal balance
+        if (d->L % (2 * d->P) != 0) return RA_ERR_NOT_DIVISIBLE;
+        if (bf16 && (d->L / (2 * d->P)) % 128 != 0) return RA_ERR_UNSUPPORTED;
+        *zig = 1;
+        return RA_OK;
+    case RA_LAYOUT_PACKED:
+        if (!d->cu_seqlens || d->n_seqs < 1 || d->B != 1) return RA_ERR_INVALID_ARG;
+        if (!aligned(d->cu_seqlens, 4)) return RA_ERR_MISALIGNED;
+        *cu = d->cu_seqlens;
+        *n_seqs = d->n_seqs;
+        return RA_OK;
+    }
+    return RA_ERR_INVALID_ARG;
+}
+
+ra_status ring_attn_fwd_ex(const ra_attn_desc* desc, const void* q, const void* k, const void* v,
+                           void* out, float* lse, int* trace, ra_stream_t stream)
+{
+    int zig = 0, n_seqs = 0;
+    const int* cu = nullptr;
+    const ra_status st = desc_layout(desc, desc && desc->dtype == RA_BF16, &zig, &cu, &n_seqs);
+    if (st != RA_OK) return st;
+    return attn_impl(q, k, v, out, lse, desc->B, desc->L, desc->H, desc->D, desc->P, desc->causal,
+                     desc->dtype, trace, reinterpret_cast<cudaStream_t>(stream), desc->H_kv, zig,
+                     cu, n_seqs);
+}
+
+ra_status ring_attn_bwd_ex(const ra_attn_desc* desc, const void* q, const void* k, const void* v,
+                           const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                           void* dv, void* workspace, unsigned long long workspace_bytes,
+                           ra_stream_t stream)
+{
+    int zig = 0, n_seqs = 0;
+    const int* cu = nullptr;
+    const ra_status st = desc_layout(desc, 1, &zig, &cu, &n_seqs);
+    if (st != RA_OK) return st;
+    if (desc->dtype != RA_BF16) return RA_ERR_UNSUPPORTED;
+    return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, desc->B,
+                    desc->L, desc->H, desc->H_kv, desc->D, desc->P, desc->causal, stream, zig, cu,
+                    n_seqs);
+}
+
 ra_status ra_check_status(ra_stream_t stream)
 {
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -351,13 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int n_blocks = n_head * p.group;
     // block n: query head h, query shard r, query tile qt (modes 1 and 2: n = 0, 1, ...
-    // in order, one head)
+    // in order; the walk restarts for each query head of the group)
     auto block = [&](int n, int& r, int& qt, int& h) {
         if constexpr (kMode != 0) {
-            walk.at(n);
+            const int g = p.group == 1 ? 0 : n / n_head;
+            walk.at(n - g * n_head);
             r = walk.x;
             qt = walk.tile();
-            h = hk;
+            h = hk * p.group + g;
             return;
         }
         const int g = p.group == 1 ? 0 : n / n_head;

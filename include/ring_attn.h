@@ -331,6 +331,69 @@ ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
                                 int B, int L, int H, int D, int P, int causal, ra_stream_t stream);
 
 /*
+ * Shard layouts of the general entry points below.
+ *   RA_LAYOUT_CONTIGUOUS  shard r holds positions [r L/P, (r+1) L/P) (ring_attn_fwd);
+ *   RA_LAYOUT_ZIGZAG      shard r holds chunks r and 2P-1-r of 2P chunks
+ *                         (ring_attn_fwd_zigzag; causal only);
+ *   RA_LAYOUT_PACKED      packed variable-length sequences over contiguous shards,
+ *                         boundaries in cu_seqlens (ring_attn_fwd_varlen; B == 1).
+ */
+typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_ZIGZAG = 1, RA_LAYOUT_PACKED = 2 } ra_layout;
+
+/*
+ * Problem description of ring_attn_fwd_ex / ring_attn_bwd_ex: every option of the
+ * specialised entry points in one place, so that they combine -- grouped key/value
+ * heads with the zigzag or the packed layout in particular (a grouped-head model
+ * trained with zigzag ring shards or packed samples needs both at once).
+ *   B, L, H, D, P  as ring_attn_fwd; H_kv key/value heads (H % H_kv == 0; H_kv == H
+ *                  for plain attention), query head h reading head h / (H / H_kv);
+ *   causal         0 / 1 (RA_LAYOUT_ZIGZAG requires 1: RA_ERR_UNSUPPORTED otherwise);
+ *   layout         one of ra_layout;
+ *   cu_seqlens     RA_LAYOUT_PACKED only (else NULL): device int32 [n_seqs + 1], as
+ *                  ring_attn_fwd_varlen takes it;
+ *   dtype          RA_BF16 or RA_F32 for the forward, RA_BF16 for the backward.
+ * The descriptor is read during the call only.
+ */
+typedef struct {
+    int B, L, H, H_kv, D, P;
+    int causal;
+    ra_layout layout;
+    const int* cu_seqlens;
+    int n_seqs;
+    ra_dtype dtype;
+} ra_attn_desc;
+
+/*
+ * ring_attn_fwd_ex -- the forward for any combination of the options in *desc: the
+ * operation of ring_attn_fwd ("序列并行与 Ring Attention", sections 3.1-3.4) with the
+ * key/value head grouping of ring_attn_fwd_gqa (sections 3.5, 6.4), the zigzag layout
+ * of ring_attn_fwd_zigzag (section 3.4) or the packed sequences of
+ * ring_attn_fwd_varlen (section 6.5).  q, out: [B, L, H, D]; k, v: [B, L, H_kv, D];
+ * lse [B, L, H] or NULL; trace [P, P] or NULL (as ring_attn_fwd_trace).  Argument
+ * checks and errors: those of the specialised entry point of the same options, plus
+ * RA_ERR_INVALID_ARG for a NULL descriptor, an unknown layout, cu_seqlens with a
+ * non-packed layout or B != 1 with the packed one.  With the options of a specialised
+ * entry point it launches the same kernel on the same arguments (same bits).
+ */
+ra_status ring_attn_fwd_ex(const ra_attn_desc* desc, const void* q, const void* k, const void* v,
+                           void* out, float* lse, int* trace, ra_stream_t stream);
+
+/*
+ * ring_attn_bwd_ex -- the backward of ring_attn_fwd_ex (bf16) for the same *desc:
+ * the operation of ring_attn_bwd (sections 3.3 and 6.2) under the descriptor's
+ * visibility rule and head grouping.  q, out, dout, dq: [B, L, H, D]; k, v, dk, dv:
+ * [B, L, H_kv, D], each key/value head's gradients summed over its query heads (as
+ * ring_attn_bwd_gqa); lse: the forward's [B, L, H]; workspace of at least
+ * ring_attn_bwd_workspace_bytes(B, L, H).  Deterministic (no atomics).  Checks and
+ * errors as ring_attn_fwd_ex and ring_attn_bwd; dtype other than RA_BF16 returns
+ * RA_ERR_UNSUPPORTED.
+ */
+ra_status ring_attn_bwd_ex(const ra_attn_desc* desc, const void* q, const void* k, const void* v,
+                           const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                           void* dv, void* workspace, unsigned long long workspace_bytes,
+                           ra_stream_t stream);
+
+/*
  * ra_check_status -- synchronise `stream`, then read and clear the status word
  * of the current device.  Returns RA_ERR_TIMEOUT if a kernel gave up on a
  * bounded wait since the last check, RA_ERR_CUDA if the stream reports an

@@ -137,3 +137,39 @@ def test_host_workspace_size():
         assert lib.ring_attn_fwd_host_workspace_bytes(B, L, H, D, g) == 3 * slot + r(rows * H * 4)
     assert lib.ring_attn_fwd_host_workspace_bytes(1, 256, 8, 128, 3) == 0
     assert lib.ring_attn_fwd_host_workspace_bytes(1, 256, 8, 128, 16) == 0
+
+
+def test_descriptor_layout_and_argument_errors(lib):
+    """The ctypes mirror of ra_attn_desc has the C layout (eight ints, the boundary
+    pointer, two ints: 48 bytes), and the general entry points reject bad descriptors
+    on the host before touching the runtime."""
+    assert ctypes.sizeof(cea.AttnDesc) == 48
+    assert cea.AttnDesc.cu_seqlens.offset == 32 and cea.AttnDesc.dtype.offset == 44
+    fake = ctypes.c_void_p(1 << 20)
+    out = ctypes.c_void_p(1 << 40)
+    ws = ctypes.c_void_p(1 << 44)
+    null = ctypes.c_void_p(0)
+    s = ctypes.c_void_p(0)
+
+    def desc(**kw):
+        d = dict(B=1, L=1024, H=4, H_kv=2, D=128, P=4, causal=1, layout=1, cu_seqlens=None,
+                 n_seqs=0, dtype=0)
+        d.update(kw)
+        return ctypes.byref(cea.AttnDesc(**d))
+
+    fwd = lambda d: lib.ring_attn_fwd_ex(d, fake, fake, fake, out, null, null, s)
+    bwd = lambda d: lib.ring_attn_bwd_ex(d, fake, fake, fake, fake, fake, fake, out, out, out, ws,
+                                         ctypes.c_ulonglong(1 << 20), s)
+    assert lib.ring_attn_fwd_ex(None, fake, fake, fake, out, null, null, s) == 1
+    assert fwd(desc(layout=3)) == 1                         # unknown layout
+    assert fwd(desc(causal=0)) == 2                         # zigzag is causal only
+    assert fwd(desc(L=1020)) == 4                           # L % 2P
+    assert fwd(desc(L=512)) == 2                            # chunks of 64 rows (bf16)
+    assert fwd(desc(H_kv=3)) == 4                           # H % H_kv
+    assert fwd(desc(layout=0, cu_seqlens=1 << 20)) == 1     # boundaries without packed layout
+    assert fwd(desc(layout=2)) == 1                         # packed without boundaries
+    assert fwd(desc(layout=2, cu_seqlens=1 << 20, n_seqs=3, B=2)) == 1
+    assert fwd(desc(layout=2, cu_seqlens=(1 << 20) + 2, n_seqs=3)) == 3
+    assert bwd(desc(dtype=1)) == 2                          # backward is bf16 only
+    assert bwd(desc(causal=0)) == 2
+    assert bwd(desc(H_kv=0)) == 1

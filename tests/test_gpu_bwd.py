@@ -345,3 +345,99 @@ def test_bwd_varlen_one_sequence_is_plain_backward():
                                      causal=causal)
         for x, y in zip(a, b):
             assert torch.equal(x[0], y)
+
+
+# ------------------------------------- combined options (ring_attn_bwd_ex) --
+
+def _grouped_scales(q, k, v, do, causal, G):
+    """Error scales of the grouped backward: the per-query-head scales of the repeated
+    key/value heads, dk and dv summed over each group."""
+    B, L, Hkv, D = k.shape
+    sq, sk, sv = _term_scales(q, k.repeat_interleave(G, dim=2), v.repeat_interleave(G, dim=2),
+                              do, causal)
+    return sq, sk.reshape(B, L, Hkv, G, D).sum(axis=3), sv.reshape(B, L, Hkv, G, D).sum(axis=3)
+
+
+@pytest.mark.parametrize("case", [(1, 1024, 4, 2, 128, 4), (2, 768, 6, 2, 64, 3),
+                                  (1, 512, 4, 1, 128, 2)],
+                         ids=lambda c: "B%dL%dH%dHkv%dD%dP%d" % c)
+def test_bwd_ex_zigzag_grouped_heads_parity(case):
+    """Backward of grouped key/value heads over zigzag shards against the grouped fp64
+    gradient oracle in position order, rows permuted."""
+    B, L, H, Hkv, D, P = case
+    G = H // Hkv
+    qg, _, _ = make_qkv(B, L, H, D, seed=110, dtype=torch.bfloat16)
+    _, kg, vg = make_qkv(B, L, Hkv, D, seed=111, dtype=torch.bfloat16)
+    dog = torch.randn(B, L, H, D, generator=torch.Generator().manual_seed(112)).to(torch.bfloat16)
+    pos = torch.tensor(cea.zigzag_positions(L, P))
+    q, k, v, do = (t[:, pos].contiguous().to(DEV) for t in (qg, kg, vg, dog))
+    out, lse = cea.ring_attn_fwd_ex(q, k, v, P=P, causal=True, layout="zigzag")
+    dq, dk, dv = cea.ring_attn_bwd_ex(q, k, v, out, lse, do, P=P, causal=True, layout="zigzag")
+    assert cea.check_status() == 0
+    assert dk.shape == k.shape and dv.shape == v.shape
+    rq, rk, rv = oracle.attention_bwd_gqa(qg, kg, vg, dog, causal=True)
+    sq, sk, sv = _grouped_scales(qg, kg, vg, dog, True, G)
+    pz = pos.numpy()
+    _grad_close(to_np(dq), rq[:, pz], "dq", sq[:, pz])
+    _grad_close(to_np(dk), rk[:, pz], "dk", sk[:, pz])
+    _grad_close(to_np(dv), rv[:, pz], "dv", sv[:, pz])
+
+
+@pytest.mark.parametrize("case", [([37, 263, 1, 399, 324], 4, 2, 128, 2),
+                                  ([5, 600, 130, 7, 200, 1, 593, 512], 4, 1, 64, 4)],
+                         ids=lambda c: "n%d_H%dHkv%d_P%d" % (len(c[0]), c[1], c[2], c[4]))
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_ex_packed_grouped_heads_parity(case, causal):
+    """Backward of grouped key/value heads over packed sequences: each sequence against
+    the grouped fp64 gradient oracle of that sequence alone."""
+    lengths, H, Hkv, D, P = case
+    G = H // Hkv
+    L = sum(lengths)
+    q = make_qkv(1, L, H, D, seed=113, dtype=torch.bfloat16)[0][0]
+    _, k, v = (t[0] for t in make_qkv(1, L, Hkv, D, seed=114, dtype=torch.bfloat16))
+    do = torch.randn(L, H, D, generator=torch.Generator().manual_seed(115)).to(torch.bfloat16)
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = cea.ring_attn_fwd_ex(qd, kd, vd, P=P, causal=causal, layout="packed",
+                                    cu_seqlens=cu_d)
+    dq, dk, dv = cea.ring_attn_bwd_ex(qd, kd, vd, out, lse, dod, P=P, causal=causal,
+                                      layout="packed", cu_seqlens=cu_d)
+    assert cea.check_status() == 0
+    got = [to_np(t) for t in (dq, dk, dv)]
+    refs = [np.empty_like(g) for g in got]
+    scales = [np.empty_like(g) for g in got]
+    for a, b in zip(cu[:-1], cu[1:]):
+        seg = [t[None, a:b] for t in (q, k, v, do)]
+        for i, (r, s) in enumerate(zip(oracle.attention_bwd_gqa(*seg, causal=causal),
+                                       _grouped_scales(*seg, causal, G))):
+            refs[i][a:b], scales[i][a:b] = r[0], s[0]
+    for name, g, r, s in zip(("dq", "dk", "dv"), got, refs, scales):
+        _grad_close(g, r, name, s)
+
+
+def test_bwd_ex_matches_the_specialised_entry_points():
+    """Same options as a specialised backward entry point: identical bits."""
+    B, L, H, D, P = 1, 1024, 4, 128, 4
+    q, k, v = (t.to(DEV) for t in make_qkv(B, L, H, D, seed=116, dtype=torch.bfloat16))
+    do = torch.randn(B, L, H, D, generator=torch.Generator().manual_seed(117)).to(torch.bfloat16)
+    do = do.to(DEV)
+    cu_d = torch.tensor([0, 300, 301, 1024], dtype=torch.int32, device=DEV)
+    out, lse = cea.ring_attn_fwd(q, k, v, P=P, causal=True)
+    oz, lz = cea.ring_attn_fwd_zigzag(q, k, v, P=P)
+    ov, lv = cea.ring_attn_fwd_varlen(q[0], k[0], v[0], cu_d, P=P, causal=True)
+    pairs = [
+        (cea.ring_attn_bwd(q, k, v, out, lse, do, P=P, causal=True),
+         cea.ring_attn_bwd_ex(q, k, v, out, lse, do, P=P, causal=True)),
+        (cea.ring_attn_bwd_zigzag(q, k, v, oz, lz, do, P=P),
+         cea.ring_attn_bwd_ex(q, k, v, oz, lz, do, P=P, causal=True, layout="zigzag")),
+        (cea.ring_attn_bwd_varlen(q[0], k[0], v[0], ov, lv, do[0], cu_d, P=P, causal=True),
+         cea.ring_attn_bwd_ex(q[0], k[0], v[0], ov, lv, do[0], P=P, causal=True, layout="packed",
+                              cu_seqlens=cu_d)),
+    ]
+    assert cea.check_status() == 0
+    for a, b in pairs:
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)

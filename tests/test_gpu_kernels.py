@@ -443,3 +443,86 @@ def test_varlen_samples_do_not_see_each_other():
         b, _ = cea.ring_attn_fwd_varlen(*_dev(q, k2, v2), cu_d, P=4, causal=causal)
         assert torch.equal(a[:300], b[:300]) and torch.equal(a[500:], b[500:])
         assert not torch.equal(a[300:500], b[300:500])
+
+
+# ------------------------------------- combined options (ring_attn_fwd_ex) --
+
+EX_ZIGZAG_CASES = [
+    # B, L, H, H_kv, D, P, dtype
+    (1, 1024, 4, 2, 128, 4, torch.bfloat16),
+    (2, 768, 6, 2, 64, 3, torch.bfloat16),
+    (1, 512, 4, 1, 128, 2, torch.bfloat16),
+    (1, 96, 4, 2, 32, 3, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", EX_ZIGZAG_CASES, ids=lambda c: "B%dL%dH%dHkv%dD%dP%d" % c[:6])
+def test_ex_zigzag_grouped_heads_parity(case):
+    """Grouped key/value heads over zigzag shards: the grouped oracle in position order,
+    rows permuted into the zigzag order."""
+    B, L, H, Hkv, D, P, dtype = case
+    qg, _, _ = make_qkv(B, L, H, D, seed=100, dtype=dtype)
+    _, kg, vg = make_qkv(B, L, Hkv, D, seed=101, dtype=dtype)
+    pos = torch.tensor(cea.zigzag_positions(L, P))
+    q, k, v = (t[:, pos].contiguous() for t in (qg, kg, vg))
+    out, lse = cea.ring_attn_fwd_ex(*_dev(q, k, v), P=P, causal=True, layout="zigzag")
+    assert cea.check_status() == 0
+    ref, lref = oracle.attention(qg, kg, vg, causal=True)
+    check = assert_bf16_close if dtype == torch.bfloat16 else assert_f32_close
+    check(to_np(out), ref[:, pos.numpy()], "out")
+    check(to_np(lse), lref[:, pos.numpy()], "lse")
+
+
+EX_PACKED_CASES = [
+    # lengths, H, H_kv, D, P, dtype
+    ([37, 263, 1, 399, 324], 4, 2, 128, 2, torch.bfloat16),
+    ([5, 600, 130, 7, 200, 1, 593, 512], 4, 1, 64, 4, torch.bfloat16),
+    ([5, 40, 1, 50], 6, 3, 32, 3, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", EX_PACKED_CASES, ids=lambda c: "n%d_H%dHkv%d_P%d" % (len(c[0]), c[1], c[2], c[4]))
+@pytest.mark.parametrize("causal", [False, True])
+def test_ex_packed_grouped_heads_parity(case, causal):
+    """Grouped key/value heads over packed sequences: every sequence against the grouped
+    oracle run on that sequence alone."""
+    lengths, H, Hkv, D, P, dtype = case
+    L = sum(lengths)
+    q = make_qkv(1, L, H, D, seed=102, dtype=dtype)[0][0]
+    _, k, v = (t[0] for t in make_qkv(1, L, Hkv, D, seed=103, dtype=dtype))
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    out, lse = cea.ring_attn_fwd_ex(*_dev(q, k, v), P=P, causal=causal, layout="packed",
+                                    cu_seqlens=cu_d)
+    assert cea.check_status() == 0
+    check = assert_bf16_close if dtype == torch.bfloat16 else assert_f32_close
+    got, lg = to_np(out), to_np(lse)
+    for a, b in zip(cu[:-1], cu[1:]):
+        ref, lref = oracle.attention(q[None, a:b], k[None, a:b], v[None, a:b], causal=causal)
+        check(got[a:b], ref[0], f"rows {a}:{b}")
+        check(lg[a:b], lref[0], f"lse {a}:{b}")
+
+
+def test_ex_matches_the_specialised_entry_points():
+    """With the options of a specialised entry point, the general one launches the same
+    kernel on the same arguments: identical bits."""
+    B, L, H, D, P = 1, 1024, 4, 128, 4
+    q, k, v = _dev(*make_qkv(B, L, H, D, seed=104, dtype=torch.bfloat16))
+    _, k2, v2 = _dev(*make_qkv(B, L, 2, D, seed=105, dtype=torch.bfloat16))
+    cu_d = torch.tensor([0, 300, 301, 1024], dtype=torch.int32, device=DEV)
+    pairs = [
+        (cea.ring_attn_fwd(q, k, v, P=P, causal=True),
+         cea.ring_attn_fwd_ex(q, k, v, P=P, causal=True)),
+        (cea.ring_attn_fwd_gqa(q, k2, v2, P=P, causal=False),
+         cea.ring_attn_fwd_ex(q, k2, v2, P=P, causal=False)),
+        (cea.ring_attn_fwd_zigzag(q, k, v, P=P),
+         cea.ring_attn_fwd_ex(q, k, v, P=P, causal=True, layout="zigzag")),
+        (cea.ring_attn_fwd_varlen(q[0], k[0], v[0], cu_d, P=P, causal=True),
+         cea.ring_attn_fwd_ex(q[0], k[0], v[0], P=P, causal=True, layout="packed",
+                              cu_seqlens=cu_d)),
+    ]
+    assert cea.check_status() == 0
+    for a, b in pairs:
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
