@@ -331,10 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work unit: (batch, head) outer; inside, heaviest (shard, pair) first
+    // ---- work unit: heaviest (shard, pair) first, two (batch, head) pairs interleaved
     const int units_per_bh = p.P * p.n_pair;
-    const int bh = blockIdx.x / units_per_bh;
-    const int u = blockIdx.x - bh * units_per_bh;
+    int bh, u;
+    unit_of_block(blockIdx.x, p.B * p.H, units_per_bh, bh, u);
     const int r = p.P - 1 - u / p.n_pair;
     const int pair = p.n_pair - 1 - (u - (u / p.n_pair) * p.n_pair);
     const int b = bh / p.H;

@@ -307,13 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // unit: (b, key/value head hk) outer; inside, heaviest key tile first (low shard,
-    // low tile).  With grouped heads the unit's keys meet the queries of every query head
-    // of its group (h = hk * group + g), one head after the other, and dK, dV accumulate
-    // over all of them.
+    // unit: heaviest key tile first (low shard, low tile), two (b, key/value head) pairs
+    // interleaved (unit_of_block).  With grouped heads the unit's keys meet the queries of
+    // every query head of its group (h = hk * group + g), one head after the other, and
+    // dK, dV accumulate over all of them.
     const int units_per_bh = p.P * p.n_t;
-    const int bh = blockIdx.x / units_per_bh;
-    const int u = blockIdx.x - bh * units_per_bh;
+    int bh, u;
+    unit_of_block(blockIdx.x, p.B * p.Hkv, units_per_bh, bh, u);
     const int s = u / p.n_t;          // shard owning these keys
     const int kt = u - s * p.n_t;     // key tile within the shard
     const int b = bh / p.Hkv;
@@ -766,10 +766,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // unit: (b, h) outer; inside, heaviest query tile first (last shard, last tile)
+    // unit: heaviest query tile first (last shard, last tile), two (b, h) pairs
+    // interleaved (unit_of_block)
     const int units_per_bh = p.P * p.n_t;
-    const int bh = blockIdx.x / units_per_bh;
-    const int u = blockIdx.x - bh * units_per_bh;
+    int bh, u;
+    unit_of_block(blockIdx.x, p.B * p.H, units_per_bh, bh, u);
     const int r = p.P - 1 - u / p.n_t;
     const int qt = p.n_t - 1 - (u - (u / p.n_t) * p.n_t);
     const int b = bh / p.H;

@@ -22,6 +22,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// Work order of the attention grids.  Each (batch, head) has units_per_bh units listed
+// heaviest first; the grid interleaves the units of kHeadGroup consecutive (batch, head)
+// pairs (unit 0 of both, unit 1 of both, ...), so that the heaviest units of every pair
+// of heads start early (the block scheduler dispatches in index order and the light
+// units fill the tail) while only two heads' K/V are live in L2 at a time.  Block `block`
+// of a grid of n_bh * units_per_bh blocks gets (bh, u); the mapping is a bijection.
+constexpr int kHeadGroup = 2;
+__device__ __forceinline__ void unit_of_block(int block, int n_bh, int units_per_bh, int& bh,
+                                              int& u)
+{
+    const int base = block / (kHeadGroup * units_per_bh) * kHeadGroup;
+    const int cnt = min(kHeadGroup, n_bh - base);    // the last group may hold one head
+    const int k = block - base * units_per_bh;
+    u = k / cnt;
+    bh = base + (k - u * cnt);
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
