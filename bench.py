@@ -411,7 +411,16 @@ def measure_rows(cea, dev, stream, peaks):
     res["ulysses_pipeline"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                                "frac": fl / (ms * 1e-3) / 1e12 / peak,
                                "note": "3 seq2head + attention (B'=16, H'=4, P=1) + head2seq"}
-    del x, y, qs, ks, vs, bufs
+    # the same step in one kernel: the transposes folded into the tensor maps' addressing
+    o_seq = torch.empty_like(qs)
+    f = lambda: cea.ulysses_attention_fused(qs, ks, vs, w.P, out=o_seq, stream=stream)
+    for _ in range(2):
+        f()
+    ms = _time_loop(f, n2, stream) / n2
+    res["ulysses_fused"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                            "frac": fl / (ms * 1e-3) / 1e12 / peak,
+                            "note": "ulysses_attention_fused: same result, no head-sharded copies"}
+    del x, y, qs, ks, vs, bufs, o_seq
 
     # grouped key/value heads at the headline shape: 32 query heads over 8 key/value heads
     w = LM

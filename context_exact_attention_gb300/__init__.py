@@ -25,7 +25,7 @@ __all__ = [
     "zigzag_positions", "ring_attn_fwd_varlen", "varlen_padded_length", "check_status",
     "probe_wait_timeout", "ring_attn_fwd_host", "host_workspace_bytes", "ring_attn_bwd_gqa",
     "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "ring_attn_fwd_ex", "ring_attn_bwd_ex",
-    "EXPORTED_SYMBOLS",
+    "ulysses_attention_fused", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -44,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
     "ring_attn_fwd_varlen", "ring_attn_fwd_host", "ring_attn_fwd_host_workspace_bytes",
     "ring_attn_bwd_gqa", "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "ring_attn_fwd_ex",
-    "ring_attn_bwd_ex",
+    "ring_attn_bwd_ex", "ulysses_attention_fused",
 )
 
 
@@ -104,6 +104,7 @@ def load_library(build_if_missing: bool = False):
             "ring_attn_bwd_varlen": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
                                      vp, i, i, i, i, i, i, vp],
             "ring_attn_fwd_ex": [vp, vp, vp, vp, vp, f_p, vp, vp],
+            "ulysses_attention_fused": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, vp],
             "ring_attn_bwd_ex": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                  ctypes.c_ulonglong, vp],
             "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
@@ -405,6 +406,28 @@ def ulysses_attention(q_seq, k_seq, v_seq, P: int, stream=None, buffers=None):
                           causal=False, out=buffers["o"].view(shape), want_lse=False,
                           stream=stream)
     return ulysses_head2seq(buffers["o"], P, stream=stream)
+
+
+def ulysses_attention_fused(q_seq, k_seq, v_seq, P: int, causal: bool = False, out=None,
+                            lse=None, want_lse: bool = False, stream=None):
+    """The Ulysses step on sequence-sharded bf16 buffers q_seq [P, B, L/P, H, D] and
+    k_seq, v_seq [P, B, L/P, H_kv, D] in one kernel (the transposes folded into the tensor
+    maps' addressing).  Returns (out [P, B, L/P, H, D], lse [P, B, L/P, H] or None), the
+    same bits as ulysses_attention."""
+    for name, t in (("q_seq", q_seq), ("k_seq", k_seq), ("v_seq", v_seq)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 5 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor [P, B, L/P, H, D]")
+    Pp, B, Ls, H, D = q_seq.shape
+    if Pp != P or k_seq.shape != v_seq.shape or k_seq.shape[:3] != q_seq.shape[:3] \
+            or k_seq.shape[4] != D:
+        raise ValueError("q_seq, k_seq, v_seq must share P, B, L/P and D")
+    if out is None:
+        out = torch.empty_like(q_seq)
+    if lse is None and want_lse:
+        lse = torch.empty(q_seq.shape[:4], dtype=torch.float32, device=q_seq.device)
+    _call("ulysses_attention_fused", _ptr(q_seq), _ptr(k_seq), _ptr(v_seq), _ptr(out), _ptr(lse),
+          B, Ls * P, H, k_seq.shape[3], D, P, int(bool(causal)), _stream(stream))
+    return out, lse
 
 
 def ring_attn_bwd(q, k, v, out, lse, dout, P: int = 1, causal: bool = False, dq=None, dk=None,

@@ -76,6 +76,26 @@ bool encode_qkv_map(CUtensorMap* map, const void* base, int B, int L, int H, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A sequence-sharded Ulysses buffer [P][B][L/P][H][D] as a 5-D bf16 tensor
+// {D, H, L/P, B, P} (innermost first), same boxes and swizzle as encode_qkv_map: a box of
+// 128 rows stays inside one shard when (L/P) % 128 == 0.
+bool encode_seq_shard_map(CUtensorMap* map, const void* base, int P, int B, int L, int H, int D)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t Ls = static_cast<cuuint64_t>(L / P);
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), Ls,
+                                static_cast<cuuint64_t>(B), static_cast<cuuint64_t>(P)};
+    const cuuint64_t row = static_cast<cuuint64_t>(H) * D * 2;
+    const cuuint64_t strides[4] = {static_cast<cuuint64_t>(D) * 2, row, Ls * row, Ls * row * B};
+    const cuuint32_t box[5] = {64, 1, 128, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool overlap(const void* a, unsigned long long na, const void* b, unsigned long long nb)
@@ -119,7 +139,7 @@ ra_status check_attn(const void* q, const void* k, const void* v, const void* ou
 ra_status attn_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                     int L, int H, int D, int P, int causal, ra_dtype dtype, int* trace,
                     cudaStream_t stream, int Hkv = -1, int zigzag = 0,
-                    const int* cu_seqlens = nullptr, int n_seqs = 0)
+                    const int* cu_seqlens = nullptr, int n_seqs = 0, int ulysses_P = 0)
 {
     if (Hkv < 0) Hkv = H;
     if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_UNSUPPORTED;
@@ -151,10 +171,29 @@ ra_status attn_impl(const void* q, const void* k, const void* v, void* out, floa
     a.zigzag = zigzag;
     a.cu_seqlens = cu_seqlens;
     a.n_seqs = n_seqs;
+    a.u_P = 0;
+    a.u_B = 0;
+    a.u_H = 0;
     a.timeout_ns = kWaitLimitNs;
     a.stream = stream;
     st = status_word(&a.status);
     if (st != RA_OK) return st;
+    if (ulysses_P > 0) {
+        // the kernel sees ulysses_P * B head-group batches of H / ulysses_P heads (ring P = 1)
+        // and addresses the sequence-sharded sources through 5-D tensor maps
+        CUtensorMap tq, tk, tv;
+        if (!encode_seq_shard_map(&tq, q, ulysses_P, B, L, H, D) ||
+            !encode_seq_shard_map(&tk, k, ulysses_P, B, L, Hkv, D) ||
+            !encode_seq_shard_map(&tv, v, ulysses_P, B, L, Hkv, D))
+            return RA_ERR_CUDA;
+        a.u_P = ulysses_P;
+        a.u_B = B;
+        a.u_H = H;
+        a.B = ulysses_P * B;
+        a.H = H / ulysses_P;
+        a.Hkv = Hkv / ulysses_P;
+        return from_cuda(ra::launch_attn_bf16(a, tq, tk, tv));
+    }
     if (dtype == RA_F32) return from_cuda(ra::launch_attn_f32(a));
     CUtensorMap tq, tk, tv;
     if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, Hkv, D) ||
@@ -265,6 +304,20 @@ ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void
     if (!aligned(cu_seqlens, 4)) return RA_ERR_MISALIGNED;
     return attn_impl(q, k, v, out, lse, 1, L, H, D, P, causal, dtype, trace,
                      reinterpret_cast<cudaStream_t>(stream), H, 0, cu_seqlens, n_seqs);
+}
+
+ra_status ulysses_attention_fused(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int B, int L, int H, int H_kv, int D, int P,
+                                  int causal, ra_stream_t stream)
+{
+    if (P < 1 || L < 1 || H < 1 || H_kv < 1) return RA_ERR_INVALID_ARG;
+    if (L % P != 0 || H % P != 0 || H_kv % P != 0) return RA_ERR_NOT_DIVISIBLE;
+    // a 128-row tile must come from one sequence shard
+    if ((L / P) % 128 != 0) return RA_ERR_UNSUPPORTED;
+    // q, k, v, out hold as many elements as [B, L, H(_kv), D]: the common checks apply
+    // with one ring shard
+    return attn_impl(q, k, v, out, lse, B, L, H, D, 1, causal, RA_BF16, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), H_kv, 0, nullptr, 0, P);
 }
 
 ra_status attn_merge_partials(const void* o_a, const float* lse_a, const void* o_b,

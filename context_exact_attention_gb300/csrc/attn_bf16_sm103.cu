@@ -95,6 +95,7 @@ struct Params {
     const int* cu_seqlens;   // packed sequences: starts of n_seqs sequences, then L
     int n_seqs;
     int group;       // query heads per key/value head
+    int u_B, u_H, u_Ls;  // Ulysses head groups (kMode 3): batch, heads, shard rows of the sources
     int n_kt;        // K/V blocks per shard
     int n_pair;      // query-tile pairs per shard
     float scale_log2;
@@ -312,7 +313,11 @@ struct VarlenSched {
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-// kMode: 0 contiguous shards, 1 zigzag shards, 2 packed sequences (contiguous shards).
+// kMode: 0 contiguous shards, 1 zigzag shards, 2 packed sequences (contiguous shards),
+// 3 Ulysses head groups read from and written to the sequence-sharded buffers (the
+// all-to-all of "序列并行与 Ring Attention" section 3.5 done by the tensor maps' addressing:
+// batch b of the kernel is head group g = b / u_B of batch b % u_B, its head h is source
+// head g*H + h, and position l sits in source shard l / u_Ls at row l % u_Ls).
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -340,6 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = bh / p.H;
     const int h = bh - b * p.H;
     const int hk = h / p.group;                       // key/value head of this query head
+    int bo = b, h_src = h, hk_src = hk;               // indices in the source tensors (kMode 3)
+    if constexpr (kMode == 3) {
+        const int g = b / p.u_B;
+        bo = b - g * p.u_B;
+        h_src = g * p.H + h;
+        hk_src = h_src / p.group;
+    }
     const int q0_local = pair * (kTiles * kRows);     // first query row of the pair, within shard
     const int q0 = r * p.Ls + q0_local;               // global
 
@@ -413,9 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
             mbar_arrive_expect_tx(bar(kBarQ), kTiles * Lay::kTileBytes);
             for (int tq = 0; tq < kTiles; ++tq)
-                for (int bx = 0; bx < Lay::kBoxes; ++bx)
-                    tma_load_4d(sbase + Lay::kQ + tq * Lay::kTileBytes + bx * 16384, &tmap_q,
-                                bar(kBarQ), bx * 64, h, q0 + tq * kRows, b, once);
+                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                    const uint32_t dst = sbase + Lay::kQ + tq * Lay::kTileBytes + bx * 16384;
+                    const int row = q0 + tq * kRows;
+                    if constexpr (kMode == 3)
+                        tma_load_5d(dst, &tmap_q, bar(kBarQ), bx * 64, h_src, row % p.u_Ls, bo,
+                                    row / p.u_Ls, once);
+                    else
+                        tma_load_4d(dst, &tmap_q, bar(kBarQ), bx * 64, h, row, b, once);
+                }
         }
         int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
         for (int n = 0; n < n_blocks; ++n) {
@@ -427,17 +445,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc))) break;
             if (leader) {
                 mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kTileBytes);
-                for (int bx = 0; bx < Lay::kBoxes; ++bx)
-                    tma_load_4d(sbase + Lay::kK + st * Lay::kTileBytes + bx * 16384, &tmap_k,
-                                bar(kBarKFull + st), bx * 64, hk, row, b, keep);
+                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                    const uint32_t dst = sbase + Lay::kK + st * Lay::kTileBytes + bx * 16384;
+                    if constexpr (kMode == 3)
+                        tma_load_5d(dst, &tmap_k, bar(kBarKFull + st), bx * 64, hk_src,
+                                    row % p.u_Ls, bo, row / p.u_Ls, keep);
+                    else
+                        tma_load_4d(dst, &tmap_k, bar(kBarKFull + st), bx * 64, hk, row, b, keep);
+                }
             }
             last_k[st] = n;
             if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc))) break;
             if (leader) {
                 mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kTileBytes);
-                for (int bx = 0; bx < Lay::kBoxes; ++bx)
-                    tma_load_4d(sbase + Lay::kV + st * Lay::kTileBytes + bx * 16384, &tmap_v,
-                                bar(kBarVFull + st), bx * 64, hk, row, b, keep);
+                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                    const uint32_t dst = sbase + Lay::kV + st * Lay::kTileBytes + bx * 16384;
+                    if constexpr (kMode == 3)
+                        tma_load_5d(dst, &tmap_v, bar(kBarVFull + st), bx * 64, hk_src,
+                                    row % p.u_Ls, bo, row / p.u_Ls, keep);
+                    else
+                        tma_load_4d(dst, &tmap_v, bar(kBarVFull + st), bx * 64, hk, row, b, keep);
+                }
             }
             last_v[st] = n;
         }
@@ -667,8 +695,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool valid = row_local < p.Ls;
             const float inv_l = l > 0.f ? 1.f / l : 0.f;        // a row that saw no key: 0
-            __nv_bfloat16* dst =
-                p.out + ((static_cast<size_t>(b) * p.L + row_glob) * p.H + h) * static_cast<size_t>(D);
+            // index of (row, head) among the output's rows of D elements
+            size_t orow = (static_cast<size_t>(b) * p.L + row_glob) * p.H + h;
+            if constexpr (kMode == 3) {
+                const int rs = row_glob / p.u_Ls;
+                orow = (static_cast<size_t>(rs * p.u_B + bo) * p.u_Ls + (row_glob - rs * p.u_Ls)) *
+                           p.u_H + h_src;
+            }
+            __nv_bfloat16* dst = p.out + orow * static_cast<size_t>(D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -684,9 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
             }
-            if (valid && p.lse != nullptr)
-                p.lse[(static_cast<size_t>(b) * p.L + row_glob) * p.H + h] =
-                    l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            if (valid && p.lse != nullptr) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
     }
 
@@ -729,6 +761,9 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     p.cu_seqlens = a.cu_seqlens;
     p.n_seqs = a.n_seqs;
     p.group = a.H / a.Hkv;
+    p.u_B = a.u_B;
+    p.u_H = a.u_H;
+    p.u_Ls = a.u_P > 0 ? a.L / a.u_P : 0;
     p.n_kt = (p.Ls + kKeys - 1) / kKeys;
     p.n_pair = (p.n_kt + kTiles - 1) / kTiles;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
@@ -744,7 +779,10 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
 cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv)
 {
-    if (a.cu_seqlens != nullptr) {
+    if (a.u_P > 0) {
+        if (a.D == 64) return launch_d<64, 3>(a, tq, tk, tv);
+        if (a.D == 128) return launch_d<128, 3>(a, tq, tk, tv);
+    } else if (a.cu_seqlens != nullptr) {
         if (a.D == 64) return launch_d<64, 2>(a, tq, tk, tv);
         if (a.D == 128) return launch_d<128, 2>(a, tq, tk, tv);
     } else if (a.zigzag) {

@@ -22,6 +22,10 @@ struct AttnArgs {
     int zigzag;                    // zigzag shard layout (causal)
     const int* cu_seqlens;         // packed sequences (device), or null
     int n_seqs;
+    // Ulysses head groups read from / written to the sequence-sharded buffers
+    // [u_P][u_B][L/u_P][u_H][D] (0 = not used): B = u_P * u_B head-group batches of
+    // H = u_H / u_P heads, ring P = 1; the tensor maps are then 5-D.
+    int u_P, u_B, u_H;
     unsigned int* status;          // device status word
     unsigned long long timeout_ns; // limit of one bounded wait
     cudaStream_t stream;

@@ -221,6 +221,30 @@ ra_status ulysses_head2seq(const void* in, void* out, int B, int L, int H, int D
                            int elem_bytes, ra_stream_t stream);
 
 /*
+ * ulysses_attention_fused -- the whole Ulysses step of "序列并行与 Ring Attention",
+ * section 3.5 (all-to-all to head shards, attention over the full sequence for each
+ * head group, all-to-all back) without materialising the head-sharded buffers: the
+ * attention kernel's tensor maps address the sequence-sharded inputs directly, so head
+ * group g's query tile of positions [l, l+128) is read from shard l / (L/P), rows
+ * l % (L/P), heads g*H/P .. (g+1)*H/P - 1, and each output row is written back to its
+ * sequence shard.  The result is bit-identical to ulysses_seq2head on q, k, v, then
+ * ring_attn_fwd_gqa(B' = P*B, H' = H/P, H_kv' = H_kv/P, P = 1), then ulysses_head2seq.
+ *
+ * q, out:   device bf16 sequence-sharded [P][B][L/P][H][D];
+ * k, v:     device bf16 [P][B][L/P][H_kv][D] (query head h reads key/value head
+ *           h / (H / H_kv), as ring_attn_fwd_gqa);
+ * lse:      device fp32 [P][B][L/P][H] or NULL;
+ * causal:   0 / 1 on the global position r*L/P + l.
+ * Requires L % P == 0, H % P == 0, H_kv % P == 0 (RA_ERR_NOT_DIVISIBLE), (L/P) % 128 == 0
+ * and D in {64, 128} (RA_ERR_UNSUPPORTED); alignment and overlap as ring_attn_fwd.
+ * (On several GPUs the all-to-all moves data between devices; with every shard in one
+ * HBM it reduces to the addressing above.)
+ */
+ra_status ulysses_attention_fused(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int B, int L, int H, int H_kv, int D, int P,
+                                  int causal, ra_stream_t stream);
+
+/*
  * ring_attn_bwd_workspace_bytes -- bytes of device workspace ring_attn_bwd needs
  * for a [B, L, H] problem (one fp32 per query row); 0 for invalid sizes.
  */

@@ -526,3 +526,58 @@ def test_ex_matches_the_specialised_entry_points():
     assert cea.check_status() == 0
     for a, b in pairs:
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ------------------------------------------------- fused Ulysses (one kernel) --
+
+FUSED_CASES = [
+    # P, B, L, H, H_kv, D
+    (4, 2, 512, 8, 8, 128),
+    (8, 1, 1024, 16, 8, 128),
+    (2, 1, 512, 4, 2, 64),
+    (3, 1, 1152, 6, 3, 128),      # odd number of 128-row tiles per head group
+]
+
+
+def _to_seq(t, P):
+    Ls = t.shape[1] // P
+    return torch.stack([t[:, r * Ls:(r + 1) * Ls] for r in range(P)]).contiguous()
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: "P%dB%dL%dH%dHkv%dD%d" % c)
+@pytest.mark.parametrize("causal", [False, True])
+def test_ulysses_fused_parity(case, causal):
+    """The fused step against the fp64 oracle on the global sequence (out and lse, shard by
+    shard), and bit for bit against the three-step path (transposes + attention + transpose)."""
+    P, B, L, H, Hkv, D = case
+    q, _, _ = make_qkv(B, L, H, D, seed=120, dtype=torch.bfloat16)
+    _, k, v = make_qkv(B, L, Hkv, D, seed=121, dtype=torch.bfloat16)
+    qs, ks, vs = _dev(_to_seq(q, P), _to_seq(k, P), _to_seq(v, P))
+    out, lse = cea.ulysses_attention_fused(qs, ks, vs, P, causal=causal, want_lse=True)
+    assert cea.check_status() == 0
+    ref, lref = oracle.attention(q, k, v, causal=causal)
+    glob = lambda a: np.concatenate([a[r] for r in range(P)], axis=1)
+    assert_bf16_close(glob(to_np(out)), ref, "out")
+    assert_bf16_close(glob(to_np(lse)), lref, "lse")
+    # the three-step path with the same attention kernel math
+    Hg, Hkg = H // P, Hkv // P
+    qh, kh, vh = (cea.ulysses_seq2head(t, P) for t in (qs, ks, vs))
+    oh, _ = cea.ring_attn_fwd_gqa(qh.view(P * B, L, Hg, D), kh.view(P * B, L, Hkg, D),
+                                  vh.view(P * B, L, Hkg, D), P=1, causal=causal)
+    three = cea.ulysses_head2seq(oh.view(P, B, L, Hg, D), P)
+    assert torch.equal(out, three)
+    if not causal and Hkv == H:
+        assert torch.equal(out, cea.ulysses_attention(qs, ks, vs, P))
+
+
+def test_ulysses_fused_argument_errors():
+    P, B, L, H, D = 4, 1, 256, 8, 128             # shards of 64 rows: a tile would straddle
+    qs, ks, vs = _dev(*(_to_seq(t, P) for t in make_qkv(B, L, H, D, seed=0, dtype=torch.bfloat16)))
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ulysses_attention_fused(qs, ks, vs, P)
+    assert e.value.code == 2
+    P, L, H = 4, 512, 6                           # 6 heads over 4 shards
+    qs, ks, vs = _dev(*(_to_seq(t, P) for t in make_qkv(B, L, H, D, seed=0, dtype=torch.bfloat16)))
+    with pytest.raises(cea.RingAttnError) as e:
+        cea.ulysses_attention_fused(qs, ks, vs, P)
+    assert e.value.code == 4
