@@ -61,8 +61,9 @@ def test_long_context_full_size():
 
 def test_ulysses_full_size():
     """B=2 L=8192 H=32 D=128 P=8: the three seq->head transposes are bit-exact against
-    the oracle, and the head->seq result of full attention per head group matches the
-    oracle's attention of the global tensors on 64 rows x 64 (batch, head) pairs."""
+    the oracle, the head->seq result of full attention per head group matches the
+    oracle's attention of the global tensors on 64 rows x 64 (batch, head) pairs, and the
+    fused one-kernel step gives the same bits."""
     w = ULYSSES
     q, k, v = make_workload_inputs(w, seed=0)
     Ls = w.L // w.P
@@ -79,6 +80,10 @@ def test_ulysses_full_size():
     assert_bf16_close(to_np(glob[:, rows]), ref, "ulysses out")
     back = cea.ulysses_head2seq(head, w.P)
     assert torch.equal(back.cpu(), qs)
+    # the fused step (transposes folded into the attention's addressing): the same bits
+    fused, _ = cea.ulysses_attention_fused(qs.to(DEV), ks.to(DEV), vs.to(DEV), w.P)
+    assert cea.check_status() == 0
+    assert torch.equal(fused, o_seq)
 
 
 def test_merge_causal_lm_size():
