@@ -314,3 +314,17 @@ def test_packed_backward_at_causal_lm_size():
                 scale = _dq_row_bound(qf, kf, vf, dof, i, h, slice(a, i + 1), w.D)
                 r = ref[0, ri, h]
                 assert (np.abs(dqn[i, h] - r) <= 2 * u * (np.abs(r) + scale) + 1e-6).all(), (i, h)
+
+
+def test_max_length_forward():
+    """L = 2^20 (one head, D = 128, P = 8 shards of 131072, causal): positions, tile
+    indices and row offsets far beyond the benchmark sizes in the kernels' index arithmetic;
+    sampled rows (shard edges included) against the oracle."""
+    B, L, H, D, P = 1, 1 << 20, 1, 128, 8
+    q, k, v = make_qkv(B, L, H, D, seed=7, dtype=torch.bfloat16)
+    out, lse = cea.ring_attn_fwd(*(t.to(DEV) for t in (q, k, v)), P=P, causal=True)
+    assert cea.check_status() == 0
+    rows = sample_rows(L, P, 48, seed=3)
+    ref, lref = oracle.attention(q, k, v, causal=True, rows=rows)
+    assert_bf16_close(to_np(out[:, rows]), ref, "out")
+    assert_bf16_close(to_np(lse[:, rows]), lref, "lse")
