@@ -17,15 +17,17 @@
 // (template parameter kMode; see "shard layouts" below): only the walk over tiles
 // and the visibility masks change.
 //
-// Kernels (384 threads: warp 0 TMA producer, warp 1 MMA issuer, in the dK/dV kernel
-// warps 2-3 the per-query statistics, warps 4-11 the elementwise step -- two warps per
-// TMEM lane quarter, warps 4-7 taking columns
-// [0,64) and warps 8-11 columns [64,128) of the same rows, each writing its bf16
-// results inside its own column range; warp-uniform schedules with one elected
-// lane issuing):
+// Kernels (warp 0 TMA producer, warp 1 MMA issuer; warp-uniform schedules with one
+// elected lane issuing).  dK/dV kernel, 640 threads: warps 2-3 the per-query statistics,
+// warps 4-19 the elementwise step, four warps per TMEM lane quarter each taking 32 of the
+// 128 query columns of its rows.  dQ kernel, 384 threads: warps 4-11 the elementwise step,
+// two warps per lane quarter taking 64 key columns each.  Each warp writes its bf16
+// results inside the fp32 columns it read; the MMA issuers address the bf16 operand
+// accordingly:
 //   bwd_rowdot_kernel   Dvec = rowsum(dO o O), fp32 workspace [B, L, H]
 //   bwd_dkdv_kernel<D, kMode>  TMEM: S^T [0,128), dP^T [128,256), dV, dK (D columns each)
-//       S^T = K Q^T, dP^T = V dO^T (SS); P^T, dS^T (bf16) written over them;
+//       S^T = K Q^T, dP^T = V dO^T (SS); P^T, dS^T (bf16) written over them, the pairs
+//       of query columns [16 k, 16 k + 16) in columns [16 k, 16 k + 8);
 //       dV += P^T dO, dK += dS^T Q (A from TMEM, B = dO / Q as MN-major SMEM).
 //       Tensor-pipe order per block: dV(n) S^T(n+1) dK(n) dP^T(n+1), so that
 //       P^T(n) is computed while dP^T(n) runs, dS^T(n) while dV(n) and S^T(n+1) run.
@@ -44,7 +46,7 @@ namespace ra {
 namespace {
 
 constexpr int kRows = 128;     // rows per tile (TMEM lanes), both queries and keys
-constexpr int kThreads = 384;   // warps 0-3: producer, MMA issuer, statistics (dK/dV); 4-11: elementwise
+constexpr int kThreads = 384;   // dQ kernel: warps 0-1 producer, MMA issuer; 4-11 elementwise
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -242,6 +244,11 @@ __global__ void __launch_bounds__(256)
 // ------------------------------------------------------------------ dK, dV --
 
 constexpr int kQStages = 3;          // Q is read last by dK, late in a block: three stages
+// dK/dV kernel: 20 warps -- 0 producer, 1 MMA issuer, 2-3 statistics, 4-19 elementwise, four
+// warps per TMEM lane quarter, each taking 32 of the 128 query columns of its rows
+constexpr int kKVParts = 4;
+constexpr int kKVCols = kRows / kKVParts;
+constexpr int kKVThreads = (4 + 4 * kKVParts) * 32;
 constexpr int kMaxSmem = 232448;     // opt-in shared memory limit of one block (227 KiB)
 
 enum : int {
@@ -276,7 +283,7 @@ struct KVSmem {
 };
 
 template <int D, int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKVThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
@@ -388,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(kKVSFull), 1);
         mbar_init(bar(kKVDPFull), 1);
-        mbar_init(bar(kKVPFull), 2 * kRows);
-        mbar_init(bar(kKVDSFull), 2 * kRows);
+        mbar_init(bar(kKVPFull), kKVParts * kRows);
+        mbar_init(bar(kKVDSFull), kKVParts * kRows);
         mbar_init(bar(kKVOFull), 1);
         mbar_init(bar(kKVDone), 1);
         *abort_flag = 0;
@@ -467,13 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_ss(tmem + dcol, a0 + off, b0 + off, kIdescS, k > 0 ? 1u : 0u);
             }
         };
-        // A operand in TMEM: query columns [64 h, 64 h + 64) as bf16 pairs sit in columns
-        // [acol + 64 h, acol + 64 h + 32)
+        // A operand in TMEM: the bf16 pairs of query columns [16 k, 16 k + 16) sit in
+        // columns [acol + 16 k, acol + 16 k + 8), inside the fp32 columns they replace
         auto ts = [&](uint32_t dcol, uint32_t acol, uint64_t b0, bool acc) {
 #pragma unroll
             for (int k = 0; k < kRows / 16; ++k)
-                mma_ts(tmem + dcol, tmem + acol + 64 * (k >> 2) + (k & 3) * 8,
-                       b0 + ((k * 2048) >> 4), kIdescAcc, (acc || k > 0) ? 1u : 0u);
+                mma_ts(tmem + dcol, tmem + acol + 16 * k, b0 + ((k * 2048) >> 4), kIdescAcc,
+                       (acc || k > 0) ? 1u : 0u);
         };
         auto wait_q = [&](int n) {
             return __all_sync(0xffffffffu,
@@ -588,11 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------------ elementwise
         const int quarter = warp & 3;
-        const int half = (warp - 4) >> 2;                 // query columns [64 half, 64 half + 64)
+        const int part = (warp - 4) >> 2;                 // query columns [32 part, 32 part + 32)
         const int row = quarter * 32 + lane;              // key row of the tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + 64 * half;        // S^T, then P^T
-        const uint32_t tP = tmem + lane_off + 128 + 64 * half;  // dP^T, then dS^T
+        const uint32_t tS = tmem + lane_off + kKVCols * part;        // S^T, then P^T
+        const uint32_t tP = tmem + lane_off + 128 + kKVCols * part;  // dP^T, then dS^T
         const int key_local = kt * kRows + row;           // within shard s
         const bool key_valid = key_local < p.Ls;
         const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
@@ -633,17 +640,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!key_valid) lo = kRows;
             const bool masked = __any_sync(0xffffffffu, lo > 0 || hi < kRows - 1);
-            const float* nl2 = stats_nlse2(n % kQStages) + 64 * half;
-            const float* ndv = stats_ndvec(st) + 64 * half;
-            // P^T = exp2(S^T scale log2(e) - lse log2(e)); kept in fp32 for dS^T.  One TMEM
-            // load and one store for the warp's 64 columns (fewer dependent round trips).
-            uint64_t pp[32];
+            const float* nl2 = stats_nlse2(n % kQStages) + kKVCols * part;
+            const float* ndv = stats_ndvec(st) + kKVCols * part;
+            // P^T = exp2(S^T scale log2(e) - lse log2(e)); kept in fp32 for dS^T.  The bf16
+            // pairs of the warp's two 16-query chunks go to the first 8 of each chunk's 16
+            // fp32 columns (the layout the MMA issuer reads them in).
+            uint64_t pp[16];
             {
-                uint32_t sr[64];
-                tmem_ld64(tS, sr);
-                uint32_t pk[32];
+                uint32_t sr[32];
+                tmem_ld32(tS, sr);
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     const ulonglong2 nl = *reinterpret_cast<const ulonglong2*>(nl2 + 4 * i);
                     const uint64_t x0 = ffma2(f2pack(u2f(sr[4 * i]), u2f(sr[4 * i + 1])), sl2, nl.x);
                     const uint64_t x1 = ffma2(f2pack(u2f(sr[4 * i + 2]), u2f(sr[4 * i + 3])), sl2, nl.y);
@@ -654,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (masked) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const int c = 64 * half + 4 * i + j;
+                            const int c = kKVCols * part + 4 * i + j;
                             e[j] = (c >= lo && c <= hi) ? e[j] : 0.f;
                         }
                     }
@@ -663,8 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[2 * i] = pack_bf16x2(e[0], e[1]);
                     pk[2 * i + 1] = pack_bf16x2(e[2], e[3]);
                 }
-                // 64 query columns as bf16 pairs: 32 columns, inside the ones just read
-                tmem_st32(tS, pk);
+                tmem_st8x2(tS, tS + 16, pk);
             }
             tc_fence_before();
             mbar_arrive(bar(kKVPFull));
@@ -674,11 +681,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = __all_sync(0xffffffffu, ok))) break;
             tc_fence_after();
             {
-                uint32_t dr[64];
-                tmem_ld64(tP, dr);
-                uint32_t pk[32];
+                uint32_t dr[32];
+                tmem_ld32(tP, dr);
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     const ulonglong2 nd = *reinterpret_cast<const ulonglong2*>(ndv + 4 * i);
                     const uint64_t d0 = fadd2(f2pack(u2f(dr[4 * i]), u2f(dr[4 * i + 1])), nd.x);
                     const uint64_t d1 = fadd2(f2pack(u2f(dr[4 * i + 2]), u2f(dr[4 * i + 3])), nd.y);
@@ -688,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[2 * i] = pack_bf16x2(g0, g1);
                     pk[2 * i + 1] = pack_bf16x2(g2, g3);
                 }
-                tmem_st32(tP, pk);
+                tmem_st8x2(tP, tP + 16, pk);
             }
             tc_fence_before();
             mbar_arrive(bar(kKVDSFull));
@@ -698,13 +705,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             tc_fence_after();
-            // half 0 writes dV, half 1 writes dK
-            const size_t base = ((static_cast<size_t>(b) * p.L + key0 + row) * p.Hkv + hk) * D;
-            const uint32_t tA = tmem + lane_off + 256 + half * D;
-            const float mul = half ? p.scale : 1.f;
-            __nv_bfloat16* dst = (half ? p.dk : p.dv) + base;
+            // parts 0-1 write the two column halves of dV, parts 2-3 those of dK
+            const int which = part >> 1;
+            const int col0 = (part & 1) * (D / 2);
+            const size_t base = ((static_cast<size_t>(b) * p.L + key0 + row) * p.Hkv + hk) * D + col0;
+            const uint32_t tA = tmem + lane_off + 256 + which * D + col0;
+            const float mul = which ? p.scale : 1.f;
+            __nv_bfloat16* dst = (which ? p.dk : p.dv) + base;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tA + 32 * c, o);
                 uint32_t pk[16];
@@ -1165,7 +1174,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     const long long grid_kv = static_cast<long long>(a.B) * a.Hkv * a.P * p.n_t;
     const long long grid = static_cast<long long>(a.B) * a.H * a.P * p.n_t;
     if (grid <= 0 || grid > 0x7fffffffLL || grid_kv <= 0) return cudaErrorInvalidConfiguration;
-    bwd_dkdv_kernel<D, kMode><<<static_cast<unsigned>(grid_kv), kThreads, kSmemKV, a.stream>>>(
+    bwd_dkdv_kernel<D, kMode><<<static_cast<unsigned>(grid_kv), kKVThreads, kSmemKV, a.stream>>>(
         tq, tk, tv, tdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
