@@ -190,6 +190,22 @@ struct PosWalk {
     }
 };
 
+// The g-th 128-row tile in global position order of the zigzag layout (2P chunks of n_t/2
+// tiles; chunk j < P is the first half of shard j, chunk j >= P the second half of shard
+// 2P-1-j): its shard and its tile within the shard.
+__device__ __forceinline__ void zigzag_tile_at(int g, int P, int n_t, int& shard, int& tile)
+{
+    const int per_chunk = n_t >> 1;
+    const int chunk = g / per_chunk, within = g - chunk * per_chunk;
+    if (chunk < P) {
+        shard = chunk;
+        tile = within;
+    } else {
+        shard = 2 * P - 1 - chunk;
+        tile = per_chunk + within;
+    }
+}
+
 // Zero rows [row0, row0 + n) of a [B, L, heads, D] bf16 tensor's head `head` (gradients of
 // a tile that no pair reaches: possible only with malformed sequence boundaries).
 template <int D>
@@ -250,6 +266,10 @@ constexpr int kKVParts = 4;
 constexpr int kKVCols = kRows / kKVParts;
 constexpr int kKVThreads = (4 + 4 * kKVParts) * 32;
 constexpr int kMaxSmem = 232448;     // opt-in shared memory limit of one block (227 KiB)
+// Byte offset, within the 256-byte barrier area of either kernel, of the per-stage tile
+// records (int2: layout position of the tile's first row, number of valid rows) that the
+// loading warps publish with each stage, so the elementwise warps need no schedule walk.
+constexpr int kInfoOff = 160;
 
 enum : int {
     kKVFull = 0,
@@ -279,7 +299,7 @@ struct KVSmem {
     static constexpr int kNeed = kBar + 256;
     static constexpr int kAlloc = kNeed + 1023 < kMaxSmem ? kNeed + 1023 : kMaxSmem;
     static_assert(kNeed <= kMaxSmem, "dK/dV shared memory layout exceeds the limit");
-    static_assert(kKVBars * 8 + 8 <= 256, "barrier area");
+    static_assert(kKVBars * 8 + 8 <= kInfoOff && kInfoOff + 8 * kQStages <= 256, "barrier area");
 };
 
 template <int D, int kMode>
@@ -305,6 +325,8 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     const uint32_t sbase = smem_addr(smem);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBar + kKVBars * 8);
     int* abort_flag = reinterpret_cast<int*>(smem + kBar + kKVBars * 8 + 4);
+    // per Q stage: first query position and valid query rows (written by warp 2)
+    int2* qinfo = reinterpret_cast<int2*>(smem + kBar + kInfoOff);
     auto bar = [&](int i) -> uint32_t { return sbase + kBar + 8u * i; };
     // per-query statistics, negated for the packed adds: -lse log2(e) with the Q stage,
     // -Dvec with the dO stage
@@ -321,8 +343,13 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     const int units_per_bh = p.P * p.n_t;
     int bh, u;
     unit_of_block(blockIdx.x, p.B * p.Hkv, units_per_bh, bh, u);
-    const int s = u / p.n_t;          // shard owning these keys
-    const int kt = u - s * p.n_t;     // key tile within the shard
+    int s = u / p.n_t;                // shard owning these keys
+    int kt = u - s * p.n_t;           // key tile within the shard
+    if constexpr (kMode == 1) {
+        // zigzag: a key tile's work falls with its global position (it meets every later
+        // query), so heaviest first is position order: unit u is the u-th tile by position
+        zigzag_tile_at(u, p.P, p.n_t, s, kt);
+    }
     const int b = bh / p.Hkv;
     const int hk = bh - b * p.Hkv;
     const int key0 = s * p.Ls + kt * kRows;
@@ -555,7 +582,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         const bool is_lse = warp == 2;
         const float* src = is_lse ? p.lse : p.dvec;
         const float mul = is_lse ? -kLog2e : -1.f;
-        auto fetch = [&](int n, float (&v)[4]) {
+        auto fetch = [&](int n, float (&v)[4], int2& info) {
             int r, qt, h;
             block(n, r, qt, h);
             const int qrow = r * p.Ls + qt * kRows;
@@ -565,12 +592,16 @@ __global__ void __launch_bounds__(kKVThreads, 1)
                 const size_t idx = (static_cast<size_t>(b) * p.L + qrow + c) * p.H + h;
                 v[j] = (qt * kRows + c < p.Ls) ? src[idx] * mul : 0.f;
             }
+            info = make_int2(layout_position(r, qt * kRows, p.Ls, p.P, kZig),
+                             min(kRows, p.Ls - qt * kRows));
         };
         float v[4];
-        fetch(0, v);
+        int2 info;
+        fetch(0, v, info);
         for (int n = 0; n < n_blocks; ++n) {
             float nxt[4] = {0.f, 0.f, 0.f, 0.f};
-            if (n + 1 < n_blocks) fetch(n + 1, nxt);
+            int2 nxt_info = info;
+            if (n + 1 < n_blocks) fetch(n + 1, nxt, nxt_info);
             float* dst;
             uint32_t full;
             bool ok;
@@ -588,9 +619,11 @@ __global__ void __launch_bounds__(kKVThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
 #pragma unroll
             for (int j = 0; j < 4; ++j) dst[lane + 32 * j] = v[j];
+            if (is_lse && lane == 0) qinfo[n % kQStages] = info;
             mbar_arrive(full);
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = nxt[j];
+            info = nxt_info;
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------ elementwise
@@ -603,41 +636,31 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         const int key_local = kt * kRows + row;           // within shard s
         const bool key_valid = key_local < p.Ls;
         const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
-        // modes 1 and 2: the positions of the queries that see this key, [vis_lo, vis_hi]
+        // the positions of the queries that see this key, [vis_lo, vis_hi]
         int vis_lo = 0, vis_hi = kFar;
-        if constexpr (kMode != 0) {
-            if (key_valid) {
-                const int kp = layout_position(s, key_local, p.Ls, p.P, kZig);
-                vis_lo = kp;
-                if constexpr (kMode == 2) {
-                    int f, l;
-                    seq_range(p.cu_seqlens, p.n_seqs, kp, f, l);
-                    if (!p.causal) vis_lo = f;
-                    vis_hi = l;
-                }
+        if (key_valid) {
+            const int kp = layout_position(s, key_local, p.Ls, p.P, kZig);
+            if (p.causal || kZig) vis_lo = kp;
+            if constexpr (kMode == 2) {
+                int f, l;
+                seq_range(p.cu_seqlens, p.n_seqs, kp, f, l);
+                if (!p.causal) vis_lo = f;
+                vis_hi = l;
             }
         }
         bool ok = true;
         for (int n = 0; n < n_blocks; ++n) {
-            int r, qt, h;
-            block(n, r, qt, h);
             const int st = n & 1;
             ok = mbar_wait(bar(kKVSFull), n & 1, wc);
             ok = ok && mbar_wait(bar(kQFull + n % kQStages), (n / kQStages) & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            // visible query columns [lo, hi] of this tile for this key row
-            int hi = min(kRows - 1, p.Ls - qt * kRows - 1);
-            int lo = 0;
-            if constexpr (kMode == 0) {
-                if (p.causal && r == s) lo = max(0, key_local - qt * kRows);
-            } else {
-                // a query tile holds consecutive positions in every layout
-                const int qp0 = layout_position(r, qt * kRows, p.Ls, p.P, kZig);
-                lo = max(0, vis_lo - qp0);
-                hi = min(hi, vis_hi - qp0);
-            }
+            // visible query columns [lo, hi] of this tile for this key row (a query tile
+            // holds consecutive positions in every layout)
+            const int2 qi = qinfo[n % kQStages];
+            int lo = max(0, vis_lo - qi.x);
+            const int hi = min(qi.y - 1, vis_hi - qi.x);
             if (!key_valid) lo = kRows;
             const bool masked = __any_sync(0xffffffffu, lo > 0 || hi < kRows - 1);
             const float* nl2 = stats_nlse2(n % kQStages) + kKVCols * part;
@@ -770,6 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_addr(smem);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBar + kDBars * 8);
     int* abort_flag = reinterpret_cast<int*>(smem + kBar + kDBars * 8 + 4);
+    // per K stage: first key position and valid key rows (written by the producer)
+    int2* kinfo = reinterpret_cast<int2*>(smem + kBar + kInfoOff);
+    static_assert(kDBars * 8 + 8 <= kInfoOff && kInfoOff + 8 * kKStages <= 256, "barrier area");
     auto bar = [&](int i) -> uint32_t { return sbase + kBar + 8u * i; };
 
     const int warp = threadIdx.x >> 5;
@@ -780,8 +806,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int units_per_bh = p.P * p.n_t;
     int bh, u;
     unit_of_block(blockIdx.x, p.B * p.H, units_per_bh, bh, u);
-    const int r = p.P - 1 - u / p.n_t;
-    const int qt = p.n_t - 1 - (u - (u / p.n_t) * p.n_t);
+    int r = p.P - 1 - u / p.n_t;
+    int qt = p.n_t - 1 - (u - (u / p.n_t) * p.n_t);
+    if constexpr (kMode == 1) {
+        // zigzag: a query tile's work grows with its global position, so heaviest first
+        // is descending position order
+        zigzag_tile_at(p.P * p.n_t - 1 - u, p.P, p.n_t, r, qt);
+    }
     const int b = bh / p.H;
     const int h = bh - b * p.H;
     const int hk = h / p.group;                       // key/value head of this query head
@@ -895,6 +926,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = s * p.Ls + kt * kRows;
             if (!__all_sync(0xffffffffu, mbar_wait(bar(kDKEmpty + kst), kph ^ 1, wc))) break;
             if (leader) {
+                kinfo[kst] = make_int2(layout_position(s, kt * kRows, p.Ls, p.P, kZig),
+                                       min(kRows, p.Ls - kt * kRows));
                 mbar_arrive_expect_tx(bar(kDKFull + kst), T);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx)
                     tma_load_4d(sbase + kK + kst * T + bx * 16384, &tmap_k, bar(kDKFull + kst),
@@ -1013,37 +1046,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t ndvx2 = f2pack(ndv, ndv);
         const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
         const uint32_t tP = tmem + lane_off + 256 + 64 * half;                  // dP
-        // modes 1 and 2: the positions of the keys this query sees, [vis_lo, vis_hi]
+        // the positions of the keys this query sees, [vis_lo, vis_hi]
         int vis_lo = 0, vis_hi = kFar;
-        if constexpr (kMode != 0) {
-            if (row_valid) {
-                const int qp = layout_position(r, row_local, p.Ls, p.P, kZig);
-                vis_hi = qp;
-                if constexpr (kMode == 2) {
-                    int f, l;
-                    seq_range(p.cu_seqlens, p.n_seqs, qp, f, l);
-                    vis_lo = f;
-                    if (!p.causal) vis_hi = l;
-                }
+        if (row_valid) {
+            const int qp = layout_position(r, row_local, p.Ls, p.P, kZig);
+            if (p.causal || kZig) vis_hi = qp;
+            if constexpr (kMode == 2) {
+                int f, l;
+                seq_range(p.cu_seqlens, p.n_seqs, qp, f, l);
+                vis_lo = f;
+                if (!p.causal) vis_hi = l;
             }
         }
         bool ok = true;
         for (int n = 0; n < n_blocks; ++n) {
-            int s, kt;
-            block(n, s, kt);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kDSFull + (n & 1)), (n >> 1) & 1, wc));
+            // S(n), and the K stage of block n for its record: that stage is refilled
+            // only after dQ(n), which waits for this warp's dS(n)
+            ok = __all_sync(0xffffffffu, mbar_wait2(bar(kDSFull + (n & 1)), (n >> 1) & 1,
+                                                    bar(kDKFull + n % kKStages), (n / kKStages) & 1, wc));
             if (!ok) break;
             tc_fence_after();
-            int lim = min(kRows - 1, p.Ls - kt * kRows - 1);
-            int lo = 0;
-            if constexpr (kMode == 0) {
-                if (p.causal && s == r) lim = min(lim, row_local - kt * kRows);
-            } else {
-                // a K/V tile holds consecutive positions in every layout
-                const int kp0 = layout_position(s, kt * kRows, p.Ls, p.P, kZig);
-                lim = min(lim, vis_hi - kp0);
-                lo = vis_lo - kp0;
-            }
+            // visible key columns [lo, lim] (a K/V tile holds consecutive positions in
+            // every layout)
+            const int2 ki = kinfo[n % kKStages];
+            int lim = min(ki.y - 1, vis_hi - ki.x);
+            const int lo = vis_lo - ki.x;
             if (!row_valid) lim = -1;
             const bool masked = __any_sync(0xffffffffu, lim < kRows - 1 || lo > 0);
             const uint32_t tS = tmem + lane_off + 128u * (n & 1) + 64 * half;  // S, then dS
