@@ -466,14 +466,19 @@ def measure_rows(cea, dev, stream, peaks):
                for _ in range(3))
     out = torch.empty_like(q)
     lse = torch.empty((w.L, w.H), dtype=torch.float32, device=dev)
-    f = lambda: cea.ring_attn_fwd_varlen(q, k, v, cu_d, P=w.P, causal=True, out=out, lse=lse,
-                                         stream=stream)
+
+    def f():
+        # the heaviest-first unit order is computed from cu_seqlens inside every step
+        sched = cea.varlen_schedule(cu_d, w.L, w.P, True, stream=stream)
+        cea.ring_attn_fwd_varlen(q, k, v, cu_d, P=w.P, causal=True, out=out, lse=lse,
+                                 stream=stream, schedule=sched)
     f()
     ms = _time_loop(f, 5, stream) / 5
     fl = sum(attention_flops(1, n, w.H, w.D, True) for n in lengths)
     res["lm_varlen_causal"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                                "frac": fl / (ms * 1e-3) / 1e12 / peak, "n_seqs": len(lengths),
-                               "note": "lengths U[256, 8192) packed to 32768 tokens, 32 heads"}
+                               "note": "lengths U[256, 8192) packed to 32768 tokens, 32 heads; "
+                                       "schedule computed in each step"}
     del q, k, v, out, lse
 
     # backward of the headline workload (dq, dk, dv): algorithmic FLOPs are 2.5x the
@@ -534,14 +539,17 @@ def measure_rows(cea, dev, stream, peaks):
     out, lse = cea.ring_attn_fwd_varlen(q, k, v, cu_d, P=w.P, causal=True)
     ws = torch.empty(w.L * w.H, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    f = lambda: cea.ring_attn_bwd_varlen(q, k, v, out, lse, do, cu_d, P=w.P, causal=True, dq=dq,
-                                         dk=dk, dv=dv, workspace=ws, stream=stream)
+    def f():
+        sched = cea.varlen_schedule(cu_d, w.L, w.P, True, stream=stream)
+        cea.ring_attn_bwd_varlen(q, k, v, out, lse, do, cu_d, P=w.P, causal=True, dq=dq, dk=dk,
+                                 dv=dv, workspace=ws, stream=stream, schedule=sched)
     f()
     ms = _time_loop(f, 5, stream) / 5
     fl = 2.5 * sum(attention_flops(1, n, w.H, w.D, True) for n in lengths)
     res["lm_varlen_backward"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                                  "frac": fl / (ms * 1e-3) / 1e12 / peak, "n_seqs": len(lengths),
-                                 "note": "packed sequences of the forward row; 2.5x forward FLOPs"}
+                                 "note": "packed sequences of the forward row; 2.5x forward "
+                                         "FLOPs; schedule computed in each step"}
     del q, k, v, do, out, lse, ws, dq, dk, dv, cu_d
 
     # long-context causal

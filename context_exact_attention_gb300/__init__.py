@@ -25,7 +25,7 @@ __all__ = [
     "zigzag_positions", "ring_attn_fwd_varlen", "varlen_padded_length", "check_status",
     "probe_wait_timeout", "ring_attn_fwd_host", "host_workspace_bytes", "ring_attn_bwd_gqa",
     "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "ring_attn_fwd_ex", "ring_attn_bwd_ex",
-    "ulysses_attention_fused", "EXPORTED_SYMBOLS",
+    "ulysses_attention_fused", "varlen_schedule", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -44,7 +44,8 @@ EXPORTED_SYMBOLS = (
     "ring_attn_bwd_noalloc", "ring_attn_fwd_gqa", "ring_attn_fwd_zigzag",
     "ring_attn_fwd_varlen", "ring_attn_fwd_host", "ring_attn_fwd_host_workspace_bytes",
     "ring_attn_bwd_gqa", "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "ring_attn_fwd_ex",
-    "ring_attn_bwd_ex", "ulysses_attention_fused",
+    "ring_attn_bwd_ex", "ulysses_attention_fused", "ring_attn_varlen_schedule",
+    "ring_attn_varlen_schedule_bytes",
 )
 
 
@@ -57,7 +58,7 @@ class AttnDesc(ctypes.Structure):
                 ("H_kv", ctypes.c_int), ("D", ctypes.c_int), ("P", ctypes.c_int),
                 ("causal", ctypes.c_int), ("layout", ctypes.c_int),
                 ("cu_seqlens", ctypes.c_void_p), ("n_seqs", ctypes.c_int),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("schedule", ctypes.c_void_p)]
 
 
 class RingAttnError(RuntimeError):
@@ -112,6 +113,7 @@ def load_library(build_if_missing: bool = False):
             "ring_attn_fwd_varlen": [vp, vp, vp, vp, f_p, vp, i, i, i, i, i, i, i, vp, vp],
             "ring_attn_fwd_host": [vp, vp, vp, vp, f_p, vp, ctypes.c_ulonglong, i, i, i, i, i, i,
                                    i, vp],
+            "ring_attn_varlen_schedule": [vp, i, i, i, i, vp, ctypes.c_ulonglong, vp],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -121,6 +123,8 @@ def load_library(build_if_missing: bool = False):
         lib.ring_attn_fwd_host_workspace_bytes.restype = ctypes.c_ulonglong
         lib.ring_attn_bwd_workspace_bytes.argtypes = [i, i, i]
         lib.ring_attn_bwd_workspace_bytes.restype = ctypes.c_ulonglong
+        lib.ring_attn_varlen_schedule_bytes.argtypes = [i, i]
+        lib.ring_attn_varlen_schedule_bytes.restype = ctypes.c_ulonglong
         lib.ra_status_string.argtypes = [ctypes.c_int]
         lib.ra_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -295,10 +299,17 @@ def varlen_padded_length(total: int, P: int, multiple: int = 1) -> int:
 
 
 def ring_attn_fwd_varlen(q, k, v, cu_seqlens, P: int = 1, causal: bool = False, out=None,
-                         lse=None, want_lse: bool = True, trace: bool = False, stream=None):
+                         lse=None, want_lse: bool = True, trace: bool = False, stream=None,
+                         schedule=None):
     """Ring attention over packed sequences.  q, k, v: [L, H, D] (bf16 or fp32);
-    cu_seqlens: int32 CUDA tensor [n_seqs + 1] of sequence starts ending with L.
-    Returns (out, lse) or (out, lse, trace)."""
+    cu_seqlens: int32 CUDA tensor [n_seqs + 1] of sequence starts ending with L;
+    schedule: None, or varlen_schedule(cu_seqlens, L, P, causal) (same results, heaviest
+    work units first; passed through ring_attn_fwd_ex).  Returns (out, lse) or
+    (out, lse, trace)."""
+    if schedule is not None:
+        return ring_attn_fwd_ex(q, k, v, P=P, causal=causal, layout="packed",
+                                cu_seqlens=cu_seqlens, out=out, lse=lse, want_lse=want_lse,
+                                trace=trace, stream=stream, schedule=schedule)
     dtype = q.dtype
     if dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("q must be bf16 or fp32")
@@ -511,9 +522,14 @@ def ring_attn_bwd_zigzag(q, k, v, out, lse, dout, P: int = 1, dq=None, dk=None, 
 
 
 def ring_attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, P: int = 1, causal: bool = False,
-                         dq=None, dk=None, dv=None, workspace=None, stream=None):
+                         dq=None, dk=None, dv=None, workspace=None, stream=None, schedule=None):
     """Gradients of ring_attn_fwd_varlen (bf16): q, k, v, out, dout [L, H, D], lse [L, H],
-    cu_seqlens the forward's int32 CUDA tensor.  Returns (dq, dk, dv), each [L, H, D]."""
+    cu_seqlens the forward's int32 CUDA tensor; schedule as ring_attn_fwd_varlen.
+    Returns (dq, dk, dv), each [L, H, D]."""
+    if schedule is not None:
+        return ring_attn_bwd_ex(q, k, v, out, lse, dout, P=P, causal=causal, layout="packed",
+                                cu_seqlens=cu_seqlens, dq=dq, dk=dk, dv=dv, workspace=workspace,
+                                stream=stream, schedule=schedule)
     if q.dim() != 3:
         raise ValueError("packed q, k, v are [L, H, D]")
     _check_qkv(q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), torch.bfloat16)
@@ -529,11 +545,16 @@ def ring_attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, P: int = 1, causal
     return dq, dk, dv
 
 
-def _desc(q, k, P, causal, layout, cu_seqlens):
+def _desc(q, k, P, causal, layout, cu_seqlens, schedule=None):
     """Descriptor and the [B, L, H, D] view of q for ring_attn_fwd_ex / ring_attn_bwd_ex."""
     if layout not in LAYOUTS:
         raise ValueError(f"layout must be one of {sorted(LAYOUTS)}")
     packed = layout == "packed"
+    if schedule is not None:
+        if not packed:
+            raise ValueError("schedule belongs to the packed layout only")
+        if schedule.dtype != torch.int32 or not schedule.is_cuda or not schedule.is_contiguous():
+            raise ValueError("schedule must be the int32 CUDA tensor varlen_schedule returns")
     if packed:
         if q.dim() != 3 or k.dim() != 3:
             raise ValueError("packed q, k, v are [L, H, D] / [L, H_kv, D]")
@@ -548,13 +569,35 @@ def _desc(q, k, P, causal, layout, cu_seqlens):
     d = AttnDesc(B=B, L=L, H=H, H_kv=k.shape[-2], D=D, P=P, causal=int(bool(causal)),
                  layout=LAYOUTS[layout], cu_seqlens=cu_seqlens.data_ptr() if packed else None,
                  n_seqs=cu_seqlens.numel() - 1 if packed else 0,
-                 dtype=RA_BF16 if q.dtype == torch.bfloat16 else RA_F32)
+                 dtype=RA_BF16 if q.dtype == torch.bfloat16 else RA_F32,
+                 schedule=schedule.data_ptr() if schedule is not None else None)
+    if schedule is not None and schedule.numel() * 4 < _schedule_bytes(L, P):
+        raise ValueError("schedule is too short for this L and P")
     return d, (B, L, H, D)
+
+
+def _schedule_bytes(L: int, P: int) -> int:
+    return int(load_library().ring_attn_varlen_schedule_bytes(L, P))
+
+
+def varlen_schedule(cu_seqlens, L: int, P: int = 1, causal: bool = False, stream=None):
+    """Heaviest-first unit orders for the packed layout (ring_attn_varlen_schedule): an
+    int32 CUDA tensor to pass as schedule= to the packed forward and backward with the
+    same cu_seqlens, L and P.  Written asynchronously on `stream`."""
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    nbytes = _schedule_bytes(L, P)
+    if nbytes == 0:
+        raise ValueError("L and P must be positive with L % P == 0")
+    sched = torch.empty(nbytes // 4, dtype=torch.int32, device=cu_seqlens.device)
+    _call("ring_attn_varlen_schedule", _ptr(cu_seqlens), cu_seqlens.numel() - 1, L, P,
+          int(bool(causal)), _ptr(sched), nbytes, _stream(stream))
+    return sched
 
 
 def ring_attn_fwd_ex(q, k, v, P: int = 1, causal: bool = False, layout: str = "contiguous",
                      cu_seqlens=None, out=None, lse=None, want_lse: bool = True,
-                     trace: bool = False, stream=None):
+                     trace: bool = False, stream=None, schedule=None):
     """The forward for any combination of options: grouped key/value heads (k, v with
     fewer heads than q) with the contiguous, zigzag or packed layout.  q, k, v: [B, L, H, D]
     / [B, L, H_kv, D], or [L, H, D] / [L, H_kv, D] for layout="packed" (with cu_seqlens).
@@ -562,7 +605,7 @@ def ring_attn_fwd_ex(q, k, v, P: int = 1, causal: bool = False, layout: str = "c
     dtype = q.dtype
     if dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("q must be bf16 or fp32")
-    d, (B, L, H, D) = _desc(q, k, P, causal, layout, cu_seqlens)
+    d, (B, L, H, D) = _desc(q, k, P, causal, layout, cu_seqlens, schedule)
     view = (lambda t: t.unsqueeze(0)) if layout == "packed" else (lambda t: t)
     _check_qkv(view(q), view(k), view(v), dtype, grouped=True)
     if out is None:
@@ -577,10 +620,10 @@ def ring_attn_fwd_ex(q, k, v, P: int = 1, causal: bool = False, layout: str = "c
 
 def ring_attn_bwd_ex(q, k, v, out, lse, dout, P: int = 1, causal: bool = False,
                      layout: str = "contiguous", cu_seqlens=None, dq=None, dk=None, dv=None,
-                     workspace=None, stream=None):
+                     workspace=None, stream=None, schedule=None):
     """Gradients of ring_attn_fwd_ex (bf16) for the same options: returns (dq, dk, dv),
     dq shaped like q and dk, dv like k (summed over each key/value head's query heads)."""
-    d, (B, L, H, D) = _desc(q, k, P, causal, layout, cu_seqlens)
+    d, (B, L, H, D) = _desc(q, k, P, causal, layout, cu_seqlens, schedule)
     view = (lambda t: t.unsqueeze(0)) if layout == "packed" else (lambda t: t)
     _check_qkv(view(q), view(k), view(v), torch.bfloat16, grouped=True)
     dq, dk, dv, workspace = _bwd_outputs(q, k, v, out, lse, dout, tuple(q.shape[:-1]), dq, dk,

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libringattn.so")
 SOURCES = ["api.cu", "attn_bf16_sm103.cu", "attn_bwd_sm103.cu", "attn_f32.cu", "merge.cu",
-           "ulysses.cu", "host_pipeline.cu", "bwd_noalloc.cu"]
+           "ulysses.cu", "host_pipeline.cu", "bwd_noalloc.cu", "varlen_schedule.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -139,7 +139,8 @@ ra_status check_attn(const void* q, const void* k, const void* v, const void* ou
 ra_status attn_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                     int L, int H, int D, int P, int causal, ra_dtype dtype, int* trace,
                     cudaStream_t stream, int Hkv = -1, int zigzag = 0,
-                    const int* cu_seqlens = nullptr, int n_seqs = 0, int ulysses_P = 0)
+                    const int* cu_seqlens = nullptr, int n_seqs = 0, int ulysses_P = 0,
+                    const int* schedule = nullptr)
 {
     if (Hkv < 0) Hkv = H;
     if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_UNSUPPORTED;
@@ -147,6 +148,12 @@ ra_status attn_impl(const void* q, const void* k, const void* v, void* out, floa
     unsigned long long n = 0;
     ra_status st = check_attn(q, k, v, out, lse, B, L, H, D, P, elem, &n, Hkv);
     if (st != RA_OK) return st;
+    if (schedule) {
+        const unsigned long long sb = ring_attn_varlen_schedule_bytes(L, P);
+        if (overlap(schedule, sb, out, n * elem) ||
+            (lse && overlap(schedule, sb, lse, static_cast<unsigned long long>(B) * L * H * 4)))
+            return RA_ERR_INVALID_ARG;
+    }
     if (dtype == RA_BF16 && D != 64 && D != 128) return RA_ERR_UNSUPPORTED;
     if (dtype == RA_F32 && (D % 4 != 0 || D > 256)) return RA_ERR_UNSUPPORTED;
     if (trace) {
@@ -171,6 +178,7 @@ ra_status attn_impl(const void* q, const void* k, const void* v, void* out, floa
     a.zigzag = zigzag;
     a.cu_seqlens = cu_seqlens;
     a.n_seqs = n_seqs;
+    a.schedule = schedule;
     a.u_P = 0;
     a.u_B = 0;
     a.u_H = 0;
@@ -377,7 +385,7 @@ ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
                    const void* dout, void* dq, void* dk, void* dv, void* workspace,
                    unsigned long long workspace_bytes, int B, int L, int H, int Hkv, int D, int P,
                    int causal, ra_stream_t stream, int zigzag = 0, const int* cu_seqlens = nullptr,
-                   int n_seqs = 0)
+                   int n_seqs = 0, const int* schedule = nullptr)
 {
     unsigned long long n = 0;
     ra_status st = check_attn(q, k, v, out, lse, B, L, H, D, P, 2, &n, Hkv);
@@ -400,6 +408,9 @@ ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
             if (overlap(outs[i], out_bytes[i], ins[j], in_bytes[j])) return RA_ERR_INVALID_ARG;
         for (int j = i + 1; j < 4; ++j)
             if (overlap(outs[i], out_bytes[i], outs[j], out_bytes[j])) return RA_ERR_INVALID_ARG;
+        if (schedule &&
+            overlap(outs[i], out_bytes[i], schedule, ring_attn_varlen_schedule_bytes(L, P)))
+            return RA_ERR_INVALID_ARG;
     }
     ra::BwdArgs a;
     a.out = out;
@@ -419,6 +430,7 @@ ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     a.zigzag = zigzag;
     a.cu_seqlens = cu_seqlens;
     a.n_seqs = n_seqs;
+    a.schedule = schedule;
     a.timeout_ns = kWaitLimitNs;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     st = status_word(&a.status);
@@ -478,9 +490,10 @@ ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
                     P, causal, stream, 0, cu_seqlens, n_seqs);
 }
 
-// The layout part of a descriptor, checked: zigzag flag, packed boundaries, batch.
+// The layout part of a descriptor, checked: zigzag flag, packed boundaries and
+// schedule, batch.
 static ra_status desc_layout(const ra_attn_desc* d, int bf16, int* zig, const int** cu,
-                             int* n_seqs)
+                             int* n_seqs, const int** sched)
 {
     if (!d) return RA_ERR_INVALID_ARG;
     if (d->B < 1 || d->L < 1 || d->H < 1 || d->H_kv < 1 || d->D < 1 || d->P < 1)
@@ -488,6 +501,8 @@ static ra_status desc_layout(const ra_attn_desc* d, int bf16, int* zig, const in
     *zig = 0;
     *cu = nullptr;
     *n_seqs = 0;
+    *sched = nullptr;
+    if (d->layout != RA_LAYOUT_PACKED && d->schedule) return RA_ERR_INVALID_ARG;
     switch (d->layout) {
     case RA_LAYOUT_CONTIGUOUS:
         if (d->cu_seqlens) return RA_ERR_INVALID_ARG;
@@ -502,8 +517,10 @@ static ra_status desc_layout(const ra_attn_desc* d, int bf16, int* zig, const in
     case RA_LAYOUT_PACKED:
         if (!d->cu_seqlens || d->n_seqs < 1 || d->B != 1) return RA_ERR_INVALID_ARG;
         if (!aligned(d->cu_seqlens, 4)) return RA_ERR_MISALIGNED;
+        if (d->schedule && !aligned(d->schedule, 4)) return RA_ERR_MISALIGNED;
         *cu = d->cu_seqlens;
         *n_seqs = d->n_seqs;
+        *sched = d->schedule;
         return RA_OK;
     }
     return RA_ERR_INVALID_ARG;
@@ -514,11 +531,13 @@ ra_status ring_attn_fwd_ex(const ra_attn_desc* desc, const void* q, const void* 
 {
     int zig = 0, n_seqs = 0;
     const int* cu = nullptr;
-    const ra_status st = desc_layout(desc, desc && desc->dtype == RA_BF16, &zig, &cu, &n_seqs);
+    const int* sched = nullptr;
+    const ra_status st =
+        desc_layout(desc, desc && desc->dtype == RA_BF16, &zig, &cu, &n_seqs, &sched);
     if (st != RA_OK) return st;
     return attn_impl(q, k, v, out, lse, desc->B, desc->L, desc->H, desc->D, desc->P, desc->causal,
                      desc->dtype, trace, reinterpret_cast<cudaStream_t>(stream), desc->H_kv, zig,
-                     cu, n_seqs);
+                     cu, n_seqs, 0, sched);
 }
 
 ra_status ring_attn_bwd_ex(const ra_attn_desc* desc, const void* q, const void* k, const void* v,
@@ -528,12 +547,35 @@ ra_status ring_attn_bwd_ex(const ra_attn_desc* desc, const void* q, const void* 
 {
     int zig = 0, n_seqs = 0;
     const int* cu = nullptr;
-    const ra_status st = desc_layout(desc, 1, &zig, &cu, &n_seqs);
+    const int* sched = nullptr;
+    const ra_status st = desc_layout(desc, 1, &zig, &cu, &n_seqs, &sched);
     if (st != RA_OK) return st;
     if (desc->dtype != RA_BF16) return RA_ERR_UNSUPPORTED;
     return bwd_impl(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, desc->B,
                     desc->L, desc->H, desc->H_kv, desc->D, desc->P, desc->causal, stream, zig, cu,
-                    n_seqs);
+                    n_seqs, sched);
+}
+
+unsigned long long ring_attn_varlen_schedule_bytes(int L, int P)
+{
+    if (L < 1 || P < 1 || P > L || L % P != 0) return 0;
+    return static_cast<unsigned long long>(ra::varlen_sched_layout(L, P).total) * sizeof(int);
+}
+
+ra_status ring_attn_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, int P, int causal,
+                                    int* schedule, unsigned long long schedule_bytes,
+                                    ra_stream_t stream)
+{
+    if (!cu_seqlens || !schedule || n_seqs < 1 || L < 1 || P < 1 || P > L)
+        return RA_ERR_INVALID_ARG;
+    if (L % P != 0) return RA_ERR_NOT_DIVISIBLE;
+    if (!aligned(cu_seqlens, 4) || !aligned(schedule, 4)) return RA_ERR_MISALIGNED;
+    const unsigned long long need = ring_attn_varlen_schedule_bytes(L, P);
+    if (schedule_bytes < need) return RA_ERR_INVALID_ARG;
+    if (overlap(schedule, need, cu_seqlens, (static_cast<unsigned long long>(n_seqs) + 1) * 4))
+        return RA_ERR_INVALID_ARG;
+    return from_cuda(ra::launch_varlen_schedule(cu_seqlens, n_seqs, L, P, causal, schedule,
+                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ra_status ra_check_status(ra_stream_t stream)

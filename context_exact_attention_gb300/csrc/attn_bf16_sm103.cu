@@ -94,6 +94,7 @@ struct Params {
     int zigzag;      // shard r holds chunks r and 2P-1-r of 2P chunks (causal only)
     const int* cu_seqlens;   // packed sequences: starts of n_seqs sequences, then L
     int n_seqs;
+    const int* schedule;     // packed sequences: units heaviest first (r * n_pair + pair), or null
     int group;       // query heads per key/value head
     int u_B, u_H, u_Ls;  // Ulysses head groups (kMode 3): batch, heads, shard rows of the sources
     int n_kt;        // K/V blocks per shard
@@ -340,8 +341,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int units_per_bh = p.P * p.n_pair;
     int bh, u;
     unit_of_block(blockIdx.x, p.B * p.H, units_per_bh, bh, u);
-    const int r = p.P - 1 - u / p.n_pair;
-    const int pair = p.n_pair - 1 - (u - (u / p.n_pair) * p.n_pair);
+    int r = p.P - 1 - u / p.n_pair;
+    int pair = p.n_pair - 1 - (u - (u / p.n_pair) * p.n_pair);
+    if constexpr (kMode == 2) {
+        // packed sequences: work follows the offset inside a sequence, not the position;
+        // a precomputed order (entries outside the unit range are ignored) puts the
+        // heaviest units first
+        if (p.schedule != nullptr) {
+            const int x = __ldg(p.schedule + u);
+            if (static_cast<unsigned>(x) < static_cast<unsigned>(units_per_bh)) {
+                r = x / p.n_pair;
+                pair = x - r * p.n_pair;
+            }
+        }
+    }
     const int b = bh / p.H;
     const int h = bh - b * p.H;
     const int hk = h / p.group;                       // key/value head of this query head
@@ -760,6 +773,7 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     p.zigzag = a.zigzag;
     p.cu_seqlens = a.cu_seqlens;
     p.n_seqs = a.n_seqs;
+    p.schedule = a.schedule != nullptr ? a.schedule + varlen_sched_layout(a.L, a.P).fwd : nullptr;
     p.group = a.H / a.Hkv;
     p.u_B = a.u_B;
     p.u_H = a.u_H;

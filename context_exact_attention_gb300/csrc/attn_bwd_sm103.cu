@@ -73,6 +73,8 @@ struct BwdParams {
     float scale;             // 1 / sqrt(D)
     const int* cu_seqlens;   // packed sequences: starts of n_seqs sequences, then L
     int n_seqs;
+    const int* sched_k;      // packed sequences: key tiles heaviest first (s * n_t + kt), or null
+    const int* sched_q;      // packed sequences: query tiles heaviest first (r * n_t + qt), or null
 };
 
 // ------------------------------------------------------- shard layouts --
@@ -349,6 +351,17 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         // zigzag: a key tile's work falls with its global position (it meets every later
         // query), so heaviest first is position order: unit u is the u-th tile by position
         zigzag_tile_at(u, p.P, p.n_t, s, kt);
+    }
+    if constexpr (kMode == 2) {
+        // packed sequences: a precomputed heaviest-first order, if given (entries outside
+        // the unit range are ignored)
+        if (p.sched_k != nullptr) {
+            const int x = __ldg(p.sched_k + u);
+            if (static_cast<unsigned>(x) < static_cast<unsigned>(units_per_bh)) {
+                s = x / p.n_t;
+                kt = x - s * p.n_t;
+            }
+        }
     }
     const int b = bh / p.Hkv;
     const int hk = bh - b * p.Hkv;
@@ -813,6 +826,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is descending position order
         zigzag_tile_at(p.P * p.n_t - 1 - u, p.P, p.n_t, r, qt);
     }
+    if constexpr (kMode == 2) {
+        if (p.sched_q != nullptr) {
+            const int x = __ldg(p.sched_q + u);
+            if (static_cast<unsigned>(x) < static_cast<unsigned>(units_per_bh)) {
+                r = x / p.n_t;
+                qt = x - r * p.n_t;
+            }
+        }
+    }
     const int b = bh / p.H;
     const int h = bh - b * p.H;
     const int hk = h / p.group;                       // key/value head of this query head
@@ -1197,6 +1219,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     p.scale_log2 = kLog2e * p.scale;
     p.cu_seqlens = a.cu_seqlens;
     p.n_seqs = a.n_seqs;
+    p.sched_k = p.sched_q = nullptr;
+    if (a.schedule != nullptr) {
+        const VarlenSchedLayout lay = varlen_sched_layout(a.L, a.P);
+        p.sched_k = a.schedule + lay.bwd_k;
+        p.sched_q = a.schedule + lay.bwd_q;
+    }
     // dK/dV: one CTA per key tile of each key/value head; dQ: per query tile of each head
     const long long grid_kv = static_cast<long long>(a.B) * a.Hkv * a.P * p.n_t;
     const long long grid = static_cast<long long>(a.B) * a.H * a.P * p.n_t;

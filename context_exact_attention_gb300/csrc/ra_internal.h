@@ -22,6 +22,7 @@ struct AttnArgs {
     int zigzag;                    // zigzag shard layout (causal)
     const int* cu_seqlens;         // packed sequences (device), or null
     int n_seqs;
+    const int* schedule;           // packed sequences: unit orders (VarlenSchedLayout), or null
     // Ulysses head groups read from / written to the sequence-sharded buffers
     // [u_P][u_B][L/u_P][u_H][D] (0 = not used): B = u_P * u_B head-group batches of
     // H = u_H / u_P heads, ring P = 1; the tensor maps are then 5-D.
@@ -30,6 +31,31 @@ struct AttnArgs {
     unsigned long long timeout_ns; // limit of one bounded wait
     cudaStream_t stream;
 };
+
+// Packed-sequence schedule (ring_attn_varlen_schedule), in int32 entries: the forward's
+// query-tile pairs, the backward's key tiles and query tiles, each a permutation of the
+// units of one (batch, head) given by their natural index (shard * per-shard units +
+// tile or pair), heaviest first; then scratch for the work counts.
+struct VarlenSchedLayout {
+    long long n_t, n_pair;           // 128-row tiles and tile pairs per shard
+    long long fwd, bwd_k, bwd_q;     // offsets of the three orders
+    long long scratch, total;        // offset of the scratch, total entries
+};
+inline VarlenSchedLayout varlen_sched_layout(int L, int P)
+{
+    VarlenSchedLayout s;
+    const long long Ls = static_cast<long long>(L) / P;
+    s.n_t = (Ls + 127) / 128;
+    s.n_pair = (s.n_t + 1) / 2;
+    s.fwd = 0;
+    s.bwd_k = s.fwd + P * s.n_pair;
+    s.bwd_q = s.bwd_k + P * s.n_t;
+    s.scratch = s.bwd_q + P * s.n_t;
+    s.total = s.scratch + P * s.n_t;
+    return s;
+}
+cudaError_t launch_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, int P, int causal,
+                                   int* schedule, cudaStream_t stream);
 
 // bf16 tcgen05 kernel; tensor maps describe q, k, v as 4-D [B][L][H][D] with
 // 64-element, 128-byte-swizzled boxes of 128 rows.
@@ -53,6 +79,7 @@ struct BwdArgs {
     int zigzag;          // zigzag shard layout (causal; Hkv == H)
     const int* cu_seqlens;   // packed sequences (device; B == 1, Hkv == H), or null
     int n_seqs;
+    const int* schedule;     // packed sequences: unit orders (VarlenSchedLayout), or null
     unsigned int* status;
     unsigned long long timeout_ns;
     cudaStream_t stream;

@@ -375,7 +375,13 @@ typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_ZIGZAG = 1, RA_LAYOUT_PACKED 
  *   layout         one of ra_layout;
  *   cu_seqlens     RA_LAYOUT_PACKED only (else NULL): device int32 [n_seqs + 1], as
  *                  ring_attn_fwd_varlen takes it;
- *   dtype          RA_BF16 or RA_F32 for the forward, RA_BF16 for the backward.
+ *   dtype          RA_BF16 or RA_F32 for the forward, RA_BF16 for the backward;
+ *   schedule       RA_LAYOUT_PACKED only (else NULL): NULL, or the device array that
+ *                  ring_attn_varlen_schedule wrote for the same cu_seqlens, L and P.  It
+ *                  sets only which CTA takes which work unit (heaviest first instead of
+ *                  position order): the results are the same bits either way.  An array
+ *                  that is not such a schedule gives undefined results, never
+ *                  out-of-bounds accesses.
  * The descriptor is read during the call only.
  */
 typedef struct {
@@ -385,7 +391,44 @@ typedef struct {
     const int* cu_seqlens;
     int n_seqs;
     ra_dtype dtype;
+    const int* schedule;
 } ra_attn_desc;
+
+/*
+ * ring_attn_varlen_schedule_bytes -- device bytes ring_attn_varlen_schedule writes for
+ * L packed rows over P shards (0 when L < 1, P < 1 or L % P != 0).
+ */
+unsigned long long ring_attn_varlen_schedule_bytes(int L, int P);
+
+/*
+ * ring_attn_varlen_schedule -- the order, heaviest first, in which the packed-layout
+ * kernels of ring_attn_fwd_ex / ring_attn_bwd_ex take their work units (no counterpart
+ * on the pages: an addition of this library).
+ *
+ * With packed sequences (section 6.5 of "序列并行与 Ring Attention") the work of a unit
+ * -- the key tiles a query tile sees, or the query tiles that see a key tile -- grows
+ * with the tile's offset inside its sequence, which only cu_seqlens tells.  Without a
+ * schedule the kernels take units in position order, which can leave the heaviest ones
+ * for the end of the grid while most SMs idle.  This call launches one CTA on `stream`
+ * that counts each unit's tiles from cu_seqlens (same visibility rule as the kernels:
+ * own sequence, causal or not) and writes three orders, heaviest first and ties in
+ * position order: the forward's query-tile pairs, the backward's key tiles and its
+ * query tiles.  Pass the array as ra_attn_desc.schedule with the same cu_seqlens, L and
+ * P (a schedule made for the other causal flag is valid but less balanced).  It depends
+ * only on these arguments, so one schedule serves every head, layer and the backward of
+ * a batch.
+ *
+ * cu_seqlens: DEVICE int32 [n_seqs + 1], as ring_attn_fwd_varlen takes it (malformed
+ *             contents give a poor order, never out-of-bounds accesses).
+ * schedule:   DEVICE memory of at least ring_attn_varlen_schedule_bytes(L, P) bytes,
+ *             4-byte aligned, owned by the caller; written by the launched kernel, so
+ *             read it only in work ordered after it on the device.
+ * Errors: RA_ERR_INVALID_ARG (NULL pointer, n_seqs < 1, L < 1, P < 1, P > L, short
+ * schedule), RA_ERR_NOT_DIVISIBLE (L % P != 0), RA_ERR_MISALIGNED, RA_ERR_CUDA.
+ */
+ra_status ring_attn_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, int P, int causal,
+                                    int* schedule, unsigned long long schedule_bytes,
+                                    ra_stream_t stream);
 
 /*
  * ring_attn_fwd_ex -- the forward for any combination of the options in *desc: the
@@ -395,8 +438,9 @@ typedef struct {
  * ring_attn_fwd_varlen (section 6.5).  q, out: [B, L, H, D]; k, v: [B, L, H_kv, D];
  * lse [B, L, H] or NULL; trace [P, P] or NULL (as ring_attn_fwd_trace).  Argument
  * checks and errors: those of the specialised entry point of the same options, plus
- * RA_ERR_INVALID_ARG for a NULL descriptor, an unknown layout, cu_seqlens with a
- * non-packed layout or B != 1 with the packed one.  With the options of a specialised
+ * RA_ERR_INVALID_ARG for a NULL descriptor, an unknown layout, cu_seqlens or schedule
+ * with a non-packed layout or B != 1 with the packed one, and RA_ERR_MISALIGNED for a
+ * schedule not 4-byte aligned.  With the options of a specialised
  * entry point it launches the same kernel on the same arguments (same bits).
  */
 ra_status ring_attn_fwd_ex(const ra_attn_desc* desc, const void* q, const void* k, const void* v,

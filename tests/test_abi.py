@@ -141,10 +141,11 @@ def test_host_workspace_size():
 
 def test_descriptor_layout_and_argument_errors(lib):
     """The ctypes mirror of ra_attn_desc has the C layout (eight ints, the boundary
-    pointer, two ints: 48 bytes), and the general entry points reject bad descriptors
-    on the host before touching the runtime."""
-    assert ctypes.sizeof(cea.AttnDesc) == 48
+    pointer, two ints, the schedule pointer: 56 bytes), and the general entry points
+    reject bad descriptors on the host before touching the runtime."""
+    assert ctypes.sizeof(cea.AttnDesc) == 56
     assert cea.AttnDesc.cu_seqlens.offset == 32 and cea.AttnDesc.dtype.offset == 44
+    assert cea.AttnDesc.schedule.offset == 48
     fake = ctypes.c_void_p(1 << 20)
     out = ctypes.c_void_p(1 << 40)
     ws = ctypes.c_void_p(1 << 44)
@@ -153,7 +154,7 @@ def test_descriptor_layout_and_argument_errors(lib):
 
     def desc(**kw):
         d = dict(B=1, L=1024, H=4, H_kv=2, D=128, P=4, causal=1, layout=1, cu_seqlens=None,
-                 n_seqs=0, dtype=0)
+                 n_seqs=0, dtype=0, schedule=None)
         d.update(kw)
         return ctypes.byref(cea.AttnDesc(**d))
 
@@ -170,6 +171,39 @@ def test_descriptor_layout_and_argument_errors(lib):
     assert fwd(desc(layout=2)) == 1                         # packed without boundaries
     assert fwd(desc(layout=2, cu_seqlens=1 << 20, n_seqs=3, B=2)) == 1
     assert fwd(desc(layout=2, cu_seqlens=(1 << 20) + 2, n_seqs=3)) == 3
+    assert fwd(desc(layout=0, schedule=1 << 36)) == 1       # schedule without packed layout
+    assert fwd(desc(layout=1, schedule=1 << 36)) == 1
+    assert fwd(desc(layout=2, cu_seqlens=1 << 20, n_seqs=3, schedule=(1 << 36) + 2)) == 3
+    assert bwd(desc(layout=2, cu_seqlens=1 << 20, n_seqs=3, schedule=(1 << 36) + 2)) == 3
+    # a schedule overlapping the output
+    assert fwd(desc(layout=2, cu_seqlens=1 << 20, n_seqs=3, H_kv=4, schedule=1 << 40)) == 1
     assert bwd(desc(dtype=1)) == 2                          # backward is bf16 only
     assert bwd(desc(causal=0)) == 2
     assert bwd(desc(H_kv=0)) == 1
+
+
+def test_varlen_schedule_size_and_argument_errors(lib):
+    """ring_attn_varlen_schedule_bytes counts three unit orders (forward tile pairs,
+    backward key tiles, backward query tiles) plus a scratch of one backward order, and
+    ring_attn_varlen_schedule rejects bad arguments before launching anything."""
+    def n_units(L, P):
+        n_t = -(-(L // P) // 128)
+        return n_t, -(-n_t // 2)
+    for L, P in ((32768, 8), (1000, 4), (1, 1), (4096, 1), (300, 3)):
+        n_t, n_pair = n_units(L, P)
+        assert lib.ring_attn_varlen_schedule_bytes(L, P) == 4 * P * (n_pair + 3 * n_t)
+    assert lib.ring_attn_varlen_schedule_bytes(1000, 3) == 0
+    assert lib.ring_attn_varlen_schedule_bytes(0, 1) == 0
+    assert lib.ring_attn_varlen_schedule_bytes(4, 8) == 0
+    cu = ctypes.c_void_p(1 << 20)
+    sched = ctypes.c_void_p(1 << 30)
+    s = ctypes.c_void_p(0)
+    nb = lib.ring_attn_varlen_schedule_bytes(4096, 4)
+    call = lambda *a: lib.ring_attn_varlen_schedule(*a, s)
+    assert call(None, 3, 4096, 4, 1, sched, nb) == 1
+    assert call(cu, 3, 4096, 4, 1, None, nb) == 1
+    assert call(cu, 0, 4096, 4, 1, sched, nb) == 1
+    assert call(cu, 3, 4096, 4, 1, sched, nb - 4) == 1       # short schedule
+    assert call(cu, 3, 4098, 4, 1, sched, nb) == 4           # L % P
+    assert call(cu, 3, 4096, 4, 1, ctypes.c_void_p((1 << 30) + 2), nb) == 3
+    assert call(cu, 3, 4096, 4, 1, ctypes.c_void_p((1 << 20) - 8), nb) == 1   # overlaps cu
