@@ -81,7 +81,8 @@ enum : int {
     kBarPFull = 11,  // +2*tile +half: P columns of keys [0,64) and [64,128)
     kBarOFull = 15,  // +tile
     kBarDone = 17,
-    kBarCount = 18
+    kBarQ1 = 18,     // query tile 1 (tile 0 on kBarQ), so that tile 0's first S starts earlier
+    kBarCount = 19
 };
 
 struct Params {
@@ -407,8 +408,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarOFull + i), 1);
         }
         mbar_init(bar(kBarDone), 1);
+        mbar_init(bar(kBarQ1), 1);
         *abort_flag = 0;
         fence_mbar_init();
+        // Start the loads the first products need (Q0 and K0 for tile 0's first S, then
+        // Q1) before the TMEM allocation and the block-wide barrier: every CTA of a wave
+        // starts by loading at once, so the sooner they are queued the better.  The
+        // producer loop below issues V0 and everything after it.
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        const uint64_t once = l2_policy_evict_first();
+        auto load_q = [&](int tq, uint32_t full) {
+            mbar_arrive_expect_tx(bar(full), Lay::kTileBytes);
+            for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                const uint32_t dst = sbase + Lay::kQ + tq * Lay::kTileBytes + bx * 16384;
+                const int row = q0 + tq * kRows;
+                if constexpr (kMode == 3)
+                    tma_load_5d(dst, &tmap_q, bar(full), bx * 64, h_src, row % p.u_Ls, bo,
+                                row / p.u_Ls, once);
+                else
+                    tma_load_4d(dst, &tmap_q, bar(full), bx * 64, h, row, b, once);
+            }
+        };
+        load_q(0, kBarQ);
+        if (n_blocks > 0) {
+            walk.at(0);
+            const int row = walk.s * p.Ls + walk.kt() * kKeys;
+            const uint64_t keep = l2_policy_evict_last();
+            mbar_arrive_expect_tx(bar(kBarKFull + 0), Lay::kTileBytes);
+            for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                const uint32_t dst = sbase + Lay::kK + bx * 16384;
+                if constexpr (kMode == 3)
+                    tma_load_5d(dst, &tmap_k, bar(kBarKFull + 0), bx * 64, hk_src, row % p.u_Ls,
+                                bo, row / p.u_Ls, keep);
+                else
+                    tma_load_4d(dst, &tmap_k, bar(kBarKFull + 0), bx * 64, hk, row, b, keep);
+            }
+        }
+        load_q(1, kBarQ1);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
@@ -434,20 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tracing && leader)
             for (int t = 0; t < p.P; ++t) p.trace[r * p.P + t] = -1;
         const uint64_t keep = l2_policy_evict_last();    // K/V: read by every tile pair of the head
-        const uint64_t once = l2_policy_evict_first();   // Q: read once
-        if (leader) {
-            mbar_arrive_expect_tx(bar(kBarQ), kTiles * Lay::kTileBytes);
-            for (int tq = 0; tq < kTiles; ++tq)
-                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
-                    const uint32_t dst = sbase + Lay::kQ + tq * Lay::kTileBytes + bx * 16384;
-                    const int row = q0 + tq * kRows;
-                    if constexpr (kMode == 3)
-                        tma_load_5d(dst, &tmap_q, bar(kBarQ), bx * 64, h_src, row % p.u_Ls, bo,
-                                    row / p.u_Ls, once);
-                    else
-                        tma_load_4d(dst, &tmap_q, bar(kBarQ), bx * 64, h, row, b, once);
-                }
-        }
+        // Q0, Q1 (read once) and K0 were issued by thread 0 before the block-wide barrier
         int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
         for (int n = 0; n < n_blocks; ++n) {
             walk.at(n);
@@ -456,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph = (n >> 1) & 1;
             const int row = walk.s * p.Ls + walk.kt() * kKeys;   // physical row of the tile
             if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc))) break;
-            if (leader) {
+            if (leader && n > 0) {
                 mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kTileBytes);
                 for (int bx = 0; bx < Lay::kBoxes; ++bx) {
                     const uint32_t dst = sbase + Lay::kK + st * Lay::kTileBytes + bx * 16384;
@@ -484,6 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // let this CTA's own copies land before anyone leaves
         mbar_wait_drain(bar(kBarQ), 0, wc);
+        mbar_wait_drain(bar(kBarQ1), 0, wc);
+        if (n_blocks > 0 && last_k[0] < 0) mbar_wait_drain(bar(kBarKFull + 0), 0, wc);
         for (int st = 0; st < 2; ++st) {
             if (last_k[st] >= 0) mbar_wait_drain(bar(kBarKFull + st), (last_k[st] >> 1) & 1, wc);
             if (last_v[st] >= 0) mbar_wait_drain(bar(kBarVFull + st), (last_v[st] >> 1) & 1, wc);
@@ -535,6 +561,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) {
                 issue_qk(0, 0);
                 tc_commit(bar(kBarSFull + 0));
+            }
+            __syncwarp();
+        }
+        if (ok && (ok = wait_all(kBarQ1, 0))) {
+            tc_fence_after();
+            if (leader) {
                 issue_qk(1, 0);
                 tc_commit(bar(kBarSFull + 1));
                 tc_commit(bar(kBarKEmpty + 0));
