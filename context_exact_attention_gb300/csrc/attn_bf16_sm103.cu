@@ -634,7 +634,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + Lay::col_s(tq);
         const uint32_t tO = tmem + lane_off + Lay::col_o(tq);
         const int row_local = q0_local + tq * kRows + row;   // within shard r
-        const int row_glob = r * p.Ls + row_local;           // physical row
         const int row_pos = position(r, row_local, p.P, p.Ls, kZig ? 1 : 0);
         int seq_lo = 0, seq_hi = 0;                            // packed sequences only
         if constexpr (kVarlen) {
@@ -740,14 +739,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool valid = row_local < p.Ls;
             const float inv_l = l > 0.f ? 1.f / l : 0.f;        // a row that saw no key: 0
-            // index of (row, head) among the output's rows of D elements
-            size_t orow = (static_cast<size_t>(b) * p.L + row_glob) * p.H + h;
+            // index of (row, head) among the output's rows of D elements, for this warp's
+            // first row; the warp's 32 rows lie in one tile, so `ostride` apart
+            const int x0 = q0_local + tq * kRows + quarter * 32;   // within shard r
+            const int g0 = r * p.Ls + x0;
+            size_t orow0 = (static_cast<size_t>(b) * p.L + g0) * p.H + h;
+            size_t ostride = p.H;
             if constexpr (kMode == 3) {
-                const int rs = row_glob / p.u_Ls;
-                orow = (static_cast<size_t>(rs * p.u_B + bo) * p.u_Ls + (row_glob - rs * p.u_Ls)) *
-                           p.u_H + h_src;
+                const int rs = g0 / p.u_Ls;
+                orow0 = (static_cast<size_t>(rs * p.u_B + bo) * p.u_Ls + (g0 - rs * p.u_Ls)) *
+                            p.u_H + h_src;
+                ostride = p.u_H;
             }
-            __nv_bfloat16* dst = p.out + orow * static_cast<size_t>(D);
+            // The rows go out through the warp's 32-row slice of this tile's query buffer,
+            // free once O is final (the tile's last Q K^T finished before its last P V), so
+            // that every global store covers whole rows instead of one 16-byte piece of 32
+            // rows.  A thread writes its row's 16-byte chunk c at slot c ^ (row mod
+            // kChunks): conflict-free for both the row-wise writes and the chunk-wise reads.
+            constexpr int kChunks = D / 8;                     // 16-byte chunks per row
+            constexpr int kRowsPerStore = 32 / kChunks;        // rows one warp store covers
+            uint8_t* stage = smem + Lay::kQ + tq * Lay::kTileBytes + quarter * 32 * (2 * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -756,14 +767,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
-                if (valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                for (int j = 0; j < 4; ++j) {
+                    const int slot = (4 * c + j) ^ (lane & (kChunks - 1));
+                    *reinterpret_cast<uint4*>(stage + lane * (2 * D) + slot * 16) =
+                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
             }
-            if (valid && p.lse != nullptr) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            __syncwarp();
+            {
+                const int sub = lane / kChunks, cc = lane % kChunks;
+#pragma unroll
+                for (int k = 0; k < 32 / kRowsPerStore; ++k) {
+                    const int rr = k * kRowsPerStore + sub;         // row within the warp's 32
+                    const uint4 val = *reinterpret_cast<const uint4*>(
+                        stage + rr * (2 * D) + ((cc ^ (rr & (kChunks - 1))) * 16));
+                    if (x0 + rr < p.Ls)
+                        *reinterpret_cast<uint4*>(p.out + (orow0 + rr * ostride) * D + cc * 8) = val;
+                }
+            }
+            if (valid && p.lse != nullptr)
+                p.lse[orow0 + lane * ostride] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
     }
 
