@@ -224,6 +224,42 @@ __device__ void zero_tile_rows(__nv_bfloat16* t, int b, int L, int heads, int he
 
 // ------------------------------------------------------------------ row dot --
 
+// Output staging of the elementwise warps' epilogues.  A warp holds 32 rows of kCols
+// bf16 columns, one row per lane; written straight to global memory every store
+// instruction would touch 32 rows.  Each lane first writes its row's 16-byte chunks
+// (four per call, starting at chunk `first`) to a 32-row staging slice, chunk j at slot
+// j ^ (row mod chunks) so that neither the row-wise writes nor the chunk-wise reads
+// conflict on banks; store_staged_rows then stores whole row pieces per instruction.
+template <int kCols>
+__device__ __forceinline__ void stage_row_chunks(uint8_t* stage, int lane, int first,
+                                                 const uint32_t (&pk)[16])
+{
+    constexpr int kChunks = kCols / 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int slot = (first + j) ^ (lane & (kChunks - 1));
+        *reinterpret_cast<uint4*>(stage + lane * (2 * kCols) + slot * 16) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    }
+}
+
+// Rows 0..31 of the slice to dst + row * stride (elements), rows < n_valid only.
+template <int kCols>
+__device__ __forceinline__ void store_staged_rows(const uint8_t* stage, int lane, __nv_bfloat16* dst,
+                                                  size_t stride, int n_valid)
+{
+    constexpr int kChunks = kCols / 8;
+    constexpr int kRowsPerStore = 32 / kChunks;
+    const int sub = lane / kChunks, cc = lane % kChunks;
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k) {
+        const int rr = k * kRowsPerStore + sub;
+        const uint4 val = *reinterpret_cast<const uint4*>(stage + rr * (2 * kCols) +
+                                                          ((cc ^ (rr & (kChunks - 1))) * 16));
+        if (rr < n_valid) *reinterpret_cast<uint4*>(dst + rr * stride + cc * 8) = val;
+    }
+}
+
 // Dvec[row] = sum_d dO[row, d] * O[row, d] for every (b, l, h) row; a group of
 // D/8 lanes takes one row, one 16-byte vector each.
 template <int D>
@@ -744,10 +780,11 @@ __global__ void __launch_bounds__(kKVThreads, 1)
             // parts 0-1 write the two column halves of dV, parts 2-3 those of dK
             const int which = part >> 1;
             const int col0 = (part & 1) * (D / 2);
-            const size_t base = ((static_cast<size_t>(b) * p.L + key0 + row) * p.Hkv + hk) * D + col0;
             const uint32_t tA = tmem + lane_off + 256 + which * D + col0;
             const float mul = which ? p.scale : 1.f;
-            __nv_bfloat16* dst = (which ? p.dk : p.dv) + base;
+            // the warp's 32 rows of D/2 columns leave through its slice of the Q stages (no
+            // product reads them any more), so that each store covers whole row halves
+            uint8_t* stage = smem + kQ + (warp - 4) * 32 * D;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t o[32];
@@ -756,13 +793,13 @@ __global__ void __launch_bounds__(kKVThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack_bf16x2(u2f(o[2 * i]) * mul, u2f(o[2 * i + 1]) * mul);
-                if (key_valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                }
+                stage_row_chunks<D / 2>(stage, lane, 4 * c, pk);
             }
+            __syncwarp();
+            const int krow0 = kt * kRows + quarter * 32;      // within shard s
+            __nv_bfloat16* dst = (which ? p.dk : p.dv) +
+                                 ((static_cast<size_t>(b) * p.L + s * p.Ls + krow0) * p.Hkv + hk) * D + col0;
+            store_staged_rows<D / 2>(stage, lane, dst, static_cast<size_t>(p.Hkv) * D, p.Ls - krow0);
         }
     }
 
@@ -1137,8 +1174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kDOFull), 0, wc));
         if (ok) {
             tc_fence_after();
-            // each half writes half of the D output columns
-            __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(b) * p.L + q0 + row) * p.H + h) * D;
+            // each half writes half of the D output columns, through the warp's slice of the
+            // K stages (no product reads them any more) so that stores cover row halves
+            uint8_t* stage = smem + kK + (warp - 4) * 32 * D;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 const int col = half * (D / 2) + 32 * c;
@@ -1148,13 +1186,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack_bf16x2(u2f(o[2 * i]) * p.scale, u2f(o[2 * i + 1]) * p.scale);
-                if (row_valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + col);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                }
+                stage_row_chunks<D / 2>(stage, lane, 4 * c, pk);
             }
+            __syncwarp();
+            const int qrow0 = q_local0 + quarter * 32;        // within shard r
+            __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(b) * p.L + r * p.Ls + qrow0) * p.H + h) * D +
+                                 half * (D / 2);
+            store_staged_rows<D / 2>(stage, lane, dst, static_cast<size_t>(p.H) * D, p.Ls - qrow0);
         }
     }
 
