@@ -35,7 +35,7 @@ struct AttnArgs {
 // Packed-sequence schedule (ring_attn_varlen_schedule), in int32 entries: the forward's
 // query-tile pairs, the backward's key tiles and query tiles, each a permutation of the
 // units of one (batch, head) given by their natural index (shard * per-shard units +
-// tile or pair), heaviest first; then scratch for the work counts.
+// tile or pair), heaviest first; then scratch for the work counts of all three.
 struct VarlenSchedLayout {
     long long n_t, n_pair;           // 128-row tiles and tile pairs per shard
     long long fwd, bwd_k, bwd_q;     // offsets of the three orders
@@ -51,7 +51,7 @@ inline VarlenSchedLayout varlen_sched_layout(int L, int P)
     s.bwd_k = s.fwd + P * s.n_pair;
     s.bwd_q = s.bwd_k + P * s.n_t;
     s.scratch = s.bwd_q + P * s.n_t;
-    s.total = s.scratch + P * s.n_t;
+    s.total = s.scratch + s.scratch;
     return s;
 }
 cudaError_t launch_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, int P, int causal,

@@ -10,10 +10,10 @@
 // kernel counts every unit's tiles from cu_seqlens and writes the units in descending
 // work (ties: ascending natural index), which the kernels then read by block index.
 //
-// One CTA: all threads count (two binary searches over cu_seqlens per unit), then a
-// counting sort over work values -- histogram in shared memory, a descending exclusive
-// scan and a stable scatter by one warp (__match_any_sync ranks the lanes of equal
-// bins in lane order, so the order is deterministic).
+// One CTA per unit kind: all threads count (two binary searches over cu_seqlens per
+// unit), then a counting sort over work values -- histogram in shared memory, a
+// descending exclusive scan and a stable scatter by one warp (__match_any_sync ranks
+// the lanes of equal bins in lane order, so the order is deterministic).
 #include "ra_internal.h"
 
 namespace ra {
@@ -70,13 +70,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int Ls = L / P;
     const int max_work = P * static_cast<int>(lay.n_t);
     const int nb = min(max_work + 1, kMaxBins);
-    for (int kind = 0; kind < 3; ++kind) {
+    {
         // kind 0: forward query-tile pairs; 1: backward key tiles; 2: backward query tiles
+        const int kind = blockIdx.x;
         const int per = static_cast<int>(kind == 0 ? lay.n_pair : lay.n_t);   // units per shard
         const int rows = kind == 0 ? 2 * kTileRows : kTileRows;
         const int U = P * per;
-        int* order = sched + (kind == 0 ? lay.fwd : kind == 1 ? lay.bwd_k : lay.bwd_q);
-        int* work = U <= kSmemWork ? work_s : sched + lay.scratch;
+        const long long off = kind == 0 ? lay.fwd : kind == 1 ? lay.bwd_k : lay.bwd_q;
+        int* order = sched + off;
+        // each kind's scratch sits as far past the scratch base as its order past the first
+        int* work = U <= kSmemWork ? work_s : sched + lay.scratch + off;
         for (int i = threadIdx.x; i < nb; i += kThreads) bins[i] = 0;
         __syncthreads();
         for (int u = threadIdx.x; u < U; u += kThreads) {
@@ -128,7 +131,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
         }
-        __syncthreads();
     }
 }
 
@@ -138,7 +140,7 @@ cudaError_t launch_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, int
                                    int* schedule, cudaStream_t stream)
 {
     const VarlenSchedLayout lay = varlen_sched_layout(L, P);
-    varlen_schedule_kernel<<<1, kThreads, 0, stream>>>(cu_seqlens, n_seqs, L, P, causal ? 1 : 0,
+    varlen_schedule_kernel<<<3, kThreads, 0, stream>>>(cu_seqlens, n_seqs, L, P, causal ? 1 : 0,
                                                        schedule, lay);
     return cudaGetLastError();
 }
