@@ -63,12 +63,21 @@ def _host_schedule(cu, L, P, causal):
     return orders
 
 
+def _many(n, P, seed):
+    """n sequences of 1..59 rows, the last one stretched so that P divides the total."""
+    lengths = [int(x) for x in np.random.default_rng(seed).integers(1, 60, n)]
+    lengths[-1] += -sum(lengths) % P
+    return lengths
+
+
 SCHED_CASES = [
     ([6755, 4302, 6383, 701, 4326, 4982, 5319], 8),     # the benchmark's length draw
     ([300, 1, 1000, 0, 747], 4),                         # ragged shards, an empty sequence
     ([2048] * 4, 2),
     ([5000], 5),                                         # one sequence
     ([17, 900, 83, 2000, 1, 1, 1, 93], 3),
+    ([5, 7, 100, 200], 4),                               # shards shorter than one tile
+    (_many(400, 8, 3), 8),                               # many short sequences
 ]
 
 
@@ -111,6 +120,8 @@ BIT_CASES = [
     ([6755, 4302, 6383, 701, 4326, 4982, 5319], 4, 2, 128, 8),
     ([300, 1, 1000, 0, 747], 2, 2, 64, 4),
     ([129, 2000, 255, 1], 3, 1, 128, 5),
+    ([5, 7, 100, 200], 2, 2, 128, 4),
+    (_many(400, 8, 4), 2, 1, 64, 8),
 ]
 
 
