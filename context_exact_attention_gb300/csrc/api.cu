@@ -79,6 +79,32 @@ bool encode_qkv_map(CUtensorMap* map, const void* base, int B, int L, int H, int
 // A sequence-sharded Ulysses buffer [P][B][L/P][H][D] as a 5-D bf16 tensor
 // {D, H, L/P, B, P} (innermost first), same boxes and swizzle as encode_qkv_map: a box of
 // 128 rows stays inside one shard when (L/P) % 128 == 0.
+// The sequence-sharded buffer [P][B][L/P][H][D] of the Ulysses transposes as the 5-D
+// view {D, H/P, P, L/P, P*B} (innermost first: head dim, head within a group, group,
+// position within the shard, source rank and batch), box {D, H/P, 1, R, 1}: one group's
+// heads at R consecutive positions.  No swizzle, so a box lands in shared memory as the
+// dense run [R][H/P][D] it is on the head-sharded side; elements are moved as 16- or
+// 32-bit words.
+bool encode_permute_map(CUtensorMap* map, const void* base, int B, int L, int H, int D, int P,
+                        int elem_bytes, int R)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t e = static_cast<cuuint64_t>(elem_bytes);
+    const cuuint64_t hg = static_cast<cuuint64_t>(H / P), Ls = static_cast<cuuint64_t>(L / P);
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(D), hg, static_cast<cuuint64_t>(P), Ls,
+                                static_cast<cuuint64_t>(P) * B};
+    const cuuint64_t strides[4] = {D * e, hg * D * e, static_cast<cuuint64_t>(H) * D * e,
+                                   Ls * H * D * e};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(hg), 1,
+                               static_cast<cuuint32_t>(R), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 5,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_seq_shard_map(CUtensorMap* map, const void* base, int P, int B, int L, int H, int D)
 {
     EncodeTiledFn fn = encode_fn();
@@ -223,6 +249,20 @@ ra_status permute_impl(const void* in, void* out, int B, int L, int H, int D, in
     if (!aligned(in, 16) || !aligned(out, 16)) return RA_ERR_MISALIGNED;
     const unsigned long long bytes = n * elem_bytes;
     if (overlap(in, bytes, out, bytes)) return RA_ERR_INVALID_ARG;
+    if (ra::ulysses_permute_tma_fits(H, D, P, elem_bytes)) {
+        // copy engines: the sequence-sharded side as a 5-D view {D, H/P, P, L/P, P*B}
+        const int R = ra::ulysses_permute_tma_rows(L, H, D, P, elem_bytes);
+        CUtensorMap map;
+        const void* seq_side = dir == 0 ? in : out;
+        void* head_side = dir == 0 ? out : const_cast<void*>(in);
+        if (encode_permute_map(&map, seq_side, B, L, H, D, P, elem_bytes, R)) {
+            unsigned int* status = nullptr;
+            const ra_status st = status_word(&status);
+            if (st != RA_OK) return st;
+            return from_cuda(ra::launch_ulysses_permute_tma(map, head_side, B, L, H, D, P, elem_bytes,
+                                                            dir, R, status, kWaitLimitNs, stream));
+        }
+    }
     return from_cuda(ra::launch_ulysses_permute(in, out, B, L, H, D, P, elem_bytes, dir, stream));
 }
 

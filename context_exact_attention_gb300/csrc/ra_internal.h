@@ -93,6 +93,16 @@ cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, c
                          cudaStream_t stream);
 
 // dir = 0: seq2head, dir = 1: head2seq.
+// Copy-engine path of the same transposes: seq_map is the 5-D view {D, H/P, P, L/P, P*B}
+// of the sequence-sharded buffer with box {D, H/P, 1, R, 1} (encoded by the caller),
+// head_side the head-sharded buffer.  Valid when ulysses_permute_tma_fits.
+bool ulysses_permute_tma_fits(int H, int D, int P, int elem_bytes);
+int ulysses_permute_tma_rows(int L, int H, int D, int P, int elem_bytes);
+cudaError_t launch_ulysses_permute_tma(const CUtensorMap& seq_map, void* head_side, int B, int L,
+                                       int H, int D, int P, int elem_bytes, int dir, int R,
+                                       unsigned int* status, unsigned long long timeout_ns,
+                                       cudaStream_t stream);
+
 cudaError_t launch_ulysses_permute(const void* in, void* out, int B, int L, int H, int D, int P,
                                    int elem_bytes, int dir, cudaStream_t stream);
 

@@ -10,6 +10,16 @@
 // and writes are coalesced, and the data is touched once (streaming hints).
 // The grid is one resident wave (occupancy query); index math is 32-bit when
 // the buffer has fewer than 2^31 vectors.
+//
+// The usual shapes (D and H/P up to 256, a run of H/P heads at most 32 KB) take a
+// copy-engine path instead (permute_tma_kernel): for a fixed source rank r and batch
+// b, R consecutive positions of head group g are one box {D, H/P, 1, R, 1} of a 5-D
+// view {D, H/P, P, L/P, P*B} of the sequence-sharded buffer, and one contiguous run of
+// R*H/P*D elements of the head-sharded buffer.  One thread per CTA streams such tiles
+// through four shared-memory stages: a TMA tiled load and a 1-D bulk store (seq ->
+// head), or a bulk load and a TMA tiled store (head -> seq).  The view's row dimension
+// ends at L/P, so a ragged last box reads zeros past the shard and a store of it writes
+// only the shard's rows.
 #include "ra_device.cuh"
 #include "ra_internal.h"
 
@@ -109,7 +119,188 @@ cudaError_t launch_typed(const void* in, void* out, int B, int L, int H, int D, 
     return cudaGetLastError();
 }
 
+// -------------------------------------------------------- copy-engine path --
+
+constexpr int kTStages = 4;
+constexpr int kTStageMax = 32768;     // bytes of one stage (a tile of R rows)
+
+struct TmaPermute {
+    long long n_tiles;       // (P*B) * row blocks * P
+    int n_rblk;              // row blocks per (r, b): ceil(Ls / R)
+    int R;                   // rows per tile (the box's row extent)
+    int P, B, Ls, L;
+    int row_bytes;           // one position's run of H/P heads: H/P * D * elem
+    int stage_bytes;         // R * row_bytes rounded up to 1024
+    unsigned int* status;
+    unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2, int c3, int c4)
+{
+    asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+                 "r"(c4)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// every committed store group but the most recent one has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all_but_one()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// dir 0 (seq -> head): tiled load from the 5-D view, bulk store to the head side.
+// dir 1 (head -> seq): bulk load from the head side, tiled store to the 5-D view.
+template <int kDir>
+__global__ void __launch_bounds__(32, 1)
+    permute_tma_kernel(const __grid_constant__ CUtensorMap seq_map, uint8_t* head, const TmaPermute p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    if (threadIdx.x != 0) return;   // one thread drives every copy of the CTA
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t bars = sbase + kTStages * p.stage_bytes;
+    int* abort_flag = reinterpret_cast<int*>(smem + kTStages * p.stage_bytes + 8 * kTStages);
+    *abort_flag = 0;
+    for (int s = 0; s < kTStages; ++s) mbar_init(bars + 8 * s, 1);
+    fence_mbar_init();
+    const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+    const uint64_t once = l2_policy_evict_first();
+
+    // tile t = (rb * n_rblk + k) * P + g: neighbouring tiles read or write neighbouring
+    // head groups of the same positions on the sequence side
+    auto decode = [&](long long t, int& rb, int& g, int& l0, int& rows, size_t& off) {
+        g = static_cast<int>(t % p.P);
+        const long long rest = t / p.P;
+        const int k = static_cast<int>(rest % p.n_rblk);
+        rb = static_cast<int>(rest / p.n_rblk);
+        l0 = k * p.R;
+        rows = min(p.R, p.Ls - l0);
+        const int r = rb / p.B, b = rb - r * p.B;
+        off = ((static_cast<size_t>(g) * p.B + b) * p.L + static_cast<size_t>(r) * p.Ls + l0) *
+              static_cast<size_t>(p.row_bytes);
+    };
+    auto tile_of = [&](long long j) { return static_cast<long long>(blockIdx.x) + j * gridDim.x; };
+    auto load = [&](long long j) {
+        int rb, g, l0, rows;
+        size_t off;
+        decode(tile_of(j), rb, g, l0, rows, off);
+        const int s = static_cast<int>(j % kTStages);
+        const uint32_t dst = sbase + s * p.stage_bytes;
+        if constexpr (kDir == 0) {
+            mbar_arrive_expect_tx(bars + 8 * s, static_cast<uint32_t>(p.R * p.row_bytes));
+            tma_load_5d(dst, &seq_map, bars + 8 * s, 0, 0, g, l0, rb, once);
+        } else {
+            mbar_arrive_expect_tx(bars + 8 * s, static_cast<uint32_t>(rows * p.row_bytes));
+            bulk_load(dst, head + off, static_cast<uint32_t>(rows * p.row_bytes), bars + 8 * s, once);
+        }
+    };
+    long long n_mine = 0;                       // tiles of this CTA
+    if (blockIdx.x < p.n_tiles) n_mine = (p.n_tiles - 1 - blockIdx.x) / gridDim.x + 1;
+    long long issued = 0;
+    for (; issued < n_mine && issued < kTStages; ++issued) load(issued);
+    long long j = 0;
+    for (; j < n_mine; ++j) {
+        const int s = static_cast<int>(j % kTStages);
+        if (!mbar_wait(bars + 8 * s, static_cast<uint32_t>((j / kTStages) & 1), wc)) break;
+        int rb, g, l0, rows;
+        size_t off;
+        decode(tile_of(j), rb, g, l0, rows, off);
+        const uint32_t src = sbase + s * p.stage_bytes;
+        if constexpr (kDir == 0)
+            bulk_store(head + off, src, static_cast<uint32_t>(rows * p.row_bytes));
+        else
+            tma_store_5d(&seq_map, src, 0, 0, g, l0, rb);
+        bulk_commit();
+        // the previous tile's stage is free once its store has read it: refill it
+        if (j >= 1 && issued < n_mine) {
+            bulk_wait_read_all_but_one();
+            load(issued);
+            ++issued;
+        }
+    }
+    // loads still in flight (only after a timed-out wait, from tile j on) land before
+    // the CTA leaves
+    for (long long x = j; x < issued; ++x)
+        mbar_wait_drain(bars + 8 * static_cast<int>(x % kTStages), static_cast<uint32_t>((x / kTStages) & 1), wc);
+    bulk_wait_all();
+}
+
 }  // namespace
+
+bool ulysses_permute_tma_fits(int H, int D, int P, int elem_bytes)
+{
+    const long long hg = H / P;
+    return D <= 256 && hg <= 256 && hg * D * elem_bytes <= kTStageMax;
+}
+
+int ulysses_permute_tma_rows(int L, int H, int D, int P, int elem_bytes)
+{
+    const int row_bytes = H / P * D * elem_bytes;
+    int R = kTStageMax / row_bytes;
+    if (R > 256) R = 256;
+    if (R > L / P) R = L / P;
+    return R < 1 ? 1 : R;
+}
+
+cudaError_t launch_ulysses_permute_tma(const CUtensorMap& seq_map, void* head_side, int B, int L,
+                                       int H, int D, int P, int elem_bytes, int dir, int R,
+                                       unsigned int* status, unsigned long long timeout_ns,
+                                       cudaStream_t stream)
+{
+    TmaPermute p;
+    p.P = P;
+    p.B = B;
+    p.L = L;
+    p.Ls = L / P;
+    p.R = R;
+    p.n_rblk = (p.Ls + R - 1) / R;
+    p.row_bytes = H / P * D * elem_bytes;
+    p.stage_bytes = (R * p.row_bytes + 1023) & ~1023;
+    p.n_tiles = static_cast<long long>(P) * B * p.n_rblk * P;
+    p.status = status;
+    p.timeout_ns = timeout_ns;
+    constexpr int kSmemMax = kTStages * kTStageMax + 1024 + 8 * kTStages + 16;
+    const int smem = kTStages * p.stage_bytes + 1024 + 8 * kTStages + 16;
+    static int configured[64][2] = {};   // shared memory attribute, once per device and direction
+    int dev = 0, sms = 148;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    auto kern = dir == 0 ? permute_tma_kernel<0> : permute_tma_kernel<1>;
+    if (!configured[dev][dir ? 1 : 0]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+        if (e != cudaSuccess) return e;
+        configured[dev][dir ? 1 : 0] = 1;
+    }
+    long long grid = p.n_tiles < sms ? p.n_tiles : sms;
+    if (grid < 1) grid = 1;
+    kern<<<static_cast<unsigned>(grid), 32, smem, stream>>>(seq_map, static_cast<uint8_t*>(head_side), p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_ulysses_permute(const void* in, void* out, int B, int L, int H, int D, int P,
                                    int elem_bytes, int dir, cudaStream_t stream)

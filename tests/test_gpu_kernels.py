@@ -223,7 +223,10 @@ def test_merge_in_place_and_of_attention_partials():
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("shape", [(4, 2, 64, 8, 16), (8, 1, 128, 32, 128), (2, 3, 30, 6, 8),
-                                   (3, 1, 10, 3, 8)])
+                                   (3, 1, 10, 3, 8),
+                                   (2, 1, 100, 4, 128),     # ragged last row block of a shard
+                                   (4, 2, 300, 8, 64),      # several row blocks, ragged tail
+                                   (2, 1, 16, 2, 512)])     # D > 256: the vector-copy kernel
 def test_permutes_bit_exact(dtype, shape):
     P, B, Ls, H, D = shape
     g = torch.Generator().manual_seed(11)
