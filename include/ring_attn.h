@@ -377,11 +377,13 @@ typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_ZIGZAG = 1, RA_LAYOUT_PACKED 
  *                  ring_attn_fwd_varlen takes it;
  *   dtype          RA_BF16 or RA_F32 for the forward, RA_BF16 for the backward;
  *   schedule       RA_LAYOUT_PACKED only (else NULL): NULL, or the device array that
- *                  ring_attn_varlen_schedule wrote for the same cu_seqlens, L and P.  It
- *                  sets only which CTA takes which work unit (heaviest first instead of
- *                  position order): the results are the same bits either way.  An array
- *                  that is not such a schedule gives undefined results, never
- *                  out-of-bounds accesses.
+ *                  ring_attn_varlen_schedule wrote for the same cu_seqlens, L and P
+ *                  (at least ring_attn_varlen_schedule_bytes(L, P) bytes: the kernels
+ *                  read its entries by unit index, and the descriptor carries no size
+ *                  to check).  It sets only which CTA takes which work unit (heaviest
+ *                  first instead of position order): the results are the same bits
+ *                  either way.  Other contents of an array of that size give undefined
+ *                  results, never out-of-bounds accesses.
  * The descriptor is read during the call only.
  */
 typedef struct {
