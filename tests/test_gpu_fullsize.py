@@ -133,8 +133,13 @@ def test_variants_at_causal_lm_size():
         cu.append(cu[-1] + n)
     q, k, v = (t[0] for t in make_qkv(1, w.L, 8, w.D, seed=7, dtype=torch.bfloat16))
     cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
-    out, lse = cea.ring_attn_fwd_varlen(*(t.to(DEV) for t in (q, k, v)), cu_d, P=w.P, causal=True)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    out, lse = cea.ring_attn_fwd_varlen(qd, kd, vd, cu_d, P=w.P, causal=True)
+    # the heaviest-first schedule changes which CTA takes which unit, not the bits
+    sched = cea.varlen_schedule(cu_d, w.L, w.P, True)
+    out_s, lse_s = cea.ring_attn_fwd_varlen(qd, kd, vd, cu_d, P=w.P, causal=True, schedule=sched)
     assert cea.check_status() == 0
+    assert torch.equal(out, out_s) and torch.equal(lse, lse_s)
     got, lg = to_np(out), to_np(lse)
     for a, b in zip(cu[:-1], cu[1:]):
         pick = [i - a for i in rows if a <= i < b]
@@ -296,7 +301,12 @@ def test_packed_backward_at_causal_lm_size():
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
     out, lse = cea.ring_attn_fwd_varlen(qd, kd, vd, cu_d, P=w.P, causal=True)
     dq, dk, dv = cea.ring_attn_bwd_varlen(qd, kd, vd, out, lse, dod, cu_d, P=w.P, causal=True)
+    sched = cea.varlen_schedule(cu_d, w.L, w.P, True)
+    scheduled = cea.ring_attn_bwd_varlen(qd, kd, vd, out, lse, dod, cu_d, P=w.P, causal=True,
+                                         schedule=sched)
     assert cea.check_status() == 0
+    for a, b in zip((dq, dk, dv), scheduled):
+        assert torch.equal(a, b)
     dqn, dkn, dvn = (t.double().cpu().numpy() for t in (dq, dk, dv))
     qf, kf, vf, dof = (t.double().numpy() for t in (q, k, v, do))
     rows = sample_rows(w.L, w.P, 24, seed=5)
