@@ -23,6 +23,10 @@ computes, and the passage it follows:
   (section 3.5), as byte copies.
 * :func:`attention_bwd` -- gradients dQ, dK, dV of the attention output by the
   chain rule (the backward of sections 3.3 and 6.2, summed on one device).
+* :func:`attention_bwd_dq_rows` / :func:`attention_bwd_dkdv_rows` -- the same
+  gradients for chosen query rows (dq) or key rows (dk, dv) only, for long
+  sequences: a query row needs only its own scores; a key row needs every query's
+  softmax normaliser and row dot, computed first by the naive loops.
 
 Every pin of these routines is in ``tests/test_oracle.py``.
 """
@@ -79,6 +83,10 @@ def _load():
             lib.oracle_attention_bwd_dq_rows.argtypes = [dp, dp, dp, dp, dp, L, L, L, L,
                                                          ctypes.c_int, lp, L, ctypes.c_int]
             lib.oracle_attention_bwd_dq_rows.restype = ctypes.c_int
+            lib.oracle_attention_bwd_dkdv_rows.argtypes = [dp, dp, dp, dp, dp, dp, L, L, L, L,
+                                                           ctypes.c_int, lp, L, dp, dp,
+                                                           ctypes.c_int]
+            lib.oracle_attention_bwd_dkdv_rows.restype = ctypes.c_int
             for name in ("oracle_seq2head", "oracle_head2seq"):
                 fn = getattr(lib, name)
                 fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, L, L, L, L, L, L]
@@ -232,6 +240,35 @@ def attention_bwd_dq_rows(q, k, v, dout, rows, causal: bool = False, threads: in
     if rc != 0:
         raise ValueError(f"oracle_attention_bwd_dq_rows failed ({rc})")
     return out
+
+
+def attention_bwd_dkdv_rows(q, k, v, dout, rows, causal: bool = False,
+                            threads: int | None = None, stats: bool = False):
+    """dk and dv of the listed key rows only: dk_j and dv_j sum over every query that sees
+    key j, so the routine first evaluates the naive forward of every query row (its lse
+    and output O_i, whence the row dot dO_i . O_i), one pass over all query/key pairs,
+    then the listed key rows.  Works at any sequence length.  Returns (dk, dv), each
+    [B, len(rows), H, D]; with stats=True also the per-query lse [B, L, H] and output
+    O [B, L, H, D] it computed on the way."""
+    lib = _load()
+    q, k, v, dout = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    B, L, H, D = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and dout.shape == q.shape
+    rows_a = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    dk = np.empty((B, rows_a.shape[0], H, D), dtype=np.float64)
+    dv = np.empty_like(dk)
+    lse = np.empty((B, L, H), dtype=np.float64) if stats else None
+    o = np.empty((B, L, H, D), dtype=np.float64) if stats else None
+    null = ctypes.POINTER(ctypes.c_double)()
+    rc = lib.oracle_attention_bwd_dkdv_rows(_dp(q), _dp(k), _dp(v), _dp(dout), _dp(dk), _dp(dv),
+                                            B, L, H, D, int(bool(causal)),
+                                            rows_a.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
+                                            rows_a.shape[0], _dp(lse) if stats else null,
+                                            _dp(o) if stats else null,
+                                            threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd_dkdv_rows failed ({rc})")
+    return (dk, dv, lse, o) if stats else (dk, dv)
 
 
 def merge(o_a, lse_a, o_b, lse_b):

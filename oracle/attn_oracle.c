@@ -27,6 +27,10 @@
  *   oracle_seq2head /      Ulysses layout transpose [B, L/P, H, D] per rank
  *   oracle_head2seq        <-> [B, L, H/P, D] per rank ("序列并行与 Ring
  *                          Attention", section 3.5)
+ *   oracle_attention_bwd   gradients dQ, dK, dV by the chain rule (the backward
+ *                          of sections 3.3 and 6.2, summed on one device), and
+ *                          the same for chosen query rows (..._dq_rows) or key
+ *                          rows (..._dkdv_rows) at long sequence lengths
  *
  * Conventions for sets with no visible key (cannot arise under the causal rule
  * j <= i, but can for a merge input): output 0 and lse = -inf, which is the
@@ -527,4 +531,129 @@ int oracle_attention_bwd_dq_rows(const double* q, const double* k, const double*
     long n_items = B * H * n_rows;
     if (n_items == 0) return 0;
     return run_pool(bwd_rows_item, &c, n_items, 2 * L, n_threads);
+}
+
+/* ------------------------------------------------------------------------- */
+/* backward for chosen key rows: dk_j and dv_j sum over every query that      */
+/* sees key j, so they need each such query's softmax normaliser and row dot; */
+/* the naive forward gives both for every query row first, then the key rows  */
+/* are the chain rule's column sums.                                          */
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    double *lse, *rowdot;       /* [B, L, H]: per query row */
+    double* o;                  /* [B, L, H, D]: the attention output of every query row */
+    double *dk, *dv;            /* [B, n_rows, H, D] */
+    long B, L, H, D;
+    int causal;
+    const long* rows;
+    long n_rows;
+} bwd_key_rows_ctx_t;
+
+/* Query row i of (b, h), the stable softmax of section 3.1: lse_i = ln sum_j e^{s_ij}
+ * over the keys it sees (s_ij = q_i . k_j / sqrt(D); causal: j <= i), its output
+ * O_i = sum_j e^{s_ij - lse_i} v_j, and rowdot_i = dO_i . O_i, which equals
+ * sum_j P_ij dP_ij (dP_ij = dO_i . v_j): the term the chain rule subtracts in
+ * dS_ij = P_ij (dP_ij - rowdot_i).  scratch: the row's scores (L). */
+static void query_stats_item(void* vctx, long item, double* scratch)
+{
+    const bwd_key_rows_ctx_t* c = (const bwd_key_rows_ctx_t*)vctx;
+    const long L = c->L, H = c->H, D = c->D;
+    const long i = item % L;
+    const long bh = item / L;
+    const long h = bh % H, b = bh / H;
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+    const long n = c->causal ? i + 1 : L;     /* visible keys 0..n-1 */
+#define AT(t, r) ((t) + ((b * L + (r)) * H + h) * D)
+    double m = -INFINITY;
+    for (long j = 0; j < n; ++j) {
+        double s = 0.0;
+        for (long d = 0; d < D; ++d) s += AT(c->q, i)[d] * AT(c->k, j)[d];
+        scratch[j] = s * inv_sqrt_d;
+        if (scratch[j] > m) m = scratch[j];
+    }
+    double den = 0.0;
+    for (long j = 0; j < n; ++j) den += exp(scratch[j] - m);
+    const double lse = m + log(den);
+    double* o = AT(c->o, i);
+    for (long d = 0; d < D; ++d) o[d] = 0.0;
+    for (long j = 0; j < n; ++j) {
+        const double p = exp(scratch[j] - lse);
+        for (long d = 0; d < D; ++d) o[d] += p * AT(c->v, j)[d];
+    }
+    double rowdot = 0.0;
+    for (long d = 0; d < D; ++d) rowdot += AT(c->dout, i)[d] * o[d];
+    c->lse[(b * L + i) * H + h] = lse;
+    c->rowdot[(b * L + i) * H + h] = rowdot;
+#undef AT
+}
+
+/* Key row j of (b, h):
+ *   dv_j = sum_i P_ij dO_i,   dk_j = sum_i dS_ij q_i / sqrt(D),
+ * over the queries i that see key j (causal: i >= j), with P_ij = e^{s_ij - lse_i}
+ * and dS_ij = P_ij (dO_i . v_j - rowdot_i): the columns of the chain rule that
+ * bwd_item evaluates as whole matrices. */
+static void key_rows_item(void* vctx, long item, double* scratch)
+{
+    (void)scratch;
+    const bwd_key_rows_ctx_t* c = (const bwd_key_rows_ctx_t*)vctx;
+    const long L = c->L, H = c->H, D = c->D;
+    const long rj = item % c->n_rows;
+    const long bh = item / c->n_rows;
+    const long h = bh % H, b = bh / H;
+    const long j = c->rows[rj];
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+#define AT(t, r) ((t) + ((b * L + (r)) * H + h) * D)
+    double* dk = c->dk + ((b * c->n_rows + rj) * H + h) * D;
+    double* dv = c->dv + ((b * c->n_rows + rj) * H + h) * D;
+    for (long d = 0; d < D; ++d) { dk[d] = 0.0; dv[d] = 0.0; }
+    for (long i = c->causal ? j : 0; i < L; ++i) {
+        double s = 0.0, dp = 0.0;
+        for (long d = 0; d < D; ++d) {
+            s += AT(c->q, i)[d] * AT(c->k, j)[d];
+            dp += AT(c->dout, i)[d] * AT(c->v, j)[d];
+        }
+        const long si = (b * L + i) * H + h;
+        const double p = exp(s * inv_sqrt_d - c->lse[si]);
+        const double ds = p * (dp - c->rowdot[si]);
+        for (long d = 0; d < D; ++d) {
+            dv[d] += p * AT(c->dout, i)[d];
+            dk[d] += ds * AT(c->q, i)[d];
+        }
+    }
+    for (long d = 0; d < D; ++d) dk[d] *= inv_sqrt_d;
+#undef AT
+}
+
+/* dk and dv of the listed key rows only: dk_rows, dv_rows [B, n_rows, H, D].  The
+ * per-query pass costs one sweep over all (query, key) pairs; the key rows then cost
+ * O(L D) each, so this works at long sequence lengths.  lse_out [B, L, H] and
+ * o_out [B, L, H, D] (either may be NULL) receive the per-query lse and output the
+ * routine computed on the way. */
+int oracle_attention_bwd_dkdv_rows(const double* q, const double* k, const double* v,
+                                   const double* dout, double* dk_rows, double* dv_rows,
+                                   long B, long L, long H, long D, int causal,
+                                   const long* rows, long n_rows, double* lse_out,
+                                   double* o_out, int n_threads)
+{
+    if (!q || !k || !v || !dout || !dk_rows || !dv_rows || !rows || B < 0 || L <= 0 || H < 0 ||
+        D <= 0 || n_rows < 0)
+        return -1;
+    for (long r = 0; r < n_rows; ++r) if (rows[r] < 0 || rows[r] >= L) return -1;
+    if (B * H * n_rows == 0) return 0;
+    double* stats = (double*)malloc((size_t)(2 * B * L * H) * sizeof(double));
+    double* o = o_out ? o_out : (double*)malloc((size_t)(B * L * H * D) * sizeof(double));
+    if (!stats || !o) {
+        free(stats);
+        if (!o_out) free(o);
+        return -2;
+    }
+    bwd_key_rows_ctx_t c = { q, k, v, dout, stats, stats + B * L * H, o, dk_rows, dv_rows,
+                             B, L, H, D, causal, rows, n_rows };
+    int rc = run_pool(query_stats_item, &c, B * H * L, L, n_threads);
+    if (rc == 0) rc = run_pool(key_rows_item, &c, B * H * n_rows, 0, n_threads);
+    if (rc == 0 && lse_out) memcpy(lse_out, stats, (size_t)(B * L * H) * sizeof(double));
+    free(stats);
+    if (!o_out) free(o);
+    return rc;
 }

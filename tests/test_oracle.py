@@ -481,6 +481,64 @@ def test_backward_dq_rows_match_full_backward(causal):
     np.testing.assert_allclose(part, dq[:, rows], rtol=0, atol=1e-14)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_dkdv_rows_match_full_backward(causal):
+    """The per-key-row dk, dv routine (for long sequences) reproduces the key rows of the
+    full backward, which the finite-difference and autograd pins tie down, and its
+    per-query pass reproduces the forward oracle."""
+    B, L, H, D = 2, 29, 2, 6
+    q, k, v, do = (_rand((B, L, H, D), 110 + i) for i in range(4))
+    _, dk, dv = oracle.attention_bwd(q, k, v, do, causal=causal)
+    rows = [0, 1, 13, 27, 28]
+    pk, pv, lse, o = oracle.attention_bwd_dkdv_rows(q, k, v, do, rows, causal=causal,
+                                                    stats=True)
+    np.testing.assert_allclose(pk, dk[:, rows], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(pv, dv[:, rows], rtol=0, atol=1e-14)
+    # the per-query pass is the naive forward: same output and lse as the forward oracle
+    ref, lref = oracle.attention(q, k, v, causal=causal)
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lref, rtol=0, atol=1e-14)
+
+
+def test_backward_dkdv_rows_match_torch_autograd():
+    """Key rows of fp64 torch autograd of softmax(q k^T / sqrt(D)) v (a library route,
+    independent of both chain-rule routines), causal and not."""
+    torch = pytest.importorskip("torch")
+    B, L, H, D = 1, 41, 3, 8
+    q, k, v, do = (_rand((B, L, H, D), 120 + i) for i in range(4))
+    rows = [0, 7, 20, 39, 40]
+    for causal in (False, True):
+        tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+        s = torch.einsum("bihd,bjhd->bhij", tq, tk) / math.sqrt(D)
+        if causal:
+            s = s.masked_fill(torch.ones(L, L, dtype=torch.bool).triu(1), float("-inf"))
+        o = torch.einsum("bhij,bjhd->bihd", torch.softmax(s, dim=-1), tv)
+        o.backward(torch.tensor(do))
+        pk, pv = oracle.attention_bwd_dkdv_rows(q, k, v, do, rows, causal=causal)
+        np.testing.assert_allclose(pk, tk.grad.numpy()[:, rows], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(pv, tv.grad.numpy()[:, rows], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_dkdv_rows_closed_forms(causal):
+    """With every key row listed: the dv rows sum to the sum of dO over queries (rows of P
+    sum to 1) and the dk rows sum to zero (rows of dS sum to 0); under causal masking the
+    last key is seen by the last query alone, so its dv is that query's dO times its
+    weight on it."""
+    B, L, H, D = 1, 17, 2, 5
+    q, k, v, do = (_rand((B, L, H, D), 130 + i) for i in range(4))
+    pk, pv = oracle.attention_bwd_dkdv_rows(q, k, v, do, list(range(L)), causal=causal)
+    np.testing.assert_allclose(pv.sum(axis=1), do.sum(axis=1), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(pk.sum(axis=1), 0.0, rtol=0, atol=1e-12)
+    if causal:
+        cross = np.cross(pv[0, L - 1, 0, :3], do[0, L - 1, 0, :3])
+        assert np.abs(cross).max() < 1e-12
+        # and its weight is the last query's softmax weight on it, computed by scipy
+        s = q[0, L - 1, 0] @ k[0, :, 0].T / math.sqrt(D)
+        w = scipy.special.softmax(s)[L - 1]
+        np.testing.assert_allclose(pv[0, L - 1, 0], w * do[0, L - 1, 0], rtol=1e-13, atol=1e-14)
+
+
 @pytest.mark.parametrize("Hk", [1, 2])
 @pytest.mark.parametrize("causal", [False, True])
 def test_grouped_backward_matches_finite_differences(Hk, causal):
