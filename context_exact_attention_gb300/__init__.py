@@ -45,7 +45,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_fwd_varlen", "ring_attn_fwd_host", "ring_attn_fwd_host_workspace_bytes",
     "ring_attn_bwd_gqa", "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "ring_attn_fwd_ex",
     "ring_attn_bwd_ex", "ulysses_attention_fused", "ring_attn_varlen_schedule",
-    "ring_attn_varlen_schedule_bytes",
+    "ring_attn_varlen_schedule_bytes", "ra_padded_length",
 )
 
 
@@ -127,6 +127,8 @@ def load_library(build_if_missing: bool = False):
         lib.ring_attn_varlen_schedule_bytes.restype = ctypes.c_ulonglong
         lib.ra_status_string.argtypes = [ctypes.c_int]
         lib.ra_status_string.restype = ctypes.c_char_p
+        lib.ra_padded_length.argtypes = [ctypes.c_longlong, i, i]
+        lib.ra_padded_length.restype = ctypes.c_longlong
         _lib = lib
         return lib
 
@@ -293,9 +295,12 @@ def ring_attn_fwd_zigzag(q, k, v, P: int = 1, out=None, lse=None, want_lse: bool
 def varlen_padded_length(total: int, P: int, multiple: int = 1) -> int:
     """Smallest length >= total that P shards of a multiple of `multiple` rows divide:
     ceil(total / (P * multiple)) * P * multiple (the Ulysses guideline page's
-    padded_seq_len rule, e.g. 3000 tokens, 4 shards, multiple 8 -> 3008)."""
-    step = P * multiple
-    return -(-total // step) * step
+    padded_seq_len rule, e.g. 3000 tokens, 4 shards, multiple 8 -> 3008), computed by
+    the library's ra_padded_length."""
+    n = load_library().ra_padded_length(int(total), int(P), int(multiple))
+    if n < 0:
+        raise ValueError(f"no padded length for total={total}, P={P}, multiple={multiple}")
+    return int(n)
 
 
 def ring_attn_fwd_varlen(q, k, v, cu_seqlens, P: int = 1, causal: bool = False, out=None,

@@ -14,26 +14,19 @@
 namespace {
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s for any single wait
-constexpr int kMaxDevices = 64;
 
 // Status word of each device: bit RA_STATUS_TIMEOUT is set by a kernel whose
 // bounded wait ran out.  Read and cleared by ra_check_status().
 __device__ unsigned int g_status_word;
 
-unsigned int* g_status_ptr[kMaxDevices] = {nullptr};
-std::mutex g_mutex;
-
+// Device address of the current device's status word.  Looked up on every call (a
+// table lookup once the module is loaded): a cached address would go stale if the
+// caller reset the device and the module were loaded again elsewhere.
 ra_status status_word(unsigned int** out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RA_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_status_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return RA_ERR_CUDA;
-        g_status_ptr[dev] = static_cast<unsigned int*>(p);
-    }
-    *out = g_status_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return RA_ERR_CUDA;
+    *out = static_cast<unsigned int*>(p);
     return RA_OK;
 }
 
@@ -616,6 +609,15 @@ ra_status ring_attn_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, in
         return RA_ERR_INVALID_ARG;
     return from_cuda(ra::launch_varlen_schedule(cu_seqlens, n_seqs, L, P, causal, schedule,
                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+long long ra_padded_length(long long total, int P, int multiple)
+{
+    if (total < 0 || P < 1 || multiple < 1) return -1;
+    const long long step = static_cast<long long>(P) * multiple;   // < 2^62: no overflow
+    const long long n = (total + step - 1) / step * step;          // total < 2^63 - step
+    if (total > 0x7fffffffLL || n > 0x7fffffffLL) return -1;
+    return n;
 }
 
 ra_status ra_check_status(ra_stream_t stream)

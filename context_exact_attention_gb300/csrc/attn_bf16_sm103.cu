@@ -803,17 +803,12 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
                      const CUtensorMap& tv)
 {
     using Lay = Layout<D>;
-    static int configured[64] = {0};  // dynamic shared memory attribute, once per device
+    static std::atomic<int> configured[kMaxDevices];  // shared-memory limit set, per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(ring_attn_bf16_kernel<D, kMode>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
-        if (e != cudaSuccess) return e;
-        configured[dev] = 1;
-    }
+    e = smem_limit_once(configured, dev, ring_attn_bf16_kernel<D, kMode>, Lay::kSmem);
+    if (e != cudaSuccess) return e;
     Params p;
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.lse = a.lse;

@@ -1210,20 +1210,14 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     using Lay = BwdLayout<D>;
     constexpr int kSmemKV = KVSmem<D>::kAlloc;
     constexpr int kSmemQ = (4 + kKStages) * Lay::kTileBytes + 256 + 1024;
-    static int configured[64] = {0};
+    static std::atomic<int> configured_kv[kMaxDevices], configured_q[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemKV);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(bwd_dq_kernel<D, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemQ);
-        if (e != cudaSuccess) return e;
-        configured[dev] = 1;
-    }
+    e = smem_limit_once(configured_kv, dev, bwd_dkdv_kernel<D, kMode>, kSmemKV);
+    if (e != cudaSuccess) return e;
+    e = smem_limit_once(configured_q, dev, bwd_dq_kernel<D, kMode>, kSmemQ);
+    if (e != cudaSuccess) return e;
     // Dvec = rowsum(dO o O) into the workspace
     const long long rows = static_cast<long long>(a.B) * a.L * a.H;
     int sms = 148;

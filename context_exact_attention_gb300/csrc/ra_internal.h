@@ -5,9 +5,28 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "ring_attn.h"
 
 namespace ra {
+
+constexpr int kMaxDevices = 64;
+
+// Raises a kernel's dynamic shared-memory limit the first time a device launches it.
+// `done` is one flag per device (static storage: starts at zero).  Safe to call from
+// several host threads at once: the flag is atomic, and the attribute call is
+// idempotent, so two threads that both see the flag clear both make it harmlessly.
+template <typename Kernel>
+cudaError_t smem_limit_once(std::atomic<int>* done, int dev, Kernel kernel, int bytes)
+{
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
+}
 
 // Everything one attention launch needs; validated by the ABI layer.
 struct AttnArgs {

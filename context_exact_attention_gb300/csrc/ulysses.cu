@@ -284,18 +284,16 @@ cudaError_t launch_ulysses_permute_tma(const CUtensorMap& seq_map, void* head_si
     p.timeout_ns = timeout_ns;
     constexpr int kSmemMax = kTStages * kTStageMax + 1024 + 8 * kTStages + 16;
     const int smem = kTStages * p.stage_bytes + 1024 + 8 * kTStages + 16;
-    static int configured[64][2] = {};   // shared memory attribute, once per device and direction
+    // shared-memory limit set, per direction and device
+    static std::atomic<int> configured[2][kMaxDevices];
     int dev = 0, sms = 148;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     auto kern = dir == 0 ? permute_tma_kernel<0> : permute_tma_kernel<1>;
-    if (!configured[dev][dir ? 1 : 0]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-        if (e != cudaSuccess) return e;
-        configured[dev][dir ? 1 : 0] = 1;
-    }
+    e = smem_limit_once(configured[dir ? 1 : 0], dev, kern, kSmemMax);
+    if (e != cudaSuccess) return e;
     long long grid = p.n_tiles < sms ? p.n_tiles : sms;
     if (grid < 1) grid = 1;
     kern<<<static_cast<unsigned>(grid), 32, smem, stream>>>(seq_map, static_cast<uint8_t*>(head_side), p);

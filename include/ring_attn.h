@@ -142,6 +142,19 @@ ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void
                                int P, int causal, ra_dtype dtype, int* trace, ra_stream_t stream);
 
 /*
+ * ra_padded_length -- the pad rule for packed sequences that do not fill a multiple
+ * of P shards ("Finalize Guidelines for Ulysses based context parallel attention",
+ * sections 四 and 六, padded_seq_len): the smallest length >= total that P shards of
+ * a multiple of `multiple` rows each divide,
+ *   ceil(total / (P * multiple)) * P * multiple,
+ * e.g. 3000 tokens over P = 4 shards with multiple 8 -> 3008.  The caller appends
+ * the padding rows to cu_seqlens as one more sequence and ignores its output.
+ * Pure host arithmetic (no device, no stream).  Returns -1 for total < 0, P < 1,
+ * multiple < 1, or a result above 2^31 - 1 (the longest L the kernels take).
+ */
+long long ra_padded_length(long long total, int P, int multiple);
+
+/*
  * ring_attn_fwd_host -- ring_attn_fwd (bf16) on tensors in HOST memory, with the
  * host<->device copies overlapped with the attention (no counterpart on the pages:
  * an addition of this library for callers whose activations live on the host).
@@ -342,9 +355,15 @@ ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
  * Limits and sharing:
  * - B*L*H must not exceed RA_BWD_NOALLOC_MAX_ROWS; larger problems return
  *   RA_ERR_INVALID_ARG without launching anything (use ring_attn_bwd for them).
- * - The array holds 4 MiB on every GPU that loads the library, until exit.
- * - The first call on each device looks up the array's device address (with
- *   that device current); later calls reuse it.
+ * - The array holds 4 MiB on every GPU that loads the library, until exit.  It
+ *   comes into being when the CUDA runtime loads the library's module on a
+ *   device: at context creation under CUDA_MODULE_LOADING=EAGER, otherwise (lazy
+ *   loading, the default) during the first call on that device.  A caller that
+ *   must not allocate after some point should make one call on each device
+ *   before it.
+ * - Every call looks up the array's device address with the device current (a
+ *   table lookup once the module is loaded), so a device reset leaves no stale
+ *   address behind.
  * - All calls on a device share the array; calls whose GPU work overlaps (for
  *   example on different streams) race and must be ordered by the caller.
  *   Nothing in it needs clearing: each call writes every row before reading it.

@@ -101,6 +101,26 @@ def test_varlen_padded_length_rule():
             assert n >= total and n % (2 * P) == 0 and n - total < 2 * P
 
 
+def test_padded_length_through_the_c_abi(lib):
+    """ra_padded_length called through ctypes: the guideline page's example, exact
+    multiples, zero, the largest length the kernels take, and the refused arguments."""
+    f = lib.ra_padded_length
+    f.argtypes = [ctypes.c_longlong, ctypes.c_int, ctypes.c_int]
+    f.restype = ctypes.c_longlong
+    assert f(3000, 4, 8) == 3008
+    assert f(3008, 4, 8) == 3008
+    assert f(0, 4, 8) == 0
+    assert f(32768, 8, 128) == 32768 and f(32769, 8, 128) == 33792
+    assert f(2 ** 31 - 1, 1, 1) == 2 ** 31 - 1
+    assert f(2 ** 31 - 1, 2, 1) == -1                  # would be 2^31: beyond int
+    assert f(2 ** 40, 1, 1) == -1
+    assert f(-1, 4, 8) == -1 and f(10, 0, 8) == -1 and f(10, 4, 0) == -1
+    for total in range(0, 300, 7):
+        for P, m in ((1, 1), (3, 5), (8, 16)):
+            n = f(total, P, m)
+            assert n >= total and n % (P * m) == 0 and n - total < P * m
+
+
 def test_host_entry_argument_errors(lib):
     """ring_attn_fwd_host checks its arguments on the host before touching the runtime."""
     fake = ctypes.c_void_p(1 << 20)
