@@ -10,44 +10,32 @@
 // routine (no cudaMalloc / cudaFree, nothing of torch's).
 //
 // The array: `g_bwd_noalloc_scratch` below, RA_BWD_NOALLOC_MAX_ROWS floats
-// (4 MiB).  Every GPU that loads the library holds it until the process exits.
-// In host code its name is only a host-side stand-in, so the entry point looks
-// up its device address once per device, with that device current, through
-// cudaGetSymbolAddress, and passes that address on.  That lookup happens inside
-// the first call on each device.  Every call on a device shares the one array
-// and leaves its contents behind; nothing in it needs to start at zero, since
-// each call writes every row it later reads.  Calls whose work overlaps on the
-// GPU (for example on two streams) race on the array.
+// (4 MiB).  It comes into being on a device when the CUDA runtime loads this
+// file's module there: at context creation when the process runs with
+// CUDA_MODULE_LOADING=EAGER, otherwise (lazy loading, the default) on the first
+// call on that device.  Its 4 MiB are then held until the process exits.  A
+// caller that must not allocate after some point makes one call on each device
+// before it (or runs with eager loading).
+//
+// In host code the array's name is only a host-side stand-in, so every call
+// looks up its device address through cudaGetSymbolAddress with the device
+// current, and passes that address on.  The lookup is repeated on each call (it
+// is a table lookup once the module is loaded), so a device reset, after which
+// the module may be loaded again at another address, leaves no stale pointer.
+//
+// Every call on a device shares the one array and leaves its contents behind;
+// nothing in it needs to start at zero, since each call writes every row it later
+// reads.  Calls whose work overlaps on the GPU (for example on two streams) race
+// on the array: the caller must order them.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "ring_attn.h"
 
 namespace {
 
 constexpr unsigned long long kMaxRows = RA_BWD_NOALLOC_MAX_ROWS;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_bwd_noalloc_scratch[kMaxRows];
-
-float* g_scratch_dev_ptr[kMaxDevices] = {nullptr};
-std::mutex g_scratch_mutex;
-
-// Device address of the array on the current device (looked up on first use).
-ra_status scratch_on_current_device(float** out)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RA_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_dev_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess) return RA_ERR_CUDA;
-        g_scratch_dev_ptr[dev] = static_cast<float*>(p);
-    }
-    *out = g_scratch_dev_ptr[dev];
-    return RA_OK;
-}
 
 }  // namespace
 
@@ -59,9 +47,9 @@ extern "C" ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const v
     if (B < 1 || L < 1 || H < 1) return RA_ERR_INVALID_ARG;
     const unsigned long long rows = static_cast<unsigned long long>(B) * L * H;
     if (rows > kMaxRows) return RA_ERR_INVALID_ARG;   // larger problems: use ring_attn_bwd
-    float* scratch = nullptr;
-    const ra_status st = scratch_on_current_device(&scratch);
-    if (st != RA_OK) return st;
+    // device address of the array on the current device
+    void* scratch = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_bwd_noalloc_scratch) != cudaSuccess) return RA_ERR_CUDA;
     return ring_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, scratch, kMaxRows * sizeof(float), B,
                          L, H, D, P, causal, stream);
 }
