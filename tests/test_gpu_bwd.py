@@ -22,7 +22,7 @@ import torch
 import context_exact_attention_gb300 as cea
 import oracle
 from context_exact_attention_gb300.workloads import make_qkv
-from helpers import cosine, to_np
+from helpers import BF16_TOL, cosine, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -62,7 +62,10 @@ def _grad_close(got, ref, what, scale):
     err = np.abs(got - ref)
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     worst = (err / (2 * U * (np.abs(ref) + scale) + 1e-6)).max()
-    print(f"{what}: rel_l2 {rel:.2e} cos {cosine(got, ref):.7f} worst/bound {worst:.3f}")
+    # the precision page's bf16 criterion (atol = rtol = 5e-3), reported beside the bound
+    p3 = (err / (BF16_TOL + BF16_TOL * np.abs(ref))).max()
+    print(f"{what}: rel_l2 {rel:.2e} cos {cosine(got, ref):.7f} worst/bound {worst:.3f} "
+          f"p3 ratio {p3:.3f}")
     assert rel <= 4 * U, (what, rel)
     assert cosine(got, ref) > 0.9999, what
     assert worst <= 1.0, (what, worst)

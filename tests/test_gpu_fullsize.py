@@ -10,10 +10,11 @@ import context_exact_attention_gb300 as cea
 import oracle
 from context_exact_attention_gb300.workloads import (DIT, LM, LONG, ULYSSES, make_qkv,
                                                      make_workload_inputs, sample_rows)
-from helpers import assert_bf16_close, to_np
+from helpers import BF16_TOL, assert_bf16_close, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
+U = 2.0 ** -9
 
 
 def _check_rows(w, out, lse, q, k, v, n_rows):
@@ -22,6 +23,47 @@ def _check_rows(w, out, lse, q, k, v, n_rows):
     got = to_np(out[:, rows])
     assert_bf16_close(got, ref, f"{w.name} out")
     assert_bf16_close(to_np(lse[:, rows]), lref, f"{w.name} lse")
+
+
+def _key_rows_close(q, k, v, do, dk, dv, key_rows, q_heads, kv_head, causal, what):
+    """dk and dv of key/value head `kv_head` on the key rows `key_rows`, against the fp64
+    oracle's key-row routine, element by element.  q, do: CPU [L, H, D]; k, v: CPU
+    [L, H_kv, D]; dk, dv: the GPU's [L, H_kv, D] (fp64 numpy), rows in the same order as
+    k.  `q_heads` are the query heads reading this key/value head: the reference is the
+    sum of their per-head gradients (one head: plain attention).
+
+    Bound: the first-order rounding bound of tests/test_gpu_bwd.py, 2u (|ref| + scale) +
+    1e-6 with u = 2^-9, where the scale sums the magnitudes of each element's terms from
+    the oracle's own fp64 quantities (P_ij from its lse, the Dvec error term from its
+    output O): scale(dk_j) = sum_i (|dS_ij| + P_ij sum_d |dO_id O_id|) |q_i| / sqrt(D),
+    scale(dv_j) = sum_i P_ij |dO_i|."""
+    G = len(q_heads)
+    qs, ds = q[None, :, q_heads], do[None, :, q_heads]
+    ks, vs = k[None, :, [kv_head] * G], v[None, :, [kv_head] * G]
+    rk, rv, lse, o = oracle.attention_bwd_dkdv_rows(qs, ks, vs, ds, key_rows, causal=causal,
+                                                    stats=True)
+    ref_k, ref_v = rk[0].sum(axis=1), rv[0].sum(axis=1)          # [n, D]
+    qf, kf, vf, dof = (oracle.to_f64(t)[0] for t in (qs, ks, vs, ds))
+    L, D = qf.shape[0], qf.shape[2]
+    c = 1.0 / np.sqrt(D)
+    sk, sv = np.zeros_like(ref_k), np.zeros_like(ref_v)
+    for g in range(G):
+        rowdot = (dof[:, g] * o[0, :, g]).sum(axis=-1)
+        dvec_abs = np.abs(dof[:, g] * o[0, :, g]).sum(axis=-1)
+        for ri, j in enumerate(key_rows):
+            i0 = j if causal else 0
+            p = np.exp(qf[i0:, g] @ kf[j, g] * c - lse[0, i0:, g])
+            dsij = p * (dof[i0:, g] @ vf[j, g] - rowdot[i0:])
+            sk[ri] += (np.abs(dsij) + p * dvec_abs[i0:]) @ np.abs(qf[i0:, g]) * c
+            sv[ri] += p @ np.abs(dof[i0:, g])
+    for name, got, ref, scale in (("dk", dk[key_rows, kv_head], ref_k, sk),
+                                  ("dv", dv[key_rows, kv_head], ref_v, sv)):
+        assert np.isfinite(got).all(), (what, name)
+        err = np.abs(got - ref)
+        worst = (err / (2 * U * (np.abs(ref) + scale) + 1e-6)).max()
+        p3 = (err / (BF16_TOL + BF16_TOL * np.abs(ref))).max()
+        print(f"{what} {name} key rows: worst/bound {worst:.3f}, p3 criterion ratio {p3:.3f}")
+        assert worst <= 1.0, (what, name, worst)
 
 
 def test_dit_full_attention_40_calls():
@@ -154,8 +196,9 @@ def test_variants_at_causal_lm_size():
 def test_backward_at_causal_lm_size():
     """Backward at the causal-LM size (8 heads): identities that hold at any size -- the
     sum of dv over keys equals the sum of dout over queries, the sum of dk over keys is
-    zero -- within the accumulated bf16 rounding, and dq on sampled rows against the fp64
-    chain rule for those rows (one query row needs only its own scores)."""
+    zero -- within the accumulated bf16 rounding, dq on sampled rows against the fp64
+    chain rule for those rows (one query row needs only its own scores), and dk, dv on
+    sampled key rows of two heads against the oracle's key-row routine."""
     w = LM
     H = 8
     q, k, v = make_qkv(1, w.L, H, w.D, seed=8, dtype=torch.bfloat16, head_scale=True)
@@ -189,13 +232,19 @@ def test_backward_at_causal_lm_size():
             got = dq[0, i, h].double().cpu().numpy()
             r = ref[0, ri, h]
             assert (np.abs(got - r) <= 2 * u * (np.abs(r) + scale) + 1e-6).all(), (i, h)
+    # dk, dv element-wise on sampled key rows (shard edges and seeded rows) of two heads
+    key_rows = sample_rows(w.L, w.P, 24, seed=12)
+    dkn, dvn = (t[0].double().cpu().numpy() for t in (dk, dv))
+    for h in (1, 6):
+        _key_rows_close(q[0], k[0], v[0], do[0], dkn, dvn, key_rows, [h], h, True, f"head {h}")
 
 
 def test_grouped_backward_at_causal_lm_size():
     """Grouped backward at the causal-LM length (8 query heads over 2 key/value heads):
     sum of dv over keys per key/value head equals the sum of dout over queries and the
-    group's query heads, sum of dk over keys is zero, and dq on sampled rows matches the
-    fp64 chain rule through the repeated heads."""
+    group's query heads, sum of dk over keys is zero, dq on sampled rows matches the
+    fp64 chain rule through the repeated heads, and dk, dv of one key/value head on
+    sampled key rows match the oracle summed over the group's query heads."""
     w = LM
     H, Hkv = 8, 2
     G = H // Hkv
@@ -221,6 +270,11 @@ def test_grouped_backward_at_causal_lm_size():
     # relative to each row's largest component: the first-order bound of the plain
     # backward's full-size test, taken conservatively per row
     assert (np.abs(got - ref) <= 4 * u * (np.abs(ref) + scale) + 1e-5).all()
+    # dk, dv of key/value head 1 (the sum over its four query heads) on sampled key rows
+    key_rows = sample_rows(w.L, w.P, 16, seed=13)
+    dkn, dvn = (t[0].double().cpu().numpy() for t in (dk, dv))
+    _key_rows_close(q[0], k[0], v[0], do[0], dkn, dvn, key_rows, list(range(G, 2 * G)), 1, True,
+                    "grouped")
 
 
 def _dq_row_bound(q, k, v, do, i, h, keys, D):
@@ -239,8 +293,9 @@ def _dq_row_bound(q, k, v, do, i, h, keys, D):
 
 def test_zigzag_backward_at_causal_lm_size():
     """Zigzag backward at the causal-LM size (8 heads): the sum identities over all rows,
-    agreement with the contiguous layout's backward after the permutation, and dq on
-    sampled rows against the fp64 chain rule in position order."""
+    agreement with the contiguous layout's backward after the permutation, dq on sampled
+    rows against the fp64 chain rule in position order, and dk, dv on sampled key rows
+    of one head against the oracle's key-row routine in position order."""
     w = LM
     H = 8
     u = 2.0 ** -9
@@ -276,13 +331,20 @@ def test_zigzag_backward_at_causal_lm_size():
             got = dq[0, i, h].double().cpu().numpy()
             r = ref[0, ri, h]
             assert (np.abs(got - r) <= 2 * u * (np.abs(r) + scale) + 1e-6).all(), (i, h)
+    # dk, dv on sampled key rows (zigzag row index -> position) of one head
+    key_rows = sample_rows(w.L, w.P, 16, seed=14)
+    order = np.argsort(pos.numpy())                 # position -> zigzag row
+    dkn, dvn = (t[0, torch.from_numpy(order).to(DEV)].double().cpu().numpy() for t in (dk, dv))
+    _key_rows_close(qg[0], kg[0], vg[0], dog[0], dkn, dvn, pos[key_rows].tolist(), [3], 3, True,
+                    "zigzag head 3")
 
 
 def test_packed_backward_at_causal_lm_size():
     """Packed-sequence backward at the causal-LM length (8 heads, lengths as in the
     forward's full-size test): per sequence, the sum of dv over its keys equals the sum
-    of dout over its queries and the sum of dk is zero; dq on sampled rows of every
-    sequence against the fp64 chain rule of that sequence alone."""
+    of dout over its queries and the sum of dk is zero; dq on sampled rows and dk, dv on
+    sampled key rows (each sequence's first and last among them) of every sequence
+    against the fp64 chain rule of that sequence alone."""
     w = LM
     H = 8
     u = 2.0 ** -9
@@ -324,6 +386,14 @@ def test_packed_backward_at_causal_lm_size():
                 scale = _dq_row_bound(qf, kf, vf, dof, i, h, slice(a, i + 1), w.D)
                 r = ref[0, ri, h]
                 assert (np.abs(dqn[i, h] - r) <= 2 * u * (np.abs(r) + scale) + 1e-6).all(), (i, h)
+    # dk, dv on sampled key rows of every sequence, two heads, that sequence alone
+    key_rows = sample_rows(w.L, w.P, 32, seed=15)
+    for a, b in zip(cu[:-1], cu[1:]):
+        pick = [j - a for j in key_rows if a <= j < b] + [0, b - a - 1]
+        pick = sorted(set(pick))
+        for h in (2, 5):
+            _key_rows_close(q[a:b], k[a:b], v[a:b], do[a:b], dkn[a:b], dvn[a:b], pick, [h], h,
+                            True, f"sequence {a}:{b} head {h}")
 
 
 def test_max_length_forward():
