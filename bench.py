@@ -83,11 +83,16 @@ def _traffic_per_launch():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clock, utilisation, power and throttle reasons while a
+    timed loop runs (every 50 ms).  The summary's sm_mhz is the median over the samples
+    taken under load (GPU utilisation >= 50 %), so idle samples before and after the
+    loop do not enter it; reasons are those seen in any sample."""
 
-    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, uuid=None):
         self.uuid = uuid
@@ -101,20 +106,24 @@ class ClockSampler:
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
-                                          "-lms", "200"], stdout=self.out,
+                                          "-lms", "50"], stdout=self.out,
                                          stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         return self
 
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.out.close()
+
+    @staticmethod
+    def _num(x):
+        return float(x.split()[0])
 
     def summary(self):
         if not self.path:
@@ -123,28 +132,28 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
+                if len(parts) < 11:
                     continue
                 if self.uuid and parts[1] != self.uuid:
                     continue
                 try:
-                    rows.append((float(parts[2].split()[0]), float(parts[3].split()[0]),
-                                 parts[4], parts[5:]))
-                except ValueError:
+                    rows.append({"sm": self._num(parts[2]), "max": self._num(parts[3]),
+                                 "power": self._num(parts[4]), "util": self._num(parts[5]),
+                                 "reasons": [n for n, v in zip(self.REASONS, parts[7:11])
+                                             if v.lower() == "active"]})
+                except (ValueError, IndexError):
                     continue
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                 "sw_power_cap"]
-        reasons = set()
-        for _, _, _, rs in rows:
-            for n, val in zip(names[1:], rs[1:]):
-                if val.lower() == "active":
-                    reasons.add(n)
-        loaded = [r[0] for r in rows]
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "samples": len(rows), "power_w_max": None, "reasons": sorted(reasons)}
+        loaded = [r for r in rows if r["util"] >= 50]
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded) if loaded else None,
+                "sm_mhz_min_under_load": min(r["sm"] for r in loaded) if loaded else None,
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r["power"] for r in rows),
+                "reasons": sorted({n for r in rows for n in r["reasons"]}),
+                "reasons_under_load": sorted({n for r in loaded for n in r["reasons"]})}
 
 
 def _time_loop(fn, steps, stream):
@@ -192,6 +201,95 @@ def cpu_oracle_sample(w, budget_s=15.0, seed=0):
     dt = time.perf_counter() - t0
     fl = _flops_rows(w.L, w.D, w.causal, rows, w.B * w.H)
     return fl / dt / 1e12, dt, len(rows), threads
+
+
+class FwdSample:
+    """Host copies of what the oracle needs to check a few query rows of one forward
+    result: q, k, v of the chosen heads (position order), the query rows (positions),
+    and the GPU's out / lse at those rows.  Evaluated only in the CPU-baseline leg."""
+
+    def __init__(self, q, k, v, rows, out_rows, lse_rows, causal):
+        self.q, self.k, self.v = q, k, v
+        self.rows, self.out, self.lse, self.causal = list(rows), out_rows, lse_rows, causal
+
+    def evaluate(self, oracle):
+        ref, lref = oracle.attention(self.q, self.k, self.v, causal=self.causal, rows=self.rows)
+        return _accuracy(self.out, ref, self.lse, lref)
+
+
+class SegmentsSample:
+    """A packed-sequence result: one FwdSample per sequence (that sequence alone)."""
+
+    def __init__(self, parts):
+        self.parts = parts
+
+    def evaluate(self, oracle):
+        acc = [p.evaluate(oracle) for p in self.parts]
+        return _combine_accuracy(acc)
+
+
+class DqSample:
+    """dq of a few query rows of a backward result (chosen heads), against the oracle's
+    per-row chain rule."""
+
+    def __init__(self, q, k, v, do, rows, dq_rows, causal):
+        self.q, self.k, self.v, self.do = q, k, v, do
+        self.rows, self.dq, self.causal = list(rows), dq_rows, causal
+
+    def evaluate(self, oracle):
+        ref = oracle.attention_bwd_dq_rows(self.q, self.k, self.v, self.do, self.rows,
+                                           causal=self.causal)
+        return _accuracy(self.dq, ref)
+
+
+class MergeSample:
+    """A few rows of an LSE merge and its inputs."""
+
+    def __init__(self, oa, la, ob, lb, oo, lo):
+        self.args, self.oo, self.lo = (oa, la, ob, lb), oo, lo
+
+    def evaluate(self, oracle):
+        ref, lref = oracle.merge(*self.args)
+        return _accuracy(self.oo, ref, self.lo, lref)
+
+
+def _accuracy(got, ref, got_lse=None, ref_lse=None):
+    import numpy as np
+
+    g = got.double().numpy() if hasattr(got, "double") else np.asarray(got, np.float64)
+    r = np.asarray(ref, np.float64).reshape(g.shape)
+    err = np.abs(g - r)
+    res = {"elements": int(g.size), "max_abs": float(err.max()),
+           "p3_ratio": float((err / (5e-3 + 5e-3 * np.abs(r))).max()),
+           "cos": float((g * r).sum() / np.sqrt((g * g).sum() * (r * r).sum()))}
+    if got_lse is not None:
+        gl = got_lse.double().numpy()
+        res["lse_max_abs"] = float(np.abs(gl - np.asarray(ref_lse, np.float64).reshape(gl.shape)).max())
+    return res
+
+
+def _combine_accuracy(parts):
+    res = {"elements": sum(p["elements"] for p in parts),
+           "max_abs": max(p["max_abs"] for p in parts),
+           "p3_ratio": max(p["p3_ratio"] for p in parts),
+           "cos": min(p["cos"] for p in parts)}
+    if all("lse_max_abs" in p for p in parts):
+        res["lse_max_abs"] = max(p["lse_max_abs"] for p in parts)
+    return res
+
+
+def _host(t):
+    return t.detach().to("cpu", copy=True)
+
+
+def _fwd_sample(q, k, v, out, lse, rows, heads, causal, kv_heads=None):
+    """FwdSample of query rows `rows` (position order) of heads `heads` of a [B, L, H, D]
+    result; kv_heads: the key/value heads those query heads read (default: the same)."""
+    kv_heads = heads if kv_heads is None else kv_heads
+    idx = torch.tensor(rows, device=out.device)
+    return FwdSample(_host(q[:, :, heads]), _host(k[:, :, kv_heads]), _host(v[:, :, kv_heads]),
+                     rows, _host(out[:, idx][:, :, heads]), _host(lse[:, idx][:, :, heads]),
+                     causal)
 
 
 def run_reference(args, rank, world):
@@ -273,6 +371,25 @@ def run_gpu(args, rank, world, local_rank):
     ms_step = ms_max / args.steps
     value = flops * world / (ms_step * 1e-3) / 1e12
 
+    # the same step back to back for >= sustained_s seconds: the figure at the power cap
+    # (the short headline loop is a burst figure), with its own clock record
+    sustained = None
+    if args.sustained_s > 0:
+        n_sus = max(args.steps, int(args.sustained_s * 1e3 / ms_step) + 1)
+        with ClockSampler(uuid) as clk2:
+            ms_sus = _time_loop(step, n_sus, stream) / n_sus
+        sustained = {"steps": n_sus, "ms_per_step": ms_sus, "seconds": ms_sus * n_sus / 1e3,
+                     "value": flops / (ms_sus * 1e-3) / 1e12, "clocks": clk2.summary()}
+        if cea.check_status(stream) != 0:
+            raise RuntimeError("kernel reported a device-side timeout in the sustained loop")
+
+    # host copy of the result on sampled rows, checked against the oracle in the
+    # CPU-baseline leg (inputs qc, kc, vc are already on the host)
+    acc_rows = sample_rows(w.L, w.P, args.acc_rows, seed=1)
+    ridx = torch.tensor(acc_rows, device=dev)
+    samples = {"headline": FwdSample(qc, kc, vc, acc_rows, _host(out[:, ridx]), _host(lse[:, ridx]),
+                                     w.causal)}
+
     # -- end to end through the public API: pinned host inputs in, host results out.
     # ring_attn_fwd_host copies head groups in, runs the attention and copies the results
     # back inside the call, overlapping the three; the device workspace is allocated once.
@@ -297,24 +414,41 @@ def run_gpu(args, rank, world, local_rank):
 
     peaks, peak_src = _peaks()
     peak = float(peaks["bf16_tflops"])
+    peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
     achieved = flops / (ms_step * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": _traffic_per_launch(),
                 "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback 1.9 PFLOP/s bf16",
-                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "frac_of_sustained": achieved / peak_sus,
                 "kernel": "ring_attn_bf16_kernel<128>"}
+    if sustained is not None:
+        sustained.update({"unit": "TFLOP/s", "peak": peak_sus,
+                          "frac": sustained["value"] / peak_sus,
+                          "frac_of_burst": sustained["value"] / peak,
+                          "peak_source": f"{peak_src} bf16 sustained (MEASURED_PEAKS.json)"})
 
     rows = {}
     if not args.no_rows and rank == 0:
-        rows = measure_rows(cea, dev, stream, peaks)
+        rows = measure_rows(cea, dev, stream, peaks, samples)
 
     cpu = None
+    accuracy = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, n, threads = cpu_oracle_sample(w, budget_s=args.cpu_budget)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} sampled query rows x {w.B * w.H} heads of the causal-LM workload "
                          f"({dt:.1f} s, fp64)"}
+        # the GPU results on sampled rows against the fp64 oracle (not timed)
+        import oracle
+
+        for name, smp in samples.items():
+            acc = smp.evaluate(oracle)
+            if name == "headline":
+                accuracy = dict(acc, rows=len(acc_rows), heads=w.H,
+                                tolerance="|err| <= 5e-3 + 5e-3 |ref| (p3_ratio <= 1), cos > 0.999")
+            elif name in rows:
+                rows[name]["accuracy"] = acc
 
     if rank == 0:
         line = {
@@ -327,7 +461,8 @@ def run_gpu(args, rank, world, local_rank):
                        "parallelism": f"replicas{world}",
                        "l2": f"inputs {3 * hq.numel() * 2 / 1e6:.0f} MB per step > 129 MB L2 "
                              "(no flush needed)"},
-            "roofline": roofline, "cpu_baseline": cpu,
+            "roofline": roofline, "sustained": sustained, "cpu_baseline": cpu,
+            "accuracy": accuracy,
             "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms,
@@ -340,8 +475,10 @@ def run_gpu(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
-def measure_rows(cea, dev, stream, peaks):
-    """Secondary measurements: every other hot-path row, a few timed repetitions each."""
+def measure_rows(cea, dev, stream, peaks, samples):
+    """Secondary measurements: every other hot-path row, a few timed repetitions each.
+    Each row also leaves in `samples` a host copy of its result on a few sampled rows, for
+    the accuracy check of the CPU-baseline leg."""
     res = {}
     hbm = float(peaks["hbm_gbs"])
     peak = float(peaks["bf16_tflops"])
@@ -360,6 +497,8 @@ def measure_rows(cea, dev, stream, peaks):
                            "tflops": fl * w.repeats / (ms * 1e-3) / 1e12,
                            "frac": fl * w.repeats / (ms * 1e-3) / 1e12 / peak,
                            "note": "inputs 72 MiB fit in L2; back-to-back calls"}
+    samples["dit_full_x40"] = _fwd_sample(q, k, v, out, lse, sample_rows(w.L, w.P, 16, seed=1),
+                                          [0, 13], False)
     del q, k, v, out, lse
 
     # LSE merge at the causal-LM size: two partials of 1,048,576 rows x 128 bf16
@@ -379,6 +518,8 @@ def measure_rows(cea, dev, stream, peaks):
     res["merge_lm_size"] = {"ms": ms, "GB/s": by / (ms * 1e-3) / 1e9,
                             "frac": by / (ms * 1e-3) / 1e9 / hbm, "bytes": by,
                             "note": "working set 805 MB > L2"}
+    pick = torch.randperm(rows, generator=torch.Generator().manual_seed(3))[:64].to(dev)
+    samples["merge_lm_size"] = MergeSample(*(_host(t[pick]) for t in (oa, la, ob, lb, oo, lo)))
     del oa, ob, la, lb, oo, lo
 
     # Ulysses transposes and pipeline
@@ -420,6 +561,13 @@ def measure_rows(cea, dev, stream, peaks):
     res["ulysses_fused"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                             "frac": fl / (ms * 1e-3) / 1e12 / peak,
                             "note": "ulysses_attention_fused: same result, no head-sharded copies"}
+    # position order [B, L, H, D]: position r * L/P + i of batch b is row i of shard r
+    seq_to_pos = lambda t: t.permute(1, 0, *range(2, t.dim())).reshape(w.B, w.L, *t.shape[3:])
+    _, lse_seq = cea.ulysses_attention_fused(qs, ks, vs, w.P, out=o_seq, want_lse=True,
+                                             stream=stream)
+    samples["ulysses_fused"] = _fwd_sample(seq_to_pos(qs), seq_to_pos(ks), seq_to_pos(vs),
+                                           seq_to_pos(o_seq), seq_to_pos(lse_seq),
+                                           sample_rows(w.L, w.P, 16, seed=1), [0, 21], False)
     del x, y, qs, ks, vs, bufs, o_seq
 
     # grouped key/value heads at the headline shape: 32 query heads over 8 key/value heads
@@ -436,6 +584,8 @@ def measure_rows(cea, dev, stream, peaks):
     fl = attention_flops(w.B, w.L, w.H, w.D, True)
     res["lm_gqa_32q_8kv"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                              "frac": fl / (ms * 1e-3) / 1e12 / peak}
+    samples["lm_gqa_32q_8kv"] = _fwd_sample(q, kk, vv, out, lse, sample_rows(w.L, w.P, 16, seed=1),
+                                            [0, 21], True, kv_heads=[0, 5])
     del q, kk, vv, out, lse
 
     # zigzag layout of the headline workload (shard r holds chunks r and 2P-1-r)
@@ -449,6 +599,10 @@ def measure_rows(cea, dev, stream, peaks):
     fl = attention_flops(w.B, w.L, w.H, w.D, True)
     res["lm_zigzag"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                         "frac": fl / (ms * 1e-3) / 1e12 / peak}
+    # zigzag row i holds position pos[i]: position order is the inverse permutation
+    inv = torch.argsort(torch.tensor(cea.zigzag_positions(w.L, w.P))).to(dev)
+    samples["lm_zigzag"] = _fwd_sample(q[:, inv], k[:, inv], v[:, inv], out[:, inv], lse[:, inv],
+                                       sample_rows(w.L, w.P, 16, seed=1), [2, 30], True)
     del q, k, v, out, lse
 
     # packed variable-length sequences filling the headline length (causal)
@@ -479,6 +633,14 @@ def measure_rows(cea, dev, stream, peaks):
                                "frac": fl / (ms * 1e-3) / 1e12 / peak, "n_seqs": len(lengths),
                                "note": "lengths U[256, 8192) packed to 32768 tokens, 32 heads; "
                                        "schedule computed in each step"}
+    picked = sample_rows(w.L, w.P, 32, seed=1)
+    parts = []
+    for a, b in zip(cu[:-1], cu[1:]):
+        sel = sorted({a, b - 1} | {i for i in picked if a <= i < b})
+        sl = slice(a, b)
+        parts.append(_fwd_sample(q[None, sl], k[None, sl], v[None, sl], out[None, sl],
+                                 lse[None, sl], [i - a for i in sel], [4, 17], True))
+    samples["lm_varlen_causal"] = SegmentsSample(parts)
     del q, k, v, out, lse
 
     # backward of the headline workload (dq, dk, dv): algorithmic FLOPs are 2.5x the
@@ -497,6 +659,10 @@ def measure_rows(cea, dev, stream, peaks):
     res["lm_backward"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                           "frac": fl / (ms * 1e-3) / 1e12 / peak,
                           "note": "row dots + dK/dV kernel + dQ kernel; 2.5x forward FLOPs"}
+    brows = sample_rows(w.L, w.P, 12, seed=2)
+    bidx = torch.tensor(brows, device=dev)
+    samples["lm_backward"] = DqSample(*(_host(t[:, :, [3, 26]]) for t in (q, k, v, do)), brows,
+                                      _host(dq[:, bidx][:, :, [3, 26]]), True)
     del q, k, v, do, out, lse, ws, dq, dk, dv
 
     # backward with grouped key/value heads: 32 query heads over 8 key/value heads at the
@@ -515,6 +681,10 @@ def measure_rows(cea, dev, stream, peaks):
     res["lm_gqa_backward"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                               "frac": fl / (ms * 1e-3) / 1e12 / peak,
                               "note": "32 query heads over 8 key/value heads; 2.5x forward FLOPs"}
+    # query heads 3 and 26 read key/value heads 0 and 6
+    samples["lm_gqa_backward"] = DqSample(_host(q[:, :, [3, 26]]), _host(k[:, :, [0, 6]]),
+                                          _host(v[:, :, [0, 6]]), _host(do[:, :, [3, 26]]), brows,
+                                          _host(dq[:, bidx][:, :, [3, 26]]), True)
     del q, k, v, do, out, lse, ws, dq, dk, dv
 
     # backward over zigzag shards (same causal problem and FLOPs as the plain backward)
@@ -531,6 +701,8 @@ def measure_rows(cea, dev, stream, peaks):
     res["lm_zigzag_backward"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                                  "frac": fl / (ms * 1e-3) / 1e12 / peak,
                                  "note": "zigzag shards; 2.5x forward FLOPs"}
+    samples["lm_zigzag_backward"] = DqSample(*(_host(t[:, inv][:, :, [3, 26]]) for t in (q, k, v, do)),
+                                             brows, _host(dq[:, inv][:, bidx][:, :, [3, 26]]), True)
     del q, k, v, do, out, lse, ws, dq, dk, dv
 
     # backward of the packed sequences of the forward row above (same lengths)
@@ -550,6 +722,14 @@ def measure_rows(cea, dev, stream, peaks):
                                  "frac": fl / (ms * 1e-3) / 1e12 / peak, "n_seqs": len(lengths),
                                  "note": "packed sequences of the forward row; 2.5x forward "
                                          "FLOPs; schedule computed in each step"}
+    parts = []
+    for a, b in zip(cu[:-1], cu[1:]):
+        sel = sorted({b - 1} | {i for i in brows if a <= i < b})
+        sl = slice(a, b)
+        sidx = torch.tensor(sel, device=dev)
+        parts.append(DqSample(*(_host(t[None, sl][:, :, [3, 26]]) for t in (q, k, v, do)),
+                              [i - a for i in sel], _host(dq[None, sidx][:, :, [3, 26]]), True))
+    samples["lm_varlen_backward"] = SegmentsSample(parts)
     del q, k, v, do, out, lse, ws, dq, dk, dv, cu_d
 
     # long-context causal
@@ -564,6 +744,8 @@ def measure_rows(cea, dev, stream, peaks):
     fl = attention_flops(w.B, w.L, w.H, w.D, True)
     res["long_causal"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
                           "frac": fl / (ms * 1e-3) / 1e12 / peak}
+    samples["long_causal"] = _fwd_sample(q, k, v, out, lse, sample_rows(w.L, w.P, 16, seed=1),
+                                         [1, 6], True)
     del q, k, v, out, lse
     if cea.check_status(stream) != 0:
         raise RuntimeError("kernel reported a device-side timeout in the secondary rows")
@@ -640,6 +822,10 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--sustained-s", type=float, default=2.0,
+                    help="seconds of the sustained loop after the headline loop (0: skip)")
+    ap.add_argument("--acc-rows", type=int, default=32,
+                    help="sampled query rows (all heads) of the headline accuracy check")
     ap.add_argument("--profile-case", action="store_true",
                     help="headline workload with 8 heads instead of 32 (201 MB of inputs, "
                          "still larger than L2): the small case for profiler captures")

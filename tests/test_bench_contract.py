@@ -53,9 +53,47 @@ def test_timing_rules_are_enforced():
     assert r.returncode != 0 and "warmup" in r.stderr
 
 
+def test_accuracy_samples_report_exact_results_as_exact():
+    """The bench's accuracy samples (evaluated in its CPU-baseline leg) give zero error
+    when handed the oracle's own results, and see a planted error of the right size."""
+    import numpy as np
+    import torch
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from context_exact_attention_gb300.workloads import make_qkv
+
+    B, L, H, D = 1, 96, 3, 16
+    q, k, v = make_qkv(B, L, H, D, seed=4, dtype=torch.bfloat16)
+    rows = [0, 5, 95]
+    ref, lref = oracle.attention(q, k, v, causal=True, rows=rows)
+    got = torch.from_numpy(ref.copy())
+    smp = bench.FwdSample(q, k, v, rows, got, torch.from_numpy(lref.copy()), True)
+    acc = smp.evaluate(oracle)
+    assert acc["max_abs"] == 0 and acc["lse_max_abs"] == 0 and abs(acc["cos"] - 1) < 1e-12
+    bad = got.clone()
+    bad[0, 1, 2, 3] += 0.25
+    acc = bench.FwdSample(q, k, v, rows, bad, torch.from_numpy(lref.copy()), True).evaluate(oracle)
+    assert abs(acc["max_abs"] - 0.25) < 1e-12 and acc["p3_ratio"] > 1
+    both = bench.SegmentsSample([smp, smp]).evaluate(oracle)
+    assert both["elements"] == 2 * got.numel() and both["max_abs"] == 0
+    do = torch.randn(B, L, H, D, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    dref = oracle.attention_bwd_dq_rows(q, k, v, do, rows, causal=True)
+    acc = bench.DqSample(q, k, v, do, rows, torch.from_numpy(dref.copy()), True).evaluate(oracle)
+    assert acc["max_abs"] == 0
+    oa, ob = torch.randn(7, D), torch.randn(7, D)
+    la, lb = torch.randn(7), torch.randn(7)
+    mo, ml = oracle.merge(oa, la, ob, lb)
+    acc = bench.MergeSample(oa, la, ob, lb, torch.from_numpy(np.asarray(mo)),
+                            torch.from_numpy(np.asarray(ml))).evaluate(oracle)
+    assert acc["max_abs"] == 0 and acc["lse_max_abs"] == 0
+
+
 @pytest.mark.gpu
 def test_native_arm_line():
-    r = _run(["--steps", "5", "--warmup", "3", "--no-rows", "--no-cpu-baseline"], 900)
+    r = _run(["--steps", "5", "--warmup", "3", "--no-rows", "--no-cpu-baseline",
+              "--sustained-s", "0.5"], 900)
     assert r.returncode == 0, r.stderr[-3000:]
     d = _last_json(r.stdout)
     _check_common(d, 5, 3)
@@ -68,5 +106,10 @@ def test_native_arm_line():
     assert d["gpu_launches"] >= d["steps"]
     c = d["clocks"]
     assert c["sm_max_mhz"] > 0 and isinstance(c["reasons"], list)
+    assert c["samples"] >= c["samples_under_load"] >= 0
+    su = d["sustained"]
+    assert su["seconds"] >= 0.4 and su["value"] > 0 and su["unit"] == "TFLOP/s"
+    assert abs(su["frac"] - su["value"] / su["peak"]) < 1e-9
+    assert su["clocks"]["samples_under_load"] >= 1
     e = d["e2e"]
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
