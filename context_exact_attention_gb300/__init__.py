@@ -30,12 +30,15 @@ __all__ = [
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libringattn.so")
+_DEBUG_LIB_PATH = os.path.join(_PKG, "libringattn_debug.so")
 _lock = threading.Lock()
 _lib = None
+_debug_lib = None
 
 RA_BF16, RA_F32 = 0, 1
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned",
-           4: "not divisible", 5: "CUDA error", 6: "device-side wait timed out"}
+           4: "not divisible", 5: "CUDA error", 6: "device-side wait timed out",
+           7: "index check of the debug build failed"}
 
 EXPORTED_SYMBOLS = (
     "ring_attn_fwd", "ring_attn_fwd_f32", "ring_attn_fwd_trace", "attn_merge_partials",
@@ -45,7 +48,7 @@ EXPORTED_SYMBOLS = (
     "ring_attn_fwd_varlen", "ring_attn_fwd_host", "ring_attn_fwd_host_workspace_bytes",
     "ring_attn_bwd_gqa", "ring_attn_bwd_zigzag", "ring_attn_bwd_varlen", "ring_attn_fwd_ex",
     "ring_attn_bwd_ex", "ulysses_attention_fused", "ring_attn_varlen_schedule",
-    "ring_attn_varlen_schedule_bytes", "ra_padded_length",
+    "ring_attn_varlen_schedule_bytes", "ra_padded_length", "ra_probe_bounds_check",
 )
 
 
@@ -77,60 +80,76 @@ def load_library(build_if_missing: bool = False):
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(_LIB_PATH):
-            if not build_if_missing:
-                raise RuntimeError(
-                    f"{_LIB_PATH} is missing: build it with "
-                    "`python -c 'import __graft_entry__ as g; g.build()'`")
-            from . import _build
-            _build.build()
-        lib = ctypes.CDLL(_LIB_PATH)
-        vp, i, ll, f_p = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p
-        sigs = {
-            "ring_attn_fwd": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp],
-            "ring_attn_fwd_f32": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp],
-            "ring_attn_fwd_trace": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, vp, vp],
-            "attn_merge_partials": [vp, vp, vp, vp, vp, vp, ll, i, i, vp],
-            "ulysses_seq2head": [vp, vp, i, i, i, i, i, i, vp],
-            "ulysses_head2seq": [vp, vp, i, i, i, i, i, i, vp],
-            "ra_check_status": [vp],
-            "ra_probe_wait_timeout": [ctypes.c_ulonglong, vp],
-            "ring_attn_bwd": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
-                              i, i, i, i, i, i, vp],
-            "ring_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
-            "ring_attn_bwd_gqa": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
-                                  i, i, i, i, i, i, i, vp],
-            "ring_attn_bwd_zigzag": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
-                                     i, i, i, i, i, vp],
-            "ring_attn_bwd_varlen": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
-                                     vp, i, i, i, i, i, i, vp],
-            "ring_attn_fwd_ex": [vp, vp, vp, vp, vp, f_p, vp, vp],
-            "ulysses_attention_fused": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, vp],
-            "ring_attn_bwd_ex": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                 ctypes.c_ulonglong, vp],
-            "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
-            "ring_attn_fwd_zigzag": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp, vp],
-            "ring_attn_fwd_varlen": [vp, vp, vp, vp, f_p, vp, i, i, i, i, i, i, i, vp, vp],
-            "ring_attn_fwd_host": [vp, vp, vp, vp, f_p, vp, ctypes.c_ulonglong, i, i, i, i, i, i,
-                                   i, vp],
-            "ring_attn_varlen_schedule": [vp, i, i, i, i, vp, ctypes.c_ulonglong, vp],
-        }
-        for name, args in sigs.items():
-            fn = getattr(lib, name)
-            fn.argtypes = args
-            fn.restype = ctypes.c_int
-        lib.ring_attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i]
-        lib.ring_attn_fwd_host_workspace_bytes.restype = ctypes.c_ulonglong
-        lib.ring_attn_bwd_workspace_bytes.argtypes = [i, i, i]
-        lib.ring_attn_bwd_workspace_bytes.restype = ctypes.c_ulonglong
-        lib.ring_attn_varlen_schedule_bytes.argtypes = [i, i]
-        lib.ring_attn_varlen_schedule_bytes.restype = ctypes.c_ulonglong
-        lib.ra_status_string.argtypes = [ctypes.c_int]
-        lib.ra_status_string.restype = ctypes.c_char_p
-        lib.ra_padded_length.argtypes = [ctypes.c_longlong, i, i]
-        lib.ra_padded_length.restype = ctypes.c_longlong
-        _lib = lib
-        return lib
+        _lib = _open(_LIB_PATH, build_if_missing, debug_bounds=False)
+        return _lib
+
+
+def load_debug_library(build_if_missing: bool = False):
+    """Load libringattn_debug.so: the same entry points compiled with an index check on
+    every global load and store of the kernels (a failed check is skipped and reported
+    by ra_check_status as status 7).  For tests and debugging, not for speed."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            _debug_lib = _open(_DEBUG_LIB_PATH, build_if_missing, debug_bounds=True)
+        return _debug_lib
+
+
+def _open(path, build_if_missing, debug_bounds):
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(
+                f"{path} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        from . import _build
+        _build.build(debug_bounds=debug_bounds)
+    lib = ctypes.CDLL(path)
+    vp, i, ll, f_p = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p
+    sigs = {
+        "ring_attn_fwd": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp],
+        "ring_attn_fwd_f32": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp],
+        "ring_attn_fwd_trace": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, vp, vp],
+        "attn_merge_partials": [vp, vp, vp, vp, vp, vp, ll, i, i, vp],
+        "ulysses_seq2head": [vp, vp, i, i, i, i, i, i, vp],
+        "ulysses_head2seq": [vp, vp, i, i, i, i, i, i, vp],
+        "ra_check_status": [vp],
+        "ra_probe_wait_timeout": [ctypes.c_ulonglong, vp],
+        "ra_probe_bounds_check": [vp],
+        "ring_attn_bwd": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
+                          i, i, i, i, i, i, vp],
+        "ring_attn_bwd_noalloc": [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp],
+        "ring_attn_bwd_gqa": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
+                              i, i, i, i, i, i, i, vp],
+        "ring_attn_bwd_zigzag": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
+                                 i, i, i, i, i, vp],
+        "ring_attn_bwd_varlen": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong,
+                                 vp, i, i, i, i, i, i, vp],
+        "ring_attn_fwd_ex": [vp, vp, vp, vp, vp, f_p, vp, vp],
+        "ulysses_attention_fused": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, vp],
+        "ring_attn_bwd_ex": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                             ctypes.c_ulonglong, vp],
+        "ring_attn_fwd_gqa": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, i, i, vp],
+        "ring_attn_fwd_zigzag": [vp, vp, vp, vp, f_p, i, i, i, i, i, i, vp, vp],
+        "ring_attn_fwd_varlen": [vp, vp, vp, vp, f_p, vp, i, i, i, i, i, i, i, vp, vp],
+        "ring_attn_fwd_host": [vp, vp, vp, vp, f_p, vp, ctypes.c_ulonglong, i, i, i, i, i, i,
+                               i, vp],
+        "ring_attn_varlen_schedule": [vp, i, i, i, i, vp, ctypes.c_ulonglong, vp],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.ring_attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.ring_attn_fwd_host_workspace_bytes.restype = ctypes.c_ulonglong
+    lib.ring_attn_bwd_workspace_bytes.argtypes = [i, i, i]
+    lib.ring_attn_bwd_workspace_bytes.restype = ctypes.c_ulonglong
+    lib.ring_attn_varlen_schedule_bytes.argtypes = [i, i]
+    lib.ring_attn_varlen_schedule_bytes.restype = ctypes.c_ulonglong
+    lib.ra_status_string.argtypes = [ctypes.c_int]
+    lib.ra_status_string.restype = ctypes.c_char_p
+    lib.ra_padded_length.argtypes = [ctypes.c_longlong, i, i]
+    lib.ra_padded_length.restype = ctypes.c_longlong
+    return lib
 
 
 def _call(name, *args):

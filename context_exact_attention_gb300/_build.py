@@ -17,6 +17,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libringattn.so")
+# the debug build: same sources with every computed global index checked (-DRA_DEBUG_BOUNDS)
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libringattn_debug.so")
 SOURCES = ["api.cu", "attn_bf16_sm103.cu", "attn_bwd_sm103.cu", "attn_f32.cu", "merge.cu",
            "ulysses.cu", "host_pipeline.cu", "bwd_noalloc.cu", "varlen_schedule.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -37,22 +40,28 @@ def _inputs():
     return deps
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug_bounds: bool = False) -> str:
+    """Compile libringattn.so, or with debug_bounds=True libringattn_debug.so (every
+    computed global index checked against its tensor's extent; see ra_check.cuh)."""
+    out_lib, out_dir = (LIB_DEBUG, BUILD_DEBUG) if debug_bounds else (LIB, BUILD)
+    if not force and up_to_date(out_lib):
+        return out_lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug_bounds:
+        extra.append("-DRA_DEBUG_BOUNDS")
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,16 +72,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out_lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":
     import sys
 
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug_bounds="--debug-bounds" in sys.argv))

@@ -242,21 +242,21 @@ ra_status permute_impl(const void* in, void* out, int B, int L, int H, int D, in
     if (!aligned(in, 16) || !aligned(out, 16)) return RA_ERR_MISALIGNED;
     const unsigned long long bytes = n * elem_bytes;
     if (overlap(in, bytes, out, bytes)) return RA_ERR_INVALID_ARG;
+    unsigned int* status = nullptr;
+    const ra_status st = status_word(&status);
+    if (st != RA_OK) return st;
     if (ra::ulysses_permute_tma_fits(H, D, P, elem_bytes)) {
         // copy engines: the sequence-sharded side as a 5-D view {D, H/P, P, L/P, P*B}
         const int R = ra::ulysses_permute_tma_rows(L, H, D, P, elem_bytes);
         CUtensorMap map;
         const void* seq_side = dir == 0 ? in : out;
         void* head_side = dir == 0 ? out : const_cast<void*>(in);
-        if (encode_permute_map(&map, seq_side, B, L, H, D, P, elem_bytes, R)) {
-            unsigned int* status = nullptr;
-            const ra_status st = status_word(&status);
-            if (st != RA_OK) return st;
+        if (encode_permute_map(&map, seq_side, B, L, H, D, P, elem_bytes, R))
             return from_cuda(ra::launch_ulysses_permute_tma(map, head_side, B, L, H, D, P, elem_bytes,
                                                             dir, R, status, kWaitLimitNs, stream));
-        }
     }
-    return from_cuda(ra::launch_ulysses_permute(in, out, B, L, H, D, P, elem_bytes, dir, stream));
+    return from_cuda(
+        ra::launch_ulysses_permute(in, out, B, L, H, D, P, elem_bytes, dir, status, stream));
 }
 
 }  // namespace
@@ -285,6 +285,27 @@ cudaError_t launch_wait_probe(unsigned int* status, unsigned long long timeout_n
                               cudaStream_t stream)
 {
     wait_probe_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+    return cudaGetLastError();
+}
+
+ra_status current_status_word(unsigned int** out) { return status_word(out); }
+
+namespace {
+
+__device__ unsigned int g_bounds_probe_sink;
+
+// One checked access that must fail: index 1 of a one-element extent.  The write it
+// guards goes to a word of this library, so it is harmless even if the check passed.
+__global__ void bounds_probe_kernel(unsigned int* status)
+{
+    if (in_bounds(1, 1, 1, status)) g_bounds_probe_sink = 1u;
+}
+
+}  // namespace
+
+cudaError_t launch_bounds_probe(unsigned int* status, cudaStream_t stream)
+{
+    bounds_probe_kernel<<<1, 1, 0, stream>>>(status);
     return cudaGetLastError();
 }
 
@@ -386,7 +407,10 @@ ra_status attn_merge_partials(const void* o_a, const float* lse_a, const void* o
     if (overlap(o_out, ob, lse_out, lb) || overlap(o_out, ob, lse_a, lb) ||
         overlap(o_out, ob, lse_b, lb))
         return RA_ERR_INVALID_ARG;
-    return from_cuda(ra::launch_merge(o_a, lse_a, o_b, lse_b, o_out, lse_out, rows, D, elem,
+    unsigned int* status = nullptr;
+    const ra_status st = status_word(&status);
+    if (st != RA_OK) return st;
+    return from_cuda(ra::launch_merge(o_a, lse_a, o_b, lse_b, o_out, lse_out, rows, D, elem, status,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -607,7 +631,10 @@ ra_status ring_attn_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, in
     if (schedule_bytes < need) return RA_ERR_INVALID_ARG;
     if (overlap(schedule, need, cu_seqlens, (static_cast<unsigned long long>(n_seqs) + 1) * 4))
         return RA_ERR_INVALID_ARG;
-    return from_cuda(ra::launch_varlen_schedule(cu_seqlens, n_seqs, L, P, causal, schedule,
+    unsigned int* status = nullptr;
+    const ra_status st = status_word(&status);
+    if (st != RA_OK) return st;
+    return from_cuda(ra::launch_varlen_schedule(cu_seqlens, n_seqs, L, P, causal, schedule, status,
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -632,7 +659,8 @@ ra_status ra_check_status(ra_stream_t stream)
         return RA_ERR_CUDA;
     if (value == 0) return RA_OK;
     if (cudaMemset(word, 0, sizeof(value)) != cudaSuccess) return RA_ERR_CUDA;
-    return (value & RA_STATUS_TIMEOUT) ? RA_ERR_TIMEOUT : RA_ERR_CUDA;
+    if (value & RA_STATUS_TIMEOUT) return RA_ERR_TIMEOUT;
+    return (value & RA_STATUS_BOUNDS) ? RA_ERR_BOUNDS : RA_ERR_CUDA;
 }
 
 const char* ra_status_string(ra_status status)
@@ -645,8 +673,18 @@ const char* ra_status_string(ra_status status)
     case RA_ERR_NOT_DIVISIBLE: return "sequence (or head) count not divisible by P";
     case RA_ERR_CUDA: return "CUDA error";
     case RA_ERR_TIMEOUT: return "a device-side wait ran out of time";
+    case RA_ERR_BOUNDS: return "an index check of the debug build failed (access skipped)";
     }
     return "unknown status";
+}
+
+ra_status ra_probe_bounds_check(ra_stream_t stream)
+{
+    if (!ra::kCheckBounds) return RA_ERR_UNSUPPORTED;
+    unsigned int* word = nullptr;
+    ra_status st = status_word(&word);
+    if (st != RA_OK) return st;
+    return from_cuda(ra::launch_bounds_probe(word, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ra_status ra_probe_wait_timeout(unsigned long long timeout_ns, ra_stream_t stream)

@@ -101,6 +101,8 @@ struct Params {
     int n_kt;        // K/V blocks per shard
     int n_pair;      // query-tile pairs per shard
     float scale_log2;
+    long long out_elems, lse_elems;   // extents for the debug build's index checks
+    int sched_elems;                  // entries of the schedule's forward order
 };
 
 // Global position of local row i of shard `shard`.  Contiguous layout: shard r
@@ -247,16 +249,16 @@ struct ZigzagSched {
 // only keys of its own sequence (and, causal, not after itself).  Returns the
 // first and last visible key position of the query at `pos`.
 __device__ __forceinline__ void seq_bounds(const int* cu, int n_seqs, int pos, int causal, int& lo,
-                                           int& hi)
+                                           int& hi, unsigned int* status)
 {
     int a = 0, b = n_seqs;                       // invariant: cu[a] <= pos < cu[b]
     while (b - a > 1) {
         const int mid = (a + b) >> 1;
-        if (__ldg(cu + mid) <= pos) a = mid;
+        if (checked_ldg(cu, mid, n_seqs + 1, status) <= pos) a = mid;
         else b = mid;
     }
-    lo = __ldg(cu + a);
-    hi = causal ? pos : __ldg(cu + a + 1) - 1;
+    lo = checked_ldg(cu, a, n_seqs + 1, status);
+    hi = causal ? pos : checked_ldg(cu, a + 1, n_seqs + 1, status) - 1;
 }
 
 // Packed-sequence schedule: ring order as always; of shard s the key tiles that
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a precomputed order (entries outside the unit range are ignored) puts the
         // heaviest units first
         if (p.schedule != nullptr) {
-            const int x = __ldg(p.schedule + u);
+            const int x = checked_ldg(p.schedule, u, p.sched_elems, p.status);
             if (static_cast<unsigned>(x) < static_cast<unsigned>(units_per_bh)) {
                 r = x / p.n_pair;
                 pair = x - r * p.n_pair;
@@ -380,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // visible positions of the pair: from the first row's sequence start to the
             // last row's (causal) position or sequence end
             int lo0, hi0, lo1, hi1;
-            seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + q0_local, p.causal, lo0, hi0);
-            seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + last, p.causal, lo1, hi1);
+            seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + q0_local, p.causal, lo0, hi0, p.status);
+            seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + last, p.causal, lo1, hi1, p.status);
             walk.init(r, p.P, p.n_kt, p.Ls, lo0, hi1);
         } else if constexpr (kZig) {
             // last query position of the pair (positions rise within each chunk, and
@@ -469,13 +471,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the shard's last query pair meets every shard the shard visits, in either layout
         const bool tracing = p.trace != nullptr && bh == 0 && pair == p.n_pair - 1;
         if (tracing && leader)
-            for (int t = 0; t < p.P; ++t) p.trace[r * p.P + t] = -1;
+            for (int t = 0; t < p.P; ++t)
+                if (in_bounds(r * p.P + t, 1, p.P * p.P, p.status)) p.trace[r * p.P + t] = -1;
         const uint64_t keep = l2_policy_evict_last();    // K/V: read by every tile pair of the head
         // Q0, Q1 (read once) and K0 were issued by thread 0 before the block-wide barrier
         int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
         for (int n = 0; n < n_blocks; ++n) {
             walk.at(n);
-            if (tracing && walk.first_of_shard() && leader) p.trace[r * p.P + walk.t] = walk.s;
+            if (tracing && walk.first_of_shard() && leader &&
+                in_bounds(r * p.P + walk.t, 1, p.P * p.P, p.status))
+                p.trace[r * p.P + walk.t] = walk.s;
             const int st = n & 1;
             const uint32_t ph = (n >> 1) & 1;
             const int row = walk.s * p.Ls + walk.kt() * kKeys;   // physical row of the tile
@@ -555,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             return __all_sync(0xffffffffu, mbar_wait(bar(idx), parity, wc));
         };
 
-        bool ok = wait_all(kBarQ, 0) && wait_all(kBarKFull + 0, 0);
+        // an empty walk (possible only with malformed sequence boundaries) issues nothing
+        bool ok = n_blocks > 0 && wait_all(kBarQ, 0) && wait_all(kBarKFull + 0, 0);
         if (ok) {
             tc_fence_after();
             if (leader) {
@@ -637,7 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_pos = position(r, row_local, p.P, p.Ls, kZig ? 1 : 0);
         int seq_lo = 0, seq_hi = 0;                            // packed sequences only
         if constexpr (kVarlen) {
-            if (row_local < p.Ls) seq_bounds(p.cu_seqlens, p.n_seqs, row_pos, p.causal, seq_lo, seq_hi);
+            if (row_local < p.Ls)
+                seq_bounds(p.cu_seqlens, p.n_seqs, row_pos, p.causal, seq_lo, seq_hi, p.status);
             else seq_hi = -1;
         }
         const float sl2 = p.scale_log2;
@@ -731,12 +738,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = m_ref;
         }
 
+        // an empty walk leaves O unwritten: its rows saw no key and get 0 and -inf.  The
+        // staging below reuses the tile's query buffer, so its load must have landed.
+        const bool empty = n_blocks == 0;
         if (ok) {
-            ok = mbar_wait(bar(kBarOFull + tq), 0, wc);
+            ok = empty ? mbar_wait(bar(tq == 0 ? kBarQ : kBarQ1), 0, wc)
+                       : mbar_wait(bar(kBarOFull + tq), 0, wc);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
-            tc_fence_after();
+            if (!empty) tc_fence_after();
             const bool valid = row_local < p.Ls;
             const float inv_l = l > 0.f ? 1.f / l : 0.f;        // a row that saw no key: 0
             // index of (row, head) among the output's rows of D elements, for this warp's
@@ -761,8 +772,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* stage = smem + Lay::kQ + tq * Lay::kTileBytes + quarter * 32 * (2 * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + 32 * c, o);
+                uint32_t o[32] = {};
+                if (!empty) tmem_ld32(tO + 32 * c, o);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -782,11 +793,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int rr = k * kRowsPerStore + sub;         // row within the warp's 32
                     const uint4 val = *reinterpret_cast<const uint4*>(
                         stage + rr * (2 * D) + ((cc ^ (rr & (kChunks - 1))) * 16));
-                    if (x0 + rr < p.Ls)
-                        *reinterpret_cast<uint4*>(p.out + (orow0 + rr * ostride) * D + cc * 8) = val;
+                    const long long idx = static_cast<long long>(orow0 + rr * ostride) * D + cc * 8;
+                    if (x0 + rr < p.Ls && in_bounds(idx, 8, p.out_elems, p.status))
+                        *reinterpret_cast<uint4*>(p.out + idx) = val;
                 }
             }
-            if (valid && p.lse != nullptr)
+            if (valid && p.lse != nullptr &&
+                in_bounds(static_cast<long long>(orow0 + lane * ostride), 1, p.lse_elems, p.status))
                 p.lse[orow0 + lane * ostride] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
     }
@@ -832,6 +845,11 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     p.n_kt = (p.Ls + kKeys - 1) / kKeys;
     p.n_pair = (p.n_kt + kTiles - 1) / kTiles;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    // the kernel's B and H count head-group batches and heads; the element count of out
+    // and lse is the same in the Ulysses view
+    p.out_elems = static_cast<long long>(a.B) * a.L * a.H * D;
+    p.lse_elems = static_cast<long long>(a.B) * a.L * a.H;
+    p.sched_elems = static_cast<int>(a.P * p.n_pair);
     const long long grid = static_cast<long long>(a.B) * a.H * a.P * p.n_pair;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     ring_attn_bf16_kernel<D, kMode><<<static_cast<unsigned>(grid), kThreads, Lay::kSmem, a.stream>>>(

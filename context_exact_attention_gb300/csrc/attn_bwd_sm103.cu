@@ -75,6 +75,10 @@ struct BwdParams {
     int n_seqs;
     const int* sched_k;      // packed sequences: key tiles heaviest first (s * n_t + kt), or null
     const int* sched_q;      // packed sequences: query tiles heaviest first (r * n_t + qt), or null
+    // extents for the debug build's index checks: dq (and q, dout), dk and dv, lse and
+    // dvec, each schedule order
+    long long q_elems, kv_elems, row_elems;
+    int sched_elems;
 };
 
 // ------------------------------------------------------- shard layouts --
@@ -97,16 +101,17 @@ __device__ __forceinline__ int layout_position(int x, int i, int Ls, int P, bool
 // First and last position of the packed sequence that holds position pos
 // (cu: n_seqs starts, then the total; cu[a] <= pos < cu[a+1] for exactly one
 // non-empty sequence a).
-__device__ __forceinline__ void seq_range(const int* cu, int n_seqs, int pos, int& first, int& last)
+__device__ __forceinline__ void seq_range(const int* cu, int n_seqs, int pos, int& first, int& last,
+                                          unsigned int* status)
 {
     int a = 0, b = n_seqs;
     while (b - a > 1) {
         const int mid = (a + b) >> 1;
-        if (__ldg(cu + mid) <= pos) a = mid;
+        if (checked_ldg(cu, mid, n_seqs + 1, status) <= pos) a = mid;
         else b = mid;
     }
-    first = __ldg(cu + a);
-    last = __ldg(cu + a + 1) - 1;
+    first = checked_ldg(cu, a, n_seqs + 1, status);
+    last = checked_ldg(cu, a + 1, n_seqs + 1, status) - 1;
 }
 
 // Ring walk over the 128-row tiles that hold positions in [lo, hi]: at step t the
@@ -211,14 +216,16 @@ __device__ __forceinline__ void zigzag_tile_at(int g, int P, int n_t, int& shard
 // Zero rows [row0, row0 + n) of a [B, L, heads, D] bf16 tensor's head `head` (gradients of
 // a tile that no pair reaches: possible only with malformed sequence boundaries).
 template <int D>
-__device__ void zero_tile_rows(__nv_bfloat16* t, int b, int L, int heads, int head, int row0, int n)
+__device__ void zero_tile_rows(__nv_bfloat16* t, int b, int L, int heads, int head, int row0, int n,
+                               long long extent, unsigned int* status)
 {
     constexpr int kVec = D / 8;     // 16-byte vectors per row
     for (int i = threadIdx.x; i < n * kVec; i += blockDim.x) {
         const int row = row0 + i / kVec;
-        uint4* dst = reinterpret_cast<uint4*>(
-            t + ((static_cast<size_t>(b) * L + row) * heads + head) * static_cast<size_t>(D));
-        dst[i % kVec] = make_uint4(0u, 0u, 0u, 0u);
+        const long long idx =
+            ((static_cast<long long>(b) * L + row) * heads + head) * D + (i % kVec) * 8;
+        if (in_bounds(idx, 8, extent, status))
+            *reinterpret_cast<uint4*>(t + idx) = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -243,10 +250,12 @@ __device__ __forceinline__ void stage_row_chunks(uint8_t* stage, int lane, int f
     }
 }
 
-// Rows 0..31 of the slice to dst + row * stride (elements), rows < n_valid only.
+// Rows 0..31 of the slice to base + off0 + row * stride (elements), rows < n_valid only;
+// extent: elements of the tensor at base (checked in the debug build).
 template <int kCols>
-__device__ __forceinline__ void store_staged_rows(const uint8_t* stage, int lane, __nv_bfloat16* dst,
-                                                  size_t stride, int n_valid)
+__device__ __forceinline__ void store_staged_rows(const uint8_t* stage, int lane, __nv_bfloat16* base,
+                                                  long long off0, long long stride, int n_valid,
+                                                  long long extent, unsigned int* status)
 {
     constexpr int kChunks = kCols / 8;
     constexpr int kRowsPerStore = 32 / kChunks;
@@ -256,7 +265,9 @@ __device__ __forceinline__ void store_staged_rows(const uint8_t* stage, int lane
         const int rr = k * kRowsPerStore + sub;
         const uint4 val = *reinterpret_cast<const uint4*>(stage + rr * (2 * kCols) +
                                                           ((cc ^ (rr & (kChunks - 1))) * 16));
-        if (rr < n_valid) *reinterpret_cast<uint4*>(dst + rr * stride + cc * 8) = val;
+        const long long idx = off0 + rr * stride + cc * 8;
+        if (rr < n_valid && in_bounds(idx, 8, extent, status))
+            *reinterpret_cast<uint4*>(base + idx) = val;
     }
 }
 
@@ -265,7 +276,7 @@ __device__ __forceinline__ void store_staged_rows(const uint8_t* stage, int lane
 template <int D>
 __global__ void __launch_bounds__(256)
     bwd_rowdot_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                      float* __restrict__ dvec, long long rows)
+                      float* __restrict__ dvec, long long rows, unsigned int* status)
 {
     constexpr int kLanes = D / 8;
     constexpr int kRowsPerWarp = 32 / kLanes;
@@ -276,7 +287,7 @@ __global__ void __launch_bounds__(256)
     for (long long base = warp_global * kRowsPerWarp; base < rows; base += n_warps * kRowsPerWarp) {
         const long long row = base + lane / kLanes;
         float acc = 0.f;
-        if (row < rows) {
+        if (row < rows && in_bounds(row * kLanes + sub, 1, rows * kLanes, status)) {
             const uint4 a = o[row * kLanes + sub];
             const uint4 g = dout[row * kLanes + sub];
             const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(256)
         }
 #pragma unroll
         for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (row < rows && sub == 0) dvec[row] = acc;
+        if (row < rows && sub == 0 && in_bounds(row, 1, rows, status)) dvec[row] = acc;
     }
 }
 
@@ -392,7 +403,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         // packed sequences: a precomputed heaviest-first order, if given (entries outside
         // the unit range are ignored)
         if (p.sched_k != nullptr) {
-            const int x = __ldg(p.sched_k + u);
+            const int x = checked_ldg(p.sched_k, u, p.sched_elems, p.status);
             if (static_cast<unsigned>(x) < static_cast<unsigned>(units_per_bh)) {
                 s = x / p.n_t;
                 kt = x - s * p.n_t;
@@ -418,8 +429,8 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         if constexpr (kMode == 2) {
             const int kp1 = s * p.Ls + min(p.Ls - 1, kt * kRows + kRows - 1);
             int f0, l0, f1, l1;
-            seq_range(p.cu_seqlens, p.n_seqs, kp0, f0, l0);
-            seq_range(p.cu_seqlens, p.n_seqs, kp1, f1, l1);
+            seq_range(p.cu_seqlens, p.n_seqs, kp0, f0, l0, p.status);
+            seq_range(p.cu_seqlens, p.n_seqs, kp1, f1, l1, p.status);
             lo = p.causal ? kp0 : f0;
             hi = l1;
         }
@@ -427,8 +438,8 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         n_head = walk.total();
         if (n_head == 0) {          // every key of a tile sees at least its own query
             const int n = min(kRows, p.Ls - kt * kRows);
-            zero_tile_rows<D>(p.dk, b, p.L, p.Hkv, hk, key0, n);
-            zero_tile_rows<D>(p.dv, b, p.L, p.Hkv, hk, key0, n);
+            zero_tile_rows<D>(p.dk, b, p.L, p.Hkv, hk, key0, n, p.kv_elems, p.status);
+            zero_tile_rows<D>(p.dv, b, p.L, p.Hkv, hk, key0, n, p.kv_elems, p.status);
             return;
         }
     }
@@ -638,8 +649,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int c = lane + 32 * j;
-                const size_t idx = (static_cast<size_t>(b) * p.L + qrow + c) * p.H + h;
-                v[j] = (qt * kRows + c < p.Ls) ? src[idx] * mul : 0.f;
+                const long long idx = (static_cast<long long>(b) * p.L + qrow + c) * p.H + h;
+                v[j] = (qt * kRows + c < p.Ls && in_bounds(idx, 1, p.row_elems, p.status))
+                           ? src[idx] * mul : 0.f;
             }
             info = make_int2(layout_position(r, qt * kRows, p.Ls, p.P, kZig),
                              min(kRows, p.Ls - qt * kRows));
@@ -692,7 +704,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
             if (p.causal || kZig) vis_lo = kp;
             if constexpr (kMode == 2) {
                 int f, l;
-                seq_range(p.cu_seqlens, p.n_seqs, kp, f, l);
+                seq_range(p.cu_seqlens, p.n_seqs, kp, f, l, p.status);
                 if (!p.causal) vis_lo = f;
                 vis_hi = l;
             }
@@ -797,9 +809,11 @@ __global__ void __launch_bounds__(kKVThreads, 1)
             }
             __syncwarp();
             const int krow0 = kt * kRows + quarter * 32;      // within shard s
-            __nv_bfloat16* dst = (which ? p.dk : p.dv) +
-                                 ((static_cast<size_t>(b) * p.L + s * p.Ls + krow0) * p.Hkv + hk) * D + col0;
-            store_staged_rows<D / 2>(stage, lane, dst, static_cast<size_t>(p.Hkv) * D, p.Ls - krow0);
+            const long long off0 =
+                ((static_cast<long long>(b) * p.L + s * p.Ls + krow0) * p.Hkv + hk) * D + col0;
+            store_staged_rows<D / 2>(stage, lane, which ? p.dk : p.dv, off0,
+                                     static_cast<long long>(p.Hkv) * D, p.Ls - krow0, p.kv_elems,
+                                     p.status);
         }
     }
 
@@ -865,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if constexpr (kMode == 2) {
         if (p.sched_q != nullptr) {
-            const int x = __ldg(p.sched_q + u);
+            const int x = checked_ldg(p.sched_q, u, p.sched_elems, p.status);
             if (static_cast<unsigned>(x) < static_cast<unsigned>(units_per_bh)) {
                 r = x / p.n_t;
                 qt = x - r * p.n_t;
@@ -899,15 +913,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int lo = 0, hi = qp1;
         if constexpr (kMode == 2) {
             int f0, l0, f1, l1;
-            seq_range(p.cu_seqlens, p.n_seqs, qp0, f0, l0);
-            seq_range(p.cu_seqlens, p.n_seqs, qp1, f1, l1);
+            seq_range(p.cu_seqlens, p.n_seqs, qp0, f0, l0, p.status);
+            seq_range(p.cu_seqlens, p.n_seqs, qp1, f1, l1, p.status);
             lo = f0;
             if (!p.causal) hi = l1;
         }
         walk.init(r, -1, p.P, p.Ls, kZig ? 1 : 0, lo, hi);
         n_blocks = walk.total();
         if (n_blocks == 0) {        // every query of a tile sees at least its own key
-            zero_tile_rows<D>(p.dq, b, p.L, p.H, h, q0, min(kRows, p.Ls - q_local0));
+            zero_tile_rows<D>(p.dq, b, p.L, p.H, h, q0, min(kRows, p.Ls - q_local0), p.q_elems,
+                              p.status);
             return;
         }
     }
@@ -1098,9 +1113,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int row_local = q_local0 + row;
         const bool row_valid = row_local < p.Ls;
-        const size_t sidx = (static_cast<size_t>(b) * p.L + q0 + row) * p.H + h;
-        const float nl2 = row_valid ? -p.lse[sidx] * kLog2e : 0.f;
-        const float ndv = row_valid ? -p.dvec[sidx] : 0.f;
+        const long long sidx = (static_cast<long long>(b) * p.L + q0 + row) * p.H + h;
+        const bool stats_ok = row_valid && in_bounds(sidx, 1, p.row_elems, p.status);
+        const float nl2 = stats_ok ? -p.lse[sidx] * kLog2e : 0.f;
+        const float ndv = stats_ok ? -p.dvec[sidx] : 0.f;
         const uint64_t nl2x2 = f2pack(nl2, nl2);
         const uint64_t ndvx2 = f2pack(ndv, ndv);
         const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
@@ -1112,7 +1128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.causal || kZig) vis_hi = qp;
             if constexpr (kMode == 2) {
                 int f, l;
-                seq_range(p.cu_seqlens, p.n_seqs, qp, f, l);
+                seq_range(p.cu_seqlens, p.n_seqs, qp, f, l, p.status);
                 vis_lo = f;
                 if (!p.causal) vis_hi = l;
             }
@@ -1190,9 +1206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             const int qrow0 = q_local0 + quarter * 32;        // within shard r
-            __nv_bfloat16* dst = p.dq + ((static_cast<size_t>(b) * p.L + r * p.Ls + qrow0) * p.H + h) * D +
-                                 half * (D / 2);
-            store_staged_rows<D / 2>(stage, lane, dst, static_cast<size_t>(p.H) * D, p.Ls - qrow0);
+            const long long off0 =
+                ((static_cast<long long>(b) * p.L + r * p.Ls + qrow0) * p.H + h) * D + half * (D / 2);
+            store_staged_rows<D / 2>(stage, lane, p.dq, off0, static_cast<long long>(p.H) * D,
+                                     p.Ls - qrow0, p.q_elems, p.status);
         }
     }
 
@@ -1226,7 +1243,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
     if (blocks < 1) blocks = 1;
     bwd_rowdot_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
-        static_cast<const uint4*>(a.out), static_cast<const uint4*>(a.dout), a.dvec, rows);
+        static_cast<const uint4*>(a.out), static_cast<const uint4*>(a.dout), a.dvec, rows, a.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -1252,6 +1269,10 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     p.cu_seqlens = a.cu_seqlens;
     p.n_seqs = a.n_seqs;
     p.sched_k = p.sched_q = nullptr;
+    p.q_elems = static_cast<long long>(a.B) * a.L * a.H * D;
+    p.kv_elems = static_cast<long long>(a.B) * a.L * a.Hkv * D;
+    p.row_elems = static_cast<long long>(a.B) * a.L * a.H;
+    p.sched_elems = a.P * p.n_t;
     if (a.schedule != nullptr) {
         const VarlenSchedLayout lay = varlen_sched_layout(a.L, a.P);
         p.sched_k = a.schedule + lay.bwd_k;

@@ -49,8 +49,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                          const float* __restrict__ v, float* __restrict__ out,
                          float* __restrict__ lse, int* __restrict__ trace, int B, int L, int H,
                          int Hkv, int D, int P, int causal, int zig, const int* cu_seqlens,
-                         int n_seqs, float scale)
+                         int n_seqs, float scale, unsigned int* status)
 {
+    // extents of q/out and k/v (elements) for the debug build's index checks
+    const long long q_elems = static_cast<long long>(B) * L * H * D;
+    const long long kv_elems = static_cast<long long>(B) * L * Hkv * D;
     __shared__ float qs[kWarps][kMaxD];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -71,15 +74,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         int a = 0, bb = n_seqs;
         while (bb - a > 1) {
             const int mid = (a + bb) >> 1;
-            if (cu_seqlens[mid] <= q_pos) a = mid;
+            if (checked_ldg(cu_seqlens, mid, n_seqs + 1, status) <= q_pos) a = mid;
             else bb = mid;
         }
-        lo = cu_seqlens[a];
-        hi = causal ? q_pos : cu_seqlens[a + 1] - 1;
+        lo = checked_ldg(cu_seqlens, a, n_seqs + 1, status);
+        hi = causal ? q_pos : checked_ldg(cu_seqlens, a + 1, n_seqs + 1, status) - 1;
     }
     const size_t row_stride = static_cast<size_t>(H) * D;   // between consecutive positions
-    const float* qrow = q + (static_cast<size_t>(b) * L + i) * row_stride + static_cast<size_t>(h) * D;
-    for (int d = lane; d < D; d += 32) qs[warp][d] = qrow[d];
+    const long long qoff = (static_cast<long long>(b) * L + i) * row_stride + static_cast<long long>(h) * D;
+    for (int d = lane; d < D; d += 32) qs[warp][d] = in_bounds(qoff + d, 1, q_elems, status) ? q[qoff + d] : 0.f;
     __syncwarp();
 
     // the shard's last row meets every shard the shard visits, in either layout
@@ -101,7 +104,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         // whole shard outside the visible keys of this query: skipped
         const bool skip = cu_seqlens != nullptr ? (s * Ls > hi || s * Ls + Ls - 1 < lo)
                                                 : (causal && position_of(s, 0, P, Ls, zig) > q_pos);
-        if (tracing && lane == 0) trace[r * P + t] = skip ? -1 : s;
+        if (tracing && lane == 0 && in_bounds(r * P + t, 1, static_cast<long long>(P) * P, status))
+            trace[r * P + t] = skip ? -1 : s;
         if (skip) continue;
         const int j_begin = s * Ls;
         const int j_end = j_begin + Ls;
@@ -109,8 +113,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             const int j = j0 + lane;
             float sc = -INFINITY;
             const int kpos = position_of(s, j - j_begin, P, Ls, zig);
-            if (j < j_end && kpos >= lo && kpos <= hi) {
-                const float* krow = kb + static_cast<size_t>(j) * kv_stride;
+            const long long koff = (kb - k) + static_cast<long long>(j) * kv_stride;
+            if (j < j_end && kpos >= lo && kpos <= hi && in_bounds(koff, D, kv_elems, status)) {
+                const float* krow = k + koff;
                 float dot = 0.f;
                 for (int d = 0; d < D; d += 4) {
                     const float4 kk = *reinterpret_cast<const float4*>(krow + d);
@@ -130,7 +135,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             for (int c = 0; c < kMaxD / 32; ++c) acc[c] *= alpha;
             for (int jj = 0; jj < n_here; ++jj) {
                 const float pw = __shfl_sync(0xffffffffu, pj, jj);
-                const float* vrow = vb + static_cast<size_t>(j0 + jj) * kv_stride;
+                const long long voff = (vb - v) + static_cast<long long>(j0 + jj) * kv_stride;
+                if (!in_bounds(voff, D, kv_elems, status)) continue;
+                const float* vrow = v + voff;
 #pragma unroll
                 for (int c = 0; c < kMaxD / 32; ++c) {
                     const int d = lane + 32 * c;
@@ -140,15 +147,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             m = m_new;
         }
     }
-    float* orow = out + (static_cast<size_t>(b) * L + i) * row_stride + static_cast<size_t>(h) * D;
     const float inv_l = l > 0.f ? 1.f / l : 0.f;          // a row that saw no key: 0
 #pragma unroll
     for (int c = 0; c < kMaxD / 32; ++c) {
         const int d = lane + 32 * c;
-        if (d < D) orow[d] = acc[c] * inv_l;
+        if (d < D && in_bounds(qoff + d, 1, q_elems, status)) out[qoff + d] = acc[c] * inv_l;
     }
-    if (lse != nullptr && lane == 0)
-        lse[(static_cast<size_t>(b) * L + i) * H + h] = l > 0.f ? m + logf(l) : -INFINITY;
+    const long long lidx = (static_cast<long long>(b) * L + i) * H + h;
+    if (lse != nullptr && lane == 0 && in_bounds(lidx, 1, q_elems / D, status))
+        lse[lidx] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
 }  // namespace
@@ -162,7 +169,7 @@ cudaError_t launch_attn_f32(const AttnArgs& a)
         static_cast<const float*>(a.q), static_cast<const float*>(a.k),
         static_cast<const float*>(a.v), static_cast<float*>(a.out), a.lse, a.trace, a.B, a.L,
         a.H, a.Hkv, a.D, a.P, a.causal, a.zigzag, a.cu_seqlens, a.n_seqs,
-        1.0f / sqrtf(static_cast<float>(a.D)));
+        1.0f / sqrtf(static_cast<float>(a.D)), a.status);
     return cudaGetLastError();
 }
 

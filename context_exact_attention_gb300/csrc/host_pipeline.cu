@@ -27,6 +27,8 @@
 #include <cstdint>
 #include <mutex>
 
+#include "ra_check.cuh"
+#include "ra_internal.h"
 #include "ring_attn.h"
 
 namespace {
@@ -101,13 +103,14 @@ bool host_overlap(const void* a, unsigned long long na, const void* b, unsigned 
 // dst[row * H + h0 + j] = src[row * hg + j] for j < hg
 __global__ void __launch_bounds__(256)
     lse_scatter_kernel(const float* __restrict__ src, float* __restrict__ dst, long long rows,
-                       int hg, int H, int h0)
+                       int hg, int H, int h0, unsigned int* status)
 {
     const long long n = rows * hg;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long row = i / hg;
-        dst[row * H + h0 + (i - row * hg)] = src[i];
+        const long long d = row * H + h0 + (i - row * hg);
+        if (ra::in_bounds(i, 1, n, status) && ra::in_bounds(d, 1, rows * H, status)) dst[d] = src[i];
     }
 }
 
@@ -197,8 +200,11 @@ ra_status ring_attn_fwd_host(const void* q_host, const void* k_host, const void*
         if (lse_host) {
             const long long n = static_cast<long long>(rows) * hg;
             const unsigned blocks = static_cast<unsigned>(n / 256 + 1 < 1024 ? n / 256 + 1 : 1024);
+            unsigned int* status = nullptr;
+            st = ra::current_status_word(&status);
+            if (st != RA_OK) return st;
             lse_scatter_kernel<<<blocks, 256, 0, cs>>>(dlse, lse_full, static_cast<long long>(rows),
-                                                       hg, H, g * hg);
+                                                       hg, H, g * hg, status);
             if (fail(cudaGetLastError())) return RA_ERR_CUDA;
         }
         if (fail(cudaEventRecord(p.ev_comp[s], cs))) return RA_ERR_CUDA;

@@ -72,8 +72,10 @@ constexpr int kRowsInFlight = 4;   // row groups per lane group per iteration
 template <bool kBf16>
 __global__ void __launch_bounds__(kBlock)
     merge_kernel(const uint4* o_a, const float* lse_a, const uint4* o_b, const float* lse_b,
-                 uint4* o_out, float* lse_out, long long rows, int vpr, int group_log2)
+                 uint4* o_out, float* lse_out, long long rows, int vpr, int group_log2,
+                 unsigned int* status)
 {
+    const long long n_vec = rows * vpr;     // extent of the o tensors, 16-byte vectors
     const int lane = threadIdx.x & 31;
     const int G = 1 << group_log2;
     const int rows_per_warp = 32 >> group_log2;
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(kBlock)
 #pragma unroll
         for (int u = 0; u < kRowsInFlight; ++u) {
             row[u] = base + u * step + (lane >> group_log2);
-            valid[u] = row[u] < rows;
+            valid[u] = row[u] < rows && in_bounds(row[u], 1, rows, status);
             w[u] = Weights{0.f, 0.f, -INFINITY};
         }
         // issue every load of the kRowsInFlight rows before any arithmetic
@@ -102,7 +104,7 @@ __global__ void __launch_bounds__(kBlock)
             uint4 x[kRowsInFlight], y[kRowsInFlight];
 #pragma unroll
             for (int u = 0; u < kRowsInFlight; ++u) {
-                if (valid[u]) {
+                if (valid[u] && in_bounds(row[u] * vpr + c, 1, n_vec, status)) {
                     x[u] = __ldcs(o_a + row[u] * vpr + c);
                     y[u] = __ldcs(o_b + row[u] * vpr + c);
                 }
@@ -111,6 +113,7 @@ __global__ void __launch_bounds__(kBlock)
             for (int u = 0; u < kRowsInFlight; ++u) {
                 if (!valid[u]) continue;
                 if (c == sub) w[u] = merge_weights(la[u], lb[u]);
+                if (!in_bounds(row[u] * vpr + c, 1, n_vec, status)) continue;
                 __stcs(o_out + row[u] * vpr + c, kBf16 ? combine_vec_bf16(x[u], y[u], w[u].wa, w[u].wb)
                                                        : combine_vec_f32(x[u], y[u], w[u].wa, w[u].wb));
             }
@@ -133,8 +136,10 @@ constexpr int kFlatUnroll = 4;
 template <bool kBf16>
 __global__ void __launch_bounds__(kBlock)
     merge_flat_kernel(const uint4* o_a, const float* lse_a, const uint4* o_b, const float* lse_b,
-                      uint4* o_out, float* lse_out, long long n_vec, int log2_vpr)
+                      uint4* o_out, float* lse_out, long long n_vec, int log2_vpr,
+                      unsigned int* status)
 {
+    const long long rows = n_vec >> log2_vpr;
     const long long stride = static_cast<long long>(gridDim.x) * kBlock;
     const long long vpr_mask = (1ll << log2_vpr) - 1;
     for (long long v0 = static_cast<long long>(blockIdx.x) * kBlock + threadIdx.x;
@@ -146,7 +151,8 @@ __global__ void __launch_bounds__(kBlock)
 #pragma unroll
         for (int u = 0; u < kFlatUnroll; ++u) {
             v[u] = v0 + u * stride;
-            valid[u] = v[u] < n_vec;
+            valid[u] = v[u] < n_vec && in_bounds(v[u], 1, n_vec, status) &&
+                       in_bounds(v[u] >> log2_vpr, 1, rows, status);
             if (valid[u]) {
                 const long long row = v[u] >> log2_vpr;
                 la[u] = lse_a[row];
@@ -176,7 +182,7 @@ __global__ void __launch_bounds__(kBlock)
 
 cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                          void* o_out, float* lse_out, long long rows, int D, int elem_bytes,
-                         cudaStream_t stream)
+                         unsigned int* status, cudaStream_t stream)
 {
     const int vpr = D * elem_bytes / 16;
     int group_log2 = 0;
@@ -210,21 +216,21 @@ cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, c
         if (elem_bytes == 2)
             merge_flat_kernel<true><<<static_cast<unsigned>(fblocks), kBlock, 0, stream>>>(
                 static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b), lse_b,
-                static_cast<uint4*>(o_out), lse_out, n_vec, log2_vpr);
+                static_cast<uint4*>(o_out), lse_out, n_vec, log2_vpr, status);
         else
             merge_flat_kernel<false><<<static_cast<unsigned>(fblocks), kBlock, 0, stream>>>(
                 static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b), lse_b,
-                static_cast<uint4*>(o_out), lse_out, n_vec, log2_vpr);
+                static_cast<uint4*>(o_out), lse_out, n_vec, log2_vpr, status);
         return cudaGetLastError();
     }
     if (elem_bytes == 2)
         merge_kernel<true><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
             static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b), lse_b,
-            static_cast<uint4*>(o_out), lse_out, rows, vpr, group_log2);
+            static_cast<uint4*>(o_out), lse_out, rows, vpr, group_log2, status);
     else
         merge_kernel<false><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(
             static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b), lse_b,
-            static_cast<uint4*>(o_out), lse_out, rows, vpr, group_log2);
+            static_cast<uint4*>(o_out), lse_out, rows, vpr, group_log2, status);
     return cudaGetLastError();
 }
 

@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "ra_check.cuh"
 #include "tmem_ldst.cuh"
 
 // Bits of the per-device status word.

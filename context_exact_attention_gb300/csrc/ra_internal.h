@@ -74,7 +74,7 @@ inline VarlenSchedLayout varlen_sched_layout(int L, int P)
     return s;
 }
 cudaError_t launch_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, int P, int causal,
-                                   int* schedule, cudaStream_t stream);
+                                   int* schedule, unsigned int* status, cudaStream_t stream);
 
 // bf16 tcgen05 kernel; tensor maps describe q, k, v as 4-D [B][L][H][D] with
 // 64-element, 128-byte-swizzled boxes of 128 rows.
@@ -109,7 +109,7 @@ cudaError_t launch_attn_bwd_bf16(const BwdArgs& a, const CUtensorMap& tmap_q,
 
 cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                          void* o_out, float* lse_out, long long rows, int D, int elem_bytes,
-                         cudaStream_t stream);
+                         unsigned int* status, cudaStream_t stream);
 
 // dir = 0: seq2head, dir = 1: head2seq.
 // Copy-engine path of the same transposes: seq_map is the 5-D view {D, H/P, P, L/P, P*B}
@@ -123,9 +123,15 @@ cudaError_t launch_ulysses_permute_tma(const CUtensorMap& seq_map, void* head_si
                                        cudaStream_t stream);
 
 cudaError_t launch_ulysses_permute(const void* in, void* out, int B, int L, int H, int D, int P,
-                                   int elem_bytes, int dir, cudaStream_t stream);
+                                   int elem_bytes, int dir, unsigned int* status, cudaStream_t stream);
 
 cudaError_t launch_wait_probe(unsigned int* status, unsigned long long timeout_ns,
                               cudaStream_t stream);
+
+// Device address of the current device's status word (api.cu).
+ra_status current_status_word(unsigned int** out);
+
+// One thread whose index check fails (debug build): exercises RA_STATUS_BOUNDS.
+cudaError_t launch_bounds_probe(unsigned int* status, cudaStream_t stream);
 
 }  // namespace ra

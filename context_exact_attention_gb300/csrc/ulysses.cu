@@ -35,6 +35,8 @@ struct PermuteGeom {
     I cv;          // 16-byte vectors per chunk (Hg * D * elem / 16)
     I hv;          // vectors per position on the sequence side (H * D * elem / 16)
     I B, L, Ls, P;
+    long long n_vec;        // 16-byte vectors in each buffer (the debug build's extent)
+    unsigned int* status;
 };
 
 // Output chunk ch -> first vector of its source chunk.
@@ -80,6 +82,8 @@ __global__ void __launch_bounds__(kBlock)
             live[u] = ch < g.n_chunks;
             src[u] = live[u] ? source_chunk<kDir>(ch, g) : I(0);
             dst[u] = ch * g.cv;
+            live[u] = live[u] && in_bounds(src[u], g.cv, g.n_vec, g.status) &&
+                      in_bounds(dst[u], g.cv, g.n_vec, g.status);
         }
         for (I c = lane; c < g.cv; c += 32) {
             uint4 x[kBatch];
@@ -95,9 +99,11 @@ __global__ void __launch_bounds__(kBlock)
 
 template <int kDir, typename I>
 cudaError_t launch_typed(const void* in, void* out, int B, int L, int H, int D, int P,
-                         int elem_bytes, cudaStream_t stream)
+                         int elem_bytes, unsigned int* status, cudaStream_t stream)
 {
     PermuteGeom<I> g;
+    g.n_vec = static_cast<long long>(B) * L * H * D * elem_bytes / 16;
+    g.status = status;
     g.B = B;
     g.L = L;
     g.P = P;
@@ -131,6 +137,7 @@ struct TmaPermute {
     int P, B, Ls, L;
     int row_bytes;           // one position's run of H/P heads: H/P * D * elem
     int stage_bytes;         // R * row_bytes rounded up to 1024
+    long long head_bytes;    // size of the head-sharded buffer (the debug build's extent)
     unsigned int* status;
     unsigned long long timeout_ns;
 };
@@ -212,9 +219,12 @@ __global__ void __launch_bounds__(32, 1)
         if constexpr (kDir == 0) {
             mbar_arrive_expect_tx(bars + 8 * s, static_cast<uint32_t>(p.R * p.row_bytes));
             tma_load_5d(dst, &seq_map, bars + 8 * s, 0, 0, g, l0, rb, once);
-        } else {
+        } else if (in_bounds(static_cast<long long>(off), static_cast<long long>(rows) * p.row_bytes,
+                             p.head_bytes, p.status)) {
             mbar_arrive_expect_tx(bars + 8 * s, static_cast<uint32_t>(rows * p.row_bytes));
             bulk_load(dst, head + off, static_cast<uint32_t>(rows * p.row_bytes), bars + 8 * s, once);
+        } else {
+            mbar_arrive(bars + 8 * s);     // skipped copy: complete the phase without data
         }
     };
     long long n_mine = 0;                       // tiles of this CTA
@@ -229,9 +239,11 @@ __global__ void __launch_bounds__(32, 1)
         size_t off;
         decode(tile_of(j), rb, g, l0, rows, off);
         const uint32_t src = sbase + s * p.stage_bytes;
-        if constexpr (kDir == 0)
-            bulk_store(head + off, src, static_cast<uint32_t>(rows * p.row_bytes));
-        else
+        if constexpr (kDir == 0) {
+            if (in_bounds(static_cast<long long>(off), static_cast<long long>(rows) * p.row_bytes,
+                          p.head_bytes, p.status))
+                bulk_store(head + off, src, static_cast<uint32_t>(rows * p.row_bytes));
+        } else
             tma_store_5d(&seq_map, src, 0, 0, g, l0, rb);
         bulk_commit();
         // the previous tile's stage is free once its store has read it: refill it
@@ -280,6 +292,7 @@ cudaError_t launch_ulysses_permute_tma(const CUtensorMap& seq_map, void* head_si
     p.row_bytes = H / P * D * elem_bytes;
     p.stage_bytes = (R * p.row_bytes + 1023) & ~1023;
     p.n_tiles = static_cast<long long>(P) * B * p.n_rblk * P;
+    p.head_bytes = static_cast<long long>(B) * L * H * D * elem_bytes;
     p.status = status;
     p.timeout_ns = timeout_ns;
     constexpr int kSmemMax = kTStages * kTStageMax + 1024 + 8 * kTStages + 16;
@@ -301,15 +314,15 @@ cudaError_t launch_ulysses_permute_tma(const CUtensorMap& seq_map, void* head_si
 }
 
 cudaError_t launch_ulysses_permute(const void* in, void* out, int B, int L, int H, int D, int P,
-                                   int elem_bytes, int dir, cudaStream_t stream)
+                                   int elem_bytes, int dir, unsigned int* status, cudaStream_t stream)
 {
     const long long total_vec = static_cast<long long>(B) * L * H * D * elem_bytes / 16;
     const bool small = total_vec < (1ll << 30);   // headroom for the grid-stride steps
     if (dir == 0)
-        return small ? launch_typed<0, int>(in, out, B, L, H, D, P, elem_bytes, stream)
-                     : launch_typed<0, long long>(in, out, B, L, H, D, P, elem_bytes, stream);
-    return small ? launch_typed<1, int>(in, out, B, L, H, D, P, elem_bytes, stream)
-                 : launch_typed<1, long long>(in, out, B, L, H, D, P, elem_bytes, stream);
+        return small ? launch_typed<0, int>(in, out, B, L, H, D, P, elem_bytes, status, stream)
+                     : launch_typed<0, long long>(in, out, B, L, H, D, P, elem_bytes, status, stream);
+    return small ? launch_typed<1, int>(in, out, B, L, H, D, P, elem_bytes, status, stream)
+                 : launch_typed<1, long long>(in, out, B, L, H, D, P, elem_bytes, status, stream);
 }
 
 }  // namespace ra

@@ -14,6 +14,7 @@
 // unit), then a counting sort over work values -- histogram in shared memory, a
 // descending exclusive scan and a stable scatter by one warp (__match_any_sync ranks
 // the lanes of equal bins in lane order, so the order is deterministic).
+#include "ra_check.cuh"
 #include "ra_internal.h"
 
 namespace ra {
@@ -26,16 +27,17 @@ constexpr int kTileRows = 128;
 
 // First and last position of the sequence holding pos: the largest g with
 // cu[g] <= pos.  Bounded for any contents of cu.
-__device__ void seq_span(const int* cu, int n_seqs, int pos, int& first, int& last)
+__device__ void seq_span(const int* cu, int n_seqs, int pos, int& first, int& last,
+                         unsigned int* status)
 {
     int a = 0, b = n_seqs - 1;
     while (a < b) {
         const int m = (a + b + 1) >> 1;
-        if (__ldg(cu + m) <= pos) a = m;
+        if (checked_ldg(cu, m, n_seqs + 1, status) <= pos) a = m;
         else b = m - 1;
     }
-    first = __ldg(cu + a);
-    last = __ldg(cu + a + 1) - 1;
+    first = checked_ldg(cu, a, n_seqs + 1, status);
+    last = checked_ldg(cu, a + 1, n_seqs + 1, status) - 1;
 }
 
 // 128-row tiles (each within one shard of Ls rows) holding a position in [lo, hi].
@@ -62,7 +64,7 @@ __device__ __forceinline__ int bin_of(int w, int nb, int max_work)
 
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_schedule_kernel(const int* __restrict__ cu, int n_seqs, int L, int P, int causal,
-                           int* __restrict__ sched, VarlenSchedLayout lay)
+                           int* __restrict__ sched, VarlenSchedLayout lay, unsigned int* status)
 {
     __shared__ int bins[kMaxBins];
     __shared__ int work_s[kSmemWork];
@@ -79,7 +81,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long off = kind == 0 ? lay.fwd : kind == 1 ? lay.bwd_k : lay.bwd_q;
         int* order = sched + off;
         // each kind's scratch sits as far past the scratch base as its order past the first
-        int* work = U <= kSmemWork ? work_s : sched + lay.scratch + off;
+        const bool in_smem = U <= kSmemWork;
+        int* work = in_smem ? work_s : sched + lay.scratch + off;
+        // the debug build checks every global index against the schedule array
+        auto work_ok = [&](int u) {
+            return in_smem || in_bounds(lay.scratch + off + u, 1, lay.total, status);
+        };
         for (int i = threadIdx.x; i < nb; i += kThreads) bins[i] = 0;
         __syncthreads();
         for (int u = threadIdx.x; u < U; u += kThreads) {
@@ -87,8 +94,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int a = s * Ls + i * rows;
             const int b = min(s * Ls + Ls - 1, a + rows - 1);
             int fa, la, fb, lb;
-            seq_span(cu, n_seqs, a, fa, la);
-            seq_span(cu, n_seqs, b, fb, lb);
+            seq_span(cu, n_seqs, a, fa, la, status);
+            seq_span(cu, n_seqs, b, fb, lb, status);
             int lo, hi;
             if (kind == 1) {        // the queries that see some key of the tile
                 lo = causal ? a : fa;
@@ -98,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 hi = causal ? b : lb;
             }
             const int w = tiles_in(lo, hi, Ls, L);
-            work[u] = w;
+            if (work_ok(u)) work[u] = w;
             atomicAdd(&bins[bin_of(w, nb, max_work)], 1);
         }
         __syncthreads();
@@ -122,10 +129,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int base = 0; base < U; base += 32) {
                 const int u = base + lane;
                 const bool act = u < U;
-                const int key = act ? bin_of(work[u], nb, max_work) : -1 - lane;
+                const int key = act ? bin_of(work_ok(u) ? work[u] : 0, nb, max_work) : -1 - lane;
                 const unsigned peers = __match_any_sync(0xffffffffu, key);
                 const int rank = __popc(peers & ((1u << lane) - 1u));
-                if (act) order[bins[key] + rank] = u;
+                if (act && in_bounds(bins[key] + rank, 1, U, status))   // inside this order
+                    order[bins[key] + rank] = u;
                 __syncwarp();
                 if (act && rank == 0) bins[key] += __popc(peers);
                 __syncwarp();
@@ -137,11 +145,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, int P, int causal,
-                                   int* schedule, cudaStream_t stream)
+                                   int* schedule, unsigned int* status, cudaStream_t stream)
 {
     const VarlenSchedLayout lay = varlen_sched_layout(L, P);
     varlen_schedule_kernel<<<3, kThreads, 0, stream>>>(cu_seqlens, n_seqs, L, P, causal ? 1 : 0,
-                                                       schedule, lay);
+                                                       schedule, lay, status);
     return cudaGetLastError();
 }
 

@@ -40,7 +40,9 @@ typedef enum {
     RA_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
     RA_ERR_NOT_DIVISIBLE = 4, /* L % P != 0, or H % P != 0 for the Ulysses transposes */
     RA_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
-    RA_ERR_TIMEOUT = 6        /* a kernel's bounded wait ran out (reported by ra_check_status) */
+    RA_ERR_TIMEOUT = 6,       /* a kernel's bounded wait ran out (reported by ra_check_status) */
+    RA_ERR_BOUNDS = 7         /* debug build only: an index check failed and its access was
+                                 skipped (reported by ra_check_status) */
 } ra_status;
 
 typedef enum { RA_BF16 = 0, RA_F32 = 1 } ra_dtype;
@@ -485,10 +487,30 @@ ra_status ring_attn_bwd_ex(const ra_attn_desc* desc, const void* q, const void* 
 /*
  * ra_check_status -- synchronise `stream`, then read and clear the status word
  * of the current device.  Returns RA_ERR_TIMEOUT if a kernel gave up on a
- * bounded wait since the last check, RA_ERR_CUDA if the stream reports an
- * error, RA_OK otherwise.
+ * bounded wait since the last check, RA_ERR_BOUNDS (debug build) if an index
+ * check failed, RA_ERR_CUDA if the stream reports an error or a kernel could not
+ * lay out its shared memory, RA_OK otherwise.
+ *
+ * The debug build.  The library is also built as libringattn_debug.so with the
+ * same entry points, in which every global load and store that a kernel
+ * addresses by a computed index is first checked against the extent of its
+ * tensor (as the arguments of the call define it); a failed check records
+ * RA_ERR_BOUNDS and skips the access (a load yields 0) instead of touching
+ * memory outside the tensor.  Loads by TMA tensor maps are bounded by the maps
+ * in hardware and need no check.  Results are the same bits as the normal
+ * build's.  No page has a counterpart: it stands in for a memory checker.
  */
 ra_status ra_check_status(ra_stream_t stream);
+
+/*
+ * ra_probe_bounds_check -- exercises the debug build's index check without
+ * touching memory outside any buffer: launches one thread that checks an index
+ * one past the end of a one-element extent and, only if the check passed, writes
+ * a word inside the library.  In the debug build the check fails, the write is
+ * skipped and ra_check_status then returns RA_ERR_BOUNDS.  The normal build has
+ * no checks and returns RA_ERR_UNSUPPORTED without launching anything.
+ */
+ra_status ra_probe_bounds_check(ra_stream_t stream);
 
 /* Static English text for a status code (never NULL). */
 const char* ra_status_string(ra_status status);

@@ -35,8 +35,20 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(raw, name), name
 
 
+def test_debug_library_exports_every_declared_symbol():
+    """The index-checked debug build has the same entry points."""
+    dbg = cea.load_debug_library(build_if_missing=True)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+
+
+def test_bounds_probe_is_refused_by_the_normal_build(lib):
+    """The normal build has no index checks: the probe launches nothing."""
+    assert lib.ra_probe_bounds_check(ctypes.c_void_p(0)) == 2     # RA_ERR_UNSUPPORTED
+
+
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = lib.ra_status_string(code)
         assert isinstance(s, bytes) and len(s) > 0
     assert lib.ra_status_string(99) == b"unknown status"
