@@ -14,6 +14,13 @@ allows twice that, plus 1e-6.  Early causal query rows, which sum a few large
 and cancelling terms, are where the term magnitudes matter: there an error of
 several times the result's own rounding is still exact arithmetic on bf16
 operands.  Norm-wise, ||got - ref|| <= 4u ||ref|| and cosine > 0.9999.
+
+Beside the bound every check prints the bf16 criterion of the precision page
+(|err| <= 5e-3 + 5e-3 |ref|, stated there for forward outputs) as the ratio
+max |err| / (5e-3 + 5e-3 |ref|).  Without causal masking the gradients meet it,
+and the plain, grouped-head and packed parity tests assert it; with causal
+masking the early rows' cancellation takes some elements past it while the
+first-order bound holds.
 """
 import numpy as np
 import pytest
@@ -55,7 +62,7 @@ def _term_scales(q, k, v, do, causal):
     return sq, sk, sv
 
 
-def _grad_close(got, ref, what, scale):
+def _grad_close(got, ref, what, scale, p3_holds=False):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert np.isfinite(got).all(), what
@@ -66,6 +73,10 @@ def _grad_close(got, ref, what, scale):
     p3 = (err / (BF16_TOL + BF16_TOL * np.abs(ref))).max()
     print(f"{what}: rel_l2 {rel:.2e} cos {cosine(got, ref):.7f} worst/bound {worst:.3f} "
           f"p3 ratio {p3:.3f}")
+    if p3_holds:
+        # without causal masking no row sums a few large cancelling terms, and the
+        # gradients also meet the page's forward criterion
+        assert p3 <= 1.0, (what, p3)
     assert rel <= 4 * U, (what, rel)
     assert cosine(got, ref) > 0.9999, what
     assert worst <= 1.0, (what, worst)
@@ -95,9 +106,9 @@ def test_bwd_parity(case, causal):
     assert cea.check_status() == 0
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=causal)
     sq, sk, sv = _term_scales(q, k, v, do, causal)
-    _grad_close(to_np(dq), rq, "dq", sq)
-    _grad_close(to_np(dk), rk, "dk", sk)
-    _grad_close(to_np(dv), rv, "dv", sv)
+    _grad_close(to_np(dq), rq, "dq", sq, p3_holds=not causal)
+    _grad_close(to_np(dk), rk, "dk", sk, p3_holds=not causal)
+    _grad_close(to_np(dv), rv, "dv", sv, p3_holds=not causal)
 
 
 def test_bwd_deterministic_and_spread_scores():
@@ -163,9 +174,9 @@ def test_bwd_gqa_parity(case, causal):
     sq, sk, sv = _term_scales(q, kr, vr, do, causal)
     sk = sk.reshape(B, L, Hkv, G, D).sum(axis=3)
     sv = sv.reshape(B, L, Hkv, G, D).sum(axis=3)
-    _grad_close(to_np(dq), rq, "dq", sq)
-    _grad_close(to_np(dk), rk, "dk", sk)
-    _grad_close(to_np(dv), rv, "dv", sv)
+    _grad_close(to_np(dq), rq, "dq", sq, p3_holds=not causal)
+    _grad_close(to_np(dk), rk, "dk", sk, p3_holds=not causal)
+    _grad_close(to_np(dv), rv, "dv", sv, p3_holds=not causal)
 
 
 def test_bwd_gqa_with_h_kv_equal_h_is_plain_backward():
@@ -306,7 +317,7 @@ def test_bwd_varlen_parity(case, causal):
                                        _term_scales(*seg, causal))):
             refs[i][a:b], scales[i][a:b] = r[0], s[0]
     for name, g, r, s in zip(("dq", "dk", "dv"), got, refs, scales):
-        _grad_close(g, r, name, s)
+        _grad_close(g, r, name, s, p3_holds=not causal)
 
 
 def test_bwd_varlen_samples_do_not_see_each_other():
