@@ -53,14 +53,19 @@ constexpr int kThreads = 384;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+// kOwnStage: the output leaves through a staging buffer of its own (persistent grids,
+// where the query buffers are refilled for the next unit while the output is written)
+// instead of through the tile's query buffer.  Either way a warp stages 32 rows of D/2
+// columns at a time.
+template <int D, bool kOwnStage = false>
 struct Layout {
     static constexpr int kBoxes = D / 64;              // 64-element (128-byte) swizzle boxes
     static constexpr int kTileBytes = kRows * D * 2;   // one Q, K or V tile
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kTiles * kTileBytes;
     static constexpr int kV = kK + 2 * kTileBytes;
-    static constexpr int kBar = kV + 2 * kTileBytes;
+    static constexpr int kStage = kV + 2 * kTileBytes; // 8 warps x 32 rows x D/2 bf16
+    static constexpr int kBar = kStage + (kOwnStage ? kTileBytes : 0);
     static constexpr int kSmem = kBar + 256 + 1024;    // barriers + alignment slack
     static constexpr uint32_t kTmemCols = 512;
     __device__ static constexpr uint32_t col_s(int tq) { return 128u * tq; }
@@ -82,8 +87,11 @@ enum : int {
     kBarOFull = 15,  // +tile
     kBarDone = 17,
     kBarQ1 = 18,     // query tile 1 (tile 0 on kBarQ), so that tile 0's first S starts earlier
-    kBarCount = 19
+    kBarUnitFull = 19,   // +slot: dynamic grids, the producer published a unit
+    kBarUnitEmpty = 21,  // +slot: every consumer warp has read it
+    kBarCount = 23
 };
+constexpr int kUnitReaders = 1 + 8;   // the MMA warp and the eight softmax warps
 
 struct Params {
     __nv_bfloat16* out;
@@ -103,6 +111,9 @@ struct Params {
     float scale_log2;
     long long out_elems, lse_elems;   // extents for the debug build's index checks
     int sched_elems;                  // entries of the schedule's forward order
+    int* claim;      // dynamic grids: the work counter (zeroed before the launch)
+    long long claim_index, claim_extent;   // its index in the schedule array, for the checks
+    int n_units;     // work units of the whole call: B * H * P * n_pair
 };
 
 // Global position of local row i of shard `shard`.  Contiguous layout: shard r
@@ -317,85 +328,141 @@ struct VarlenSched {
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-// kMode: 0 contiguous shards, 1 zigzag shards, 2 packed sequences (contiguous shards),
-// 3 Ulysses head groups read from and written to the sequence-sharded buffers (the
-// all-to-all of "序列并行与 Ring Attention" section 3.5 done by the tensor maps' addressing:
-// batch b of the kernel is head group g = b / u_B of batch b % u_B, its head h is source
-// head g*H + h, and position l sits in source shard l / u_Ls at row l % u_Ls).
-template <int D, int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
-    ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                          const __grid_constant__ CUtensorMap tmap_k,
-                          const __grid_constant__ CUtensorMap tmap_v, const Params p)
-{
-    using Lay = Layout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_s = smem_addr(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
-    const uint32_t sbase = smem_addr(smem);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kBar + kBarCount * 8);
-    int* abort_flag = reinterpret_cast<int*>(smem + Lay::kBar + kBarCount * 8 + 4);
-    auto bar = [&](int i) -> uint32_t { return sbase + Lay::kBar + 8u * i; };
+// One work unit: two 128-row query tiles of one shard of one (batch, head), and the walk
+// over the K/V blocks they meet.
+template <int kMode>
+struct Unit {
+    int bh, b, h, hk;
+    int r, pair;
+    int bo, h_src, hk_src;       // indices in the source tensors (kMode 3)
+    int q0_local, q0;            // first query row of the pair: within shard r, global
+    int n_blocks;
+    typename std::conditional<kMode == 1, ZigzagSched,
+                              typename std::conditional<kMode == 2, VarlenSched,
+                                                        ContigSched>::type>::type walk;
 
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    // ---- work unit: heaviest (shard, pair) first, two (batch, head) pairs interleaved
-    const int units_per_bh = p.P * p.n_pair;
-    int bh, u;
-    unit_of_block(blockIdx.x, p.B * p.H, units_per_bh, bh, u);
-    int r = p.P - 1 - u / p.n_pair;
-    int pair = p.n_pair - 1 - (u - (u / p.n_pair) * p.n_pair);
-    if constexpr (kMode == 2) {
-        // packed sequences: work follows the offset inside a sequence, not the position;
-        // a precomputed order (entries outside the unit range are ignored) puts the
-        // heaviest units first
-        if (p.schedule != nullptr) {
-            const int x = checked_ldg(p.schedule, u, p.sched_elems, p.status);
-            if (static_cast<unsigned>(x) < static_cast<unsigned>(units_per_bh)) {
-                r = x / p.n_pair;
-                pair = x - r * p.n_pair;
+    // Unit g of the call's order: heaviest (shard, pair) first within each (batch, head),
+    // two (batch, head) pairs interleaved; packed sequences take the schedule's order.
+    __device__ __forceinline__ void setup(int g, const Params& p)
+    {
+        const int units_per_bh = p.P * p.n_pair;
+        int u;
+        unit_of_block(g, p.B * p.H, units_per_bh, bh, u);
+        r = p.P - 1 - u / p.n_pair;
+        pair = p.n_pair - 1 - (u - (u / p.n_pair) * p.n_pair);
+        if constexpr (kMode == 2) {
+            // packed sequences: work follows the offset inside a sequence, not the position;
+            // a precomputed order (entries outside the unit range are ignored) puts the
+            // heaviest units first
+            if (p.schedule != nullptr) {
+                const int x = checked_ldg(p.schedule, u, p.sched_elems, p.status);
+                if (static_cast<unsigned>(x) < static_cast<unsigned>(units_per_bh)) {
+                    r = x / p.n_pair;
+                    pair = x - r * p.n_pair;
+                }
             }
         }
-    }
-    const int b = bh / p.H;
-    const int h = bh - b * p.H;
-    const int hk = h / p.group;                       // key/value head of this query head
-    int bo = b, h_src = h, hk_src = hk;               // indices in the source tensors (kMode 3)
-    if constexpr (kMode == 3) {
-        const int g = b / p.u_B;
-        bo = b - g * p.u_B;
-        h_src = g * p.H + h;
-        hk_src = h_src / p.group;
-    }
-    const int q0_local = pair * (kTiles * kRows);     // first query row of the pair, within shard
-    const int q0 = r * p.Ls + q0_local;               // global
-
-    constexpr bool kZig = kMode == 1;
-    constexpr bool kVarlen = kMode == 2;
-    using Sched = typename std::conditional<
-        kZig, ZigzagSched, typename std::conditional<kVarlen, VarlenSched, ContigSched>::type>::type;
-    Sched walk;
-    {
+        b = bh / p.H;
+        h = bh - b * p.H;
+        hk = h / p.group;                       // key/value head of this query head
+        bo = b;
+        h_src = h;
+        hk_src = hk;
+        if constexpr (kMode == 3) {
+            const int gg = b / p.u_B;
+            bo = b - gg * p.u_B;
+            h_src = gg * p.H + h;
+            hk_src = h_src / p.group;
+        }
+        q0_local = pair * (kTiles * kRows);
+        q0 = r * p.Ls + q0_local;
         const int last = min(p.Ls - 1, q0_local + kTiles * kRows - 1);
-        if constexpr (kVarlen) {
+        if constexpr (kMode == 2) {
             // visible positions of the pair: from the first row's sequence start to the
             // last row's (causal) position or sequence end
             int lo0, hi0, lo1, hi1;
             seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + q0_local, p.causal, lo0, hi0, p.status);
             seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + last, p.causal, lo1, hi1, p.status);
             walk.init(r, p.P, p.n_kt, p.Ls, lo0, hi1);
-        } else if constexpr (kZig) {
-            // last query position of the pair (positions rise within each chunk, and
-            // the late chunk lies after the early one)
+        } else if constexpr (kMode == 1) {
+            // last query position of the pair (positions rise within each chunk, and the
+            // late chunk lies after the early one)
             const int mid = min(p.Ls - 1, q0_local + kRows - 1);
             walk.init(r, p.P, p.n_kt, p.Ls, p.causal,
                       max(position(r, last, p.P, p.Ls, 1), position(r, mid, p.P, p.Ls, 1)));
         } else {
             walk.init(r, p.P, p.n_kt, p.Ls, p.causal, last);
         }
+        n_blocks = walk.n_blocks;
     }
-    const int n_blocks = walk.n_blocks;
+};
+
+// kMode: 0 contiguous shards, 1 zigzag shards, 2 packed sequences (contiguous shards),
+// 3 Ulysses head groups read from and written to the sequence-sharded buffers (the
+// all-to-all of "序列并行与 Ring Attention" section 3.5 done by the tensor maps' addressing:
+// batch b of the kernel is head group g = b / u_B of batch b % u_B, its head h is source
+// head g*H + h, and position l sits in source shard l / u_Ls at row l % u_Ls).
+//
+// kPersist: how CTAs get their work units.
+//   0  one CTA per unit: the grid lists the units and the block scheduler hands them to
+//      SMs as SMs free up;
+//   1  one CTA per SM, static: CTA c runs units c, c + G, c + 2G, ... of the G-CTA grid
+//      (used when all units are equal: calls without causal masking);
+//   2  one CTA per SM, dynamic: the producer warp claims each next unit from a counter in
+//      global memory (packed sequences with a schedule: the counter sits in the caller's
+//      schedule array and is zeroed before the launch) and hands it to the other warps
+//      through a two-slot ring of unit indices in shared memory.
+// A persistent CTA overlaps consecutive units: the producer loads the next unit's query
+// tiles as soon as the current unit's last products of each tile have finished and its
+// K/V blocks as ring stages free up; the issuer starts the next unit's first products
+// while the softmax warps write the previous output, which leaves through a staging
+// buffer of its own (the query buffers are already being refilled).  Barrier phases run
+// on across units: blocks and units are counted from the CTA's start.  A unit with an
+// empty walk (possible only with malformed sequence boundaries) writes 0 and -inf and
+// touches no barrier.
+template <int D, int kMode, int kPersist>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                          const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const Params p)
+{
+    using Lay = Layout<D, kPersist != 0>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kBar + kBarCount * 8);
+    int* abort_flag = reinterpret_cast<int*>(smem + Lay::kBar + kBarCount * 8 + 4);
+    volatile int* unit_slot = reinterpret_cast<volatile int*>(smem + Lay::kBar + kBarCount * 8 + 8);
+    auto bar = [&](int i) -> uint32_t { return sbase + Lay::kBar + 8u * i; };
+    static_assert(kBarCount * 8 + 16 <= 256, "barrier area");
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr bool kZig = kMode == 1;
+    constexpr bool kVarlen = kMode == 2;
+
+    // The i-th unit of this CTA (-1: no more).  Dynamic grids: the consumers' side of the
+    // ring; the producer publishes (publish_unit below).
+    WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+    auto consume_unit = [&](int i) -> int {
+        if constexpr (kPersist == 0) return i == 0 ? static_cast<int>(blockIdx.x) : -1;
+        if constexpr (kPersist == 1) {
+            const long long g = blockIdx.x + static_cast<long long>(i) * gridDim.x;
+            return g < p.n_units ? static_cast<int>(g) : -1;
+        }
+        const int slot = i & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarUnitFull + slot), (i >> 1) & 1, wc)))
+            return -1;
+        const int g = unit_slot[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarUnitEmpty + slot));
+        return g;
+    };
+
+    Unit<kMode> first;
+    const int g_first = kPersist == 2 ? -1 : consume_unit(0);
+    if (g_first >= 0) first.setup(g_first, p);
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQ), 1);
@@ -408,46 +475,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarPFull + 2 * i), kRows);
             mbar_init(bar(kBarPFull + 2 * i + 1), kRows);
             mbar_init(bar(kBarOFull + i), 1);
+            mbar_init(bar(kBarUnitFull + i), 1);
+            mbar_init(bar(kBarUnitEmpty + i), kUnitReaders);
         }
         mbar_init(bar(kBarDone), 1);
         mbar_init(bar(kBarQ1), 1);
         *abort_flag = 0;
         fence_mbar_init();
-        // Start the loads the first products need (Q0 and K0 for tile 0's first S, then
-        // Q1) before the TMEM allocation and the block-wide barrier: every CTA of a wave
-        // starts by loading at once, so the sooner they are queued the better.  The
-        // producer loop below issues V0 and everything after it.
-        tma_prefetch_desc(&tmap_q);
-        tma_prefetch_desc(&tmap_k);
-        const uint64_t once = l2_policy_evict_first();
-        auto load_q = [&](int tq, uint32_t full) {
-            mbar_arrive_expect_tx(bar(full), Lay::kTileBytes);
-            for (int bx = 0; bx < Lay::kBoxes; ++bx) {
-                const uint32_t dst = sbase + Lay::kQ + tq * Lay::kTileBytes + bx * 16384;
-                const int row = q0 + tq * kRows;
-                if constexpr (kMode == 3)
-                    tma_load_5d(dst, &tmap_q, bar(full), bx * 64, h_src, row % p.u_Ls, bo,
-                                row / p.u_Ls, once);
-                else
-                    tma_load_4d(dst, &tmap_q, bar(full), bx * 64, h, row, b, once);
+        if constexpr (kPersist == 0) {
+            // Start the loads the first products need (Q0 and K0 for tile 0's first S,
+            // then Q1) before the TMEM allocation and the block-wide barrier: every CTA of
+            // a wave starts by loading at once, so the sooner they are queued the better.
+            // The producer loop below issues V0 and everything after it.
+            const Unit<kMode>& U = first;
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            const uint64_t once = l2_policy_evict_first();
+            auto load_q = [&](int tq, uint32_t full) {
+                mbar_arrive_expect_tx(bar(full), Lay::kTileBytes);
+                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                    const uint32_t dst = sbase + Lay::kQ + tq * Lay::kTileBytes + bx * 16384;
+                    const int row = U.q0 + tq * kRows;
+                    if constexpr (kMode == 3)
+                        tma_load_5d(dst, &tmap_q, bar(full), bx * 64, U.h_src, row % p.u_Ls, U.bo,
+                                    row / p.u_Ls, once);
+                    else
+                        tma_load_4d(dst, &tmap_q, bar(full), bx * 64, U.h, row, U.b, once);
+                }
+            };
+            load_q(0, kBarQ);
+            if (U.n_blocks > 0) {
+                Unit<kMode> W = U;
+                W.walk.at(0);
+                const int row = W.walk.s * p.Ls + W.walk.kt() * kKeys;
+                const uint64_t keep = l2_policy_evict_last();
+                mbar_arrive_expect_tx(bar(kBarKFull + 0), Lay::kTileBytes);
+                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                    const uint32_t dst = sbase + Lay::kK + bx * 16384;
+                    if constexpr (kMode == 3)
+                        tma_load_5d(dst, &tmap_k, bar(kBarKFull + 0), bx * 64, U.hk_src,
+                                    row % p.u_Ls, U.bo, row / p.u_Ls, keep);
+                    else
+                        tma_load_4d(dst, &tmap_k, bar(kBarKFull + 0), bx * 64, U.hk, row, U.b, keep);
+                }
             }
-        };
-        load_q(0, kBarQ);
-        if (n_blocks > 0) {
-            walk.at(0);
-            const int row = walk.s * p.Ls + walk.kt() * kKeys;
-            const uint64_t keep = l2_policy_evict_last();
-            mbar_arrive_expect_tx(bar(kBarKFull + 0), Lay::kTileBytes);
-            for (int bx = 0; bx < Lay::kBoxes; ++bx) {
-                const uint32_t dst = sbase + Lay::kK + bx * 16384;
-                if constexpr (kMode == 3)
-                    tma_load_5d(dst, &tmap_k, bar(kBarKFull + 0), bx * 64, hk_src, row % p.u_Ls,
-                                bo, row / p.u_Ls, keep);
-                else
-                    tma_load_4d(dst, &tmap_k, bar(kBarKFull + 0), bx * 64, hk, row, b, keep);
-            }
+            load_q(1, kBarQ1);
         }
-        load_q(1, kBarQ1);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), Lay::kTmemCols);
@@ -457,7 +530,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -468,53 +540,121 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
         }
-        // the shard's last query pair meets every shard the shard visits, in either layout
-        const bool tracing = p.trace != nullptr && bh == 0 && pair == p.n_pair - 1;
-        if (tracing && leader)
-            for (int t = 0; t < p.P; ++t)
-                if (in_bounds(r * p.P + t, 1, p.P * p.P, p.status)) p.trace[r * p.P + t] = -1;
         const uint64_t keep = l2_policy_evict_last();    // K/V: read by every tile pair of the head
-        // Q0, Q1 (read once) and K0 were issued by thread 0 before the block-wide barrier
-        int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
-        for (int n = 0; n < n_blocks; ++n) {
-            walk.at(n);
-            if (tracing && walk.first_of_shard() && leader &&
-                in_bounds(r * p.P + walk.t, 1, p.P * p.P, p.status))
-                p.trace[r * p.P + walk.t] = walk.s;
-            const int st = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
-            const int row = walk.s * p.Ls + walk.kt() * kKeys;   // physical row of the tile
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc))) break;
-            if (leader && n > 0) {
-                mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kTileBytes);
-                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
-                    const uint32_t dst = sbase + Lay::kK + st * Lay::kTileBytes + bx * 16384;
-                    if constexpr (kMode == 3)
-                        tma_load_5d(dst, &tmap_k, bar(kBarKFull + st), bx * 64, hk_src,
-                                    row % p.u_Ls, bo, row / p.u_Ls, keep);
-                    else
-                        tma_load_4d(dst, &tmap_k, bar(kBarKFull + st), bx * 64, hk, row, b, keep);
-                }
-            }
-            last_k[st] = n;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc))) break;
+        const uint64_t once = l2_policy_evict_first();
+        // Dynamic grids: claim the i-th unit and publish it to the other warps (-1: done)
+        auto publish_unit = [&](int i) -> int {
+            const int slot = i & 1;
+            if (i >= 2 &&
+                !__all_sync(0xffffffffu, mbar_wait(bar(kBarUnitEmpty + slot), ((i - 2) >> 1) & 1, wc)))
+                return -1;
+            int g = -1;
+            if (leader && in_bounds(p.claim_index, 1, p.claim_extent, p.status))
+                g = atomicAdd(p.claim, 1);
+            g = __shfl_sync(0xffffffffu, g, __ffs(__ballot_sync(0xffffffffu, leader)) - 1);
+            if (g < 0 || g >= p.n_units) g = -1;
             if (leader) {
-                mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kTileBytes);
-                for (int bx = 0; bx < Lay::kBoxes; ++bx) {
-                    const uint32_t dst = sbase + Lay::kV + st * Lay::kTileBytes + bx * 16384;
-                    if constexpr (kMode == 3)
-                        tma_load_5d(dst, &tmap_v, bar(kBarVFull + st), bx * 64, hk_src,
-                                    row % p.u_Ls, bo, row / p.u_Ls, keep);
-                    else
-                        tma_load_4d(dst, &tmap_v, bar(kBarVFull + st), bx * 64, hk, row, b, keep);
-                }
+                unit_slot[slot] = g;
+                mbar_arrive(bar(kBarUnitFull + slot));
             }
-            last_v[st] = n;
+            __syncwarp();
+            return g;
+        };
+        uint32_t N = 0;       // K/V blocks loaded by this CTA so far
+        int qn = 0;           // units with a non-empty walk so far (query barrier phases)
+        int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};   // last block loaded per stage
+        bool ok = true;
+        for (int i = 0; ok; ++i) {
+            const int g = kPersist == 2 ? publish_unit(i) : (i == 0 ? g_first : consume_unit(i));
+            if (g < 0) break;
+            Unit<kMode> U;
+            if (i == 0 && kPersist != 2) U = first;
+            else U.setup(g, p);
+            if (U.n_blocks == 0) continue;
+            // the shard's last query pair meets every shard the shard visits, in either layout
+            const bool tracing = p.trace != nullptr && U.bh == 0 && U.pair == p.n_pair - 1;
+            if (tracing && leader)
+                for (int t = 0; t < p.P; ++t)
+                    if (in_bounds(U.r * p.P + t, 1, p.P * p.P, p.status)) p.trace[U.r * p.P + t] = -1;
+            if constexpr (kPersist != 0) {
+                // query tiles: reloaded once the previous unit's products of the tile (the last
+                // readers of its buffer) have finished
+                for (int tq = 0; tq < kTiles; ++tq) {
+                    if (qn > 0 &&
+                        !(ok = __all_sync(0xffffffffu,
+                                          mbar_wait(bar(kBarOFull + tq), (qn - 1) & 1, wc))))
+                        break;
+                    if (leader) {
+                        const uint32_t full = tq == 0 ? bar(kBarQ) : bar(kBarQ1);
+                        mbar_arrive_expect_tx(full, Lay::kTileBytes);
+                        for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                            const uint32_t dst = sbase + Lay::kQ + tq * Lay::kTileBytes + bx * 16384;
+                            const int row = U.q0 + tq * kRows;
+                            if constexpr (kMode == 3)
+                                tma_load_5d(dst, &tmap_q, full, bx * 64, U.h_src, row % p.u_Ls, U.bo,
+                                            row / p.u_Ls, once);
+                            else
+                                tma_load_4d(dst, &tmap_q, full, bx * 64, U.h, row, U.b, once);
+                        }
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+            }
+            for (int n = 0; n < U.n_blocks; ++n) {
+                U.walk.at(n);
+                if (tracing && U.walk.first_of_shard() && leader &&
+                    in_bounds(U.r * p.P + U.walk.t, 1, p.P * p.P, p.status))
+                    p.trace[U.r * p.P + U.walk.t] = U.walk.s;
+                const uint32_t Nn = N + n;
+                const int st = Nn & 1;
+                const uint32_t ph = (Nn >> 1) & 1;
+                const int row = U.walk.s * p.Ls + U.walk.kt() * kKeys;   // physical row of the tile
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc)))) break;
+                // (classic grids: thread 0 issued the first K block before the block-wide barrier)
+                if (leader && (kPersist != 0 || n > 0)) {
+                    mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kTileBytes);
+                    for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                        const uint32_t dst = sbase + Lay::kK + st * Lay::kTileBytes + bx * 16384;
+                        if constexpr (kMode == 3)
+                            tma_load_5d(dst, &tmap_k, bar(kBarKFull + st), bx * 64, U.hk_src,
+                                        row % p.u_Ls, U.bo, row / p.u_Ls, keep);
+                        else
+                            tma_load_4d(dst, &tmap_k, bar(kBarKFull + st), bx * 64, U.hk, row, U.b,
+                                        keep);
+                    }
+                }
+                last_k[st] = static_cast<int>(Nn);
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc)))) break;
+                if (leader) {
+                    mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kTileBytes);
+                    for (int bx = 0; bx < Lay::kBoxes; ++bx) {
+                        const uint32_t dst = sbase + Lay::kV + st * Lay::kTileBytes + bx * 16384;
+                        if constexpr (kMode == 3)
+                            tma_load_5d(dst, &tmap_v, bar(kBarVFull + st), bx * 64, U.hk_src,
+                                        row % p.u_Ls, U.bo, row / p.u_Ls, keep);
+                        else
+                            tma_load_4d(dst, &tmap_v, bar(kBarVFull + st), bx * 64, U.hk, row, U.b,
+                                        keep);
+                    }
+                }
+                last_v[st] = static_cast<int>(Nn);
+            }
+            N += U.n_blocks;
+            ++qn;
         }
         // let this CTA's own copies land before anyone leaves
-        mbar_wait_drain(bar(kBarQ), 0, wc);
-        mbar_wait_drain(bar(kBarQ1), 0, wc);
-        if (n_blocks > 0 && last_k[0] < 0) mbar_wait_drain(bar(kBarKFull + 0), 0, wc);
+        if (qn > 0) {
+            mbar_wait_drain(bar(kBarQ), (qn - 1) & 1, wc);
+            mbar_wait_drain(bar(kBarQ1), (qn - 1) & 1, wc);
+        } else if constexpr (kPersist == 0) {
+            // classic grid, empty walk: thread 0 still loaded both query tiles
+            mbar_wait_drain(bar(kBarQ), 0, wc);
+            mbar_wait_drain(bar(kBarQ1), 0, wc);
+        }
+        if constexpr (kPersist == 0) {
+            if (first.n_blocks > 0 && last_k[0] < 0) mbar_wait_drain(bar(kBarKFull + 0), 0, wc);
+        }
         for (int st = 0; st < 2; ++st) {
             if (last_k[st] >= 0) mbar_wait_drain(bar(kBarKFull + st), (last_k[st] >> 1) & 1, wc);
             if (last_v[st] >= 0) mbar_wait_drain(bar(kBarVFull + st), (last_v[st] >> 1) & 1, wc);
@@ -560,71 +700,91 @@ __global__ void __launch_bounds__(kThreads, 1)
             return __all_sync(0xffffffffu, mbar_wait(bar(idx), parity, wc));
         };
 
-        // an empty walk (possible only with malformed sequence boundaries) issues nothing
-        bool ok = n_blocks > 0 && wait_all(kBarQ, 0) && wait_all(kBarKFull + 0, 0);
-        if (ok) {
+        uint32_t N = 0;       // K/V blocks consumed by this CTA so far
+        int qn = 0;           // units with a non-empty walk so far
+        bool ok = true;
+        for (int i = 0; ok; ++i) {
+            const int g = i == 0 && kPersist != 2 ? g_first : consume_unit(i);
+            if (g < 0) break;
+            int n_blocks;
+            if (i == 0 && kPersist != 2) {
+                n_blocks = first.n_blocks;
+            } else {
+                Unit<kMode> U;
+                U.setup(g, p);
+                n_blocks = U.n_blocks;
+            }
+            // an empty walk (possible only with malformed sequence boundaries) issues nothing
+            if (n_blocks == 0) continue;
+            const uint32_t qpar = qn & 1;
+            const int st0 = N & 1;
+            const uint32_t ph0 = (N >> 1) & 1;
+            ok = wait_all(kBarQ, qpar) && wait_all(kBarKFull + st0, ph0);
+            if (!ok) break;
             tc_fence_after();
             if (leader) {
-                issue_qk(0, 0);
+                issue_qk(0, st0);
                 tc_commit(bar(kBarSFull + 0));
             }
             __syncwarp();
-        }
-        if (ok && (ok = wait_all(kBarQ1, 0))) {
+            if (!(ok = wait_all(kBarQ1, qpar))) break;
             tc_fence_after();
             if (leader) {
-                issue_qk(1, 0);
+                issue_qk(1, st0);
                 tc_commit(bar(kBarSFull + 1));
-                tc_commit(bar(kBarKEmpty + 0));
+                tc_commit(bar(kBarKEmpty + st0));
             }
             __syncwarp();
-        }
-        for (int n = 0; ok && n < n_blocks; ++n) {
-            const int st = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
-            const bool more = n + 1 < n_blocks;
-            const int st1 = (n + 1) & 1;
-            const uint32_t ph1 = ((n + 1) >> 1) & 1;
-            // Each wait between MMA batches costs the tensor pipe ~100 cycles even when the
-            // barrier is already complete, so barriers that gate the same batch are checked
-            // together: V and the first P half of tile 0, then its second P half and the
-            // next K block.
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait2(bar(kBarVFull + st), ph,
-                                                          bar(kBarPFull + 0), n & 1, wc))))
-                break;
-            tc_fence_after();
-            if (leader) issue_pv(0, st, 0, n > 0);
-            __syncwarp();
-            ok = more ? mbar_wait2(bar(kBarPFull + 1), n & 1, bar(kBarKFull + st1), ph1, wc)
-                      : mbar_wait(bar(kBarPFull + 1), n & 1, wc);
-            if (!(ok = __all_sync(0xffffffffu, ok))) break;
-            tc_fence_after();
-            if (leader) {
-                issue_pv(0, st, 1, true);
-                if (!more) tc_commit(bar(kBarOFull + 0));
-                if (more) {
-                    issue_qk(0, st1);
-                    tc_commit(bar(kBarSFull + 0));
+            for (int n = 0; ok && n < n_blocks; ++n) {
+                const uint32_t Nn = N + n;
+                const int st = Nn & 1;
+                const uint32_t ph = (Nn >> 1) & 1;
+                const bool more = n + 1 < n_blocks;
+                const int st1 = (Nn + 1) & 1;
+                const uint32_t ph1 = ((Nn + 1) >> 1) & 1;
+                // Each wait between MMA batches costs the tensor pipe ~100 cycles even when the
+                // barrier is already complete, so barriers that gate the same batch are checked
+                // together: V and the first P half of tile 0, then its second P half and the
+                // next K block.
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait2(bar(kBarVFull + st), ph,
+                                                              bar(kBarPFull + 0), Nn & 1, wc))))
+                    break;
+                tc_fence_after();
+                if (leader) issue_pv(0, st, 0, n > 0);
+                __syncwarp();
+                ok = more ? mbar_wait2(bar(kBarPFull + 1), Nn & 1, bar(kBarKFull + st1), ph1, wc)
+                          : mbar_wait(bar(kBarPFull + 1), Nn & 1, wc);
+                if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                tc_fence_after();
+                if (leader) {
+                    issue_pv(0, st, 1, true);
+                    if (!more) tc_commit(bar(kBarOFull + 0));
+                    if (more) {
+                        issue_qk(0, st1);
+                        tc_commit(bar(kBarSFull + 0));
+                    }
                 }
-            }
-            __syncwarp();
-            if (!(ok = wait_all(kBarPFull + 2, n & 1))) break;
-            tc_fence_after();
-            if (leader) issue_pv(1, st, 0, n > 0);
-            __syncwarp();
-            if (!(ok = wait_all(kBarPFull + 3, n & 1))) break;
-            tc_fence_after();
-            if (leader) {
-                issue_pv(1, st, 1, true);
-                tc_commit(bar(kBarVEmpty + st));
-                if (!more) tc_commit(bar(kBarOFull + 1));
-                if (more) {
-                    issue_qk(1, st1);
-                    tc_commit(bar(kBarSFull + 1));
-                    tc_commit(bar(kBarKEmpty + st1));
+                __syncwarp();
+                if (!(ok = wait_all(kBarPFull + 2, Nn & 1))) break;
+                tc_fence_after();
+                if (leader) issue_pv(1, st, 0, n > 0);
+                __syncwarp();
+                if (!(ok = wait_all(kBarPFull + 3, Nn & 1))) break;
+                tc_fence_after();
+                if (leader) {
+                    issue_pv(1, st, 1, true);
+                    tc_commit(bar(kBarVEmpty + st));
+                    if (!more) tc_commit(bar(kBarOFull + 1));
+                    if (more) {
+                        issue_qk(1, st1);
+                        tc_commit(bar(kBarSFull + 1));
+                        tc_commit(bar(kBarKEmpty + st1));
+                    }
                 }
+                __syncwarp();
             }
-            __syncwarp();
+            N += n_blocks;
+            ++qn;
         }
         // every MMA this CTA issued has finished before TMEM is released
         if (leader) tc_commit(bar(kBarDone));
@@ -639,168 +799,192 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_off + Lay::col_s(tq);
         const uint32_t tO = tmem + lane_off + Lay::col_o(tq);
-        const int row_local = q0_local + tq * kRows + row;   // within shard r
-        const int row_pos = position(r, row_local, p.P, p.Ls, kZig ? 1 : 0);
-        int seq_lo = 0, seq_hi = 0;                            // packed sequences only
-        if constexpr (kVarlen) {
-            if (row_local < p.Ls)
-                seq_bounds(p.cu_seqlens, p.n_seqs, row_pos, p.causal, seq_lo, seq_hi, p.status);
-            else seq_hi = -1;
-        }
         const float sl2 = p.scale_log2;
-
-        float m = -INFINITY;   // running max of scaled scores, base-2 units
-        float l = 0.f;         // running denominator, relative to m
+        uint32_t N = 0;       // K/V blocks of the units this CTA has run
+        int qn = 0;           // units with a non-empty walk so far
         bool ok = true;
-        for (int n = 0; n < n_blocks; ++n) {
-            walk.at(n);
-            ok = mbar_wait(bar(kBarSFull + tq), n & 1, wc);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-
-            uint32_t sraw[128];
-            tmem_ld128(tS, sraw);
-            float sv[128];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) sv[c] = u2f(sraw[c]);
-
-            // visible columns: inside the shard, and under causal masking key
-            // position <= query position (global positions)
-            int lim = min(kKeys - 1, p.Ls - walk.kt() * kKeys - 1);
-            int lo_lim = 0;
+        for (int i = 0; ok; ++i) {
+            const int g = i == 0 && kPersist != 2 ? g_first : consume_unit(i);
+            if (g < 0) break;
+            Unit<kMode> U;
+            if (i == 0 && kPersist != 2) U = first;
+            else U.setup(g, p);
+            const int n_blocks = U.n_blocks;
+            const int row_local = U.q0_local + tq * kRows + row;   // within shard r
+            const int row_pos = position(U.r, row_local, p.P, p.Ls, kZig ? 1 : 0);
+            int seq_lo = 0, seq_hi = 0;                            // packed sequences only
             if constexpr (kVarlen) {
-                lim = min(lim, seq_hi - walk.pos0());
-                lo_lim = seq_lo - walk.pos0();
-            } else if (p.causal) {
-                lim = min(lim, row_pos - walk.pos0());
-            }
-            if (lim < kKeys - 1 || lo_lim > 0) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) sv[c] = (c > lim || c < lo_lim) ? -INFINITY : sv[c];
+                if (row_local < p.Ls)
+                    seq_bounds(p.cu_seqlens, p.n_seqs, row_pos, p.causal, seq_lo, seq_hi, p.status);
+                else seq_hi = -1;
             }
 
-            float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
-            float mx2 = fmaxf(sv[4], sv[5]), mx3 = fmaxf(sv[6], sv[7]);
-#pragma unroll
-            for (int c = 8; c < 128; c += 8) {
-                mx0 = fmax3(mx0, sv[c], sv[c + 1]);
-                mx1 = fmax3(mx1, sv[c + 2], sv[c + 3]);
-                mx2 = fmax3(mx2, sv[c + 4], sv[c + 5]);
-                mx3 = fmax3(mx3, sv[c + 6], sv[c + 7]);
-            }
-            const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
-            const float m_new = fmaxf(m, m_blk);
-            const bool raise = m_new > m + kRescaleThreshold;   // always on the first finite block
-            const float m_ref = raise ? m_new : m;
-            const float alpha = raise ? ex2(m - m_ref) : 1.f;    // ex2(-inf) = 0
-            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            float m = -INFINITY;   // running max of scaled scores, base-2 units
+            float l = 0.f;         // running denominator, relative to m
+            for (int n = 0; n < n_blocks; ++n) {
+                U.walk.at(n);
+                const uint32_t Nn = N + n;
+                ok = mbar_wait(bar(kBarSFull + tq), Nn & 1, wc);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
 
-            // p = 2^(s * scale*log2(e) - m_ref) for column pairs (packed fp32 FMA and
-            // adds), packed to bf16 pairs and written over S as the A operand of P V,
-            // in two halves of 64 keys so that the first half's P V overlaps the
-            // second half's exponentials.
-            const uint64_t scale2 = f2pack(sl2, sl2), negm2 = f2pack(neg_m, neg_m);
-            uint64_t sum_a = 0, sum_b = 0;
+                uint32_t sraw[128];
+                tmem_ld128(tS, sraw);
+                float sv[128];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = 64 * half + 2 * i;
-                    float x0, x1;
-                    f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), scale2, negm2), x0, x1);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    if (i & 1) sum_b = fadd2(sum_b, f2pack(p0, p1));
-                    else sum_a = fadd2(sum_a, f2pack(p0, p1));
-                    pk[i] = pack_bf16x2(p0, p1);
+                for (int c = 0; c < 128; ++c) sv[c] = u2f(sraw[c]);
+
+                // visible columns: inside the shard, and under causal masking key
+                // position <= query position (global positions)
+                int lim = min(kKeys - 1, p.Ls - U.walk.kt() * kKeys - 1);
+                int lo_lim = 0;
+                if constexpr (kVarlen) {
+                    lim = min(lim, seq_hi - U.walk.pos0());
+                    lo_lim = seq_lo - U.walk.pos0();
+                } else if (p.causal) {
+                    lim = min(lim, row_pos - U.walk.pos0());
                 }
-                tmem_st32(tS + 32 * half, pk);
-                // O was last written by P V of the previous block, which finished
-                // before this block's S (same issuing thread, in order); it is rescaled
-                // before this block's first P V can start accumulating into it.
-                if (half == 0 && n > 0 && __any_sync(0xffffffffu, raise)) {
+                if (lim < kKeys - 1 || lo_lim > 0) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + 32 * c, o);
+                    for (int c = 0; c < 128; ++c) sv[c] = (c > lim || c < lo_lim) ? -INFINITY : sv[c];
+                }
+
+                float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
+                float mx2 = fmaxf(sv[4], sv[5]), mx3 = fmaxf(sv[6], sv[7]);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-                        tmem_st32(tO + 32 * c, o);
+                for (int c = 8; c < 128; c += 8) {
+                    mx0 = fmax3(mx0, sv[c], sv[c + 1]);
+                    mx1 = fmax3(mx1, sv[c + 2], sv[c + 3]);
+                    mx2 = fmax3(mx2, sv[c + 4], sv[c + 5]);
+                    mx3 = fmax3(mx3, sv[c + 6], sv[c + 7]);
+                }
+                const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+                const float m_new = fmaxf(m, m_blk);
+                const bool raise = m_new > m + kRescaleThreshold;   // always on the first finite block
+                const float m_ref = raise ? m_new : m;
+                const float alpha = raise ? ex2(m - m_ref) : 1.f;    // ex2(-inf) = 0
+                const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+
+                // p = 2^(s * scale*log2(e) - m_ref) for column pairs (packed fp32 FMA and
+                // adds), packed to bf16 pairs and written over S as the A operand of P V,
+                // in two halves of 64 keys so that the first half's P V overlaps the
+                // second half's exponentials.
+                const uint64_t scale2 = f2pack(sl2, sl2), negm2 = f2pack(neg_m, neg_m);
+                uint64_t sum_a = 0, sum_b = 0;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i2 = 0; i2 < 32; ++i2) {
+                        const int c = 64 * half + 2 * i2;
+                        float x0, x1;
+                        f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), scale2, negm2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        if (i2 & 1) sum_b = fadd2(sum_b, f2pack(p0, p1));
+                        else sum_a = fadd2(sum_a, f2pack(p0, p1));
+                        pk[i2] = pack_bf16x2(p0, p1);
                     }
+                    tmem_st32(tS + 32 * half, pk);
+                    // O was last written by P V of the previous block, which finished
+                    // before this block's S (same issuing thread, in order); it is rescaled
+                    // before this block's first P V can start accumulating into it.
+                    if (half == 0 && n > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + 32 * c, o);
+#pragma unroll
+                            for (int i2 = 0; i2 < 32; ++i2) o[i2] = f2u(u2f(o[i2]) * alpha);
+                            tmem_st32(tO + 32 * c, o);
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(bar(kBarPFull + 2 * tq + half));
                 }
-                tc_fence_before();
-                mbar_arrive(bar(kBarPFull + 2 * tq + half));
+                float sa0, sa1;
+                f2unpack(fadd2(sum_a, sum_b), sa0, sa1);
+                l = l * alpha + (sa0 + sa1);
+                m = m_ref;
             }
-            float sa0, sa1;
-            f2unpack(fadd2(sum_a, sum_b), sa0, sa1);
-            l = l * alpha + (sa0 + sa1);
-            m = m_ref;
-        }
+            if (!ok) break;
 
-        // an empty walk leaves O unwritten: its rows saw no key and get 0 and -inf.  The
-        // staging below reuses the tile's query buffer, so its load must have landed.
-        const bool empty = n_blocks == 0;
-        if (ok) {
-            ok = empty ? mbar_wait(bar(tq == 0 ? kBarQ : kBarQ1), 0, wc)
-                       : mbar_wait(bar(kBarOFull + tq), 0, wc);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        if (ok) {
+            // An empty walk leaves O unwritten: its rows saw no key and get 0 and -inf.
+            // Classic grids stage the output in the tile's query buffer, whose load must then
+            // have landed; persistent grids stage it in a buffer of their own.
+            const bool empty = n_blocks == 0;
+            if (!empty) ok = mbar_wait(bar(kBarOFull + tq), qn & 1, wc);
+            else if constexpr (kPersist == 0) ok = mbar_wait(bar(tq == 0 ? kBarQ : kBarQ1), 0, wc);
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;
             if (!empty) tc_fence_after();
             const bool valid = row_local < p.Ls;
             const float inv_l = l > 0.f ? 1.f / l : 0.f;        // a row that saw no key: 0
             // index of (row, head) among the output's rows of D elements, for this warp's
             // first row; the warp's 32 rows lie in one tile, so `ostride` apart
-            const int x0 = q0_local + tq * kRows + quarter * 32;   // within shard r
-            const int g0 = r * p.Ls + x0;
-            size_t orow0 = (static_cast<size_t>(b) * p.L + g0) * p.H + h;
+            const int x0 = U.q0_local + tq * kRows + quarter * 32;   // within shard r
+            const int g0 = U.r * p.Ls + x0;
+            size_t orow0 = (static_cast<size_t>(U.b) * p.L + g0) * p.H + U.h;
             size_t ostride = p.H;
             if constexpr (kMode == 3) {
                 const int rs = g0 / p.u_Ls;
-                orow0 = (static_cast<size_t>(rs * p.u_B + bo) * p.u_Ls + (g0 - rs * p.u_Ls)) *
-                            p.u_H + h_src;
+                orow0 = (static_cast<size_t>(rs * p.u_B + U.bo) * p.u_Ls + (g0 - rs * p.u_Ls)) *
+                            p.u_H + U.h_src;
                 ostride = p.u_H;
             }
-            // The rows go out through the warp's 32-row slice of this tile's query buffer,
-            // free once O is final (the tile's last Q K^T finished before its last P V), so
-            // that every global store covers whole rows instead of one 16-byte piece of 32
-            // rows.  A thread writes its row's 16-byte chunk c at slot c ^ (row mod
+            // The rows go out through a 32-row staging slice of the warp (the tile's query
+            // buffer, free once O is final -- the tile's last Q K^T finished before its last
+            // P V -- or the persistent grids' own buffer), half of the columns at a time, so
+            // that every global store covers whole row halves instead of one 16-byte piece
+            // of 32 rows.  A thread writes its row's 16-byte chunk c at slot c ^ (row mod
             // kChunks): conflict-free for both the row-wise writes and the chunk-wise reads.
-            constexpr int kChunks = D / 8;                     // 16-byte chunks per row
+            constexpr int kHalfCols = D / 2;
+            constexpr int kChunks = kHalfCols / 8;             // 16-byte chunks per staged row
             constexpr int kRowsPerStore = 32 / kChunks;        // rows one warp store covers
-            uint8_t* stage = smem + Lay::kQ + tq * Lay::kTileBytes + quarter * 32 * (2 * D);
+            uint8_t* stage = kPersist != 0
+                                 ? smem + Lay::kStage + (warp - 4) * 32 * (2 * kHalfCols)
+                                 : smem + Lay::kQ + tq * Lay::kTileBytes + quarter * 32 * (2 * D);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32] = {};
-                if (!empty) tmem_ld32(tO + 32 * c, o);
-                uint32_t pk[16];
+            for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+                for (int c = 0; c < kHalfCols / 32; ++c) {
+                    uint32_t o[32] = {};
+                    if (!empty) tmem_ld32(tO + hh * kHalfCols + 32 * c, o);
+                    uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int slot = (4 * c + j) ^ (lane & (kChunks - 1));
-                    *reinterpret_cast<uint4*>(stage + lane * (2 * D) + slot * 16) =
-                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    for (int i2 = 0; i2 < 16; ++i2)
+                        pk[i2] = pack_bf16x2(u2f(o[2 * i2]) * inv_l, u2f(o[2 * i2 + 1]) * inv_l);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int slot = (4 * c + j) ^ (lane & (kChunks - 1));
+                        *reinterpret_cast<uint4*>(stage + lane * (2 * kHalfCols) + slot * 16) =
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
                 }
-            }
-            __syncwarp();
-            {
-                const int sub = lane / kChunks, cc = lane % kChunks;
+                __syncwarp();
+                {
+                    const int sub = lane / kChunks, cc = lane % kChunks;
 #pragma unroll
-                for (int k = 0; k < 32 / kRowsPerStore; ++k) {
-                    const int rr = k * kRowsPerStore + sub;         // row within the warp's 32
-                    const uint4 val = *reinterpret_cast<const uint4*>(
-                        stage + rr * (2 * D) + ((cc ^ (rr & (kChunks - 1))) * 16));
-                    const long long idx = static_cast<long long>(orow0 + rr * ostride) * D + cc * 8;
-                    if (x0 + rr < p.Ls && in_bounds(idx, 8, p.out_elems, p.status))
-                        *reinterpret_cast<uint4*>(p.out + idx) = val;
+                    for (int k = 0; k < 32 / kRowsPerStore; ++k) {
+                        const int rr = k * kRowsPerStore + sub;         // row within the warp's 32
+                        const uint4 val = *reinterpret_cast<const uint4*>(
+                            stage + rr * (2 * kHalfCols) + ((cc ^ (rr & (kChunks - 1))) * 16));
+                        const long long idx =
+                            static_cast<long long>(orow0 + rr * ostride) * D + hh * kHalfCols + cc * 8;
+                        if (x0 + rr < p.Ls && in_bounds(idx, 8, p.out_elems, p.status))
+                            *reinterpret_cast<uint4*>(p.out + idx) = val;
+                    }
                 }
+                __syncwarp();
             }
             if (valid && p.lse != nullptr &&
                 in_bounds(static_cast<long long>(orow0 + lane * ostride), 1, p.lse_elems, p.status))
                 p.lse[orow0 + lane * ostride] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            if (!empty) {
+                // this warp's reads of O are complete before the next unit's first P V
+                // (gated on its P, which this warp writes later) overwrites it
+                N += n_blocks;
+                ++qn;
+            }
         }
     }
 
@@ -811,16 +995,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int kMode>
+template <int D, int kMode, int kPersist>
 cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv)
 {
-    using Lay = Layout<D>;
+    using Lay = Layout<D, kPersist != 0>;
     static std::atomic<int> configured[kMaxDevices];  // shared-memory limit set, per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = smem_limit_once(configured, dev, ring_attn_bf16_kernel<D, kMode>, Lay::kSmem);
+    e = smem_limit_once(configured, dev, ring_attn_bf16_kernel<D, kMode, kPersist>, Lay::kSmem);
     if (e != cudaSuccess) return e;
     Params p;
     p.out = static_cast<__nv_bfloat16*>(a.out);
@@ -850,11 +1034,47 @@ cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap
     p.out_elems = static_cast<long long>(a.B) * a.L * a.H * D;
     p.lse_elems = static_cast<long long>(a.B) * a.L * a.H;
     p.sched_elems = static_cast<int>(a.P * p.n_pair);
-    const long long grid = static_cast<long long>(a.B) * a.H * a.P * p.n_pair;
-    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    ring_attn_bf16_kernel<D, kMode><<<static_cast<unsigned>(grid), kThreads, Lay::kSmem, a.stream>>>(
-        tq, tk, tv, p);
+    p.claim = nullptr;
+    p.claim_index = 0;
+    p.claim_extent = 0;
+    const long long units = static_cast<long long>(a.B) * a.H * a.P * p.n_pair;
+    if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    p.n_units = static_cast<int>(units);
+    long long grid = units;
+    if constexpr (kPersist != 0) {
+        int sms = 148;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (grid > sms) grid = sms;
+    }
+    if constexpr (kPersist == 2) {
+        // the work counter at the end of the caller's schedule array, zeroed in stream order
+        const VarlenSchedLayout lay = varlen_sched_layout(a.L, a.P);
+        p.claim_index = lay.counters;
+        p.claim_extent = lay.total;
+        p.claim = const_cast<int*>(a.schedule) + lay.counters;
+        e = cudaMemsetAsync(p.claim, 0, sizeof(int), a.stream);
+        if (e != cudaSuccess) return e;
+    }
+    ring_attn_bf16_kernel<D, kMode, kPersist>
+        <<<static_cast<unsigned>(grid), kThreads, Lay::kSmem, a.stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
+}
+
+template <int D, int kMode>
+cudaError_t launch_mode(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv)
+{
+    // persistent grids where they pay: calls whose units are all equal (no causal
+    // masking) run a static round-robin; packed sequences with a schedule claim units
+    // dynamically through the schedule array's counter; everything else (causal
+    // contiguous or zigzag shards, whose heaviest-first unit order the block scheduler
+    // balances) keeps one CTA per unit
+    if constexpr (kMode == 2) {
+        if (a.schedule != nullptr) return launch_d<D, kMode, 2>(a, tq, tk, tv);
+    } else if constexpr (kMode == 0 || kMode == 3) {
+        if (!a.causal) return launch_d<D, kMode, 1>(a, tq, tk, tv);
+    }
+    return launch_d<D, kMode, 0>(a, tq, tk, tv);
 }
 
 }  // namespace
@@ -863,17 +1083,17 @@ cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tq, const CUt
                              const CUtensorMap& tv)
 {
     if (a.u_P > 0) {
-        if (a.D == 64) return launch_d<64, 3>(a, tq, tk, tv);
-        if (a.D == 128) return launch_d<128, 3>(a, tq, tk, tv);
+        if (a.D == 64) return launch_mode<64, 3>(a, tq, tk, tv);
+        if (a.D == 128) return launch_mode<128, 3>(a, tq, tk, tv);
     } else if (a.cu_seqlens != nullptr) {
-        if (a.D == 64) return launch_d<64, 2>(a, tq, tk, tv);
-        if (a.D == 128) return launch_d<128, 2>(a, tq, tk, tv);
+        if (a.D == 64) return launch_mode<64, 2>(a, tq, tk, tv);
+        if (a.D == 128) return launch_mode<128, 2>(a, tq, tk, tv);
     } else if (a.zigzag) {
-        if (a.D == 64) return launch_d<64, 1>(a, tq, tk, tv);
-        if (a.D == 128) return launch_d<128, 1>(a, tq, tk, tv);
+        if (a.D == 64) return launch_mode<64, 1>(a, tq, tk, tv);
+        if (a.D == 128) return launch_mode<128, 1>(a, tq, tk, tv);
     } else {
-        if (a.D == 64) return launch_d<64, 0>(a, tq, tk, tv);
-        if (a.D == 128) return launch_d<128, 0>(a, tq, tk, tv);
+        if (a.D == 64) return launch_mode<64, 0>(a, tq, tk, tv);
+        if (a.D == 128) return launch_mode<128, 0>(a, tq, tk, tv);
     }
     return cudaErrorInvalidValue;
 }

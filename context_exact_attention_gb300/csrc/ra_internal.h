@@ -54,11 +54,17 @@ struct AttnArgs {
 // Packed-sequence schedule (ring_attn_varlen_schedule), in int32 entries: the forward's
 // query-tile pairs, the backward's key tiles and query tiles, each a permutation of the
 // units of one (batch, head) given by their natural index (shard * per-shard units +
-// tile or pair), heaviest first; then scratch for the work counts of all three.
+// tile or pair), heaviest first; then scratch for the work counts of all three; then
+// kCounters work counters of the persistent kernels (a claim counter and a finished-CTA
+// counter per kernel: forward, backward key tiles, backward query tiles), zeroed by the
+// schedule kernel and reset to zero by the last CTA of each launch that uses them.
+constexpr int kCounters = 8;
 struct VarlenSchedLayout {
     long long n_t, n_pair;           // 128-row tiles and tile pairs per shard
     long long fwd, bwd_k, bwd_q;     // offsets of the three orders
-    long long scratch, total;        // offset of the scratch, total entries
+    long long scratch;               // offset of the scratch
+    long long counters;              // offset of the work counters
+    long long total;                 // total entries
 };
 inline VarlenSchedLayout varlen_sched_layout(int L, int P)
 {
@@ -70,7 +76,8 @@ inline VarlenSchedLayout varlen_sched_layout(int L, int P)
     s.bwd_k = s.fwd + P * s.n_pair;
     s.bwd_q = s.bwd_k + P * s.n_t;
     s.scratch = s.bwd_q + P * s.n_t;
-    s.total = s.scratch + s.scratch;
+    s.counters = s.scratch + s.scratch;
+    s.total = s.counters + kCounters;
     return s;
 }
 cudaError_t launch_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, int P, int causal,

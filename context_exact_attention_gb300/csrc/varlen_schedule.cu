@@ -71,6 +71,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int Ls = L / P;
     const int max_work = P * static_cast<int>(lay.n_t);
+    // the persistent kernels' work counters start at zero
+    if (blockIdx.x == 0 && threadIdx.x < kCounters &&
+        in_bounds(lay.counters + threadIdx.x, 1, lay.total, status))
+        sched[lay.counters + threadIdx.x] = 0;
     const int nb = min(max_work + 1, kMaxBins);
     {
         // kind 0: forward query-tile pairs; 1: backward key tiles; 2: backward query tiles

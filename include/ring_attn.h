@@ -401,10 +401,16 @@ typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_ZIGZAG = 1, RA_LAYOUT_PACKED 
  *                  ring_attn_varlen_schedule wrote for the same cu_seqlens, L and P
  *                  (at least ring_attn_varlen_schedule_bytes(L, P) bytes: the kernels
  *                  read its entries by unit index, and the descriptor carries no size
- *                  to check).  It sets only which CTA takes which work unit (heaviest
- *                  first instead of position order): the results are the same bits
- *                  either way.  Other contents of an array of that size give undefined
- *                  results, never out-of-bounds accesses.
+ *                  to check).  It sets only which work unit runs when (heaviest first
+ *                  instead of position order, and with it the forward runs one
+ *                  persistent CTA per SM that claims units from a counter): the
+ *                  results are the same bits either way.  Other contents of an array
+ *                  of that size give undefined results, never out-of-bounds accesses.
+ *                  The forward writes that work counter (the array's last entries):
+ *                  it zeroes it in stream order before its kernel, so the counter's
+ *                  previous contents do not matter, but calls that share one
+ *                  schedule array must not overlap on the GPU (order them on one
+ *                  stream).
  * The descriptor is read during the call only.
  */
 typedef struct {
@@ -419,7 +425,9 @@ typedef struct {
 
 /*
  * ring_attn_varlen_schedule_bytes -- device bytes ring_attn_varlen_schedule writes for
- * L packed rows over P shards (0 when L < 1, P < 1 or L % P != 0).
+ * L packed rows over P shards (0 when L < 1, P < 1 or L % P != 0): with n_t = ceil(L/P
+ * / 128) tiles and n_pair = ceil(n_t / 2) tile pairs per shard,
+ * 4 * (2 * P * (n_pair + 2 * n_t) + 8).
  */
 unsigned long long ring_attn_varlen_schedule_bytes(int L, int P);
 
@@ -445,7 +453,9 @@ unsigned long long ring_attn_varlen_schedule_bytes(int L, int P);
  *             contents give a poor order, never out-of-bounds accesses).
  * schedule:   DEVICE memory of at least ring_attn_varlen_schedule_bytes(L, P) bytes,
  *             4-byte aligned, owned by the caller; written by the launched kernel, so
- *             read it only in work ordered after it on the device.
+ *             read it only in work ordered after it on the device.  Layout (int32):
+ *             the three orders, a scratch area of the same size, then eight work
+ *             counters of the persistent kernels that use the schedule.
  * Errors: RA_ERR_INVALID_ARG (NULL pointer, n_seqs < 1, L < 1, P < 1, P > L, short
  * schedule), RA_ERR_NOT_DIVISIBLE (L % P != 0), RA_ERR_MISALIGNED, RA_ERR_CUDA.
  */

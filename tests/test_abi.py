@@ -216,14 +216,15 @@ def test_descriptor_layout_and_argument_errors(lib):
 
 def test_varlen_schedule_size_and_argument_errors(lib):
     """ring_attn_varlen_schedule_bytes counts three unit orders (forward tile pairs,
-    backward key tiles, backward query tiles) plus a scratch of the same size, and
-    ring_attn_varlen_schedule rejects bad arguments before launching anything."""
+    backward key tiles, backward query tiles), a scratch of the same size and eight
+    work counters of the persistent kernels, and ring_attn_varlen_schedule rejects bad
+    arguments before launching anything."""
     def n_units(L, P):
         n_t = -(-(L // P) // 128)
         return n_t, -(-n_t // 2)
     for L, P in ((32768, 8), (1000, 4), (1, 1), (4096, 1), (300, 3)):
         n_t, n_pair = n_units(L, P)
-        assert lib.ring_attn_varlen_schedule_bytes(L, P) == 8 * P * (n_pair + 2 * n_t)
+        assert lib.ring_attn_varlen_schedule_bytes(L, P) == 8 * P * (n_pair + 2 * n_t) + 4 * 8
     assert lib.ring_attn_varlen_schedule_bytes(1000, 3) == 0
     assert lib.ring_attn_varlen_schedule_bytes(0, 1) == 0
     assert lib.ring_attn_varlen_schedule_bytes(4, 8) == 0

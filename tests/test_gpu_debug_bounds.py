@@ -71,7 +71,8 @@ def _every_entry_point():
     qp, kp, vp = (t[0].to(DEV) for t in make_qkv(1, Lp, 2, 128, seed=74, dtype=torch.bfloat16))
     dp = _bf16(Lp, 2, 128, seed=75)
     sched = cea.varlen_schedule(cu, Lp, 4, True)
-    res.append(sched[: sched.numel() // 2].clone())     # the three orders (then scratch)
+    n_t = (Lp // 4 + 127) // 128
+    res.append(sched[: 4 * ((n_t + 1) // 2) + 2 * 4 * n_t].clone())   # the three orders
     for s in (None, sched):
         out, lse = cea.ring_attn_fwd_varlen(qp, kp, vp, cu, P=4, causal=True, schedule=s)
         res += [out, lse, *cea.ring_attn_bwd_varlen(qp, kp, vp, out, lse, dp, cu, P=4,
