@@ -89,7 +89,8 @@ enum : int {
     kBarQ1 = 18,     // query tile 1 (tile 0 on kBarQ), so that tile 0's first S starts earlier
     kBarUnitFull = 19,   // +slot: dynamic grids, the producer published a unit
     kBarUnitEmpty = 21,  // +slot: every consumer warp has read it
-    kBarCount = 23
+    kBarQEmpty = 23,     // +tile: persistent grids, the unit's last Q K^T of the tile finished
+    kBarCount = 25
 };
 constexpr int kUnitReaders = 1 + 8;   // the MMA warp and the eight softmax warps
 
@@ -345,6 +346,14 @@ struct Unit {
     // two (batch, head) pairs interleaved; packed sequences take the schedule's order.
     __device__ __forceinline__ void setup(int g, const Params& p)
     {
+        decode(g, p);
+        int lo = 0, hi = 0;
+        if constexpr (kMode == 2) pair_bounds(p, lo, hi);
+        finish(p, lo, hi);
+    }
+    // (batch, head), shard and pair of unit g
+    __device__ __forceinline__ void decode(int g, const Params& p)
+    {
         const int units_per_bh = p.P * p.n_pair;
         int u;
         unit_of_block(g, p.B * p.H, units_per_bh, bh, u);
@@ -362,6 +371,22 @@ struct Unit {
                 }
             }
         }
+    }
+    // packed sequences: the positions the pair's queries see, from the first row's sequence
+    // start to the last row's (causal) position or sequence end
+    __device__ __forceinline__ void pair_bounds(const Params& p, int& lo, int& hi) const
+    {
+        const int ql = pair * (kTiles * kRows);
+        const int last = min(p.Ls - 1, ql + kTiles * kRows - 1);
+        int lo0, hi0, lo1, hi1;
+        seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + ql, p.causal, lo0, hi0, p.status);
+        seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + last, p.causal, lo1, hi1, p.status);
+        lo = lo0;
+        hi = hi1;
+    }
+    // everything else, from the decoded unit (lo, hi: packed sequences' pair bounds)
+    __device__ __forceinline__ void finish(const Params& p, int lo, int hi)
+    {
         b = bh / p.H;
         h = bh - b * p.H;
         hk = h / p.group;                       // key/value head of this query head
@@ -378,12 +403,7 @@ struct Unit {
         q0 = r * p.Ls + q0_local;
         const int last = min(p.Ls - 1, q0_local + kTiles * kRows - 1);
         if constexpr (kMode == 2) {
-            // visible positions of the pair: from the first row's sequence start to the
-            // last row's (causal) position or sequence end
-            int lo0, hi0, lo1, hi1;
-            seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + q0_local, p.causal, lo0, hi0, p.status);
-            seq_bounds(p.cu_seqlens, p.n_seqs, r * p.Ls + last, p.causal, lo1, hi1, p.status);
-            walk.init(r, p.P, p.n_kt, p.Ls, lo0, hi1);
+            walk.init(r, p.P, p.n_kt, p.Ls, lo, hi);
         } else if constexpr (kMode == 1) {
             // last query position of the pair (positions rise within each chunk, and the
             // late chunk lies after the early one)
@@ -392,6 +412,8 @@ struct Unit {
                       max(position(r, last, p.P, p.Ls, 1), position(r, mid, p.P, p.Ls, 1)));
         } else {
             walk.init(r, p.P, p.n_kt, p.Ls, p.causal, last);
+            (void)lo;
+            (void)hi;
         }
         n_blocks = walk.n_blocks;
     }
@@ -433,36 +455,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_addr(smem);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kBar + kBarCount * 8);
     int* abort_flag = reinterpret_cast<int*>(smem + Lay::kBar + kBarCount * 8 + 4);
+    // dynamic grids: two ring slots of (unit, shard, pair, walk bounds lo and hi, number
+    // of K/V blocks), everything the other warps need to run the unit without loads
+    constexpr int kSlotInts = 6;
     volatile int* unit_slot = reinterpret_cast<volatile int*>(smem + Lay::kBar + kBarCount * 8 + 8);
     auto bar = [&](int i) -> uint32_t { return sbase + Lay::kBar + 8u * i; };
-    static_assert(kBarCount * 8 + 16 <= 256, "barrier area");
+    static_assert(kBarCount * 8 + 8 + 2 * kSlotInts * 4 <= 256, "barrier area");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr bool kZig = kMode == 1;
     constexpr bool kVarlen = kMode == 2;
 
-    // The i-th unit of this CTA (-1: no more).  Dynamic grids: the consumers' side of the
-    // ring; the producer publishes (publish_unit below).
+    // The i-th unit of this CTA, set up in V (returns -1: no more).  Dynamic grids: the
+    // consumers' side of the ring; the producer publishes (publish_unit below).
     WaitCtx wc{abort_flag, p.status, p.timeout_ns};
-    auto consume_unit = [&](int i) -> int {
-        if constexpr (kPersist == 0) return i == 0 ? static_cast<int>(blockIdx.x) : -1;
-        if constexpr (kPersist == 1) {
+    auto consume_unit = [&](int i, Unit<kMode>& V) -> int {
+        if constexpr (kPersist != 2) {
             const long long g = blockIdx.x + static_cast<long long>(i) * gridDim.x;
-            return g < p.n_units ? static_cast<int>(g) : -1;
+            if (g >= p.n_units || (kPersist == 0 && i > 0)) return -1;
+            V.setup(static_cast<int>(g), p);
+            return static_cast<int>(g);
         }
         const int slot = i & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarUnitFull + slot), (i >> 1) & 1, wc)))
             return -1;
-        const int g = unit_slot[slot];
+        volatile int* e = unit_slot + kSlotInts * slot;
+        const int g = e[0];
+        if (g >= 0) {
+            int u;
+            unit_of_block(g, p.B * p.H, p.P * p.n_pair, V.bh, u);
+            V.r = e[1];
+            V.pair = e[2];
+            V.finish(p, e[3], e[4]);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarUnitEmpty + slot));
         return g;
     };
 
     Unit<kMode> first;
-    const int g_first = kPersist == 2 ? -1 : consume_unit(0);
-    if (g_first >= 0) first.setup(g_first, p);
+    const int g_first = kPersist == 2 ? -1 : consume_unit(0, first);
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQ), 1);
@@ -477,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(kBarOFull + i), 1);
             mbar_init(bar(kBarUnitFull + i), 1);
             mbar_init(bar(kBarUnitEmpty + i), kUnitReaders);
+            mbar_init(bar(kBarQEmpty + i), 1);
         }
         mbar_init(bar(kBarDone), 1);
         mbar_init(bar(kBarQ1), 1);
@@ -542,19 +576,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint64_t keep = l2_policy_evict_last();    // K/V: read by every tile pair of the head
         const uint64_t once = l2_policy_evict_first();
-        // Dynamic grids: claim the i-th unit and publish it to the other warps (-1: done)
-        auto publish_unit = [&](int i) -> int {
+        // Dynamic grids: claim the i-th unit, set it up, and publish it with its number of
+        // K/V blocks to the other warps (-1: done)
+        auto publish_unit = [&](int i, Unit<kMode>& U) -> int {
             const int slot = i & 1;
-            if (i >= 2 &&
-                !__all_sync(0xffffffffu, mbar_wait(bar(kBarUnitEmpty + slot), ((i - 2) >> 1) & 1, wc)))
-                return -1;
             int g = -1;
             if (leader && in_bounds(p.claim_index, 1, p.claim_extent, p.status))
                 g = atomicAdd(p.claim, 1);
             g = __shfl_sync(0xffffffffu, g, __ffs(__ballot_sync(0xffffffffu, leader)) - 1);
             if (g < 0 || g >= p.n_units) g = -1;
+            int lo = 0, hi = 0;
+            if (g >= 0) {
+                U.decode(g, p);
+                if constexpr (kMode == 2) U.pair_bounds(p, lo, hi);
+                U.finish(p, lo, hi);
+            }
+            if (i >= 2 &&
+                !__all_sync(0xffffffffu, mbar_wait(bar(kBarUnitEmpty + slot), ((i - 2) >> 1) & 1, wc)))
+                return -1;
             if (leader) {
-                unit_slot[slot] = g;
+                volatile int* e = unit_slot + kSlotInts * slot;
+                e[0] = g;
+                e[1] = U.r;
+                e[2] = U.pair;
+                e[3] = lo;
+                e[4] = hi;
+                e[5] = g >= 0 ? U.n_blocks : 0;
                 mbar_arrive(bar(kBarUnitFull + slot));
             }
             __syncwarp();
@@ -565,11 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};   // last block loaded per stage
         bool ok = true;
         for (int i = 0; ok; ++i) {
-            const int g = kPersist == 2 ? publish_unit(i) : (i == 0 ? g_first : consume_unit(i));
-            if (g < 0) break;
             Unit<kMode> U;
-            if (i == 0 && kPersist != 2) U = first;
-            else U.setup(g, p);
+            int g;
+            if (kPersist == 2) g = publish_unit(i, U);
+            else if (i == 0) {
+                g = g_first;
+                U = first;
+            } else {
+                g = consume_unit(i, U);
+            }
+            if (g < 0) break;
             if (U.n_blocks == 0) continue;
             // the shard's last query pair meets every shard the shard visits, in either layout
             const bool tracing = p.trace != nullptr && U.bh == 0 && U.pair == p.n_pair - 1;
@@ -577,12 +629,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < p.P; ++t)
                     if (in_bounds(U.r * p.P + t, 1, p.P * p.P, p.status)) p.trace[U.r * p.P + t] = -1;
             if constexpr (kPersist != 0) {
-                // query tiles: reloaded once the previous unit's products of the tile (the last
-                // readers of its buffer) have finished
+                // query tiles: reloaded once the previous unit's last Q K^T of the tile (the
+                // last reader of its buffer) has finished, a block before its last P V
                 for (int tq = 0; tq < kTiles; ++tq) {
                     if (qn > 0 &&
                         !(ok = __all_sync(0xffffffffu,
-                                          mbar_wait(bar(kBarOFull + tq), (qn - 1) & 1, wc))))
+                                          mbar_wait(bar(kBarQEmpty + tq), (qn - 1) & 1, wc))))
                         break;
                     if (leader) {
                         const uint32_t full = tq == 0 ? bar(kBarQ) : bar(kBarQ1);
@@ -704,14 +756,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int qn = 0;           // units with a non-empty walk so far
         bool ok = true;
         for (int i = 0; ok; ++i) {
-            const int g = i == 0 && kPersist != 2 ? g_first : consume_unit(i);
-            if (g < 0) break;
             int n_blocks;
             if (i == 0 && kPersist != 2) {
+                if (g_first < 0) break;
                 n_blocks = first.n_blocks;
             } else {
                 Unit<kMode> U;
-                U.setup(g, p);
+                if (consume_unit(i, U) < 0) break;
                 n_blocks = U.n_blocks;
             }
             // an empty walk (possible only with malformed sequence boundaries) issues nothing
@@ -721,10 +772,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph0 = (N >> 1) & 1;
             ok = wait_all(kBarQ, qpar) && wait_all(kBarKFull + st0, ph0);
             if (!ok) break;
+            // persistent grids: after the unit's last Q K^T of a tile its query buffer may be
+            // refilled for the next unit
+            const bool last_qk0 = kPersist != 0 && n_blocks == 1;
             tc_fence_after();
             if (leader) {
                 issue_qk(0, st0);
                 tc_commit(bar(kBarSFull + 0));
+                if (last_qk0) tc_commit(bar(kBarQEmpty + 0));
             }
             __syncwarp();
             if (!(ok = wait_all(kBarQ1, qpar))) break;
@@ -733,6 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_qk(1, st0);
                 tc_commit(bar(kBarSFull + 1));
                 tc_commit(bar(kBarKEmpty + st0));
+                if (last_qk0) tc_commit(bar(kBarQEmpty + 1));
             }
             __syncwarp();
             for (int n = 0; ok && n < n_blocks; ++n) {
@@ -755,6 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = more ? mbar_wait2(bar(kBarPFull + 1), Nn & 1, bar(kBarKFull + st1), ph1, wc)
                           : mbar_wait(bar(kBarPFull + 1), Nn & 1, wc);
                 if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                const bool last_qk = kPersist != 0 && n + 2 == n_blocks;
                 tc_fence_after();
                 if (leader) {
                     issue_pv(0, st, 1, true);
@@ -762,6 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (more) {
                         issue_qk(0, st1);
                         tc_commit(bar(kBarSFull + 0));
+                        if (last_qk) tc_commit(bar(kBarQEmpty + 0));
                     }
                 }
                 __syncwarp();
@@ -779,6 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         issue_qk(1, st1);
                         tc_commit(bar(kBarSFull + 1));
                         tc_commit(bar(kBarKEmpty + st1));
+                        if (last_qk) tc_commit(bar(kBarQEmpty + 1));
                     }
                 }
                 __syncwarp();
@@ -803,21 +862,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t N = 0;       // K/V blocks of the units this CTA has run
         int qn = 0;           // units with a non-empty walk so far
         bool ok = true;
-        for (int i = 0; ok; ++i) {
-            const int g = i == 0 && kPersist != 2 ? g_first : consume_unit(i);
-            if (g < 0) break;
-            Unit<kMode> U;
-            if (i == 0 && kPersist != 2) U = first;
-            else U.setup(g, p);
-            const int n_blocks = U.n_blocks;
-            const int row_local = U.q0_local + tq * kRows + row;   // within shard r
-            const int row_pos = position(U.r, row_local, p.P, p.Ls, kZig ? 1 : 0);
-            int seq_lo = 0, seq_hi = 0;                            // packed sequences only
+        // the i-th unit with this thread's row: global position and (packed sequences) the
+        // visible key positions [seq_lo, seq_hi]
+        struct Row {
+            int row_local, row_pos, seq_lo, seq_hi;
+        };
+        auto row_of = [&](const Unit<kMode>& V) {
+            Row w;
+            w.row_local = V.q0_local + tq * kRows + row;   // within shard r
+            w.row_pos = position(V.r, w.row_local, p.P, p.Ls, kZig ? 1 : 0);
+            w.seq_lo = 0;
+            w.seq_hi = 0;
             if constexpr (kVarlen) {
-                if (row_local < p.Ls)
-                    seq_bounds(p.cu_seqlens, p.n_seqs, row_pos, p.causal, seq_lo, seq_hi, p.status);
-                else seq_hi = -1;
+                if (w.row_local < p.Ls)
+                    seq_bounds(p.cu_seqlens, p.n_seqs, w.row_pos, p.causal, w.seq_lo, w.seq_hi,
+                               p.status);
+                else w.seq_hi = -1;
             }
+            return w;
+        };
+        auto get_unit = [&](int i, Unit<kMode>& V) -> int {
+            if (i == 0 && kPersist != 2) {
+                V = first;
+                return g_first;
+            }
+            return consume_unit(i, V);
+        };
+        Unit<kMode> U;
+        int g = get_unit(0, U);
+        Row R = row_of(U);
+        for (int i = 0; ok && g >= 0; ++i) {
+            const int n_blocks = U.n_blocks;
+            const int row_local = R.row_local, row_pos = R.row_pos;
+            const int seq_lo = R.seq_lo, seq_hi = R.seq_hi;
 
             float m = -INFINITY;   // running max of scaled scores, base-2 units
             float l = 0.f;         // running denominator, relative to m
@@ -909,18 +986,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
 
-            // An empty walk leaves O unwritten: its rows saw no key and get 0 and -inf.
-            // Classic grids stage the output in the tile's query buffer, whose load must then
-            // have landed; persistent grids stage it in a buffer of their own.
+            // what the epilogue needs of this unit: index of (row, head) among the output's
+            // rows of D elements for this warp's first row (the warp's 32 rows lie in one tile,
+            // so `ostride` apart)
             const bool empty = n_blocks == 0;
-            if (!empty) ok = mbar_wait(bar(kBarOFull + tq), qn & 1, wc);
-            else if constexpr (kPersist == 0) ok = mbar_wait(bar(tq == 0 ? kBarQ : kBarQ1), 0, wc);
-            if (!(ok = __all_sync(0xffffffffu, ok))) break;
-            if (!empty) tc_fence_after();
             const bool valid = row_local < p.Ls;
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;        // a row that saw no key: 0
-            // index of (row, head) among the output's rows of D elements, for this warp's
-            // first row; the warp's 32 rows lie in one tile, so `ostride` apart
             const int x0 = U.q0_local + tq * kRows + quarter * 32;   // within shard r
             const int g0 = U.r * p.Ls + x0;
             size_t orow0 = (static_cast<size_t>(U.b) * p.L + g0) * p.H + U.h;
@@ -931,6 +1001,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             p.u_H + U.h_src;
                 ostride = p.u_H;
             }
+
+            // persistent grids: the next unit and this thread's row of it are set up while
+            // this unit's last P V runs (the packed sequences' binary search included)
+            int g_next = -1;
+            if constexpr (kPersist != 0) {
+                g_next = get_unit(i + 1, U);
+                if (g_next >= 0) R = row_of(U);
+            }
+
+            // An empty walk leaves O unwritten: its rows saw no key and get 0 and -inf.
+            // Classic grids stage the output in the tile's query buffer, whose load must then
+            // have landed; persistent grids stage it in a buffer of their own.
+            if (!empty) ok = mbar_wait(bar(kBarOFull + tq), qn & 1, wc);
+            else if constexpr (kPersist == 0) ok = mbar_wait(bar(tq == 0 ? kBarQ : kBarQ1), 0, wc);
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;
+            if (!empty) tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;        // a row that saw no key: 0
             // The rows go out through a 32-row staging slice of the warp (the tile's query
             // buffer, free once O is final -- the tile's last Q K^T finished before its last
             // P V -- or the persistent grids' own buffer), half of the columns at a time, so
@@ -985,6 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 N += n_blocks;
                 ++qn;
             }
+            g = g_next;
         }
     }
 
