@@ -51,8 +51,9 @@ EncodeTiledFn encode_fn()
 }
 
 // q/k/v as a 4-D bf16 tensor {D, H, L, B} (innermost first); boxes of 64 head-dim
-// elements (128 bytes, the swizzle span) by 128 sequence rows, 128-byte swizzle.
-bool encode_qkv_map(CUtensorMap* map, const void* base, int B, int L, int H, int D)
+// elements (128 bytes, the swizzle span) by box_rows sequence rows, 128-byte swizzle.
+bool encode_qkv_map(CUtensorMap* map, const void* base, int B, int L, int H, int D,
+                    int box_rows = 128)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -61,7 +62,7 @@ bool encode_qkv_map(CUtensorMap* map, const void* base, int B, int L, int H, int
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
                                    static_cast<cuuint64_t>(H) * D * 2,
                                    static_cast<cuuint64_t>(L) * H * D * 2};
-    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -98,7 +99,8 @@ bool encode_permute_map(CUtensorMap* map, const void* base, int B, int L, int H,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_seq_shard_map(CUtensorMap* map, const void* base, int P, int B, int L, int H, int D)
+bool encode_seq_shard_map(CUtensorMap* map, const void* base, int P, int B, int L, int H, int D,
+                          int box_rows = 128)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -107,7 +109,7 @@ bool encode_seq_shard_map(CUtensorMap* map, const void* base, int P, int B, int 
                                 static_cast<cuuint64_t>(B), static_cast<cuuint64_t>(P)};
     const cuuint64_t row = static_cast<cuuint64_t>(H) * D * 2;
     const cuuint64_t strides[4] = {static_cast<cuuint64_t>(D) * 2, row, Ls * row, Ls * row * B};
-    const cuuint32_t box[5] = {64, 1, 128, 1, 1};
+    const cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(box_rows), 1, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -209,21 +211,23 @@ ra_status attn_impl(const void* q, const void* k, const void* v, void* out, floa
         // the kernel sees ulysses_P * B head-group batches of H / ulysses_P heads (ring P = 1)
         // and addresses the sequence-sharded sources through 5-D tensor maps
         CUtensorMap tq, tk, tv;
-        if (!encode_seq_shard_map(&tq, q, ulysses_P, B, L, H, D) ||
-            !encode_seq_shard_map(&tk, k, ulysses_P, B, L, Hkv, D) ||
-            !encode_seq_shard_map(&tv, v, ulysses_P, B, L, Hkv, D))
-            return RA_ERR_CUDA;
         a.u_P = ulysses_P;
         a.u_B = B;
         a.u_H = H;
         a.B = ulysses_P * B;
         a.H = H / ulysses_P;
         a.Hkv = Hkv / ulysses_P;
+        const int k_rows = ra::attn_bf16_pair_applies(a) ? 64 : 128;
+        if (!encode_seq_shard_map(&tq, q, ulysses_P, B, L, H, D) ||
+            !encode_seq_shard_map(&tk, k, ulysses_P, B, L, Hkv, D, k_rows) ||
+            !encode_seq_shard_map(&tv, v, ulysses_P, B, L, Hkv, D))
+            return RA_ERR_CUDA;
         return from_cuda(ra::launch_attn_bf16(a, tq, tk, tv));
     }
     if (dtype == RA_F32) return from_cuda(ra::launch_attn_f32(a));
     CUtensorMap tq, tk, tv;
-    if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, Hkv, D) ||
+    const int k_rows = ra::attn_bf16_pair_applies(a) ? 64 : 128;
+    if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, Hkv, D, k_rows) ||
         !encode_qkv_map(&tv, v, B, L, Hkv, D))
         return RA_ERR_CUDA;
     return from_cuda(ra::launch_attn_bf16(a, tq, tk, tv));

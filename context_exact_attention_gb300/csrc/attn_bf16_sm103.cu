@@ -1083,6 +1083,481 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------ pair of SMs --
+//
+// ring_attn_bf16_pair_kernel: the same computation with the products issued for a pair of
+// SMs (tcgen05.mma.cta_group::2, M = 256).  A cluster of two CTAs takes four consecutive
+// 128-row query tiles of one shard of one (batch, head): CTA rank c holds tiles 2c and
+// 2c + 1 (its "tile 0" and "tile 1"), and the pair's products for tile slot a cover the
+// two CTAs' tile a together.  Each CTA loads half of every K/V block: keys [64 c, 64 c + 64)
+// of K (the B operand of Q K^T, split along N = keys) and head-dim columns [64 c, 64 c + 64)
+// of V (the B operand of P V, split along N = D), so a product reads 6 KiB of shared memory
+// per SM per 16-deep step instead of 8 (Q K^T) and 2 instead of 4 (P V) -- the tensor
+// core's shared-memory read pipe, which holds single-SM products to ~71 cycles, stops
+// being the limit (a stream of these products issues at the nominal 64 cycles).
+// The even CTA's MMA warp issues everything; its barriers count both CTAs' TMA bytes and
+// both CTAs' softmax arrivals (the odd CTA's threads arrive remotely), and every commit is
+// multicast to the same barrier of both CTAs.  S and O of a CTA's rows live in its own
+// TMEM, so the softmax warps work exactly as in the single-SM kernel.  Head dim 128 only.
+template <int kMode>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    ring_attn_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                               const __grid_constant__ CUtensorMap tmap_k,
+                               const __grid_constant__ CUtensorMap tmap_v, const Params p)
+{
+    constexpr int D = 128;
+    constexpr int kTileBytes = kRows * D * 2;          // one Q tile, 32 KiB
+    constexpr int kHalfBytes = kTileBytes / 2;         // one CTA's half of a K or V block
+    constexpr int kQOff = 0;
+    constexpr int kKOff = kQOff + kTiles * kTileBytes;
+    constexpr int kVOff = kKOff + 2 * kHalfBytes;
+    constexpr int kBarOff = kVOff + 2 * kHalfBytes;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kBarCount * 8);
+    int* abort_flag = reinterpret_cast<int*>(smem + kBarOff + kBarCount * 8 + 4);
+    auto bar = [&](int i) -> uint32_t { return sbase + kBarOff + 8u * i; };
+    const uint32_t rank = cluster_ctarank();
+    const bool lead = rank == 0;
+    // the even CTA's copy of a barrier (cluster address)
+    auto lead_bar = [&](int i) -> uint32_t { return mapa_shared(bar(i), 0); };
+    constexpr uint16_t kBoth = 3;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work unit: a quad of query tiles, heaviest (shard, quad) first, two (batch,
+    // head) pairs interleaved
+    const int n_quad = (p.n_pair + 1) / 2;
+    const int units_per_bh = p.P * n_quad;
+    int bh, u;
+    unit_of_block(static_cast<int>(blockIdx.x >> 1), p.B * p.H, units_per_bh, bh, u);
+    const int r = p.P - 1 - u / n_quad;
+    const int quad = n_quad - 1 - (u - (u / n_quad) * n_quad);
+    const int b = bh / p.H;
+    const int h = bh - b * p.H;
+    const int hk = h / p.group;
+    int bo = b, h_src = h, hk_src = hk;
+    if constexpr (kMode == 3) {
+        const int g = b / p.u_B;
+        bo = b - g * p.u_B;
+        h_src = g * p.H + h;
+        hk_src = h_src / p.group;
+    }
+    const int quad0 = quad * (4 * kRows);                  // first query row of the quad
+    const int q0_local = quad0 + static_cast<int>(rank) * (kTiles * kRows);   // this CTA's
+    ContigSched walk;
+    walk.init(r, p.P, p.n_kt, p.Ls, p.causal, min(p.Ls - 1, quad0 + 4 * kRows - 1));
+    const int n_blocks = walk.n_blocks;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(kBarQ), 1);
+        mbar_init(bar(kBarQ1), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kBarKFull + i), 1);
+            mbar_init(bar(kBarKEmpty + i), 1);
+            mbar_init(bar(kBarVFull + i), 1);
+            mbar_init(bar(kBarVEmpty + i), 1);
+            mbar_init(bar(kBarSFull + i), 1);
+            mbar_init(bar(kBarPFull + 2 * i), 2 * kRows);       // both CTAs' rows
+            mbar_init(bar(kBarPFull + 2 * i + 1), 2 * kRows);
+            mbar_init(bar(kBarOFull + i), 1);
+        }
+        mbar_init(bar(kBarDone), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(tmem_slot), 512);
+        tmem_relinquish_pair();
+        tc_fence_before();
+    }
+    // both CTAs' barriers exist and the pair's TMEM is allocated before either CTA signals
+    // the other
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer (both CTAs)
+        const bool leader = elect_one();
+        if (leader) {
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+        }
+        const uint64_t keep = l2_policy_evict_last();
+        const uint64_t once = l2_policy_evict_first();
+        const bool tracing = p.trace != nullptr && lead && bh == 0 && quad == n_quad - 1;
+        if (tracing && leader)
+            for (int t = 0; t < p.P; ++t)
+                if (in_bounds(r * p.P + t, 1, p.P * p.P, p.status)) p.trace[r * p.P + t] = -1;
+        if (leader) {
+            // this CTA's two query tiles, counted on the even CTA's barriers
+            for (int tq = 0; tq < kTiles; ++tq) {
+                const int full = tq == 0 ? kBarQ : kBarQ1;
+                if (lead) mbar_arrive_expect_tx(bar(full), 2 * kTileBytes);
+                for (int bx = 0; bx < 2; ++bx) {
+                    const uint32_t dst = sbase + kQOff + tq * kTileBytes + bx * 16384;
+                    const int row = r * p.Ls + q0_local + tq * kRows;
+                    if constexpr (kMode == 3)
+                        tma_load_5d_pair(dst, &tmap_q, lead_bar(full), bx * 64, h_src, row % p.u_Ls,
+                                         bo, row / p.u_Ls, once);
+                    else
+                        tma_load_4d_pair(dst, &tmap_q, lead_bar(full), bx * 64, h, row, b, once);
+                }
+            }
+        }
+        int last[2] = {-1, -1};
+        for (int n = 0; n < n_blocks; ++n) {
+            walk.at(n);
+            if (tracing && walk.first_of_shard() && leader &&
+                in_bounds(r * p.P + walk.t, 1, p.P * p.P, p.status))
+                p.trace[r * p.P + walk.t] = walk.s;
+            const int st = n & 1;
+            const uint32_t ph = (n >> 1) & 1;
+            const int row = walk.s * p.Ls + walk.kt() * kKeys;   // first key of the block
+            // K: keys [64 rank, 64 rank + 64) of the block, both 64-column boxes
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc))) break;
+            if (leader) {
+                if (lead) mbar_arrive_expect_tx(bar(kBarKFull + st), 2 * kHalfBytes);
+                const int krow = row + 64 * static_cast<int>(rank);
+                for (int bx = 0; bx < 2; ++bx) {
+                    const uint32_t dst = sbase + kKOff + st * kHalfBytes + bx * 8192;
+                    if constexpr (kMode == 3)
+                        tma_load_5d_pair(dst, &tmap_k, lead_bar(kBarKFull + st), bx * 64, hk_src,
+                                         krow % p.u_Ls, bo, krow / p.u_Ls, keep);
+                    else
+                        tma_load_4d_pair(dst, &tmap_k, lead_bar(kBarKFull + st), bx * 64, hk, krow, b,
+                                         keep);
+                }
+            }
+            // V: head-dim columns [64 rank, 64 rank + 64) of the block's 128 keys (one box)
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc))) break;
+            if (leader) {
+                if (lead) mbar_arrive_expect_tx(bar(kBarVFull + st), 2 * kHalfBytes);
+                const uint32_t dst = sbase + kVOff + st * kHalfBytes;
+                if constexpr (kMode == 3)
+                    tma_load_5d_pair(dst, &tmap_v, lead_bar(kBarVFull + st), 64 * rank, hk_src,
+                                     row % p.u_Ls, bo, row / p.u_Ls, keep);
+                else
+                    tma_load_4d_pair(dst, &tmap_v, lead_bar(kBarVFull + st), 64 * rank, hk, row, b,
+                                     keep);
+            }
+            last[st] = n;
+        }
+        // the even CTA's barriers count both CTAs' copies: it waits for all of them to land
+        // (the odd CTA leaves only after the cluster-wide barrier that follows)
+        if (lead) {
+            mbar_wait_drain(bar(kBarQ), 0, wc);
+            mbar_wait_drain(bar(kBarQ1), 0, wc);
+            for (int st = 0; st < 2; ++st)
+                if (last[st] >= 0) {
+                    mbar_wait_drain(bar(kBarKFull + st), (last[st] >> 1) & 1, wc);
+                    mbar_wait_drain(bar(kBarVFull + st), (last[st] >> 1) & 1, wc);
+                }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer (even CTA)
+        if (lead) {
+            const bool leader = elect_one();
+            constexpr uint32_t kIdescQK = idesc_bf16_f32(2 * kRows, kKeys, false);
+            constexpr uint32_t kIdescPV = idesc_bf16_f32(2 * kRows, D, true);
+            constexpr uint64_t kTileU = kTileBytes >> 4;
+            constexpr uint64_t kHalfU = kHalfBytes >> 4;
+            // Q (A, K-major): 128 rows per 64-column box (16 KiB); K half (B, K-major): 64
+            // keys per box (8 KiB); V half (B, MN-major): one 64-column box of 128 keys, 8
+            // keys per 1024-byte swizzle atom, 16-key steps 2 KiB apart
+            const uint64_t dq = sdesc_sw128(sbase + kQOff, 16, 1024);
+            const uint64_t dk = sdesc_sw128(sbase + kKOff, 16, 1024);
+            const uint64_t dv = sdesc_sw128(sbase + kVOff, 16384, 1024);
+            auto issue_qk = [&](int tq, int st) {
+                const uint32_t d_t = tmem + Layout<D>::col_s(tq);
+                const uint64_t a0 = dq + tq * kTileU, b0 = dk + st * kHalfU;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t oa = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+                    const uint64_t ob = ((k >> 2) * 8192 + (k & 3) * 32) >> 4;
+                    mma_ss_pair(d_t, a0 + oa, b0 + ob, kIdescQK, k > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int tq, int st, int half, bool acc) {
+                const uint32_t d_t = tmem + Layout<D>::col_o(tq);
+                const uint32_t pa = tmem + Layout<D>::col_s(tq) + 32 * half;
+                const uint64_t b0 = dv + st * kHalfU + ((half * 64 * 128) >> 4);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ts_pair(d_t, pa + k * 8, b0 + ((k * 2048) >> 4), kIdescPV,
+                                (acc || k > 0) ? 1u : 0u);
+            };
+            auto wait_all = [&](int idx, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait_cluster(bar(idx), parity, wc));
+            };
+            bool ok = n_blocks > 0 && wait_all(kBarQ, 0) && wait_all(kBarKFull + 0, 0);
+            if (ok) {
+                tc_fence_after();
+                if (leader) {
+                    issue_qk(0, 0);
+                    tc_commit_pair(bar(kBarSFull + 0), kBoth);
+                }
+                __syncwarp();
+            }
+            if (ok && (ok = wait_all(kBarQ1, 0))) {
+                tc_fence_after();
+                if (leader) {
+                    issue_qk(1, 0);
+                    tc_commit_pair(bar(kBarSFull + 1), kBoth);
+                    tc_commit_pair(bar(kBarKEmpty + 0), kBoth);
+                }
+                __syncwarp();
+            }
+            for (int n = 0; ok && n < n_blocks; ++n) {
+                const int st = n & 1;
+                const uint32_t ph = (n >> 1) & 1;
+                const bool more = n + 1 < n_blocks;
+                const int st1 = (n + 1) & 1;
+                const uint32_t ph1 = ((n + 1) >> 1) & 1;
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait2_cluster(bar(kBarVFull + st), ph,
+                                                                      bar(kBarPFull + 0), n & 1, wc))))
+                    break;
+                tc_fence_after();
+                if (leader) issue_pv(0, st, 0, n > 0);
+                __syncwarp();
+                ok = more ? mbar_wait2_cluster(bar(kBarPFull + 1), n & 1, bar(kBarKFull + st1), ph1, wc)
+                          : mbar_wait_cluster(bar(kBarPFull + 1), n & 1, wc);
+                if (!(ok = __all_sync(0xffffffffu, ok))) break;
+                tc_fence_after();
+                if (leader) {
+                    issue_pv(0, st, 1, true);
+                    if (!more) tc_commit_pair(bar(kBarOFull + 0), kBoth);
+                    if (more) {
+                        issue_qk(0, st1);
+                        tc_commit_pair(bar(kBarSFull + 0), kBoth);
+                    }
+                }
+                __syncwarp();
+                if (!(ok = wait_all(kBarPFull + 2, n & 1))) break;
+                tc_fence_after();
+                if (leader) issue_pv(1, st, 0, n > 0);
+                __syncwarp();
+                if (!(ok = wait_all(kBarPFull + 3, n & 1))) break;
+                tc_fence_after();
+                if (leader) {
+                    issue_pv(1, st, 1, true);
+                    tc_commit_pair(bar(kBarVEmpty + st), kBoth);
+                    if (!more) tc_commit_pair(bar(kBarOFull + 1), kBoth);
+                    if (more) {
+                        issue_qk(1, st1);
+                        tc_commit_pair(bar(kBarSFull + 1), kBoth);
+                        tc_commit_pair(bar(kBarKEmpty + st1), kBoth);
+                    }
+                }
+                __syncwarp();
+            }
+            // every product the pair issued has finished before either CTA frees TMEM
+            if (leader) tc_commit_pair(bar(kBarDone), kBoth);
+            __syncwarp();
+        }
+        mbar_wait_drain(bar(kBarDone), 0, wc);
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ----------------------------------------------------------- softmax (both CTAs)
+        const int tq = (warp - 4) >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + Layout<D>::col_s(tq);
+        const uint32_t tO = tmem + lane_off + Layout<D>::col_o(tq);
+        const int row_local = q0_local + tq * kRows + row;   // within shard r
+        const int row_pos = r * p.Ls + row_local;
+        const float sl2 = p.scale_log2;
+        const uint32_t pfull0 = lead_bar(kBarPFull + 2 * tq), pfull1 = lead_bar(kBarPFull + 2 * tq + 1);
+
+        float m = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        for (int n = 0; n < n_blocks; ++n) {
+            walk.at(n);
+            ok = mbar_wait_cluster(bar(kBarSFull + tq), n & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+
+            uint32_t sraw[128];
+            tmem_ld128(tS, sraw);
+            float sv[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) sv[c] = u2f(sraw[c]);
+            int lim = min(kKeys - 1, p.Ls - walk.kt() * kKeys - 1);
+            if (p.causal) lim = min(lim, row_pos - walk.pos0());
+            if (lim < kKeys - 1) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) sv[c] = c > lim ? -INFINITY : sv[c];
+            }
+            float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]);
+            float mx2 = fmaxf(sv[4], sv[5]), mx3 = fmaxf(sv[6], sv[7]);
+#pragma unroll
+            for (int c = 8; c < 128; c += 8) {
+                mx0 = fmax3(mx0, sv[c], sv[c + 1]);
+                mx1 = fmax3(mx1, sv[c + 2], sv[c + 3]);
+                mx2 = fmax3(mx2, sv[c + 4], sv[c + 5]);
+                mx3 = fmax3(mx3, sv[c + 6], sv[c + 7]);
+            }
+            const float m_blk = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+            const float m_new = fmaxf(m, m_blk);
+            const bool raise = m_new > m + kRescaleThreshold;
+            const float m_ref = raise ? m_new : m;
+            const float alpha = raise ? ex2(m - m_ref) : 1.f;
+            const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            const uint64_t scale2 = f2pack(sl2, sl2), negm2 = f2pack(neg_m, neg_m);
+            uint64_t sum_a = 0, sum_b = 0;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) {
+                    const int c = 64 * half + 2 * i2;
+                    float x0, x1;
+                    f2unpack(ffma2(f2pack(sv[c], sv[c + 1]), scale2, negm2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    if (i2 & 1) sum_b = fadd2(sum_b, f2pack(p0, p1));
+                    else sum_a = fadd2(sum_a, f2pack(p0, p1));
+                    pk[i2] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + 32 * half, pk);
+                if (half == 0 && n > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32 * c, o);
+#pragma unroll
+                        for (int i2 = 0; i2 < 32; ++i2) o[i2] = f2u(u2f(o[i2]) * alpha);
+                        tmem_st32(tO + 32 * c, o);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive_cluster(half == 0 ? pfull0 : pfull1);
+            }
+            float sa0, sa1;
+            f2unpack(fadd2(sum_a, sum_b), sa0, sa1);
+            l = l * alpha + (sa0 + sa1);
+            m = m_ref;
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(kBarOFull + tq), 0, wc));
+        if (ok) {
+            tc_fence_after();
+            const bool valid = row_local < p.Ls;
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const int x0 = q0_local + tq * kRows + quarter * 32;
+            const int g0 = r * p.Ls + x0;
+            size_t orow0 = (static_cast<size_t>(b) * p.L + g0) * p.H + h;
+            size_t ostride = p.H;
+            if constexpr (kMode == 3) {
+                const int rs = g0 / p.u_Ls;
+                orow0 = (static_cast<size_t>(rs * p.u_B + bo) * p.u_Ls + (g0 - rs * p.u_Ls)) * p.u_H +
+                        h_src;
+                ostride = p.u_H;
+            }
+            // staged through the warp's 32-row slice of this CTA's query tile (free: the
+            // tile's last Q K^T finished before its last P V)
+            constexpr int kHalfCols = D / 2;
+            constexpr int kChunks = kHalfCols / 8;
+            constexpr int kRowsPerStore = 32 / kChunks;
+            uint8_t* stage = smem + kQOff + tq * kTileBytes + quarter * 32 * (2 * D);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                for (int c = 0; c < kHalfCols / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + hh * kHalfCols + 32 * c, o);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i2 = 0; i2 < 16; ++i2)
+                        pk[i2] = pack_bf16x2(u2f(o[2 * i2]) * inv_l, u2f(o[2 * i2 + 1]) * inv_l);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int slot = (4 * c + j) ^ (lane & (kChunks - 1));
+                        *reinterpret_cast<uint4*>(stage + lane * (2 * kHalfCols) + slot * 16) =
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
+                }
+                __syncwarp();
+                {
+                    const int sub = lane / kChunks, cc = lane % kChunks;
+#pragma unroll
+                    for (int k = 0; k < 32 / kRowsPerStore; ++k) {
+                        const int rr = k * kRowsPerStore + sub;
+                        const uint4 val = *reinterpret_cast<const uint4*>(
+                            stage + rr * (2 * kHalfCols) + ((cc ^ (rr & (kChunks - 1))) * 16));
+                        const long long idx =
+                            static_cast<long long>(orow0 + rr * ostride) * D + hh * kHalfCols + cc * 8;
+                        if (x0 + rr < p.Ls && in_bounds(idx, 8, p.out_elems, p.status))
+                            *reinterpret_cast<uint4*>(p.out + idx) = val;
+                    }
+                }
+                __syncwarp();
+            }
+            if (valid && p.lse != nullptr &&
+                in_bounds(static_cast<long long>(orow0 + lane * ostride), 1, p.lse_elems, p.status))
+                p.lse[orow0 + lane * ostride] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+
+    // neither CTA frees TMEM or leaves while the other may still read its shared memory
+    // or signal its barriers
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
+template <int kMode>
+cudaError_t launch_pair(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv)
+{
+    constexpr int D = 128;
+    constexpr int kSmem = kTiles * kRows * D * 2 + 4 * (kRows * D) + 256 + 1024;
+    static std::atomic<int> configured[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = smem_limit_once(configured, dev, ring_attn_bf16_pair_kernel<kMode>, kSmem);
+    if (e != cudaSuccess) return e;
+    Params p{};
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.lse = a.lse;
+    p.trace = a.trace;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.B = a.B;
+    p.L = a.L;
+    p.H = a.H;
+    p.P = a.P;
+    p.Ls = a.L / a.P;
+    p.causal = a.causal;
+    p.group = a.H / a.Hkv;
+    p.u_B = a.u_B;
+    p.u_H = a.u_H;
+    p.u_Ls = a.u_P > 0 ? a.L / a.u_P : 0;
+    p.n_kt = (p.Ls + kKeys - 1) / kKeys;
+    p.n_pair = (p.n_kt + kTiles - 1) / kTiles;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.out_elems = static_cast<long long>(a.B) * a.L * a.H * D;
+    p.lse_elems = static_cast<long long>(a.B) * a.L * a.H;
+    const long long quads = static_cast<long long>(a.B) * a.H * a.P * ((p.n_pair + 1) / 2);
+    if (quads <= 0 || 2 * quads > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    p.n_units = static_cast<int>(quads);
+    ring_attn_bf16_pair_kernel<kMode>
+        <<<static_cast<unsigned>(2 * quads), kThreads, kSmem, a.stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
 template <int D, int kMode, int kPersist>
 cudaError_t launch_d(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv)
@@ -1167,9 +1642,17 @@ cudaError_t launch_mode(const AttnArgs& a, const CUtensorMap& tq, const CUtensor
 
 }  // namespace
 
+bool attn_bf16_pair_applies(const AttnArgs& a)
+{
+    // head dim 128, contiguous shards or Ulysses head groups
+    return a.D == 128 && a.cu_seqlens == nullptr && !a.zigzag;
+}
+
 cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv)
 {
+    if (attn_bf16_pair_applies(a)) return a.u_P > 0 ? launch_pair<3>(a, tq, tk, tv)
+                                                    : launch_pair<0>(a, tq, tk, tv);
     if (a.u_P > 0) {
         if (a.D == 64) return launch_mode<64, 3>(a, tq, tk, tv);
         if (a.D == 128) return launch_mode<128, 3>(a, tq, tk, tv);

@@ -84,7 +84,9 @@ cudaError_t launch_varlen_schedule(const int* cu_seqlens, int n_seqs, int L, int
                                    int* schedule, unsigned int* status, cudaStream_t stream);
 
 // bf16 tcgen05 kernel; tensor maps describe q, k, v as 4-D [B][L][H][D] with
-// 64-element, 128-byte-swizzled boxes of 128 rows.
+// 64-element, 128-byte-swizzled boxes of 128 rows -- except that k has boxes of 64 rows
+// when attn_bf16_pair_applies(a) (the pair-of-SMs kernel loads half a key block per CTA).
+bool attn_bf16_pair_applies(const AttnArgs& a);
 cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tmap_q,
                              const CUtensorMap& tmap_k, const CUtensorMap& tmap_v);
 
