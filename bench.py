@@ -69,6 +69,14 @@ def _kernel_hash():
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+def _forward_kernel_name(w):
+    """The forward kernel a contiguous bf16 call of workload w runs: head dim 128 with
+    key walks of 8192 keys or more go to the pair-of-SMs kernel."""
+    if w.D == 128 and w.L >= 8192:
+        return "ring_attn_bf16_pair_kernel<0>"
+    return f"ring_attn_bf16_kernel<{w.D}, 0>"
+
+
 def _traffic_per_launch():
     """DRAM bytes of one ring_attn_fwd launch from a committed ncu summary, if it was
     taken on the current kernel source; else None."""
@@ -421,7 +429,7 @@ def run_gpu(args, rank, world, local_rank):
                 "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback 1.9 PFLOP/s bf16",
                 "frac_of_sustained": achieved / peak_sus,
-                "kernel": "ring_attn_bf16_kernel<128>"}
+                "kernel": _forward_kernel_name(w)}
     if sustained is not None:
         sustained.update({"unit": "TFLOP/s", "peak": peak_sus,
                           "frac": sustained["value"] / peak_sus,

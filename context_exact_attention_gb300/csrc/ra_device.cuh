@@ -373,61 +373,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
     return d;
 }
 
-// Arrive on a barrier of any CTA of the cluster (cluster address), releasing this
-// thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)
+// Arrive on a barrier of either CTA of the pair (cluster address).  The arrival
+// carries no cluster-scope memory fence (a release at cluster scope stalls the warp on
+// a fence on every call): it publishes tensor-memory rows that the arriving threads
+// stored with tcgen05.st and completed with tcgen05.wait::st before the arrival, and the
+// products that read them are ordered by the tcgen05 fences on both sides of the
+// barrier, not by the barrier's memory semantics.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// mbar_wait for a barrier that threads of the other CTA arrive on (acquire at cluster
-// scope); same bounds and abort behaviour.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtx& w)
-{
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (*w.abort_flag) return false;
-        if (globaltimer_ns() - t0 > w.limit_ns) {
-            *w.abort_flag = 1;
-            atomicOr(w.status, RA_STATUS_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ bool mbar_wait2_cluster(uint32_t bar_a, uint32_t par_a, uint32_t bar_b,
-                                                   uint32_t par_b, const WaitCtx& w)
-{
-    bool a = mbar_try_wait_cluster(bar_a, par_a), b = mbar_try_wait_cluster(bar_b, par_b);
-    if (a && b) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (!a) a = mbar_try_wait_cluster(bar_a, par_a);
-        if (!b) b = mbar_try_wait_cluster(bar_b, par_b);
-        if (a && b) return true;
-        if (*w.abort_flag) return false;
-        if (globaltimer_ns() - t0 > w.limit_ns) {
-            *w.abort_flag = 1;
-            atomicOr(w.status, RA_STATUS_TIMEOUT);
-            return false;
-        }
-    }
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 // TMA tiled loads into this CTA's shared memory whose completion is counted on a barrier

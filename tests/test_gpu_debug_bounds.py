@@ -60,6 +60,10 @@ def _every_entry_point():
     kk, vv = k[:, :, :2].contiguous(), v[:, :, :2].contiguous()
     out, lse = cea.ring_attn_fwd_gqa(q, kk, vv, P=P, causal=True)
     res += [out, lse, *cea.ring_attn_bwd_gqa(q, kk, vv, out, lse, do, P=P, causal=True)]
+    # the pair-of-SMs forward (key walks of 8192 keys and more): ragged shards of 4100
+    qx, kx, vx = (t.to(DEV) for t in make_qkv(1, 8200, 1, 128, seed=79, dtype=torch.bfloat16))
+    for causal in (False, True):
+        res += list(cea.ring_attn_fwd(qx, kx, vx, P=2, causal=causal))
     # zigzag: chunks of a multiple of 128 rows
     qz, kz, vz = (t.to(DEV) for t in make_qkv(1, 2048, 2, 64, seed=72, dtype=torch.bfloat16))
     dz = _bf16(1, 2048, 2, 64, seed=73)

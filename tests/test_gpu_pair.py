@@ -1,0 +1,83 @@
+"""Parity of the pair-of-SMs forward (tcgen05.mma.cta_group::2, head dim 128), which
+takes contiguous and Ulysses bf16 calls whose key walk spans at least 8192 keys: outputs
+and lse against the fp64 oracle on sampled query rows (every shard's first and last
+rows, the rows around each 512-row quad edge and seeded uniform rows), with ragged
+shards (not a multiple of the 512 rows a pair takes, nor of the 128-key block), two
+batches, grouped key/value heads, the ring trace, and repeated calls bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import context_exact_attention_gb300 as cea
+import oracle
+from context_exact_attention_gb300.workloads import make_qkv, sample_rows
+from helpers import assert_bf16_close, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _rows(L, P, n=96):
+    Ls = L // P
+    edges = set()
+    for r in range(P):
+        for e in range(0, Ls, 512):
+            edges |= {r * Ls + x for x in (e - 1, e, e + 255, e + 256) if 0 <= x < Ls}
+    return sorted(set(sample_rows(L, P, n, seed=3)) | edges)
+
+
+def _check(q, k, v, out, lse, causal, L, P, what):
+    rows = _rows(L, P)
+    ref, lref = oracle.attention(q, k, v, causal=causal, rows=rows)
+    assert_bf16_close(to_np(out[:, rows]), ref, f"{what} out")
+    assert_bf16_close(to_np(lse[:, rows]), lref, f"{what} lse")
+
+
+CASES = [
+    # B, L, H, P: shards of 2048 (whole quads), 3000 (ragged quad), 4100 (ragged block)
+    (1, 8192, 2, 4),
+    (2, 9000, 1, 3),
+    (1, 8200, 2, 2),
+    (1, 16384, 1, 1),
+]
+
+
+@pytest.mark.parametrize("B,L,H,P", CASES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_pair_forward_matches_oracle(B, L, H, P, causal):
+    q, k, v = make_qkv(B, L, H, 128, seed=90 + L % 97, head_scale=True)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    out, lse = cea.ring_attn_fwd(qd, kd, vd, P=P, causal=causal)
+    assert cea.check_status() == 0
+    _check(q, k, v, out, lse, causal, L, P, f"B{B} L{L} H{H} P{P} causal={causal}")
+    again, lagain = cea.ring_attn_fwd(qd, kd, vd, P=P, causal=causal)
+    assert torch.equal(out, again) and torch.equal(lse, lagain)
+
+
+def test_pair_forward_gqa_and_no_lse():
+    """Four query heads over two key/value heads; the call without lse gives the same
+    output bits."""
+    B, L, H, Hkv, P = 1, 8192, 4, 2, 4
+    q, _, _ = make_qkv(B, L, H, 128, seed=93)
+    _, k, v = make_qkv(B, L, Hkv, 128, seed=94)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    out, lse = cea.ring_attn_fwd_gqa(qd, kd, vd, P=P, causal=True)
+    _check(q, k, v, out, lse, True, L, P, "gqa")
+    out2, none = cea.ring_attn_fwd_gqa(qd, kd, vd, P=P, causal=True, want_lse=False)
+    assert none is None and cea.check_status() == 0
+    assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_pair_forward_trace(causal):
+    """The ring trace of the pair kernel: the K/V source of every (shard, ring step), -1
+    where a causal step is skipped, as the oracle's ring schedule gives it (the schedule
+    depends on P and causality only, so the oracle runs it on a small input)."""
+    P, L = 4, 8192
+    q, k, v = make_qkv(1, L, 1, 128, seed=95)
+    out, lse, trace = cea.ring_attn_fwd_trace(*(t.to(DEV) for t in (q, k, v)), P=P,
+                                              causal=causal)
+    small = make_qkv(1, 16 * P, 1, 8, seed=95)
+    _, _, tref = oracle.ring_attention(*small, P, causal=causal)
+    assert np.array_equal(trace.cpu().numpy(), tref)
+    _check(q, k, v, out, lse, causal, L, P, "trace call")
