@@ -615,14 +615,7 @@ def measure_rows(cea, dev, stream, peaks, samples):
 
     # packed variable-length sequences filling the headline length (causal)
     w = LM
-    gl = torch.Generator().manual_seed(5)
-    lengths = []
-    while sum(lengths) < w.L:
-        lengths.append(int(torch.randint(256, 8192, (1,), generator=gl)))
-    lengths[-1] -= sum(lengths) - w.L
-    cu = [0]
-    for n in lengths:
-        cu.append(cu[-1] + n)
+    lengths, cu = packed_lengths(w.L)
     cu_d = torch.tensor(cu, dtype=torch.int32, device=dev)
     q, k, v = (torch.randn(w.L, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
                for _ in range(3))
@@ -787,6 +780,60 @@ def run_profile_backward(args):
                       "tflops": fl / (ms * 1e-3) / 1e12}), flush=True)
 
 
+def packed_lengths(L):
+    """The packed-sequence workload's lengths: U[256, 8192) from a CPU generator seeded
+    with 5, drawn until they reach L (the last one cut).  Returns (lengths, cu_seqlens)."""
+    gl = torch.Generator().manual_seed(5)
+    lengths = []
+    while sum(lengths) < L:
+        lengths.append(int(torch.randint(256, 8192, (1,), generator=gl)))
+    lengths[-1] -= sum(lengths) - L
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    return lengths, cu
+
+
+def run_profile_packed(args):
+    """The packed-sequence workload alone (the lm_varlen rows' lengths, H=32, D=128, P=8,
+    causal, with a schedule), for profiler captures of the dynamic persistent kernels:
+    `warmup` + `steps` forward calls, then `warmup` + `steps` backward calls, one line out."""
+    import context_exact_attention_gb300 as cea
+
+    dev = torch.device("cuda", 0)
+    cea.load_library()
+    stream = torch.cuda.current_stream(dev)
+    w = LM
+    lengths, cu = packed_lengths(w.L)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    q, k, v, do = (torch.randn(w.L, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
+                   for _ in range(4))
+    sched = cea.varlen_schedule(cu_d, w.L, w.P, True, stream=stream)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.L, w.H), dtype=torch.float32, device=dev)
+    fwd = lambda: cea.ring_attn_fwd_varlen(q, k, v, cu_d, P=w.P, causal=True, out=out, lse=lse,
+                                           stream=stream, schedule=sched)
+    for _ in range(args.warmup):
+        fwd()
+    ms_f = _time_loop(fwd, args.steps, stream) / args.steps
+    ws = torch.empty(w.L * w.H, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    bwd = lambda: cea.ring_attn_bwd_varlen(q, k, v, out, lse, do, cu_d, P=w.P, causal=True,
+                                           dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream,
+                                           schedule=sched)
+    for _ in range(args.warmup):
+        bwd()
+    ms_b = _time_loop(bwd, args.steps, stream) / args.steps
+    if cea.check_status(stream) != 0:
+        raise RuntimeError("kernel reported a device-side timeout")
+    fl = sum(attention_flops(1, n, w.H, w.D, True) for n in lengths)
+    print(json.dumps({"case": f"packed sequences {lengths}, H32 D128 P8 bf16, causal",
+                      "forward_ms": ms_f, "forward_tflops": fl / (ms_f * 1e-3) / 1e12,
+                      "backward_ms": ms_b, "backward_tflops": 2.5 * fl / (ms_b * 1e-3) / 1e12}),
+          flush=True)
+
+
 def run_profile_hbm(args):
     """The HBM-stream kernels alone, for profiler captures: the LSE merge at the causal-LM
     size (1,048,576 rows x 128, bf16) and the two Ulysses transposes at the Ulysses size
@@ -839,6 +886,8 @@ def main():
                          "still larger than L2): the small case for profiler captures")
     ap.add_argument("--profile-backward", action="store_true",
                     help="only the backward of the headline workload with 8 heads (profiler case)")
+    ap.add_argument("--profile-packed", action="store_true",
+                    help="only the packed-sequence forward and backward (profiler case)")
     ap.add_argument("--profile-hbm", action="store_true",
                     help="only the merge and Ulysses transpose kernels (profiler case)")
     ap.add_argument("--ref-rows", type=int, default=8,
@@ -853,6 +902,8 @@ def main():
         run_profile_backward(args)
     elif args.profile_hbm:
         run_profile_hbm(args)
+    elif args.profile_packed:
+        run_profile_packed(args)
     elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
