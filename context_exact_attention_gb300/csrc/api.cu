@@ -496,11 +496,16 @@ ra_status bwd_impl(const void* q, const void* k, const void* v, const void* out,
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     st = status_word(&a.status);
     if (st != RA_OK) return st;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tk64, tv64;
     if (!encode_qkv_map(&tq, q, B, L, H, D) || !encode_qkv_map(&tk, k, B, L, Hkv, D) ||
         !encode_qkv_map(&tv, v, B, L, Hkv, D) || !encode_qkv_map(&tdo, dout, B, L, H, D))
         return RA_ERR_CUDA;
-    return from_cuda(ra::launch_attn_bwd_bf16(a, tq, tk, tv, tdo));
+    const bool pair = ra::bwd_dq_pair_applies(a);
+    if (pair && (!encode_qkv_map(&tk64, k, B, L, Hkv, D, 64) ||
+                 !encode_qkv_map(&tv64, v, B, L, Hkv, D, 64)))
+        return RA_ERR_CUDA;
+    return from_cuda(ra::launch_attn_bwd_bf16(a, tq, tk, tv, tdo, pair ? &tk64 : nullptr,
+                                              pair ? &tv64 : nullptr));
 }
 
 }  // namespace

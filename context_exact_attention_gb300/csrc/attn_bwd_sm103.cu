@@ -1728,9 +1728,368 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------ dQ on pairs of SMs --
+//
+// bwd_dq_pair_kernel: the dQ kernel's products issued for a pair of SMs
+// (tcgen05.mma.cta_group::2, M = 256), contiguous shards, head dim 128.  A cluster of two
+// CTAs takes two consecutive query tiles (2j, 2j + 1) of one shard of one (batch, head):
+// CTA rank c holds tile 2j + c -- its Q and dO, and its rows of S/dS, dP and dQ in TMEM.
+// Of every K/V block each CTA stages half, so a product reads half of its B operand from
+// each SM's shared memory:
+//   S = Q K^T (N = keys):    K keys [64 c, 64 c + 64), all head-dim columns;
+//   dP = dO V^T (N = keys):  V keys [64 c, 64 c + 64);
+//   dQ += dS K (N = D):      K head-dim columns [64 c, 64 c + 64) of all 128 keys.
+// Per block and CTA that is 6 KiB + 4 KiB + 2 KiB of operand reads per 16-deep step
+// instead of 8 + 8 + 4, and 48 instead of 64 KiB of K/V staging.  The pair walks the
+// union of its tiles' key blocks (causal: tile 2j + 1's, one diagonal block more than
+// tile 2j needs, which is all masked for it, so its dS rows are 0).  The even CTA's MMA
+// warp issues every product; the even CTA's barriers count both CTAs' TMA bytes and both
+// CTAs' dS (one arrival per elementwise warp); every commit goes to the same barrier of
+// both CTAs.  Bounded waits and the exit handshake as in the pair forward.
+template <int D>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    bwd_dq_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                       const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_k64,
+                       const __grid_constant__ CUtensorMap tmap_v64,
+                       const __grid_constant__ CUtensorMap tmap_do, const BwdParams p)
+{
+    static_assert(D == 128, "pair dQ kernel: head dim 128");
+    constexpr int T = kRows * D * 2;        // one 128-row tile, 32 KiB
+    constexpr int H2 = T / 2;               // one CTA's half of a K or V block
+    constexpr int kQ = 0, kDO = T, kK = 2 * T, kV = 5 * T, kBar = 6 * T;
+    // per K stage: keys half (two 64-column boxes of 64 rows), then the head-dim half (one
+    // 64-column box of 128 rows); per V stage: keys half
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBar + kDBars * 8);
+    int* abort_flag = reinterpret_cast<int*>(smem + kBar + kDBars * 8 + 4);
+    static_assert(kDBars * 8 + 8 <= kDBarArea, "barrier area");
+    auto bar = [&](int i) -> uint32_t { return sbase + kBar + 8u * i; };
+    const uint32_t rank = cluster_ctarank();
+    const bool lead = rank == 0;
+    auto lead_bar = [&](int i) -> uint32_t { return mapa_shared(bar(i), 0); };
+    constexpr uint16_t kBoth = 3;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work unit: a pair of query tiles, heaviest (shard, pair) first, two (batch,
+    // head) pairs interleaved
+    const int n_pair = (p.n_t + 1) / 2;
+    int bh, u;
+    unit_of_block(static_cast<int>(blockIdx.x >> 1), p.B * p.H, p.P * n_pair, bh, u);
+    const int r = p.P - 1 - u / n_pair;
+    const int pj = n_pair - 1 - (u - (u / n_pair) * n_pair);
+    const int qt = 2 * pj + static_cast<int>(rank);        // this CTA's query tile
+    const int b = bh / p.H;
+    const int h = bh - b * p.H;
+    const int hk = h / p.group;
+    const int q_local0 = qt * kRows;
+    const int q0 = r * p.Ls + q_local0;
+    // the pair's ring walk: K/V shard (r - t) mod P at step t, future shards skipped; of the
+    // diagonal shard the tiles up to the pair's last query
+    int n_first = p.n_t, n_blocks = p.P * p.n_t;
+    if (p.causal) {
+        const int q_last = min(p.Ls - 1, (2 * pj + 1) * kRows + kRows - 1);
+        n_first = min(p.n_t, q_last / kRows + 1);
+        n_blocks = n_first + r * p.n_t;
+    }
+    auto block_of = [&](int n, int& s, int& kt) {
+        if (n < n_first) {
+            s = r;
+            kt = n;
+            return;
+        }
+        const int m = n - n_first;
+        const int t = 1 + m / p.n_t;
+        kt = m - (t - 1) * p.n_t;
+        s = r - t;
+        if (s < 0) s += p.P;
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(kQDFull), 1);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(bar(kDKFull + i), 1);
+            mbar_init(bar(kDKEmpty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kDVFull + i), 1);
+            mbar_init(bar(kDVEmpty + i), 1);
+            mbar_init(bar(kDSFull + i), 1);
+            mbar_init(bar(kDDSFull + i), 2 * 8);   // one arrival per elementwise warp, both CTAs
+        }
+        mbar_init(bar(kDOFull), 1);
+        mbar_init(bar(kDDone), 1);
+        mbar_init(bar(kDPFull), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(tmem_slot), 512);
+        tmem_relinquish_pair();
+        tc_fence_before();
+    }
+    // both CTAs' barriers exist and the pair's TMEM is allocated before either CTA signals
+    // the other
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer (both CTAs)
+        const bool leader = elect_one();
+        const uint64_t keep = l2_policy_evict_last();
+        const uint64_t once = l2_policy_evict_first();
+        if (leader) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_k64);
+            tma_prefetch_desc(&tmap_v64);
+            // this CTA's Q and dO tiles, counted on the even CTA's barrier
+            if (lead) mbar_arrive_expect_tx(bar(kQDFull), 4 * T);
+            for (int bx = 0; bx < 2; ++bx) {
+                tma_load_4d_pair(sbase + kQ + bx * 16384, &tmap_q, lead_bar(kQDFull), bx * 64, h, q0,
+                                 b, once);
+                tma_load_4d_pair(sbase + kDO + bx * 16384, &tmap_do, lead_bar(kQDFull), bx * 64, h,
+                                 q0, b, once);
+            }
+        }
+        int last_k[kKStages] = {-1, -1, -1}, last_v[2] = {-1, -1};
+        for (int n = 0; n < n_blocks; ++n) {
+            int s, kt;
+            block_of(n, s, kt);
+            const int st = n & 1;
+            const uint32_t ph = (n >> 1) & 1;
+            const int kst = n % kKStages;
+            const uint32_t kph = (n / kKStages) & 1;
+            const int row = s * p.Ls + kt * kRows;               // first key of the block
+            const int krow = row + 64 * static_cast<int>(rank);  // this CTA's keys
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kDKEmpty + kst), kph ^ 1, wc))) break;
+            if (leader) {
+                if (lead) mbar_arrive_expect_tx(bar(kDKFull + kst), 2 * (H2 + H2));
+                const uint32_t base = sbase + kK + kst * T;
+                for (int bx = 0; bx < 2; ++bx)
+                    tma_load_4d_pair(base + bx * 8192, &tmap_k64, lead_bar(kDKFull + kst), bx * 64, hk,
+                                     krow, b, keep);
+                tma_load_4d_pair(base + H2, &tmap_k, lead_bar(kDKFull + kst), 64 * static_cast<int>(rank),
+                                 hk, row, b, keep);
+            }
+            last_k[kst] = n;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kDVEmpty + st), ph ^ 1, wc))) break;
+            if (leader) {
+                if (lead) mbar_arrive_expect_tx(bar(kDVFull + st), 2 * H2);
+                for (int bx = 0; bx < 2; ++bx)
+                    tma_load_4d_pair(sbase + kV + st * H2 + bx * 8192, &tmap_v64, lead_bar(kDVFull + st),
+                                     bx * 64, hk, krow, b, keep);
+            }
+            last_v[st] = n;
+        }
+        // the even CTA's barriers count both CTAs' copies: it waits for all of them to land
+        // (the odd CTA leaves only after the cluster-wide barrier that follows)
+        if (lead) {
+            mbar_wait_drain(bar(kQDFull), 0, wc);
+            for (int st = 0; st < kKStages; ++st)
+                if (last_k[st] >= 0) mbar_wait_drain(bar(kDKFull + st), (last_k[st] / kKStages) & 1, wc);
+            for (int st = 0; st < 2; ++st)
+                if (last_v[st] >= 0) mbar_wait_drain(bar(kDVFull + st), (last_v[st] >> 1) & 1, wc);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer (even CTA)
+        if (lead) {
+            const bool leader = elect_one();
+            constexpr uint32_t kIdescS = idesc_bf16_f32(2 * kRows, kRows, false);
+            constexpr uint32_t kIdescAcc = idesc_bf16_f32(2 * kRows, D, true);
+            // Q, dO (A, K-major): 128 rows per 64-column box (16 KiB); K, V keys half (B,
+            // K-major): 64 keys per box (8 KiB); K head-dim half (B, MN-major): one
+            // 64-column box of 128 keys, 8 keys per 1024-byte swizzle atom, 16-key steps
+            // 2 KiB apart
+            const uint64_t dQ_A = sdesc_sw128(sbase + kQ, 16, 1024);
+            const uint64_t dDO_A = sdesc_sw128(sbase + kDO, 16, 1024);
+            const uint64_t dK_B = sdesc_sw128(sbase + kK, 16, 1024);
+            const uint64_t dV_B = sdesc_sw128(sbase + kV, 16, 1024);
+            const uint64_t dK_MN = sdesc_sw128(sbase + kK + H2, 16384, 1024);
+            constexpr uint64_t kTU = static_cast<uint64_t>(T) >> 4, kHU = static_cast<uint64_t>(H2) >> 4;
+            auto ss = [&](uint32_t dcol, uint64_t a0, uint64_t b0) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t oa = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+                    const uint64_t ob = ((k >> 2) * 8192 + (k & 3) * 32) >> 4;
+                    mma_ss_pair(tmem + dcol, a0 + oa, b0 + ob, kIdescS, k > 0 ? 1u : 0u);
+                }
+            };
+            // TMEM columns as in the single-SM dQ kernel: S, then dS, alternate between
+            // [0,128) and [128,256) by block parity; dP in [256,384); dQ in [384,512).  The
+            // issue order and the reasons each product may overwrite what it does are the
+            // single-SM kernel's.
+            constexpr uint32_t kDPCol = 256, kDQCol = 384;
+            auto wait_kv = [&](uint32_t n) {
+                return __all_sync(0xffffffffu,
+                                  mbar_wait2(bar(kDKFull + n % kKStages), (n / kKStages) & 1,
+                                             bar(kDVFull + (n & 1)), (n >> 1) & 1, wc));
+            };
+            auto issue_s = [&](uint32_t n) {     // S(n) = Q K_n^T
+                ss(128u * (n & 1), dQ_A, dK_B + (n % kKStages) * kTU);
+                tc_commit_pair(bar(kDSFull + (n & 1)), kBoth);
+            };
+            auto issue_dp = [&](uint32_t n) {    // dP(n) = dO V_n^T
+                ss(kDPCol, dDO_A, dV_B + (n & 1) * kHU);
+                tc_commit_pair(bar(kDPFull), kBoth);
+                tc_commit_pair(bar(kDVEmpty + (n & 1)), kBoth);
+            };
+            bool ok = n_blocks > 0 &&
+                      __all_sync(0xffffffffu, mbar_wait(bar(kQDFull), 0, wc)) && wait_kv(0);
+            if (ok) {
+                tc_fence_after();
+                if (leader) {
+                    issue_s(0);
+                    issue_dp(0);
+                }
+                __syncwarp();
+            }
+            for (int n = 0; ok && n < n_blocks; ++n) {
+                const uint32_t Nn = n;
+                const bool more = n + 1 < n_blocks;
+                if (more) {
+                    if (!(ok = wait_kv(Nn + 1))) break;
+                    tc_fence_after();
+                    if (leader) issue_s(Nn + 1);
+                    __syncwarp();
+                }
+                if (!(ok = __all_sync(0xffffffffu,
+                                      mbar_wait(bar(kDDSFull + (Nn & 1)), (Nn >> 1) & 1, wc))))
+                    break;
+                tc_fence_after();
+                if (leader) {
+                    if (more) issue_dp(Nn + 1);
+                    const uint64_t b0 = dK_MN + (Nn % kKStages) * kTU;
+                    const uint32_t a0 = tmem + 128u * (Nn & 1);
+                    // dQ += dS K; dS of keys [64 x, 64 x + 64) sits in columns [64 x, 64 x + 32)
+#pragma unroll
+                    for (int k = 0; k < kRows / 16; ++k)
+                        mma_ts_pair(tmem + kDQCol, a0 + 64 * (k >> 2) + (k & 3) * 8,
+                                    b0 + ((k * 2048) >> 4), kIdescAcc, (n > 0 || k > 0) ? 1u : 0u);
+                    tc_commit_pair(bar(kDKEmpty + Nn % kKStages), kBoth);
+                    if (!more) tc_commit_pair(bar(kDOFull), kBoth);
+                }
+                __syncwarp();
+            }
+            // every product the pair issued has finished before either CTA frees TMEM
+            if (leader) tc_commit_pair(bar(kDDone), kBoth);
+            __syncwarp();
+        }
+        mbar_wait_drain(bar(kDDone), 0, wc);
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------ elementwise (both CTAs)
+        const int quarter = warp & 3;
+        const int half = (warp - 4) >> 2;                   // key columns [64 half, 64 half + 64)
+        const int row = quarter * 32 + lane;                // query row of this CTA's tile
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
+        const uint32_t tP = tmem + lane_off + 256 + 64 * half;                  // dP
+        const int row_local = q_local0 + row;
+        const bool row_valid = row_local < p.Ls;
+        const long long sidx = (static_cast<long long>(b) * p.L + q0 + row) * p.H + h;
+        const bool stats_ok = row_valid && in_bounds(sidx, 1, p.row_elems, p.status);
+        const float nl2 = stats_ok ? -p.lse[sidx] * kLog2e : 0.f;
+        const float ndv = stats_ok ? -p.dvec[sidx] : 0.f;
+        const int vis_hi = p.causal ? r * p.Ls + row_local : kFar;
+        const uint64_t nl2x2 = f2pack(nl2, nl2), ndvx2 = f2pack(ndv, ndv);
+        bool ok = true;
+        for (int n = 0; n < n_blocks; ++n) {
+            const uint32_t Nn = n;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kDSFull + (Nn & 1)), (Nn >> 1) & 1, wc));
+            if (!ok) break;
+            tc_fence_after();
+            // visible key columns [0, lim] of the block
+            int s, kt;
+            block_of(n, s, kt);
+            int lim = min(min(kRows, p.Ls - kt * kRows) - 1, vis_hi - (s * p.Ls + kt * kRows));
+            if (!row_valid) lim = -1;
+            const bool masked = __any_sync(0xffffffffu, lim < kRows - 1);
+            const uint32_t tS = tmem + lane_off + 128u * (Nn & 1) + 64 * half;  // S, then dS
+            // P = exp2(S scale log2(e) - lse log2(e)) of this warp's 64 columns, in fp32
+            uint64_t pp[32];
+            {
+                uint32_t sr[64];
+                tmem_ld64(tS, sr);
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) {
+                    float a0, a1;
+                    f2unpack(ffma2(f2pack(u2f(sr[2 * i2]), u2f(sr[2 * i2 + 1])), sl2, nl2x2), a0, a1);
+                    float e0 = ex2(a0), e1 = ex2(a1);
+                    if (masked) {
+                        const int c = 64 * half + 2 * i2;
+                        e0 = c <= lim ? e0 : 0.f;
+                        e1 = c + 1 <= lim ? e1 : 0.f;
+                    }
+                    pp[i2] = f2pack(e0, e1);
+                }
+            }
+            // dS = P (dP - Dvec), bf16, written over this warp's S columns
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(kDPFull), Nn & 1, wc)))) break;
+            tc_fence_after();
+            {
+                uint32_t dr[64];
+                tmem_ld64(tP, dr);
+                uint32_t pk[32];
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) {
+                    const uint64_t d = fadd2(f2pack(u2f(dr[2 * i2]), u2f(dr[2 * i2 + 1])), ndvx2);
+                    float g0, g1;
+                    f2unpack(fmul2(pp[i2], d), g0, g1);
+                    pk[i2] = pack_bf16x2(g0, g1);
+                }
+                tmem_st32(tS, pk);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(lead_bar(kDDSFull + (Nn & 1)));
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(kDOFull), 0, wc));
+        if (ok) {
+            tc_fence_after();
+            // each half writes half of the D output columns of this CTA's rows, through the
+            // warp's slice of the K stages (no product reads them any more) so that stores
+            // cover row halves
+            const int qrow0 = q_local0 + quarter * 32;         // within shard r
+            const long long off0 =
+                ((static_cast<long long>(b) * p.L + r * p.Ls + qrow0) * p.H + h) * D + half * (D / 2);
+            uint8_t* stage = smem + kK + (warp - 4) * 32 * D;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                const int col = half * (D / 2) + 32 * c;
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + 384 + col, o);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2)
+                    pk[i2] = pack_bf16x2(u2f(o[2 * i2]) * p.scale, u2f(o[2 * i2 + 1]) * p.scale);
+                stage_row_chunks<D / 2>(stage, lane, 4 * c, pk);
+            }
+            __syncwarp();
+            store_staged_rows<D / 2>(stage, lane, p.dq, off0, static_cast<long long>(p.H) * D,
+                                     p.Ls - qrow0, p.q_elems, p.status);
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
 template <int D, int kMode, int kPersist>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tdo)
+                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap* tk64,
+                         const CUtensorMap* tv64)
 {
     using Lay = BwdLayout<D>;
     constexpr int kSmemKV = KVSmem<D>::kAlloc;
@@ -1817,6 +2176,23 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
         <<<static_cast<unsigned>(grid_kv), kKVThreads, kSmemKV, a.stream>>>(tq, tk, tv, tdo, pk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if constexpr (D == 128 && kMode == 0 && kPersist == 0) {
+        if (tk64 != nullptr && tv64 != nullptr) {
+            // dQ on pairs of SMs: one cluster per pair of query tiles
+            constexpr int kSmemPair = 6 * Lay::kTileBytes + kDBarArea + 1024;
+            static_assert(kSmemPair <= kMaxSmem, "pair dQ shared memory layout exceeds the limit");
+            static std::atomic<int> configured_pair[kMaxDevices];
+            e = smem_limit_once(configured_pair, dev, bwd_dq_pair_kernel<D>, kSmemPair);
+            if (e != cudaSuccess) return e;
+            const long long pairs = static_cast<long long>(a.B) * a.H * a.P * ((p.n_t + 1) / 2);
+            if (2 * pairs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+            bwd_dq_pair_kernel<D><<<static_cast<unsigned>(2 * pairs), kThreads, kSmemPair, a.stream>>>(
+                tq, tk, *tk64, *tv64, tdo, pq);
+            return cudaGetLastError();
+        }
+    }
+    (void)tk64;
+    (void)tv64;
     bwd_dq_kernel<D, kMode, kPersist>
         <<<static_cast<unsigned>(grid_q), kThreads, kSmemQ, a.stream>>>(tq, tk, tv, tdo, pq);
     return cudaGetLastError();
@@ -1824,26 +2200,34 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
 
 template <int D>
 cudaError_t launch_bwd_layout(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const CUtensorMap& tv, const CUtensorMap& tdo)
+                              const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap* tk64,
+                              const CUtensorMap* tv64)
 {
     // packed sequences with a schedule: persistent grids that claim units heaviest first;
     // the other layouts keep one CTA per tile (the block scheduler balances their
     // heaviest-first order)
     if (a.cu_seqlens != nullptr) {
-        if (a.schedule != nullptr) return launch_bwd_d<D, 2, 2>(a, tq, tk, tv, tdo);
-        return launch_bwd_d<D, 2, 0>(a, tq, tk, tv, tdo);
+        if (a.schedule != nullptr) return launch_bwd_d<D, 2, 2>(a, tq, tk, tv, tdo, nullptr, nullptr);
+        return launch_bwd_d<D, 2, 0>(a, tq, tk, tv, tdo, nullptr, nullptr);
     }
-    if (a.zigzag) return launch_bwd_d<D, 1, 0>(a, tq, tk, tv, tdo);
-    return launch_bwd_d<D, 0, 0>(a, tq, tk, tv, tdo);
+    if (a.zigzag) return launch_bwd_d<D, 1, 0>(a, tq, tk, tv, tdo, nullptr, nullptr);
+    return launch_bwd_d<D, 0, 0>(a, tq, tk, tv, tdo, tk64, tv64);
 }
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_bf16(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                                 const CUtensorMap& tv, const CUtensorMap& tdo)
+bool bwd_dq_pair_applies(const BwdArgs& a)
 {
-    if (a.D == 64) return launch_bwd_layout<64>(a, tq, tk, tv, tdo);
-    if (a.D == 128) return launch_bwd_layout<128>(a, tq, tk, tv, tdo);
+    // head dim 128 over contiguous shards (plain and grouped heads)
+    return a.D == 128 && a.cu_seqlens == nullptr && !a.zigzag;
+}
+
+cudaError_t launch_attn_bwd_bf16(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo,
+                                 const CUtensorMap* tk64, const CUtensorMap* tv64)
+{
+    if (a.D == 64) return launch_bwd_layout<64>(a, tq, tk, tv, tdo, nullptr, nullptr);
+    if (a.D == 128) return launch_bwd_layout<128>(a, tq, tk, tv, tdo, tk64, tv64);
     return cudaErrorInvalidValue;
 }
 

@@ -112,9 +112,13 @@ struct BwdArgs {
     unsigned long long timeout_ns;
     cudaStream_t stream;
 };
+// tmap_k64, tmap_v64: k and v with 64-row boxes, required when bwd_dq_pair_applies(a) (the
+// pair-of-SMs dQ kernel stages half a key block per CTA), else null.
 cudaError_t launch_attn_bwd_bf16(const BwdArgs& a, const CUtensorMap& tmap_q,
                                  const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                 const CUtensorMap& tmap_do);
+                                 const CUtensorMap& tmap_do, const CUtensorMap* tmap_k64,
+                                 const CUtensorMap* tmap_v64);
+bool bwd_dq_pair_applies(const BwdArgs& a);
 
 cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                          void* o_out, float* lse_out, long long rows, int D, int elem_bytes,

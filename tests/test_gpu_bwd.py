@@ -90,6 +90,7 @@ CASES = [
     (1, 192, 1, 64, 3),      # shard of 64
     (1, 640, 2, 64, 5),
     (1, 1024, 2, 128, 8),
+    (1, 1280, 2, 128, 2),    # 5 tiles per shard: the last pair of query tiles has one
 ]
 
 
