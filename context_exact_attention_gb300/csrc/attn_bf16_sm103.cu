@@ -1359,12 +1359,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            // every product the pair issued has finished before either CTA frees TMEM
+            // every product the pair issued has finished before either CTA frees TMEM: the
+            // even CTA's issuer waits for them here; the odd CTA's issuer goes to the cluster
+            // barrier below without spinning through the kernel (the even one arrives there
+            // only after this wait) and then sees the same commit's arrival on its own barrier
             if (leader) tc_commit_pair(bar(kBarDone), kBoth);
             __syncwarp();
+            mbar_wait_drain(bar(kBarDone), 0, wc);
+            __syncwarp();
         }
-        mbar_wait_drain(bar(kBarDone), 0, wc);
-        __syncwarp();
     } else if (warp >= 4) {
         // ----------------------------------------------------------- softmax (both CTAs)
         const int tq = (warp - 4) >> 2;
@@ -1515,6 +1518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     cluster_sync_all();
     if (warp == 1) {
+        if (!lead) mbar_wait_drain(bar(kBarDone), 0, wc);
         tc_fence_after();
         tmem_dealloc_pair(tmem, 512);
     }

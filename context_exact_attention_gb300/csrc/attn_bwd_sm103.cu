@@ -1797,17 +1797,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         n_first = min(p.n_t, q_last / kRows + 1);
         n_blocks = n_first + r * p.n_t;
     }
-    auto block_of = [&](int n, int& s, int& kt) {
-        if (n < n_first) {
-            s = r;
-            kt = n;
-            return;
+    // walked in order: block n + 1 from block n (the diagonal shard's first n_first tiles,
+    // then whole shards r - 1, r - 2, ... mod P)
+    struct Walk {
+        int s, kt;
+        __device__ __forceinline__ void next(int n, int n_first, int n_t, int P)
+        {
+            if (++kt == (n + 1 == n_first ? n_first : n_t)) {
+                kt = 0;
+                s = s == 0 ? P - 1 : s - 1;
+            }
         }
-        const int m = n - n_first;
-        const int t = 1 + m / p.n_t;
-        kt = m - (t - 1) * p.n_t;
-        s = r - t;
-        if (s < 0) s += p.P;
     };
 
     if (threadIdx.x == 0) {
@@ -1859,9 +1859,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         }
         int last_k[kKStages] = {-1, -1, -1}, last_v[2] = {-1, -1};
-        for (int n = 0; n < n_blocks; ++n) {
-            int s, kt;
-            block_of(n, s, kt);
+        Walk w{r, 0};
+        for (int n = 0; n < n_blocks; w.next(n, n_first, p.n_t, p.P), ++n) {
+            const int s = w.s, kt = w.kt;
             const int st = n & 1;
             const uint32_t ph = (n >> 1) & 1;
             const int kst = n % kKStages;
@@ -1978,12 +1978,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            // every product the pair issued has finished before either CTA frees TMEM
+            // every product the pair issued has finished before either CTA frees TMEM: the
+            // even CTA's issuer waits for them here; the odd CTA's issuer goes to the cluster
+            // barrier below without spinning through the kernel (the even one arrives there
+            // only after this wait) and then sees the same commit's arrival on its own barrier
             if (leader) tc_commit_pair(bar(kDDone), kBoth);
             __syncwarp();
+            mbar_wait_drain(bar(kDDone), 0, wc);
+            __syncwarp();
         }
-        mbar_wait_drain(bar(kDDone), 0, wc);
-        __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------ elementwise (both CTAs)
         const int quarter = warp & 3;
@@ -2001,14 +2004,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int vis_hi = p.causal ? r * p.Ls + row_local : kFar;
         const uint64_t nl2x2 = f2pack(nl2, nl2), ndvx2 = f2pack(ndv, ndv);
         bool ok = true;
-        for (int n = 0; n < n_blocks; ++n) {
+        Walk w{r, 0};
+        for (int n = 0; n < n_blocks; w.next(n, n_first, p.n_t, p.P), ++n) {
             const uint32_t Nn = n;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(kDSFull + (Nn & 1)), (Nn >> 1) & 1, wc));
             if (!ok) break;
             tc_fence_after();
             // visible key columns [0, lim] of the block
-            int s, kt;
-            block_of(n, s, kt);
+            const int s = w.s, kt = w.kt;
             int lim = min(min(kRows, p.Ls - kt * kRows) - 1, vis_hi - (s * p.Ls + kt * kRows));
             if (!row_valid) lim = -1;
             const bool masked = __any_sync(0xffffffffu, lim < kRows - 1);
@@ -2081,6 +2084,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     cluster_sync_all();
     if (warp == 1) {
+        if (!lead) mbar_wait_drain(bar(kDDone), 0, wc);
         tc_fence_after();
         tmem_dealloc_pair(tmem, 512);
     }
