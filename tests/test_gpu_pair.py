@@ -81,3 +81,22 @@ def test_pair_forward_trace(causal):
     _, _, tref = oracle.ring_attention(*small, P, causal=causal)
     assert np.array_equal(trace.cpu().numpy(), tref)
     _check(q, k, v, out, lse, causal, L, P, "trace call")
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_pair_forward_random_shapes(seed):
+    """Seeded draws of batch, length (8192 to 12288 keys, any multiple of P), heads,
+    grouped key/value heads, shard count and causal masking through the pair kernel, on
+    sampled rows against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    P = int(rng.choice([1, 2, 3, 4, 5, 8]))
+    L = P * int(rng.integers(8192 // P + 1, 12288 // P + 1))
+    Hkv = int(rng.choice([1, 2]))
+    H = Hkv * int(rng.choice([1, 2]))
+    B = int(rng.integers(1, 3))
+    causal = bool(rng.integers(0, 2))
+    q, _, _ = make_qkv(B, L, H, 128, seed=2000 + seed)
+    _, k, v = make_qkv(B, L, Hkv, 128, seed=3000 + seed)
+    out, lse = cea.ring_attn_fwd_gqa(*(t.to(DEV) for t in (q, k, v)), P=P, causal=causal)
+    assert cea.check_status() == 0
+    _check(q, k, v, out, lse, causal, L, P, f"B{B} L{L} H{H} Hkv{Hkv} P{P} causal={causal}")
