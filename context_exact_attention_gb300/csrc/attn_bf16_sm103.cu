@@ -1096,9 +1096,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // core's shared-memory read pipe, which holds single-SM products to ~71 cycles, stops
 // being the limit (a stream of these products issues at the nominal 64 cycles).
 // The even CTA's MMA warp issues everything; its barriers count both CTAs' TMA bytes and
-// both CTAs' softmax arrivals (the odd CTA's threads arrive remotely), and every commit is
-// multicast to the same barrier of both CTAs.  S and O of a CTA's rows live in its own
-// TMEM, so the softmax warps work exactly as in the single-SM kernel.  Head dim 128 only.
+// both CTAs' P (one arrival per softmax warp, the odd CTA's through its cluster address),
+// and every commit is multicast to the same barrier of both CTAs.  S and O of a CTA's rows
+// live in its own TMEM, so the softmax warps work exactly as in the single-SM kernel.
+// Head dim 128 only.
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ring_attn_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
