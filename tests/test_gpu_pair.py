@@ -34,11 +34,14 @@ def _check(q, k, v, out, lse, causal, L, P, what):
 
 
 CASES = [
-    # B, L, H, P: shards of 2048 (whole quads), 3000 (ragged quad), 4100 (ragged block)
+    # B, L, H, P: shards of 2048 (whole quads), 3000 (ragged quad), 4100 (ragged block),
+    # then shards shorter than the four tiles a pair of CTAs takes
     (1, 8192, 2, 4),
     (2, 9000, 1, 3),
     (1, 8200, 2, 2),
     (1, 16384, 1, 1),
+    (1, 8192, 1, 32),        # shards of 256: the odd CTA's two tiles lie past every shard
+    (1, 8320, 1, 65),        # shards of one tile
 ]
 
 
