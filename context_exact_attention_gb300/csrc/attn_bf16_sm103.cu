@@ -1149,8 +1149,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     const int quad0 = quad * (4 * kRows);                  // first query row of the quad
     const int q0_local = quad0 + static_cast<int>(rank) * (kTiles * kRows);   // this CTA's
-    ContigSched walk;
-    walk.init(r, p.P, p.n_kt, p.Ls, p.causal, min(p.Ls - 1, quad0 + 4 * kRows - 1));
+    // the quad's walk: contiguous shards see up to the quad's last row; zigzag shards up to
+    // the largest position among the quad's four tiles (their last rows: positions rise
+    // within each chunk, and the late chunk lies after the early one), walked in order
+    typename std::conditional<kMode == 1, ZigzagSched, ContigSched>::type walk;
+    if constexpr (kMode == 1) {
+        int maxq = 0;
+        for (int k = 0; k < 4; ++k)
+            maxq = max(maxq, position(r, min(p.Ls - 1, quad0 + k * kRows + kRows - 1), p.P, p.Ls, 1));
+        walk.init(r, p.P, p.n_kt, p.Ls, p.causal, maxq);
+    } else {
+        walk.init(r, p.P, p.n_kt, p.Ls, p.causal, min(p.Ls - 1, quad0 + 4 * kRows - 1));
+    }
     const int n_blocks = walk.n_blocks;
 
     if (threadIdx.x == 0) {
@@ -1378,7 +1388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + Layout<D>::col_s(tq);
         const uint32_t tO = tmem + lane_off + Layout<D>::col_o(tq);
         const int row_local = q0_local + tq * kRows + row;   // within shard r
-        const int row_pos = r * p.Ls + row_local;
+        const int row_pos = position(r, row_local, p.P, p.Ls, kMode == 1 ? 1 : 0);
         const float sl2 = p.scale_log2;
         // P ready: one arrival per warp of either CTA, after the warp's TMEM stores
         const uint32_t pfull0 = lead_bar(kBarPFull + 2 * tq);      // half 1: the next word
@@ -1549,6 +1559,7 @@ cudaError_t launch_pair(const AttnArgs& a, const CUtensorMap& tq, const CUtensor
     p.P = a.P;
     p.Ls = a.L / a.P;
     p.causal = a.causal;
+    p.zigzag = a.zigzag;
     p.group = a.H / a.Hkv;
     p.u_B = a.u_B;
     p.u_H = a.u_H;
@@ -1652,19 +1663,22 @@ cudaError_t launch_mode(const AttnArgs& a, const CUtensorMap& tq, const CUtensor
 
 bool attn_bf16_pair_applies(const AttnArgs& a)
 {
-    // Head dim 128, contiguous shards or Ulysses head groups, and key walks of at least
-    // 64 blocks: a pair halves each SM's K/V staging and operand reads, which pays on
-    // long walks (3-4 % faster at 32k-128k keys, equal on causal 32k), while the pair's
+    // Head dim 128, contiguous or zigzag shards or Ulysses head groups, and key walks of
+    // at least 64 blocks: a pair halves each SM's K/V staging and operand reads, which
+    // pays on long walks (3-4 % faster at 32k-128k keys, equal on causal 32k; 3 % at the
+    // power cap, where the lighter traffic leaves the clock higher), while the pair's
     // fixed costs (cluster barriers, paired TMEM allocation, the lock-step of two CTAs)
     // made 4096-key walks about 3 % slower than the single-SM kernel.
-    return a.D == 128 && a.cu_seqlens == nullptr && !a.zigzag && a.L >= 8192;
+    return a.D == 128 && a.cu_seqlens == nullptr && a.L >= 8192;
 }
 
 cudaError_t launch_attn_bf16(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv)
 {
-    if (attn_bf16_pair_applies(a)) return a.u_P > 0 ? launch_pair<3>(a, tq, tk, tv)
-                                                    : launch_pair<0>(a, tq, tk, tv);
+    if (attn_bf16_pair_applies(a)) {
+        if (a.u_P > 0) return launch_pair<3>(a, tq, tk, tv);
+        return a.zigzag ? launch_pair<1>(a, tq, tk, tv) : launch_pair<0>(a, tq, tk, tv);
+    }
     if (a.u_P > 0) {
         if (a.D == 64) return launch_mode<64, 3>(a, tq, tk, tv);
         if (a.D == 128) return launch_mode<128, 3>(a, tq, tk, tv);

@@ -1,9 +1,10 @@
 """Parity of the pair-of-SMs forward (tcgen05.mma.cta_group::2, head dim 128), which
-takes contiguous and Ulysses bf16 calls whose key walk spans at least 8192 keys: outputs
-and lse against the fp64 oracle on sampled query rows (every shard's first and last
-rows, the rows around each 512-row quad edge and seeded uniform rows), with ragged
-shards (not a multiple of the 512 rows a pair takes, nor of the 128-key block), two
-batches, grouped key/value heads, the ring trace, and repeated calls bit for bit."""
+takes contiguous, zigzag and Ulysses bf16 calls whose key walk spans at least 8192
+keys: outputs and lse against the fp64 oracle on sampled query rows (every shard's
+first and last rows, the rows around each 512-row quad edge and seeded uniform rows),
+with ragged shards (not a multiple of the 512 rows a pair takes, nor of the 128-key
+block), two batches, grouped key/value heads, zigzag shards, the ring trace, and
+repeated calls bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -103,3 +104,29 @@ def test_pair_forward_random_shapes(seed):
     out, lse = cea.ring_attn_fwd_gqa(*(t.to(DEV) for t in (q, k, v)), P=P, causal=causal)
     assert cea.check_status() == 0
     _check(q, k, v, out, lse, causal, L, P, f"B{B} L{L} H{H} Hkv{Hkv} P{P} causal={causal}")
+
+
+@pytest.mark.parametrize("B,L,H,P", [
+    (1, 8192, 2, 4),         # chunks of 1024 rows: two quads per chunk
+    (1, 8960, 1, 7),         # chunks of 640 rows: a quad straddles the two chunks of a shard
+    (2, 9216, 1, 3),
+])
+def test_pair_forward_zigzag(B, L, H, P):
+    """Causal attention over the zigzag layout through the pair kernel: rows in zigzag
+    order against the oracle on the position-ordered tensors (sampled rows), the ring trace
+    (every shard meets every shard, its own first, each step passing on what the previous
+    shard held)."""
+    qg, kg, vg = make_qkv(B, L, H, 128, seed=96 + P)       # row = global position
+    pos = torch.tensor(cea.zigzag_positions(L, P))
+    q, k, v = (t[:, pos].contiguous() for t in (qg, kg, vg))
+    out, lse, trace = cea.ring_attn_fwd_zigzag(*(t.to(DEV) for t in (q, k, v)), P=P, trace=True)
+    assert cea.check_status() == 0
+    rows = _rows(L, P)
+    ref, lref = oracle.attention(qg, kg, vg, causal=True, rows=pos[rows].tolist())
+    assert_bf16_close(to_np(out[:, rows]), ref, "zigzag out")
+    assert_bf16_close(to_np(lse[:, rows]), lref, "zigzag lse")
+    tr = trace.cpu().numpy()
+    for r in range(P):
+        assert sorted(tr[r].tolist()) == list(range(P)) and tr[r, 0] == r
+        for t in range(1, P):
+            assert tr[r, t] == tr[(r - 1) % P, t - 1]
