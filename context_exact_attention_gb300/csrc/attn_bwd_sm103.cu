@@ -1731,9 +1731,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------ dQ on pairs of SMs --
 //
 // bwd_dq_pair_kernel: the dQ kernel's products issued for a pair of SMs
-// (tcgen05.mma.cta_group::2, M = 256), contiguous shards, head dim 128.  A cluster of two
-// CTAs takes two consecutive query tiles (2j, 2j + 1) of one shard of one (batch, head):
-// CTA rank c holds tile 2j + c -- its Q and dO, and its rows of S/dS, dP and dQ in TMEM.
+// (tcgen05.mma.cta_group::2, M = 256), contiguous (kMode 0) or zigzag (kMode 1) shards,
+// head dim 128.  A cluster of two CTAs takes two consecutive query tiles of one shard of
+// one (batch, head) -- (2j, 2j + 1) of a contiguous shard, or of one chunk of a zigzag
+// shard, where a chunk of an odd number of tiles leaves its last pair one tile -- and CTA
+// rank c holds the pair's tile c: its Q and dO, and its rows of S/dS, dP and dQ in TMEM.
 // Of every K/V block each CTA stages half, so a product reads half of its B operand from
 // each SM's shared memory:
 //   S = Q K^T (N = keys):    K keys [64 c, 64 c + 64), all head-dim columns;
@@ -1741,12 +1743,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   dQ += dS K (N = D):      K head-dim columns [64 c, 64 c + 64) of all 128 keys.
 // Per block and CTA that is 6 KiB + 4 KiB + 2 KiB of operand reads per 16-deep step
 // instead of 8 + 8 + 4, and 48 instead of 64 KiB of K/V staging.  The pair walks the
-// union of its tiles' key blocks (causal: tile 2j + 1's, one diagonal block more than
-// tile 2j needs, which is all masked for it, so its dS rows are 0).  The even CTA's MMA
+// union of its tiles' key blocks (causal: the later tile's, one diagonal block more than
+// the earlier tile needs, which is all masked for it, so its dS rows are 0; a CTA without
+// a tile masks every row and stores nothing).  The even CTA's MMA
 // warp issues every product; the even CTA's barriers count both CTAs' TMA bytes and both
 // CTAs' dS (one arrival per elementwise warp); every commit goes to the same barrier of
 // both CTAs.  Bounded waits and the exit handshake as in the pair forward.
-template <int D>
+template <int D, int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bwd_dq_pair_kernel(const __grid_constant__ CUtensorMap tmap_q,
                        const __grid_constant__ CUtensorMap tmap_k,
@@ -1755,6 +1758,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmap_do, const BwdParams p)
 {
     static_assert(D == 128, "pair dQ kernel: head dim 128");
+    static_assert(kMode == 0 || kMode == 1, "pair dQ kernel: contiguous or zigzag shards");
+    constexpr bool kZig = kMode == 1;
     constexpr int T = kRows * D * 2;        // one 128-row tile, 32 KiB
     constexpr int H2 = T / 2;               // one CTA's half of a K or V block
     constexpr int kQ = 0, kDO = T, kK = 2 * T, kV = 5 * T, kBar = 6 * T;
@@ -1776,34 +1781,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work unit: a pair of query tiles, heaviest (shard, pair) first, two (batch,
-    // head) pairs interleaved
-    const int n_pair = (p.n_t + 1) / 2;
-    int bh, u;
-    unit_of_block(static_cast<int>(blockIdx.x >> 1), p.B * p.H, p.P * n_pair, bh, u);
-    const int r = p.P - 1 - u / n_pair;
-    const int pj = n_pair - 1 - (u - (u / n_pair) * n_pair);
-    const int qt = 2 * pj + static_cast<int>(rank);        // this CTA's query tile
+    // ---- work unit: a pair of query tiles, heaviest first (contiguous: last shard, last
+    // pair; zigzag: descending global position), two (batch, head) pairs interleaved
+    int bh, u, r, qt;
+    bool tile_valid = true;             // zigzag: this CTA has a tile of the pair's chunk
+    PosWalk zwalk;                      // zigzag: the pair's ring walk over positions
+    int n_first = p.n_t, n_blocks = p.P * p.n_t;
+    if constexpr (kZig) {
+        const int per_chunk = p.n_t >> 1;
+        const int npc = (per_chunk + 1) >> 1;
+        unit_of_block(static_cast<int>(blockIdx.x >> 1), p.B * p.H, 2 * p.P * npc, bh, u);
+        const int g = 2 * p.P * npc - 1 - u;
+        const int chunk = g / npc, within = g - chunk * npc;
+        const int base = chunk < p.P ? 0 : per_chunk;
+        r = chunk < p.P ? chunk : 2 * p.P - 1 - chunk;
+        tile_valid = 2 * within + static_cast<int>(rank) < per_chunk;
+        qt = base + 2 * within + static_cast<int>(rank);
+        // the K/V tiles holding positions up to the pair's last query, in the forward's
+        // ring order (zigzag is causal)
+        const int last_t = base + min(2 * within + 1, per_chunk - 1);
+        zwalk.init(r, -1, p.P, p.Ls, 1, 0,
+                   layout_position(r, last_t * kRows + kRows - 1, p.Ls, p.P, true));
+        n_blocks = zwalk.total();
+    } else {
+        const int n_pair = (p.n_t + 1) / 2;
+        unit_of_block(static_cast<int>(blockIdx.x >> 1), p.B * p.H, p.P * n_pair, bh, u);
+        r = p.P - 1 - u / n_pair;
+        const int pj = n_pair - 1 - (u - (u / n_pair) * n_pair);
+        qt = 2 * pj + static_cast<int>(rank);
+        // the pair's ring walk: K/V shard (r - t) mod P at step t, future shards skipped;
+        // of the diagonal shard the tiles up to the pair's last query
+        if (p.causal) {
+            const int q_last = min(p.Ls - 1, (2 * pj + 1) * kRows + kRows - 1);
+            n_first = min(p.n_t, q_last / kRows + 1);
+            n_blocks = n_first + r * p.n_t;
+        }
+    }
     const int b = bh / p.H;
     const int h = bh - b * p.H;
     const int hk = h / p.group;
     const int q_local0 = qt * kRows;
     const int q0 = r * p.Ls + q_local0;
-    // the pair's ring walk: K/V shard (r - t) mod P at step t, future shards skipped; of the
-    // diagonal shard the tiles up to the pair's last query
-    int n_first = p.n_t, n_blocks = p.P * p.n_t;
-    if (p.causal) {
-        const int q_last = min(p.Ls - 1, (2 * pj + 1) * kRows + kRows - 1);
-        n_first = min(p.n_t, q_last / kRows + 1);
-        n_blocks = n_first + r * p.n_t;
-    }
-    // walked in order: block n + 1 from block n (the diagonal shard's first n_first tiles,
-    // then whole shards r - 1, r - 2, ... mod P)
+    // walked in order: block n + 1 from block n (contiguous: the diagonal shard's first
+    // n_first tiles, then whole shards r - 1, r - 2, ... mod P; zigzag: the position walk)
     struct Walk {
         int s, kt;
+        PosWalk pw;
+        __device__ __forceinline__ void start(int r, const PosWalk& z)
+        {
+            if constexpr (kZig) {
+                pw = z;
+                pw.at(0);
+                s = pw.x;
+                kt = pw.tile();
+            } else {
+                s = r;
+                kt = 0;
+            }
+        }
         __device__ __forceinline__ void next(int n, int n_first, int n_t, int P)
         {
-            if (++kt == (n + 1 == n_first ? n_first : n_t)) {
+            if constexpr (kZig) {
+                pw.at(n + 1);
+                s = pw.x;
+                kt = pw.tile();
+            } else if (++kt == (n + 1 == n_first ? n_first : n_t)) {
                 kt = 0;
                 s = s == 0 ? P - 1 : s - 1;
             }
@@ -1859,7 +1901,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         }
         int last_k[kKStages] = {-1, -1, -1}, last_v[2] = {-1, -1};
-        Walk w{r, 0};
+        Walk w;
+        w.start(r, zwalk);
         for (int n = 0; n < n_blocks; w.next(n, n_first, p.n_t, p.P), ++n) {
             const int s = w.s, kt = w.kt;
             const int st = n & 1;
@@ -1996,15 +2039,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint64_t sl2 = f2pack(p.scale_log2, p.scale_log2);
         const uint32_t tP = tmem + lane_off + 256 + 64 * half;                  // dP
         const int row_local = q_local0 + row;
-        const bool row_valid = row_local < p.Ls;
+        const bool row_valid = kZig ? tile_valid : row_local < p.Ls;
         const long long sidx = (static_cast<long long>(b) * p.L + q0 + row) * p.H + h;
         const bool stats_ok = row_valid && in_bounds(sidx, 1, p.row_elems, p.status);
         const float nl2 = stats_ok ? -p.lse[sidx] * kLog2e : 0.f;
         const float ndv = stats_ok ? -p.dvec[sidx] : 0.f;
-        const int vis_hi = p.causal ? r * p.Ls + row_local : kFar;
+        // causal bound: the row's global position (zigzag positions, chunks of whole tiles)
+        const int vis_hi = kZig       ? layout_position(r, row_local, p.Ls, p.P, true)
+                           : p.causal ? r * p.Ls + row_local
+                                      : kFar;
         const uint64_t nl2x2 = f2pack(nl2, nl2), ndvx2 = f2pack(ndv, ndv);
         bool ok = true;
-        Walk w{r, 0};
+        Walk w;
+        w.start(r, zwalk);
         for (int n = 0; n < n_blocks; w.next(n, n_first, p.n_t, p.P), ++n) {
             const uint32_t Nn = n;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(kDSFull + (Nn & 1)), (Nn >> 1) & 1, wc));
@@ -2012,7 +2059,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // visible key columns [0, lim] of the block
             const int s = w.s, kt = w.kt;
-            int lim = min(min(kRows, p.Ls - kt * kRows) - 1, vis_hi - (s * p.Ls + kt * kRows));
+            const int kp0 = kZig ? layout_position(s, kt * kRows, p.Ls, p.P, true) : s * p.Ls + kt * kRows;
+            int lim = min(min(kRows, p.Ls - kt * kRows) - 1, vis_hi - kp0);
             if (!row_valid) lim = -1;
             const bool masked = __any_sync(0xffffffffu, lim < kRows - 1);
             const uint32_t tS = tmem + lane_off + 128u * (Nn & 1) + 64 * half;  // S, then dS
@@ -2077,7 +2125,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             store_staged_rows<D / 2>(stage, lane, p.dq, off0, static_cast<long long>(p.H) * D,
-                                     p.Ls - qrow0, p.q_elems, p.status);
+                                     tile_valid ? p.Ls - qrow0 : 0, p.q_elems, p.status);
         }
     }
 
@@ -2180,17 +2228,19 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
         <<<static_cast<unsigned>(grid_kv), kKVThreads, kSmemKV, a.stream>>>(tq, tk, tv, tdo, pk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if constexpr (D == 128 && kMode == 0 && kPersist == 0) {
+    if constexpr (D == 128 && (kMode == 0 || kMode == 1) && kPersist == 0) {
         if (tk64 != nullptr && tv64 != nullptr) {
-            // dQ on pairs of SMs: one cluster per pair of query tiles
+            // dQ on pairs of SMs: one cluster per pair of query tiles (zigzag: per pair
+            // within a chunk, a chunk of an odd number of tiles ending in a lone tile)
             constexpr int kSmemPair = 6 * Lay::kTileBytes + kDBarArea + 1024;
             static_assert(kSmemPair <= kMaxSmem, "pair dQ shared memory layout exceeds the limit");
             static std::atomic<int> configured_pair[kMaxDevices];
-            e = smem_limit_once(configured_pair, dev, bwd_dq_pair_kernel<D>, kSmemPair);
+            e = smem_limit_once(configured_pair, dev, bwd_dq_pair_kernel<D, kMode>, kSmemPair);
             if (e != cudaSuccess) return e;
-            const long long pairs = static_cast<long long>(a.B) * a.H * a.P * ((p.n_t + 1) / 2);
+            const int pairs_per_shard = kMode == 1 ? 2 * ((p.n_t / 2 + 1) / 2) : (p.n_t + 1) / 2;
+            const long long pairs = static_cast<long long>(a.B) * a.H * a.P * pairs_per_shard;
             if (2 * pairs > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-            bwd_dq_pair_kernel<D><<<static_cast<unsigned>(2 * pairs), kThreads, kSmemPair, a.stream>>>(
+            bwd_dq_pair_kernel<D, kMode><<<static_cast<unsigned>(2 * pairs), kThreads, kSmemPair, a.stream>>>(
                 tq, tk, *tk64, *tv64, tdo, pq);
             return cudaGetLastError();
         }
@@ -2214,7 +2264,7 @@ cudaError_t launch_bwd_layout(const BwdArgs& a, const CUtensorMap& tq, const CUt
         if (a.schedule != nullptr) return launch_bwd_d<D, 2, 2>(a, tq, tk, tv, tdo, nullptr, nullptr);
         return launch_bwd_d<D, 2, 0>(a, tq, tk, tv, tdo, nullptr, nullptr);
     }
-    if (a.zigzag) return launch_bwd_d<D, 1, 0>(a, tq, tk, tv, tdo, nullptr, nullptr);
+    if (a.zigzag) return launch_bwd_d<D, 1, 0>(a, tq, tk, tv, tdo, tk64, tv64);
     return launch_bwd_d<D, 0, 0>(a, tq, tk, tv, tdo, tk64, tv64);
 }
 
@@ -2222,8 +2272,8 @@ cudaError_t launch_bwd_layout(const BwdArgs& a, const CUtensorMap& tq, const CUt
 
 bool bwd_dq_pair_applies(const BwdArgs& a)
 {
-    // head dim 128 over contiguous shards (plain and grouped heads)
-    return a.D == 128 && a.cu_seqlens == nullptr && !a.zigzag;
+    // head dim 128 over contiguous or zigzag shards (plain and grouped heads)
+    return a.D == 128 && a.cu_seqlens == nullptr;
 }
 
 cudaError_t launch_attn_bwd_bf16(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,

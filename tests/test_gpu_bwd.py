@@ -211,6 +211,11 @@ ZIGZAG_CASES = [
     (1, 768, 2, 64, 3),
     (1, 2048, 1, 128, 8),
     (1, 256, 2, 128, 1),
+    # chunks of several tiles (head dim 128: dQ on pairs of SMs, a pair within a chunk):
+    # 5 and 3 tiles (a lone tile ends each chunk), 4 tiles (whole pairs)
+    (1, 2560, 2, 128, 2),
+    (1, 1536, 2, 128, 2),
+    (1, 4096, 1, 128, 4),
 ]
 
 
@@ -374,7 +379,7 @@ def _grouped_scales(q, k, v, do, causal, G):
 
 
 @pytest.mark.parametrize("case", [(1, 1024, 4, 2, 128, 4), (2, 768, 6, 2, 64, 3),
-                                  (1, 512, 4, 1, 128, 2)],
+                                  (1, 512, 4, 1, 128, 2), (1, 2048, 4, 2, 128, 2)],
                          ids=lambda c: "B%dL%dH%dHkv%dD%dP%d" % c)
 def test_bwd_ex_zigzag_grouped_heads_parity(case):
     """Backward of grouped key/value heads over zigzag shards against the grouped fp64
