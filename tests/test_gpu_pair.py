@@ -130,3 +130,19 @@ def test_pair_forward_zigzag(B, L, H, P):
         assert sorted(tr[r].tolist()) == list(range(P)) and tr[r, 0] == r
         for t in range(1, P):
             assert tr[r, t] == tr[(r - 1) % P, t - 1]
+
+
+def test_pair_forward_zigzag_grouped_heads():
+    """Zigzag shards with four query heads over two key/value heads (the descriptor entry
+    point), on sampled rows against the oracle on the position-ordered tensors."""
+    B, L, H, Hkv, P = 1, 8192, 4, 2, 4
+    qg, _, _ = make_qkv(B, L, H, 128, seed=97)
+    _, kg, vg = make_qkv(B, L, Hkv, 128, seed=98)
+    pos = torch.tensor(cea.zigzag_positions(L, P))
+    q, k, v = (t[:, pos].contiguous().to(DEV) for t in (qg, kg, vg))
+    out, lse = cea.ring_attn_fwd_ex(q, k, v, P=P, causal=True, layout="zigzag")
+    assert cea.check_status() == 0
+    rows = _rows(L, P)
+    ref, lref = oracle.attention(qg, kg, vg, causal=True, rows=pos[rows].tolist())
+    assert_bf16_close(to_np(out[:, rows]), ref, "zigzag gqa out")
+    assert_bf16_close(to_np(lse[:, rows]), lref, "zigzag gqa lse")
