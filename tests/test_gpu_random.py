@@ -154,3 +154,29 @@ def test_random_backward(layout, draw):
         for name, g, r, sc in zip(("dq", "dk", "dv"), got, refs, scales):
             _close(g[:, rows.numpy()], r, sc, f"{name} {layout} B{B} L{L} H{H}/{Hkv} D{D} P{P} "
                                               f"causal={causal} rows {a}:{b}")
+
+
+@pytest.mark.parametrize("draw,P,c", [(0, 1, 5), (1, 2, 3), (2, 3, 2), (3, 4, 2), (4, 1, 8)])
+def test_random_zigzag_backward_multi_tile_chunks(draw, P, c):
+    """Zigzag backward at head dim 128 with chunks of c 128-row tiles (odd counts leave a
+    lone tile at the end of each chunk: the pair-of-SMs dQ forms its pairs inside a
+    chunk), with seeded draws of the query and key/value head counts."""
+    rng = np.random.default_rng(9000 + draw)
+    B, L, D = 1, 2 * P * 128 * c, 128
+    Hkv = int(rng.choice([1, 2]))
+    H = Hkv * int(rng.choice([1, 2]))
+    G = H // Hkv
+    q = make_qkv(B, L, H, D, seed=700 + draw, dtype=torch.bfloat16)[0]
+    _, k, v = make_qkv(B, L, Hkv, D, seed=800 + draw, dtype=torch.bfloat16)
+    do = torch.randn(B, L, H, D, generator=torch.Generator().manual_seed(900 + draw)).to(torch.bfloat16)
+    pos = _positions("zigzag", L, P)
+    inv = torch.as_tensor(np.argsort(pos))
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = cea.ring_attn_fwd_ex(qd, kd, vd, P=P, causal=True, layout="zigzag")
+    dq, dk, dv = cea.ring_attn_bwd_ex(qd, kd, vd, out, lse, dod, P=P, causal=True, layout="zigzag")
+    assert cea.check_status() == 0
+    seg = [t[:, inv] for t in (q, k, v, do)]                  # position order
+    refs = oracle.attention_bwd_gqa(*seg, causal=True)
+    scales = _grad_scale(*seg, True, G)
+    for name, g, r, sc in zip(("dq", "dk", "dv"), (dq, dk, dv), refs, scales):
+        _close(to_np(g)[:, inv.numpy()], r, sc, f"{name} zigzag L{L} H{H}/{Hkv} P{P} chunk {c} tiles")
