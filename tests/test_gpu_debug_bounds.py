@@ -69,6 +69,14 @@ def _every_entry_point():
     dz = _bf16(1, 2048, 2, 64, seed=73)
     out, lse = cea.ring_attn_fwd_zigzag(qz, kz, vz, P=4)
     res += [out, lse, *cea.ring_attn_bwd_zigzag(qz, kz, vz, out, lse, dz, P=4)]
+    # zigzag at head dim 128 with chunks of 5 tiles (pair-of-SMs dQ, a lone tile ending
+    # each chunk), and the pair-of-SMs zigzag forward with a quad across a shard's chunks
+    qz, kz, vz = (t.to(DEV) for t in make_qkv(1, 2560, 2, 128, seed=82, dtype=torch.bfloat16))
+    dz = _bf16(1, 2560, 2, 128, seed=83)
+    out, lse = cea.ring_attn_fwd_zigzag(qz, kz, vz, P=2)
+    res += [out, lse, *cea.ring_attn_bwd_zigzag(qz, kz, vz, out, lse, dz, P=2)]
+    qz, kz, vz = (t.to(DEV) for t in make_qkv(1, 8960, 1, 128, seed=84, dtype=torch.bfloat16))
+    res += list(cea.ring_attn_fwd_zigzag(qz, kz, vz, P=7))
     # packed sequences, with and without the schedule
     Lp = 1024
     cu = torch.tensor([0, 5, 300, 301, 777, 1024], dtype=torch.int32, device=DEV)
