@@ -211,19 +211,21 @@ struct ContigSched {
             n_blocks = P * n_kt;
         }
     }
+    // block n, walked in order (at(n) must see n = 0, 1, 2, ...): the diagonal shard's
+    // first n_first tiles, then whole shards r - 1, r - 2, ... mod P
     __device__ __forceinline__ void at(int n)
     {
-        if (n < n_first) {
+        if (n == 0) {
             t = 0;
             s = r;
-            kt_ = n;
+            kt_ = 0;
             return;
         }
-        const int m = n - n_first;
-        t = 1 + m / n_kt;
-        kt_ = m - (t - 1) * n_kt;
-        s = r - t;
-        if (s < 0) s += P;
+        if (++kt_ == (t == 0 ? n_first : n_kt)) {
+            kt_ = 0;
+            ++t;
+            s = s == 0 ? P - 1 : s - 1;
+        }
     }
     __device__ __forceinline__ int kt() const { return kt_; }
     __device__ __forceinline__ bool first_of_shard() const { return kt_ == 0; }
