@@ -1131,14 +1131,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work unit: a quad of query tiles, heaviest (shard, quad) first, two (batch,
-    // head) pairs interleaved
+    // ---- work unit: a quad of query tiles, heaviest first, two (batch, head) pairs
+    // interleaved.  Contiguous shards: last shard, last quad first.  Zigzag shards whose
+    // chunks hold whole quads: descending global position (chunk 2P - 1, the late half of
+    // shard 0, first), since there a quad's work grows with its position, not its shard;
+    // other zigzag shapes keep the contiguous order.
     const int n_quad = (p.n_pair + 1) / 2;
     const int units_per_bh = p.P * n_quad;
     int bh, u;
     unit_of_block(static_cast<int>(blockIdx.x >> 1), p.B * p.H, units_per_bh, bh, u);
-    const int r = p.P - 1 - u / n_quad;
-    const int quad = n_quad - 1 - (u - (u / n_quad) * n_quad);
+    int r = p.P - 1 - u / n_quad;
+    int quad = n_quad - 1 - (u - (u / n_quad) * n_quad);
+    if constexpr (kMode == 1) {
+        const int per_chunk = p.n_kt >> 1;              // tiles per chunk
+        if ((per_chunk & 3) == 0) {
+            const int qpc = per_chunk >> 2;             // quads per chunk
+            const int g = units_per_bh - 1 - u;         // position order of the quad
+            const int chunk = g / qpc, within = g - chunk * qpc;
+            r = chunk < p.P ? chunk : 2 * p.P - 1 - chunk;
+            quad = (chunk < p.P ? 0 : qpc) + within;
+        }
+    }
     const int b = bh / p.H;
     const int h = bh - b * p.H;
     const int hk = h / p.group;
