@@ -345,7 +345,8 @@ struct Unit {
                                                         ContigSched>::type>::type walk;
 
     // Unit g of the call's order: heaviest (shard, pair) first within each (batch, head),
-    // two (batch, head) pairs interleaved; packed sequences take the schedule's order.
+    // two (batch, head) pairs interleaved (zigzag shards: by global position); packed
+    // sequences take the schedule's order.
     __device__ __forceinline__ void setup(int g, const Params& p)
     {
         decode(g, p);
@@ -361,6 +362,19 @@ struct Unit {
         unit_of_block(g, p.B * p.H, units_per_bh, bh, u);
         r = p.P - 1 - u / p.n_pair;
         pair = p.n_pair - 1 - (u - (u / p.n_pair) * p.n_pair);
+        if constexpr (kMode == 1) {
+            // zigzag shards whose chunks hold whole pairs: descending global position (a
+            // pair's work grows with its position, not its shard); other shapes keep the
+            // order above
+            const int per_chunk = p.n_kt >> 1;          // tiles per chunk
+            if ((per_chunk & 1) == 0) {
+                const int ppc = per_chunk >> 1;         // pairs per chunk
+                const int gp = units_per_bh - 1 - u;    // position order of the pair
+                const int chunk = gp / ppc, within = gp - chunk * ppc;
+                r = chunk < p.P ? chunk : 2 * p.P - 1 - chunk;
+                pair = (chunk < p.P ? 0 : ppc) + within;
+            }
+        }
         if constexpr (kMode == 2) {
             // packed sequences: work follows the offset inside a sequence, not the position;
             // a precomputed order (entries outside the unit range are ignored) puts the
