@@ -834,6 +834,42 @@ def run_profile_packed(args):
           flush=True)
 
 
+def run_profile_zigzag(args):
+    """The causal-LM zigzag workload with 8 heads (B=1, L=32768, D=128, P=8; inputs above
+    L2 at 201 MB), for profiler captures of the zigzag pair-of-SMs kernels: `warmup` +
+    `steps` forward calls, then as many backward calls, one line out."""
+    import context_exact_attention_gb300 as cea
+
+    dev = torch.device("cuda", 0)
+    cea.load_library()
+    stream = torch.cuda.current_stream(dev)
+    w = LM
+    H = 8
+    g = torch.Generator(device=dev).manual_seed(0)
+    q, k, v, do = (torch.randn(w.B, w.L, H, w.D, device=dev, generator=g).to(torch.bfloat16)
+                   for _ in range(4))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.L, H), dtype=torch.float32, device=dev)
+    fwd = lambda: cea.ring_attn_fwd_zigzag(q, k, v, P=w.P, out=out, lse=lse, stream=stream)
+    for _ in range(args.warmup):
+        fwd()
+    ms_f = _time_loop(fwd, args.steps, stream) / args.steps
+    ws = torch.empty(w.B * w.L * H, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    bwd = lambda: cea.ring_attn_bwd_zigzag(q, k, v, out, lse, do, P=w.P, dq=dq, dk=dk, dv=dv,
+                                           workspace=ws, stream=stream)
+    for _ in range(args.warmup):
+        bwd()
+    ms_b = _time_loop(bwd, args.steps, stream) / args.steps
+    if cea.check_status(stream) != 0:
+        raise RuntimeError("kernel reported a device-side timeout")
+    fl = attention_flops(w.B, w.L, H, w.D, True)
+    print(json.dumps({"case": "zigzag shards, B1 H8 L32768 D128 P8 bf16, causal",
+                      "forward_ms": ms_f, "forward_tflops": fl / (ms_f * 1e-3) / 1e12,
+                      "backward_ms": ms_b, "backward_tflops": 2.5 * fl / (ms_b * 1e-3) / 1e12}),
+          flush=True)
+
+
 def run_profile_hbm(args):
     """The HBM-stream kernels alone, for profiler captures: the LSE merge at the causal-LM
     size (1,048,576 rows x 128, bf16) and the two Ulysses transposes at the Ulysses size
@@ -888,6 +924,8 @@ def main():
                     help="only the backward of the headline workload with 8 heads (profiler case)")
     ap.add_argument("--profile-packed", action="store_true",
                     help="only the packed-sequence forward and backward (profiler case)")
+    ap.add_argument("--profile-zigzag", action="store_true",
+                    help="only the zigzag forward and backward with 8 heads (profiler case)")
     ap.add_argument("--profile-hbm", action="store_true",
                     help="only the merge and Ulysses transpose kernels (profiler case)")
     ap.add_argument("--ref-rows", type=int, default=8,
@@ -904,6 +942,8 @@ def main():
         run_profile_hbm(args)
     elif args.profile_packed:
         run_profile_packed(args)
+    elif args.profile_zigzag:
+        run_profile_zigzag(args)
     elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
