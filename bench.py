@@ -416,7 +416,19 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(2):
         e2e_step()
     e2e_steps = max(3, args.steps // 4)
-    e2e_ms = _time_loop(e2e_step, e2e_steps, stream) / e2e_steps
+    # one event between consecutive steps (same stream, no synchronisation): the loop's
+    # total gives the metric; the per-step times give the median beside it, since the
+    # CPU-GPU link of these boxes stalls for 50-80 ms about every 0.45 s of copying
+    e2e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    torch.cuda.synchronize()
+    e2e_ev[0].record(stream)
+    for i in range(e2e_steps):
+        e2e_step()
+        e2e_ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    e2e_each = [e2e_ev[i].elapsed_time(e2e_ev[i + 1]) for i in range(e2e_steps)]
+    e2e_ms = e2e_ev[0].elapsed_time(e2e_ev[-1]) / e2e_steps
+    e2e_median = sorted(e2e_each)[e2e_steps // 2]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
@@ -473,7 +485,8 @@ def run_gpu(args, rank, world, local_rank):
             "accuracy": accuracy,
             "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms,
+                    "ms_per_step": e2e_ms, "median_ms_per_step": e2e_median,
+                    "max_ms_per_step": max(e2e_each),
                     "api": f"ring_attn_fwd_host, pinned host buffers, heads_per_group={group}"},
             "gpu_launches": args.steps, "clocks": clocks, "rows": rows,
         }
