@@ -216,6 +216,7 @@ ZIGZAG_CASES = [
     (1, 2560, 2, 128, 2),
     (1, 1536, 2, 128, 2),
     (1, 4096, 1, 128, 4),
+    (2, 2048, 1, 128, 2),
 ]
 
 
