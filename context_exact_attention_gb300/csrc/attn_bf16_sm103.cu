@@ -359,7 +359,8 @@ struct Unit {
     {
         const int units_per_bh = p.P * p.n_pair;
         int u;
-        unit_of_block<kMode == 2 ? kVarlenHeadGroup : kHeadGroup>(g, p.B * p.H, units_per_bh, bh, u);
+        if constexpr (kMode == 2) unit_of_claim_varlen(g, p.B * p.H, units_per_bh, bh, u);
+        else unit_of_block(g, p.B * p.H, units_per_bh, bh, u);
         r = p.P - 1 - u / p.n_pair;
         pair = p.n_pair - 1 - (u - (u / p.n_pair) * p.n_pair);
         if constexpr (kMode == 1) {
@@ -500,8 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = e[0];
         if (g >= 0) {
             int u;
-            unit_of_block<kMode == 2 ? kVarlenHeadGroup : kHeadGroup>(g, p.B * p.H, p.P * p.n_pair,
-                                                                       V.bh, u);
+            if constexpr (kMode == 2) unit_of_claim_varlen(g, p.B * p.H, p.P * p.n_pair, V.bh, u);
+            else unit_of_block(g, p.B * p.H, p.P * p.n_pair, V.bh, u);
             V.r = e[1];
             V.pair = e[2];
             V.finish(p, e[3], e[4]);

@@ -30,12 +30,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
 // units fill the tail) while only two heads' K/V are live in L2 at a time.  Block `block`
 // of a grid of n_bh * units_per_bh blocks gets (bh, u); the mapping is a bijection.
 constexpr int kHeadGroup = 2;
-// The packed-sequence forward: every head has the same units (the sequence boundaries are
-// shared), and their work varies far more than in the other layouts; interleaving eight
-// heads lets the heaviest units of all of them start before the light ones end the grid,
-// while eight heads' K/V of one stretch of positions still fit in L2.  (The backward kept
-// two: eight measured 1.6 % slower there.)
-constexpr int kVarlenHeadGroup = 8;
 template <int kGroup = kHeadGroup>
 __device__ __forceinline__ void unit_of_block(int block, int n_bh, int units_per_bh, int& bh,
                                               int& u)
@@ -45,6 +39,27 @@ __device__ __forceinline__ void unit_of_block(int block, int n_bh, int units_per
     const int k = block - base * units_per_bh;
     u = k / cnt;
     bh = base + (k - u * cnt);
+}
+
+// The packed-sequence forward: every head has the same units (the sequence boundaries are
+// shared), and their work varies far more than in the other layouts, so with two heads at
+// a time the last two heads' heavy units ran on while the rest of the grid ran dry.  Its
+// claims take the heads two at a time except the last kVarlenTailHeads, which are
+// interleaved together: their heaviest units all start before the light ones end the
+// grid, while the heads before them keep the two-head K/V working set in L2.
+constexpr int kVarlenTailHeads = 8;
+__device__ __forceinline__ void unit_of_claim_varlen(int block, int n_bh, int units_per_bh,
+                                                     int& bh, int& u)
+{
+    const int tail = min(n_bh, kVarlenTailHeads);
+    const int before = (n_bh - tail) * units_per_bh;     // claims of the leading heads
+    if (block < before) {
+        unit_of_block(block, n_bh - tail, units_per_bh, bh, u);
+        return;
+    }
+    const int k = block - before;
+    u = k / tail;
+    bh = n_bh - tail + (k - u * tail);
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
