@@ -417,8 +417,8 @@ def run_gpu(args, rank, world, local_rank):
         e2e_step()
     e2e_steps = max(3, args.steps // 4)
     # one event between consecutive steps (same stream, no synchronisation): the loop's
-    # total gives the metric; the per-step times give the median beside it, since the
-    # CPU-GPU link of these boxes stalls for 50-80 ms about every 0.45 s of copying
+    # total gives the metric; the per-step times give the median and the slowest step
+    # beside it, since the CPU-GPU link can stall for tens of milliseconds now and then
     e2e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
     torch.cuda.synchronize()
     e2e_ev[0].record(stream)
